@@ -1,0 +1,64 @@
+"""Conventional per-token SSM recurrences in float64 (test infrastructure only).
+
+Both functions take a batch of sequences and return the updated state and the
+output of this token.  They are the plain definitions that ReplaySSM must
+reproduce "up to floating-point differences" ([richland] What shipped, the
+paragraph on unrolling the recurrence; [ai-jitan] ReplaySSMは何をする手法か).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+def group_of_head(n_heads: int, n_groups: int) -> np.ndarray:
+    """Group (Mamba-2 B/C group, GDN key head) used by each head: floor(h * G / H)."""
+    return (np.arange(n_heads) * n_groups) // n_heads
+
+
+def mamba2_step(S, x, dt, A, Bm, Cm):
+    """One Mamba-2 decode token, conventional form.
+
+    S_t = a_t S_{t-1} + v_t k_t^T and y_t = S_t q_t, per head, with
+    a_t = exp(dt_t A_h), v_t = dt_t x_t, k_t = B_t and q_t = C_t of the head's
+    group ([richland] What shipped: "the Mamba-2 update S_t = α_t S_{t-1} + v_t k_t^T";
+    the per-token read-update-write of the conventional decoder).
+
+    S  [b][H][P][N] float64     x  [b][H][P]      dt [b][H]
+    A  [H]                      Bm, Cm [b][G][N]
+    Returns (S_t, y_t) with y_t [b][H][P].
+    """
+    H = S.shape[1]
+    G = Bm.shape[1]
+    grp = group_of_head(H, G)
+    a = np.exp(dt * A[None, :])                      # [b][H]
+    v = dt[:, :, None] * x                           # [b][H][P]
+    k = Bm[:, grp, :]                                # [b][H][N]
+    q = Cm[:, grp, :]                                # [b][H][N]
+    S_new = a[:, :, None, None] * S + v[:, :, :, None] * k[:, :, None, :]
+    y = np.einsum("bhpn,bhn->bhp", S_new, q)
+    return S_new, y
+
+
+def gdn_step(S, q, k, v, g, beta):
+    """One Gated DeltaNet decode token, conventional form.
+
+    S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T and o_t = S_t q_t, per
+    value head, with a_t = exp(g_t) and b_t = beta_t; q and k come from the
+    head's key head.  S_{t-1}(I - b k k^T) is expanded as S_{t-1} - b (S_{t-1} k) k^T.
+
+    S  [b][Hv][dv][dk] float64   q, k [b][Hk][dk]   v [b][Hv][dv]
+    g, beta [b][Hv]
+    Returns (S_t, o_t) with o_t [b][Hv][dv].
+    """
+    Hv = S.shape[1]
+    Hk = k.shape[1]
+    kh = group_of_head(Hv, Hk)
+    a = np.exp(g)[:, :, None, None]
+    b = beta[:, :, None, None]
+    kk = k[:, kh, :]                                 # [b][Hv][dk]
+    qq = q[:, kh, :]
+    Sk = np.einsum("bhvk,bhk->bhv", S, kk)           # S_{t-1} k
+    S_new = a * (S - b * Sk[:, :, :, None] * kk[:, :, None, :]) + b * v[:, :, :, None] * kk[:, :, None, :]
+    o = np.einsum("bhvk,bhk->bhv", S_new, qq)
+    return S_new, o

@@ -1,0 +1,113 @@
+"""The pins must catch plausible oracle mistakes.
+
+Each case plants one mistake in a copy of an oracle recurrence (on the CPU),
+installs it where the pins look it up, and checks that at least one pin of
+tests/test_oracle_pins.py fails.
+"""
+
+import numpy as np
+import pytest
+
+import oracle.layer as layer_mod
+import tests.test_oracle_pins as pins
+from oracle.recurrence import group_of_head
+
+
+def m2_output_before_update(S, x, dt, A, Bm, Cm):
+    grp = group_of_head(S.shape[1], Bm.shape[1])
+    a = np.exp(dt * A[None, :])
+    y = np.einsum("bhpn,bhn->bhp", S, Cm[:, grp, :])
+    S_new = a[:, :, None, None] * S + (dt[:, :, None] * x)[:, :, :, None] * Bm[:, grp, None, :]
+    return S_new, y
+
+
+def m2_no_decay(S, x, dt, A, Bm, Cm):
+    grp = group_of_head(S.shape[1], Bm.shape[1])
+    S_new = S + (dt[:, :, None] * x)[:, :, :, None] * Bm[:, grp, None, :]
+    return S_new, np.einsum("bhpn,bhn->bhp", S_new, Cm[:, grp, :])
+
+
+def m2_decay_on_update(S, x, dt, A, Bm, Cm):
+    grp = group_of_head(S.shape[1], Bm.shape[1])
+    a = np.exp(dt * A[None, :])
+    S_new = a[:, :, None, None] * (S + (dt[:, :, None] * x)[:, :, :, None] * Bm[:, grp, None, :])
+    return S_new, np.einsum("bhpn,bhn->bhp", S_new, Cm[:, grp, :])
+
+
+def m2_swapped_bc(S, x, dt, A, Bm, Cm):
+    grp = group_of_head(S.shape[1], Bm.shape[1])
+    a = np.exp(dt * A[None, :])
+    S_new = a[:, :, None, None] * S + (dt[:, :, None] * x)[:, :, :, None] * Cm[:, grp, None, :]
+    return S_new, np.einsum("bhpn,bhn->bhp", S_new, Bm[:, grp, :])
+
+
+def m2_wrong_group(S, x, dt, A, Bm, Cm):
+    H, G = S.shape[1], Bm.shape[1]
+    grp = np.arange(H) % G
+    a = np.exp(dt * A[None, :])
+    S_new = a[:, :, None, None] * S + (dt[:, :, None] * x)[:, :, :, None] * Bm[:, grp, None, :]
+    return S_new, np.einsum("bhpn,bhn->bhp", S_new, Cm[:, grp, :])
+
+
+def m2_v_without_dt(S, x, dt, A, Bm, Cm):
+    grp = group_of_head(S.shape[1], Bm.shape[1])
+    a = np.exp(dt * A[None, :])
+    S_new = a[:, :, None, None] * S + x[:, :, :, None] * Bm[:, grp, None, :]
+    return S_new, np.einsum("bhpn,bhn->bhp", S_new, Cm[:, grp, :])
+
+
+def _gdn(variant):
+    def step(S, q, k, v, g, beta):
+        kh = group_of_head(S.shape[1], k.shape[1])
+        a = np.exp(g)[:, :, None, None]
+        b = beta[:, :, None, None]
+        kk, qq = k[:, kh, :], q[:, kh, :]
+        Sk = np.einsum("bhvk,bhk->bhv", S, kk)
+        outer_vk = v[:, :, :, None] * kk[:, :, None, :]
+        if variant == "plus_erase":
+            S_new = a * (S + b * Sk[..., None] * kk[:, :, None, :]) + b * outer_vk
+        elif variant == "left_projection":
+            kS = np.einsum("bhk,bhkv->bhv", kk, S)          # k^T S instead of S k
+            S_new = a * (S - b * kk[:, :, :, None] * kS[:, :, None, :]) + b * outer_vk
+        elif variant == "erase_without_beta":
+            S_new = a * (S - Sk[..., None] * kk[:, :, None, :]) + b * outer_vk
+        elif variant == "decay_on_write":
+            S_new = a * (S - b * Sk[..., None] * kk[:, :, None, :] + b * outer_vk)
+        o = np.einsum("bhvk,bhk->bhv", S_new, qq)
+        return S_new, o
+    return step
+
+
+M2_PINS = ["test_mamba2_dyadic_hand_values", "test_mamba2_geometric_series",
+           "test_mamba2_unit_decay_is_prefix_sum", "test_mamba2_group_mapping",
+           "test_mamba2_unrolled_identity", "test_mamba2_chunkwise_verify_matches_oracle",
+           "test_commit_advances_by_accepted_prefix"]
+GDN_PINS = ["test_gdn_dyadic_hand_values", "test_gdn_zero_beta_is_pure_decay",
+            "test_gdn_delta_rule_writes_value_at_key", "test_gdn_general_step_along_and_across_key",
+            "test_gdn_from_zero_state", "test_gdn_delta_form",
+            "test_gdn_chunkwise_verify_with_triangular_solve"]
+
+
+def _some_pin_fails(names) -> bool:
+    for name in names:
+        try:
+            getattr(pins, name)()
+        except (AssertionError, np.linalg.LinAlgError):
+            return True
+    return False
+
+
+@pytest.mark.parametrize("bad", [m2_output_before_update, m2_no_decay, m2_decay_on_update,
+                                 m2_swapped_bc, m2_wrong_group, m2_v_without_dt])
+def test_mamba2_mistake_is_caught(monkeypatch, bad):
+    monkeypatch.setattr(pins, "mamba2_step", bad)
+    monkeypatch.setattr(layer_mod, "mamba2_step", bad)
+    assert _some_pin_fails(M2_PINS)
+
+
+@pytest.mark.parametrize("variant", ["plus_erase", "left_projection", "erase_without_beta", "decay_on_write"])
+def test_gdn_mistake_is_caught(monkeypatch, variant):
+    bad = _gdn(variant)
+    monkeypatch.setattr(pins, "gdn_step", bad)
+    monkeypatch.setattr(layer_mod, "gdn_step", bad)
+    assert _some_pin_fails(GDN_PINS)
