@@ -1,0 +1,501 @@
+"""Benchmark of the ReplaySSM decode hot path on one GB300 (or N, one process per GPU).
+
+A step is one standard decode step of one Mamba-2 layer at B = 256
+(nheads 128, headdim 64, dstate 128, ngroups 8, FP32 checkpoint, L = 16):
+non-flush steps and the flush step every 16th token, at their natural
+ratio, through the C ABI.  The timed region holds whole windows of steps with
+inputs already resident in HBM; the 1 GiB state is larger than L2, so no L2
+flush is needed between steps.  Per-launch CUDA events on the launching
+stream give the roofline of the decode kernel.  Extra objects time the
+Gated DeltaNet layer (B = 256), speculative verify + commit (B = 512, T = 4)
+and the FP8 / NVFP4 read copies.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With --impl reference the CPU oracle (the conventional per-token recurrence
+in float64) is timed on the host cores on a bounded sample of the same
+workload.  Multi-GPU runs (torchrun) shard sequences: every rank runs its own
+B = 256 batch with no communication on the data path.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SSM decode seq·steps/s per layer at B=256 (Mamba-2/GDN); HBM GB/s vs 8 TB/s"
+UNIT = "seq·steps/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("decode.cu", "common.cuh", "internal.h"):
+        h.update(open(os.path.join(ROOT, "checkpoint_input_replay_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(name: str):
+    """Per-launch DRAM bytes recorded in profiles/<name>.md for the current kernel source, else None."""
+    p = os.path.join(ROOT, "profiles", name + ".md")
+    if not os.path.exists(p):
+        return None
+    fields = {}
+    for line in open(p):
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_sha")):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_sha") != kernel_sha() or "traffic_bytes_per_launch" not in fields:
+        return None
+    return float(fields["traffic_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self, skip_first: int = 2):
+        rows = []
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        rows = rows[skip_first:] or rows
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            for name, v in zip(names, r[2:]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- workloads
+
+def m2_bytes(shape, h: int, flush: bool) -> int:
+    """Algorithmic HBM bytes of one Mamba-2 decode step per sequence with h records buffered."""
+    H, G, P, N = shape.n_heads, shape.n_groups, shape.d_head, shape.d_state
+    state = H * P * N * 4
+    record = H * P * 2 + H * 2 + H * 4 + G * N * 2          # x, dt, log a, B
+    inputs = H * P * 2 + H * 2 + 2 * G * N * 2               # x, dt, B, C
+    out = H * P * 4
+    b = state + h * record + inputs + out
+    return b + (state if flush else record)
+
+
+def gdn_bytes(shape, h: int, flush: bool) -> int:
+    H, G, P, N = shape.n_heads, shape.n_groups, shape.d_head, shape.d_state
+    state = H * P * N * 4
+    record = H * P * 4 + H * 4 + G * N * 2                   # u, g, k
+    inputs = 2 * G * N * 2 + H * P * 2 + 2 * H * 4           # q, k, v, g, beta
+    out = H * P * 4
+    b = state + h * record + inputs + out
+    return b + (state if flush else record)
+
+
+def upload(inp: dict, dev) -> dict:
+    import torch
+    out = {}
+    for k, v in inp.items():
+        if v.dtype == np.uint16:
+            out[k] = torch.from_numpy(v.view(np.int16).copy()).to(dev).view(torch.bfloat16)
+        else:
+            out[k] = torch.from_numpy(np.ascontiguousarray(v)).to(dev)
+    return out
+
+
+def make_cache(wl, dev, read_mode=None, seed=0):
+    """Cache with a seeded synthetic initial state N(0, s0_std) drawn on the device."""
+    import torch
+    from checkpoint_input_replay_gb300 import ReplayCache
+    cache = ReplayCache.for_shape(wl.shape, read_mode=read_mode, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + seed)
+    ck = cache.ckpt
+    for b0 in range(0, wl.shape.batch, 32):
+        ck[b0:b0 + 32].normal_(0.0, wl.s0_std, generator=g)
+    if read_mode is not None:
+        cache.flush()
+    torch.cuda.synchronize(dev)
+    return cache
+
+
+def run_decode_loop(cache, steps_inputs, K, W, dev, barrier):
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    D = len(steps_inputs)
+    for t in range(W):
+        inp, y = steps_inputs[t % D]
+        cache.decode_step(inp, y, stream=stream)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for t in range(K):
+        inp, y = steps_inputs[(W + t) % D]
+        ev[t][0].record(stream)
+        cache.decode_step(inp, y, stream=stream)
+        ev[t][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    return start.elapsed_time(end), [a.elapsed_time(b) for a, b in ev]
+
+
+def decode_leg(wl, dev, K, W, L, bytes_fn, barrier, distinct=16):
+    """Decode steps of one layer; warm-up W rounded up so timing starts at a window boundary."""
+    import torch
+    W = int(math.ceil(W / L) * L)
+    cache = make_cache(wl, dev)
+    A = torch.from_numpy(wl.A()).to(dev) if hasattr(wl, "A") else None
+    steps = []
+    for t in range(distinct):
+        inp = upload(wl.step(t), dev)
+        if A is not None:
+            inp["A"] = A
+        y = torch.empty(wl.shape.batch, wl.shape.n_heads, wl.shape.d_head, dtype=torch.float32, device=dev)
+        steps.append((inp, y))
+    elapsed, per = run_decode_loop(cache, steps, K, W, dev, barrier)
+    err = cache.device_error()
+    nbytes = [bytes_fn(wl.shape, (W + t) % L, (W + t) % L == L - 1) * wl.shape.batch for t in range(K)]
+    flush_ms = [p for t, p in enumerate(per) if (W + t) % L == L - 1]
+    nonflush_ms = [p for t, p in enumerate(per) if (W + t) % L != L - 1]
+    flush_b = [b for t, b in enumerate(nbytes) if (W + t) % L == L - 1]
+    nonflush_b = [b for t, b in enumerate(nbytes) if (W + t) % L != L - 1]
+    res = {
+        "elapsed_ms": elapsed, "launch_ms_total": sum(per), "bytes_total": sum(nbytes),
+        "nonflush_gbs": sum(nonflush_b) / (sum(nonflush_ms) * 1e6) if nonflush_ms else None,
+        "flush_gbs": sum(flush_b) / (sum(flush_ms) * 1e6) if flush_ms else None,
+        "nonflush_us": 1e3 * statistics.mean(nonflush_ms) if nonflush_ms else None,
+        "flush_us": 1e3 * statistics.mean(flush_ms) if flush_ms else None,
+        "device_error": err, "launches": K,
+    }
+    del cache, steps
+    torch.cuda.empty_cache()
+    return res
+
+
+def e2e_leg(wl, dev, K, W):
+    """Same metric through ReplayCache.decode_step_from_host: pinned host inputs copied in,
+    the step, y copied back, every step, on one stream."""
+    import torch
+    cache = make_cache(wl, dev)
+    host = []
+    for t in range(16):
+        raw = wl.step(t)
+        h = {}
+        for k, v in raw.items():
+            ten = torch.from_numpy(v.view(np.int16).copy()).view(torch.bfloat16) if v.dtype == np.uint16 \
+                else torch.from_numpy(np.ascontiguousarray(v))
+            h[k] = ten.pin_memory()
+        h["A"] = torch.from_numpy(wl.A()).pin_memory()
+        host.append(h)
+    y_host = torch.empty(wl.shape.batch, wl.shape.n_heads, wl.shape.d_head, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    for t in range(W):
+        cache.decode_step_from_host(host[t % 16], y_host, stream=stream)
+    torch.cuda.synchronize(dev)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for t in range(K):
+        cache.decode_step_from_host(host[(W + t) % 16], y_host, stream=stream)
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = s.elapsed_time(e)
+    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
+    d2h = y_host.numel() * 4
+    assert cache.device_error() == 0
+    return {"value": wl.shape.batch * K / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms / K}
+
+
+def verify_leg(wl, dev, rounds, W, barrier):
+    """Verify (T = 4) + commit rounds at B = 512; returns throughput and verify-kernel bandwidth."""
+    import torch
+    T = 4
+    cache = make_cache(wl, dev)
+    s = wl.shape
+    is_m2 = s.kind == 0
+    A = torch.from_numpy(wl.A()).to(dev) if is_m2 else None
+    drafts, accs = [], []
+    for r in range(4):
+        inp = upload(wl.draft(r, T), dev)
+        if A is not None:
+            inp["A"] = A
+        drafts.append(inp)
+        accs.append(torch.from_numpy(wl.accepted(r, T)).to(dev))
+    y = torch.empty(s.batch, T, s.n_heads, s.d_head, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for r in range(W):
+        cache.verify(T, drafts[r % 4], y, stream=stream)
+        cache.commit(accs[r % 4], stream=stream)
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(rounds)]
+    barrier()
+    for r in range(rounds):
+        ev[r][0].record(stream)
+        cache.verify(T, drafts[r % 4], y, stream=stream)
+        ev[r][1].record(stream)
+        cache.commit(accs[r % 4], stream=stream)
+        ev[r][2].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ver = [a.elapsed_time(b) for a, b, _ in ev]
+    com = [b.elapsed_time(c) for _, b, c in ev]
+    total = ev[0][0].elapsed_time(ev[-1][2])
+    # verify reads the state once plus ~mean ring (h ~ L/2) and the drafts
+    H, P, N, G = s.n_heads, s.d_head, s.d_state, s.n_groups
+    state = H * P * N * 4
+    vbytes = s.batch * (state + T * H * P * 4)
+    assert cache.device_error() == 0
+    del cache
+    torch.cuda.empty_cache()
+    return {"workload": f"{'mamba2' if is_m2 else 'gdn'} verify T=4 + commit, B={s.batch}",
+            "tokens_per_s": s.batch * T * rounds / (total / 1e3),
+            "verify_us": 1e3 * statistics.mean(ver), "commit_us": 1e3 * statistics.mean(com),
+            "verify_state_gbs": vbytes / (statistics.mean(ver) * 1e6), "rounds": rounds}
+
+
+def read_copy_leg(wl, dev, mode, K, W):
+    """Non-flush decode with the low-precision read copy (config 1 shape)."""
+    import torch
+    s = wl.shape
+    cache = make_cache(wl, dev, read_mode=mode)
+    A = torch.from_numpy(wl.A()).to(dev)
+    steps = []
+    for t in range(16):
+        inp = upload(wl.step(t), dev)
+        inp["A"] = A
+        steps.append((inp, torch.empty(s.batch, s.n_heads, s.d_head, dtype=torch.float32, device=dev)))
+    L = s.ring_len
+    W = int(math.ceil(W / L) * L)
+    elapsed, per = run_decode_loop(cache, steps, K, W, dev, lambda: None)
+    nonflush = [p for t, p in enumerate(per) if (W + t) % L != L - 1]
+    H, P, N = s.n_heads, s.d_head, s.d_state
+    rc = H * P * N + H * P * 4 if mode == "fp8" else H * P * N // 2 + H * P * N // 16 + H * 4
+    assert cache.device_error() == 0
+    del cache
+    torch.cuda.empty_cache()
+    return {"mode": mode, "nonflush_us": 1e3 * statistics.mean(nonflush),
+            "read_copy_gbs": s.batch * rc / (statistics.mean(nonflush) * 1e6),
+            "seq_steps_per_s": s.batch * K / (elapsed / 1e3)}
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def oracle_sample(wl, steps: int, seqs: list[int]):
+    """Time the float64 oracle's conventional decode on a few sequences of the workload."""
+    from oracle.layer import OracleLayer
+    inputs = [{k: v for k, v in wl.step(t, seqs[0], seqs[-1] + 1).items()} for t in range(steps)]
+    S0 = wl.S0(seqs[0], seqs[-1] + 1)
+    lay = OracleLayer(wl.shape, seqs, S0, A=wl.A() if hasattr(wl, "A") else None)
+    t0 = time.perf_counter()
+    for t in range(steps):
+        lay.decode(inputs[t])
+    dt = time.perf_counter() - t0
+    return len(seqs) * steps / dt, dt
+
+
+# ----------------------------------------------------------------------------- main
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("BENCH_BACKEND", "nccl")
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, dev) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reference_arm(args, world, rank):
+    """--impl reference: the oracle on the host cores, same metric and workload."""
+    from workloads import configs
+    if rank != 0:
+        return 0
+    wl = configs.config1()
+    per_step_seqs = [0]
+    for _ in range(args.warmup):
+        oracle_sample(wl, 1, per_step_seqs)
+    total = 0.0
+    from oracle.layer import OracleLayer
+    inputs = [wl.step(t, 0, 1) for t in range(16)]
+    lay = OracleLayer(wl.shape, [0], wl.S0(0, 1), A=wl.A())
+    t0 = time.perf_counter()
+    for t in range(args.steps):
+        lay.decode(inputs[t % 16])
+    total = time.perf_counter() - t0
+    value = args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "mamba2 decode, config-1 layer (H128 P64 N128 G8 L16), one sequence per step",
+                       "batch": 1},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} decode steps of sequence 0 of the B=256 workload "
+                                       "(float64 numpy, one thread)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3200)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="skip the GDN / verify / read-copy objects")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+
+    import torch
+    from workloads import configs
+    import checkpoint_input_replay_gb300  # noqa: F401  (fails loudly if the library is missing)
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        barrier = lambda: dist.barrier()
+    else:
+        barrier = lambda: None
+
+    K, W = args.steps, args.warmup
+    wl1 = configs.config1()
+    with ClockSampler(local) as clk:
+        m2 = decode_leg(wl1, dev, K, W, 16, m2_bytes, barrier)
+    elapsed = max_over_ranks(m2["elapsed_ms"], world, dev)
+    value = world * wl1.shape.batch * K / (elapsed / 1e3)
+
+    hbm, peak_kind = peaks()
+    achieved = m2["bytes_total"] / (m2["launch_ms_total"] * 1e6)
+    traffic = ncu_traffic("decode_mamba2_b256")
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": traffic, "peak_kind": peak_kind,
+                "nonflush_gbs": m2["nonflush_gbs"], "nonflush_frac": m2["nonflush_gbs"] / hbm,
+                "flush_gbs": m2["flush_gbs"], "nonflush_us": m2["nonflush_us"], "flush_us": m2["flush_us"]}
+    if traffic is not None:
+        # measured DRAM bytes per L-step window over the ideal (L + 1) |S| (L reads + 1 write)
+        S = wl1.shape.n_heads * wl1.shape.d_head * wl1.shape.d_state * 4 * wl1.shape.batch
+        roofline["window_traffic_over_ideal"] = traffic * 16 / (17 * S)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": elapsed / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "mamba2 decode, 1 layer: B=256 nheads=128 headdim=64 dstate=128 ngroups=8, "
+                                   "FP32 checkpoint, bf16 x/dt/B/C, L=16 (15 non-flush + 1 flush per window)",
+                       "batch_per_gpu": wl1.shape.batch, "ring_len": 16,
+                       "l2": "no flush: the 1 GiB state per step exceeds the 129 MB L2",
+                       "inputs": "16 distinct seeded input steps resident in HBM, cycled; initial state N(0,0.1)"},
+            "roofline": roofline, "gpu_launches": m2["launches"], "clocks": clk.summary(),
+            "device_error": m2["device_error"]}
+    if rank == 0:
+        line["e2e"] = e2e_leg(wl1, dev, min(K, 320), W)
+        rate, secs = oracle_sample(wl1, 8, [0, 1])
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": "8 decode steps of sequences 0-1 of the B=256 workload "
+                                          f"(float64 numpy, one thread, {secs:.1f} s)"}
+        if not args.no_extra:
+            gdn = decode_leg(configs.config2(), dev, min(K, 1600), W, 16, gdn_bytes, lambda: None)
+            line["gdn"] = {"workload": "gdn decode, 1 layer: B=256 Hv=32 Hk=16 dk=dv=128, L=16",
+                           "value": configs.config2().shape.batch * min(K, 1600) / (gdn["elapsed_ms"] / 1e3),
+                           "unit": UNIT, "achieved_gbs": gdn["bytes_total"] / (gdn["launch_ms_total"] * 1e6),
+                           "nonflush_gbs": gdn["nonflush_gbs"], "flush_gbs": gdn["flush_gbs"],
+                           "nonflush_us": gdn["nonflush_us"], "flush_us": gdn["flush_us"],
+                           "frac": gdn["bytes_total"] / (gdn["launch_ms_total"] * 1e6) / hbm}
+            line["verify"] = [verify_leg(configs.config3_mamba2(), dev, 64, 4, lambda: None),
+                              verify_leg(configs.config3_gdn(), dev, 64, 4, lambda: None)]
+            rc = []
+            for mode in ("fp8", "nvfp4"):
+                try:
+                    rc.append(read_copy_leg(configs.config4(), dev, mode, min(K, 1600), W))
+                except Exception as e:  # read copy reported as missing, not silently dropped
+                    rc.append({"mode": mode, "error": str(e).splitlines()[0]})
+            line["read_copy"] = rc
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

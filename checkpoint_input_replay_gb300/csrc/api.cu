@@ -1,0 +1,303 @@
+// Host side of the C ABI declared in include/replayssm.h: argument
+// validation, the buffer layout, call-order rules and kernel launches.
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <new>
+
+#include "internal.h"
+#include "replayssm.h"
+
+struct rs_cache {
+  rs_config cfg;
+  rs::LayerDev dev;
+  int pending;  // drafts appended by the last rs_verify and not yet committed
+};
+
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool is_pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Layout {
+  size_t ckpt, ring, cursor, read_copy, scratch;
+  // ring section offsets (bytes)
+  size_t r0, r1, r2, r3;
+  // read-copy section offsets
+  size_t c0, c1, c2;
+};
+
+size_t decode_smem(const rs_config& c) {
+  rs::LayerDev d{};
+  d.kind = c.kind;
+  d.P = c.d_head;
+  d.N = c.d_state;
+  d.C = c.ring_len + c.max_draft;
+  return rs::decode_smem_bytes(d);
+}
+
+rs_status validate(const rs_config* c) {
+  if (!c) return RS_ERR_NULL;
+  if (c->kind != RS_MAMBA2 && c->kind != RS_GDN) return RS_ERR_RANGE;
+  if (c->read_mode < RS_READ_NONE || c->read_mode > RS_READ_NVFP4) return RS_ERR_RANGE;
+  if (c->batch < 1 || c->n_heads < 1 || c->n_groups < 1 || c->d_head < 1 || c->d_state < 1 ||
+      c->ring_len < 1 || c->max_draft < 0)
+    return RS_ERR_SHAPE;
+  if (c->n_heads % c->n_groups != 0) return RS_ERR_SHAPE;
+  if (static_cast<long long>(c->batch) * c->n_heads > (1LL << 31) - 1) return RS_ERR_SHAPE;
+  if (!is_pow2_in(c->d_state, 16, 128) || !is_pow2_in(c->d_head, 16, 128)) return RS_ERR_UNSUPPORTED;
+  if (static_cast<long long>(c->d_head) * c->d_state * 4 > rs::kMaxTileBytes) return RS_ERR_UNSUPPORTED;
+  if (c->ring_len + c->max_draft > rs::kMaxRec || c->max_draft > 4) return RS_ERR_UNSUPPORTED;
+  if (c->read_mode != RS_READ_NONE && c->kind != RS_MAMBA2) return RS_ERR_UNSUPPORTED;
+  if (decode_smem(*c) > 227 * 1024) return RS_ERR_UNSUPPORTED;
+  return RS_OK;
+}
+
+Layout layout_of(const rs_config& c) {
+  Layout L{};
+  const size_t B = c.batch, H = c.n_heads, G = c.n_groups, P = c.d_head, N = c.d_state;
+  const size_t C = static_cast<size_t>(c.ring_len) + c.max_draft;
+  L.ckpt = B * H * P * N * 4;
+  if (c.kind == RS_MAMBA2) {
+    L.r0 = 0;                                   // x  bf16 [B][H][C][P]
+    L.r1 = L.r0 + align256(B * H * C * P * 2);  // dt bf16 [B][H][C]
+    L.r2 = L.r1 + align256(B * H * C * 2);      // la f32  [B][H][C]
+    L.r3 = L.r2 + align256(B * H * C * 4);      // B  bf16 [B][G][C][N]
+    L.ring = L.r3 + align256(B * G * C * N * 2);
+  } else {
+    L.r0 = 0;                                   // u f32  [B][H][C][P]
+    L.r1 = L.r0 + align256(B * H * C * P * 4);  // g f32  [B][H][C]
+    L.r2 = L.r1 + align256(B * H * C * 4);      // k bf16 [B][G][C][N]
+    L.r3 = L.r2;
+    L.ring = L.r2 + align256(B * G * C * N * 2);
+  }
+  L.cursor = B * 16 + 16;
+  if (c.read_mode == RS_READ_FP8_ROW) {
+    L.c0 = 0;
+    L.c1 = align256(B * H * P * N);             // row scales f32 [B][H][P]
+    L.read_copy = L.c1 + align256(B * H * P * 4);
+  } else if (c.read_mode == RS_READ_NVFP4) {
+    L.c0 = 0;
+    L.c1 = align256(B * H * P * N / 2);         // block scales u8 [B][H][P][N/16]
+    L.c2 = L.c1 + align256(B * H * P * (N / 16));  // matrix scales f32 [B][H]
+    L.read_copy = L.c2 + align256(B * H * 4);
+  }
+  L.scratch = B * 4;
+  return L;
+}
+
+rs_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RS_OK : RS_ERR_CUDA; }
+
+rs_status check_inputs(const rs_cache* h, const rs_inputs* in) {
+  if (!in) return RS_ERR_NULL;
+  const void* p[5];
+  if (h->cfg.kind == RS_MAMBA2) {
+    p[0] = in->x; p[1] = in->dt; p[2] = in->A; p[3] = in->Bm; p[4] = in->Cm;
+  } else {
+    p[0] = in->q; p[1] = in->k; p[2] = in->v; p[3] = in->g; p[4] = in->beta;
+  }
+  for (const void* q : p)
+    if (!q) return RS_ERR_NULL;
+  for (const void* q : p)
+    if (!aligned16(q)) return RS_ERR_ALIGN;
+  return RS_OK;
+}
+
+rs::TokenIn token_in(const rs_inputs* in) {
+  rs::TokenIn t{};
+  t.x = static_cast<const uint16_t*>(in->x);
+  t.dt = static_cast<const uint16_t*>(in->dt);
+  t.A = in->A;
+  t.Bm = static_cast<const uint16_t*>(in->Bm);
+  t.Cm = static_cast<const uint16_t*>(in->Cm);
+  t.q = static_cast<const uint16_t*>(in->q);
+  t.k = static_cast<const uint16_t*>(in->k);
+  t.v = static_cast<const uint16_t*>(in->v);
+  t.g = in->g;
+  t.beta = in->beta;
+  return t;
+}
+
+}  // namespace
+
+namespace rs {
+
+cudaError_t set_smem_limit(const void* func, size_t bytes) {
+  // cudaFuncSetAttribute once per kernel and size: launches stay a plain <<<>>>.
+  static std::mutex mu;
+  static const void* keys[256];
+  static size_t sizes[256];
+  static int used = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (keys[i] == func && sizes[i] >= bytes) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < used; ++i)
+    if (keys[i] == func) {
+      sizes[i] = bytes;
+      return cudaSuccess;
+    }
+  if (used < 256) {
+    keys[used] = func;
+    sizes[used] = bytes;
+    ++used;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace rs
+
+extern "C" {
+
+rs_status rs_query_sizes(const rs_config* cfg, size_t bytes[5]) {
+  if (!cfg || !bytes) return RS_ERR_NULL;
+  const rs_status st = validate(cfg);
+  if (st != RS_OK) return st;
+  const Layout L = layout_of(*cfg);
+  bytes[0] = L.ckpt;
+  bytes[1] = L.ring;
+  bytes[2] = L.cursor;
+  bytes[3] = L.read_copy;
+  bytes[4] = L.scratch;
+  return RS_OK;
+}
+
+rs_status rs_create_cache(const rs_config* cfg, const rs_buffers* bufs, rs_cache** out) {
+  if (!cfg || !bufs || !out) return RS_ERR_NULL;
+  const rs_status st = validate(cfg);
+  if (st != RS_OK) return st;
+  if (!bufs->ckpt || !bufs->ring || !bufs->cursor || !bufs->scratch) return RS_ERR_NULL;
+  if (cfg->read_mode != RS_READ_NONE && !bufs->read_copy) return RS_ERR_NULL;
+  if (!aligned16(bufs->ckpt) || !aligned16(bufs->ring) || !aligned16(bufs->cursor) ||
+      !aligned16(bufs->scratch) || (bufs->read_copy && !aligned16(bufs->read_copy)))
+    return RS_ERR_ALIGN;
+
+  const Layout L = layout_of(*cfg);
+  rs::LayerDev d{};
+  d.kind = cfg->kind;
+  d.B = cfg->batch;
+  d.H = cfg->n_heads;
+  d.G = cfg->n_groups;
+  d.P = cfg->d_head;
+  d.N = cfg->d_state;
+  d.L = cfg->ring_len;
+  d.T_max = cfg->max_draft;
+  d.C = cfg->ring_len + cfg->max_draft;
+  d.read_mode = cfg->read_mode;
+  d.ckpt = static_cast<float*>(bufs->ckpt);
+  char* ring = static_cast<char*>(bufs->ring);
+  if (cfg->kind == RS_MAMBA2) {
+    d.r_x = reinterpret_cast<uint16_t*>(ring + L.r0);
+    d.r_dt = reinterpret_cast<uint16_t*>(ring + L.r1);
+    d.r_la = reinterpret_cast<float*>(ring + L.r2);
+    d.r_B = reinterpret_cast<uint16_t*>(ring + L.r3);
+  } else {
+    d.r_u = reinterpret_cast<float*>(ring + L.r0);
+    d.r_g = reinterpret_cast<float*>(ring + L.r1);
+    d.r_k = reinterpret_cast<uint16_t*>(ring + L.r2);
+  }
+  d.cursor = static_cast<int*>(bufs->cursor);
+  d.err = d.cursor + 4 * d.B;
+  d.arrive = static_cast<int*>(bufs->scratch);
+  if (cfg->read_mode != RS_READ_NONE) {
+    char* rc = static_cast<char*>(bufs->read_copy);
+    d.rc_codes = reinterpret_cast<uint8_t*>(rc + L.c0);
+    if (cfg->read_mode == RS_READ_FP8_ROW) {
+      d.rc_rowscale = reinterpret_cast<float*>(rc + L.c1);
+    } else {
+      d.rc_blkscale = reinterpret_cast<uint8_t*>(rc + L.c1);
+      d.rc_matscale = reinterpret_cast<float*>(rc + L.c2);
+    }
+  }
+
+  cudaError_t e = cudaMemset(bufs->cursor, 0, L.cursor);
+  if (e == cudaSuccess) e = cudaMemset(bufs->scratch, 0, L.scratch);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+  if (e != cudaSuccess) return RS_ERR_CUDA;
+
+  rs_cache* h = new (std::nothrow) rs_cache;
+  if (!h) return RS_ERR_CUDA;
+  h->cfg = *cfg;
+  h->dev = d;
+  h->pending = 0;
+  *out = h;
+  return RS_OK;
+}
+
+void rs_destroy_cache(rs_cache* cache) { delete cache; }
+
+rs_status rs_decode_step(rs_cache* h, const rs_inputs* in, float* y, rs_stream stream) {
+  if (!h || !y) return RS_ERR_NULL;
+  const rs_status st = check_inputs(h, in);
+  if (st != RS_OK) return st;
+  if (!aligned16(y)) return RS_ERR_ALIGN;
+  if (h->pending) return RS_ERR_STATE;
+  if (h->cfg.read_mode != RS_READ_NONE) return RS_ERR_UNSUPPORTED;
+  return from_cuda(rs::launch_decode(h->dev, token_in(in), y, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+rs_status rs_verify(rs_cache* h, int32_t T, const rs_inputs* in, float* y, rs_stream stream) {
+  if (!h || !y) return RS_ERR_NULL;
+  if (T < 1 || T > h->cfg.max_draft) return RS_ERR_RANGE;
+  const rs_status st = check_inputs(h, in);
+  if (st != RS_OK) return st;
+  if (!aligned16(y)) return RS_ERR_ALIGN;
+  if (h->pending) return RS_ERR_STATE;
+  const cudaError_t e = rs::launch_verify(h->dev, token_in(in), T, y, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return RS_ERR_CUDA;
+  h->pending = T;
+  return RS_OK;
+}
+
+rs_status rs_commit(rs_cache* h, const int32_t* accepted, rs_stream stream) {
+  if (!h || !accepted) return RS_ERR_NULL;
+  if (!aligned16(accepted)) return RS_ERR_ALIGN;
+  if (!h->pending) return RS_ERR_STATE;
+  const cudaError_t e = rs::launch_fold(h->dev, rs::FOLD_COMMIT, accepted, nullptr, h->pending,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return RS_ERR_CUDA;
+  h->pending = 0;
+  return RS_OK;
+}
+
+rs_status rs_flush(rs_cache* h, const uint8_t* seq_mask, rs_stream stream) {
+  if (!h) return RS_ERR_NULL;
+  if (seq_mask && !aligned16(seq_mask)) return RS_ERR_ALIGN;
+  if (h->pending) return RS_ERR_STATE;
+  return from_cuda(rs::launch_fold(h->dev, rs::FOLD_FLUSH, nullptr, seq_mask, 0,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+rs_status rs_get_device_error(rs_cache* h, rs_stream stream, int32_t* code) {
+  if (!h || !code) return RS_ERR_NULL;
+  int32_t word[2] = {0, 0};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(word, h->dev.err, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return RS_ERR_CUDA;
+  *code = word[0];
+  return word[0] == 0 ? RS_OK : RS_ERR_DEVICE;
+}
+
+const char* rs_status_string(rs_status s) {
+  switch (s) {
+    case RS_OK: return "ok";
+    case RS_ERR_NULL: return "a required pointer is NULL";
+    case RS_ERR_SHAPE: return "config dimensions inconsistent or out of range";
+    case RS_ERR_ALIGN: return "a device pointer is not 16-byte aligned";
+    case RS_ERR_RANGE: return "a scalar argument is out of range";
+    case RS_ERR_STATE: return "call order violated (verify must be followed by one commit)";
+    case RS_ERR_UNSUPPORTED: return "configuration outside the built kernels";
+    case RS_ERR_CUDA: return "a CUDA runtime call failed";
+    case RS_ERR_DEVICE: return "the device error word is set";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

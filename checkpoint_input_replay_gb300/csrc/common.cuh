@@ -1,0 +1,179 @@
+// Device helpers shared by the hot-path kernels: bf16 widening, segmented
+// warp reductions, mbarrier + bulk-copy staging with bounded waits, the
+// sticky error word, the per-sequence arrival counter, and the e4m3 / e2m1
+// conversions of the read copy.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace rs {
+
+__device__ __forceinline__ float bf(uint16_t v) { return __uint_as_float(static_cast<uint32_t>(v) << 16); }
+
+// 8 bf16 packed in a uint4 -> 8 floats
+__device__ __forceinline__ void bf8(const uint4 raw, float out[8]) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    out[2 * i] = __uint_as_float(w[i] << 16);
+    out[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// Sum over aligned groups of SEG lanes (SEG a power of two <= 32); every lane
+// of the group receives the total.
+template <int SEG>
+__device__ __forceinline__ float seg_sum(float v) {
+#pragma unroll
+  for (int o = SEG / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int SEG>
+__device__ __forceinline__ float seg_max(float v) {
+#pragma unroll
+  for (int o = SEG / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float dot4(const float4 a, const float4 b) {
+  return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, a.x * b.x)));
+}
+
+__device__ __forceinline__ float4 axpy4(float a, const float4 x, float4 y) {
+  y.x = fmaf(a, x.x, y.x);
+  y.y = fmaf(a, x.y, y.y);
+  y.z = fmaf(a, x.z, y.z);
+  y.w = fmaf(a, x.w, y.w);
+  return y;
+}
+
+__device__ __forceinline__ float4 scale4(float a, const float4 x) {
+  return make_float4(a * x.x, a * x.y, a * x.z, a * x.w);
+}
+
+// ---- error word and cursor bookkeeping -------------------------------------
+
+__device__ __forceinline__ void report_error(int* err, int code, int seq) {
+  if (atomicCAS(err, 0, code) == 0) atomicExch(err + 1, seq);
+}
+
+// Thread 0 of a CTA, after all of the CTA's global writes: counts this CTA in
+// and returns true for the last of the `nctas` CTAs of sequence b, after
+// resetting the counter for the next launch.
+__device__ __forceinline__ bool arrive_last(int* arrive, int b, int nctas) {
+  __threadfence();
+  const int prev = atomicAdd(arrive + b, 1);
+  if (prev == nctas - 1) {
+    atomicExch(arrive + b, 0);
+    return true;
+  }
+  return false;
+}
+
+// ---- mbarrier + bulk copy (cp.async.bulk, the untiled TMA path) -------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Global -> shared bulk copy; dst, src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of the barrier, giving up after about `limit_ns`
+// (and at most 2^22 polls).  Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = 1000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < (1u << 22); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31u) == 0 && global_ns() - t0 > limit_ns) break;
+  }
+  return mbar_try_wait(bar, parity);
+}
+
+// ---- e4m3 / e2m1 conversions (hardware cvt: round to nearest even, satfinite)
+
+// (lo, hi) -> two e4m3 codes, lo in bits 0..7
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
+  const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+  return __half22float2(hv);
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+  return e4m3x2_to_f32x2(static_cast<uint16_t>(code & 0xFFu)).x;
+}
+
+// four floats -> four e2m1 codes packed in 16 bits (element i in nibble i)
+__device__ __forceinline__ uint32_t f32x4_to_e2m1x4(float a0, float a1, float a2, float a3) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 q0, q1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+      "mov.b16 %0, {q0, q1};\n\t}"
+      : "=h"(r)
+      : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+  return r;
+}
+
+// two packed e2m1 codes (one byte, element 0 in the low nibble) -> two floats
+__device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
+  uint32_t h2;
+  const uint16_t in16 = static_cast<uint16_t>(byte & 0xFFu);
+  asm("{\n\t.reg .b8 q, qz;\n\t"
+      "mov.b16 {q, qz}, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, q;\n\t}"
+      : "=r"(h2)
+      : "h"(in16));
+  const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+  return __half22float2(hv);
+}
+
+}  // namespace rs

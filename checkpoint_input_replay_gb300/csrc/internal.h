@@ -1,0 +1,60 @@
+// Host/device shared descriptors of one cache, passed by value to every kernel.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace rs {
+
+constexpr int kThreads = 256;          // threads per CTA of every hot-path kernel
+constexpr int kMaxRec = 32;            // L + T_max limit (records per sequence)
+constexpr int kMaxTileBytes = 65536;   // P * N * 4 limit (one head's state, staged in smem)
+
+enum DevErr : int { DEVERR_NONE = 0, DEVERR_ACCEPTED = 1, DEVERR_CURSOR = 2, DEVERR_TIMEOUT = 3 };
+enum ReadMode : int { READ_NONE = 0, READ_FP8 = 1, READ_NVFP4 = 2 };
+enum FoldMode : int { FOLD_COMMIT = 0, FOLD_FLUSH = 1 };
+
+struct LayerDev {
+  int kind, B, H, G, P, N, L, C, T_max, read_mode;
+  float* ckpt;                 // [B][H][P][N]
+  // Mamba-2 ring
+  uint16_t* r_x;               // bf16 [B][H][C][P]
+  uint16_t* r_dt;              // bf16 [B][H][C]
+  float* r_la;                 // f32  [B][H][C]   log decay dt*A
+  uint16_t* r_B;               // bf16 [B][G][C][N]
+  // GDN ring
+  float* r_u;                  // f32  [B][H][C][P] delta u
+  float* r_g;                  // f32  [B][H][C]    log decay g
+  uint16_t* r_k;               // bf16 [B][G][C][N]
+  // cursor and bookkeeping
+  int* cursor;                 // [B][4] head, count, last_flush, 0
+  int* err;                    // [4] code, sequence
+  int* arrive;                 // [B]
+  // read copy
+  uint8_t* rc_codes;           // FP8: [B][H][P][N]; NVFP4: [B][H][P][N/2]
+  float* rc_rowscale;          // FP8: [B][H][P]
+  uint8_t* rc_blkscale;        // NVFP4: [B][H][P][N/16]
+  float* rc_matscale;          // NVFP4: [B][H]
+};
+
+struct TokenIn {
+  const uint16_t *x, *dt, *Bm, *Cm;   // Mamba-2
+  const float* A;
+  const uint16_t *q, *k, *v;          // GDN
+  const float *g, *beta;
+};
+
+// Launchers (one per kernel family); each returns the launch status.
+cudaError_t launch_decode(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s);
+cudaError_t launch_verify(const LayerDev& d, const TokenIn& in, int T, float* y, cudaStream_t s);
+cudaError_t launch_fold(const LayerDev& d, int mode, const int* accepted, const uint8_t* mask,
+                        int T_pending, cudaStream_t s);
+
+// Raise a kernel's dynamic shared-memory limit (once per kernel and size).
+cudaError_t set_smem_limit(const void* func, size_t bytes);
+
+// Dynamic shared memory the decode kernel needs for this layer.
+size_t decode_smem_bytes(const LayerDev& d);
+
+}  // namespace rs

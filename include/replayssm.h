@@ -1,0 +1,212 @@
+/*
+ * replayssm.h -- C ABI of the ReplaySSM decode hot path for one SSM layer on
+ * one GPU (sm_103a).
+ *
+ * The conventional SSM decoder reads the recurrent state, applies a rank-1
+ * update and writes the state back for every token.  ReplaySSM keeps instead a
+ * high-precision checkpoint plus a ring buffer of the last L input records;
+ * non-flush steps compute the output from checkpoint + buffer without storing
+ * any state, and the state is written once per window when the buffer fills
+ * ("ReplaySSM caches SSM inputs instead of state, cutting hybrid-model decode
+ * traffic in half" (richland.au), section "What shipped"; "NVIDIAとプリンストン
+ * 大Dao AI Lab、ハイブリッドモデルの推論を速める「ReplaySSM」を公開"
+ * (ai-jitan-hub.com), section "ReplaySSMは何をする手法か").
+ *
+ * Two recurrences, per head:
+ *   Mamba-2:         S_t = a_t S_{t-1} + v_t k_t^T,                     y_t = S_t q_t
+ *                    a_t = exp(dt_t A_h), v_t = dt_t x_t, k_t = B_t, q_t = C_t
+ *   Gated DeltaNet:  S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T, o_t = S_t q_t
+ *                    a_t = exp(g_t), b_t = beta_t
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every function returns rs_status.  Nothing throws across the ABI.
+ *   Argument errors are detected on the host before any launch; the cache is
+ *   then left unchanged.
+ * - Device memory is owned by the caller (rs_query_sizes gives the sizes);
+ *   the library owns only the opaque host handle rs_cache.
+ * - All device pointers must be 16-byte aligned.  Device pointers may be any
+ *   memory the GPU can load from with the same address (cudaMalloc, managed).
+ * - Calls are asynchronous and stream-ordered on the caller's stream.  Calls
+ *   on one cache must not overlap in time (use one stream, or order them).
+ * - bf16 = IEEE bfloat16 bit patterns (uint16); f32 = float.
+ * - Kernels never trap.  A problem found on the device (corrupt cursor,
+ *   accepted count out of range, a staged copy that did not arrive in time)
+ *   sets a sticky device error word and leaves that sequence untouched;
+ *   read it with rs_get_device_error.
+ *
+ * Notation: B batch, H heads (Mamba-2 nheads | GDN value heads), G groups
+ * (Mamba-2 ngroups | GDN key heads), P = d_head (Mamba-2 headdim | GDN d_v),
+ * N = d_state (Mamba-2 dstate | GDN d_k), L ring_len, T_max max_draft,
+ * C = L + T_max ring capacity.  Head h uses group h / (H / G).
+ */
+#ifndef REPLAYSSM_H
+#define REPLAYSSM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *rs_stream;
+
+typedef enum {
+  RS_OK = 0,
+  RS_ERR_NULL = 1,        /* a required pointer is NULL                         */
+  RS_ERR_SHAPE = 2,       /* config dimensions inconsistent or out of range     */
+  RS_ERR_ALIGN = 3,       /* a device pointer is not 16-byte aligned            */
+  RS_ERR_RANGE = 4,       /* a scalar argument (T, kind, mode) out of range     */
+  RS_ERR_STATE = 5,       /* call order violated (see rs_verify / rs_commit)    */
+  RS_ERR_UNSUPPORTED = 6, /* valid but not built (see rs_query_sizes)           */
+  RS_ERR_CUDA = 7,        /* a CUDA runtime call failed                         */
+  RS_ERR_DEVICE = 8       /* the device error word is set                       */
+} rs_status;
+
+typedef enum { RS_MAMBA2 = 0, RS_GDN = 1 } rs_kind;
+
+/* Low-precision read copy of the checkpoint, used only for the checkpoint
+ * read of non-flush decode steps and never fed back into the recurrence
+ * ("ReplaySSM caches SSM inputs..." (richland.au), "What shipped", the
+ * paragraph on quantization; ai-jitan-hub.com, "何がどれだけ速くなったのか",
+ * item 3).  Mamba-2 only. */
+typedef enum { RS_READ_NONE = 0, RS_READ_FP8_ROW = 1, RS_READ_NVFP4 = 2 } rs_read_mode;
+
+/* Device error codes (the sticky word read by rs_get_device_error). */
+enum {
+  RS_DEVERR_NONE = 0,
+  RS_DEVERR_ACCEPTED = 1, /* rs_commit: accepted[b] < 0 or > drafts pending   */
+  RS_DEVERR_CURSOR = 2,   /* a cursor (head, count) outside its valid range   */
+  RS_DEVERR_TIMEOUT = 3   /* a staged tile copy did not complete in time      */
+};
+
+typedef struct {
+  int32_t kind;      /* rs_kind                                            */
+  int32_t batch;     /* B >= 1                                             */
+  int32_t n_heads;   /* H, a multiple of n_groups                          */
+  int32_t n_groups;  /* G >= 1                                             */
+  int32_t d_head;    /* P in {16, 32, 64, 128}                             */
+  int32_t d_state;   /* N in {16, 32, 64, 128}; P * N * 4 <= 65536         */
+  int32_t ring_len;  /* L >= 1                                             */
+  int32_t max_draft; /* T_max >= 0 (0: standard decode only), L+T_max<=32  */
+  int32_t read_mode; /* rs_read_mode; NVFP4 needs N % 16 == 0, P*N <= 8192 */
+} rs_config;
+
+/*
+ * Caller-owned device buffers (sizes from rs_query_sizes, in this order).
+ *
+ * ckpt       f32 [B][H][P][N], N contiguous: the FP32 checkpoint S_ckpt.  The
+ *            caller writes the initial state here before the first call.
+ * ring       the input-record ring, C slots per sequence; record j since the
+ *            last flush lives in slot (head + j) mod C.  Sections, each
+ *            starting on a 256-byte boundary:
+ *              Mamba-2: x bf16 [B][H][C][P] | dt bf16 [B][H][C] |
+ *                       log a = dt*A f32 [B][H][C] | B bf16 [B][G][C][N]
+ *              GDN:     u f32 [B][H][C][P] (delta u = b (v - a S_{t-1} k)) |
+ *                       g f32 [B][H][C] | k bf16 [B][G][C][N]
+ * cursor     int32 [B][4] = {head, count, last_flush, 0} followed by the
+ *            device error word int32 [4] = {code, sequence, 0, 0}.
+ *            last_flush is 1 if the last call folded that sequence.
+ * read_copy  NULL when read_mode == RS_READ_NONE, else (256-byte sections)
+ *              FP8_ROW: e4m3 codes u8 [B][H][P][N] | row scale f32 [B][H][P]
+ *              NVFP4:   e2m1 codes u8 [B][H][P][N/2] (element 2i in the low
+ *                       nibble) | e4m3 block scales u8 [B][H][P][N/16] |
+ *                       matrix scale f32 [B][H]
+ * scratch    int32 [B] per-sequence arrival counters (the last CTA of a
+ *            sequence to finish a launch advances its cursor).  Zeroed by
+ *            rs_create_cache; every launch leaves it zero again.
+ */
+typedef struct {
+  void *ckpt, *ring, *cursor, *read_copy, *scratch;
+} rs_buffers;
+
+/*
+ * Per-call token inputs (device pointers).  Decode: one token per sequence,
+ * lead dims [B].  Verify: T draft tokens per sequence, lead dims [B][T].
+ *   Mamba-2: x bf16 [..][H][P], dt bf16 [..][H] (already softplus-ed),
+ *            A f32 [H], Bm bf16 [..][G][N], Cm bf16 [..][G][N]
+ *   GDN:     q bf16 [..][G][N], k bf16 [..][G][N], v bf16 [..][H][P],
+ *            g f32 [..][H] (log decay), beta f32 [..][H]
+ * Pointers of the other kind are ignored and may be NULL.
+ */
+typedef struct {
+  const void *x, *dt;
+  const float *A;
+  const void *Bm, *Cm;
+  const void *q, *k, *v;
+  const float *g, *beta;
+} rs_inputs;
+
+typedef struct rs_cache rs_cache;
+
+/* Byte sizes of ckpt, ring, cursor, read_copy, scratch for this config.
+ * Pure host call.  RS_ERR_SHAPE / RS_ERR_RANGE for invalid configs,
+ * RS_ERR_UNSUPPORTED for valid configs outside the built kernels. */
+rs_status rs_query_sizes(const rs_config *cfg, size_t bytes[5]);
+
+/* Bind a config to caller-owned buffers and zero the cursor, the error word
+ * and the arrival counters (synchronously, on the legacy default stream).
+ * The checkpoint is not touched.  With a read copy, call rs_flush once after
+ * the initial checkpoint is written so that the copy is quantised from it. */
+rs_status rs_create_cache(const rs_config *cfg, const rs_buffers *bufs, rs_cache **out);
+
+/* Free the handle (never the caller's buffers).  NULL is a no-op. */
+void rs_destroy_cache(rs_cache *cache);
+
+/* Standard decode step: one token per sequence, y f32 [B][H][P].
+ * Per sequence with count = c records buffered: if c + 1 < L the step is a
+ * non-flush step -- it reads the checkpoint (or its read copy) once, computes
+ * y_t = S_t q_t from checkpoint + buffer + this token, appends this token's
+ * record to slot (head + c) mod C, stores no state and sets count = c + 1.
+ * If c + 1 == L it is a flush step: it folds the L records (this token's
+ * included) into the checkpoint, writes it once (and refreshes the read
+ * copy), sets head = (head + L) mod C, count = 0, last_flush = 1
+ * ("ReplaySSM caches SSM inputs..." (richland.au), "What shipped", the
+ * paragraph on unrolling the recurrence).
+ * RS_ERR_STATE if drafts are pending (rs_verify without rs_commit). */
+rs_status rs_decode_step(rs_cache *cache, const rs_inputs *in, float *y, rs_stream stream);
+
+/* Speculative verification of T drafts per sequence (1 <= T <= max_draft):
+ * appends the T draft records after the committed ones (GDN: the draft deltas
+ * come from a unit-triangular T x T solve) and writes the outputs of all T
+ * draft positions, y f32 [B][T][H][P], in the chunkwise form
+ * O = S_ckpt Q D + V (W ⊙ (K^T Q)) with D the cumulative decay of each draft
+ * position and W the causally masked decay matrix; K^T Q is formed once per
+ * group.  The cursor does not move ("ReplaySSM caches SSM inputs..."
+ * (richland.au), "What shipped", the paragraphs on speculative decoding).
+ * Exactly one rs_commit must follow before the next decode, verify or flush
+ * (RS_ERR_STATE otherwise). */
+rs_status rs_verify(rs_cache *cache, int32_t T, const rs_inputs *in, float *y, rs_stream stream);
+
+/* Commit accepted[b] (device int32 [B], 0 <= accepted[b] <= T of the pending
+ * verify) drafts of each sequence by advancing its cursor: count += accepted.
+ * Rejected draft slots are left to be overwritten.  A sequence whose count
+ * reaches L or more is folded in the same launch (all its records), written
+ * once, and its cursor moves to head += count, count = 0.  An out-of-range
+ * accepted[b] sets RS_DEVERR_ACCEPTED and leaves that sequence unchanged.
+ * RS_ERR_STATE if no verify is pending. */
+rs_status rs_commit(rs_cache *cache, const int32_t *accepted, rs_stream stream);
+
+/* Fold all buffered records of the sequences with seq_mask[b] != 0 (device
+ * u8 [B]; NULL = all sequences) into the checkpoint and refresh their read
+ * copy; count = 0, last_flush = 1 for them, last_flush = 0 for the others.
+ * Use after writing an initial checkpoint (read-copy quantisation), to export
+ * the state (after rs_flush the checkpoint is the full state), or at the end
+ * of a sequence.  RS_ERR_STATE if drafts are pending. */
+rs_status rs_flush(rs_cache *cache, const uint8_t *seq_mask, rs_stream stream);
+
+/* Synchronise the stream and read the device error word (RS_DEVERR_*) into
+ * *code.  Returns RS_ERR_DEVICE if it is set, RS_OK otherwise.  The word is
+ * sticky; a cache with a device error should be re-created. */
+rs_status rs_get_device_error(rs_cache *cache, rs_stream stream, int32_t *code);
+
+/* Static description of a status code. */
+const char *rs_status_string(rs_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* REPLAYSSM_H */

@@ -1,0 +1,83 @@
+"""The C-ABI library without a GPU: it loads, exports every function the
+header declares, sizes buffers per the documented layout and rejects bad
+arguments on the host before touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import checkpoint_input_replay_gb300 as rs
+from checkpoint_input_replay_gb300 import _lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "replayssm.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rs_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported():
+    lib = _lib.load()
+    names = _declared()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(names) == sorted(_lib.EXPORTED)
+
+
+def test_query_sizes_config1_and_config2():
+    st, sz = rs.rs_query_sizes(rs.rs_config(0, 256, 128, 8, 64, 128, 16, 0, 0))
+    assert st == rs.RS_OK
+    assert sz[0] == 256 * 128 * 64 * 128 * 4                 # 1 GiB checkpoint
+    ring = (256 * 128 * 16 * 64 * 2) + (256 * 128 * 16 * 2) + (256 * 128 * 16 * 4) + (256 * 8 * 16 * 128 * 2)
+    assert sz[1] == ring                                      # sections already 256-aligned here
+    assert sz[2] == 256 * 16 + 16 and sz[3] == 0 and sz[4] == 256 * 4
+    st, sz = rs.rs_query_sizes(rs.rs_config(1, 256, 32, 16, 128, 128, 16, 0, 0))
+    assert st == rs.RS_OK and sz[0] == 512 * 1024 * 1024
+    st, sz = rs.rs_query_sizes(rs.rs_config(0, 256, 128, 8, 64, 128, 16, 0, 2))
+    assert st == rs.RS_OK and sz[3] == 256 * 128 * 64 * 64 + 256 * 128 * 64 * 8 + 256 * 128 * 4
+
+
+@pytest.mark.parametrize("fields,status", [
+    ((2, 1, 4, 1, 16, 16, 4, 0, 0), rs.RS_ERR_RANGE),        # kind
+    ((0, 1, 4, 1, 16, 16, 4, 0, 7), rs.RS_ERR_RANGE),        # read mode
+    ((0, 0, 4, 1, 16, 16, 4, 0, 0), rs.RS_ERR_SHAPE),        # batch
+    ((0, 1, 4, 3, 16, 16, 4, 0, 0), rs.RS_ERR_SHAPE),        # heads not a multiple of groups
+    ((0, 1, 4, 1, 16, 16, 0, 0, 0), rs.RS_ERR_SHAPE),        # ring_len
+    ((0, 1, 4, 1, 16, 24, 4, 0, 0), rs.RS_ERR_UNSUPPORTED),  # d_state not a power of two
+    ((0, 1, 4, 1, 256, 128, 4, 0, 0), rs.RS_ERR_UNSUPPORTED),  # tile above 64 KiB
+    ((0, 1, 4, 1, 16, 16, 30, 3, 0), rs.RS_ERR_UNSUPPORTED),   # L + T_max > 32
+    ((0, 1, 4, 1, 16, 16, 4, 5, 0), rs.RS_ERR_UNSUPPORTED),    # T_max > 4
+    ((1, 1, 4, 1, 16, 16, 4, 0, 1), rs.RS_ERR_UNSUPPORTED),    # read copy on GDN
+])
+def test_invalid_configs(fields, status):
+    st, _ = rs.rs_query_sizes(rs.rs_config(*fields))
+    assert st == status
+
+
+def test_null_and_alignment_errors_need_no_device():
+    cfg = rs.rs_config(0, 2, 4, 1, 16, 16, 4, 0, 0)
+    st, h = rs.rs_create_cache(cfg, rs.rs_buffers(None, None, None, None, None))
+    assert st == rs.RS_ERR_NULL
+    st, h = rs.rs_create_cache(cfg, rs.rs_buffers(4096, 4096 + 8, 8192, None, 12288))
+    assert st == rs.RS_ERR_ALIGN
+    st, h = rs.rs_create_cache(rs.rs_config(0, 2, 4, 1, 16, 16, 4, 0, 1),
+                               rs.rs_buffers(4096, 8192, 8192, None, 12288))
+    assert st == rs.RS_ERR_NULL                     # read copy buffer required
+    assert rs.rs_decode_step(None, rs.rs_inputs(), 0, 0) == rs.RS_ERR_NULL
+    assert rs.rs_verify(None, 1, rs.rs_inputs(), 0, 0) == rs.RS_ERR_NULL
+    assert rs.rs_commit(None, 0, 0) == rs.RS_ERR_NULL
+    assert rs.rs_flush(None, None, 0) == rs.RS_ERR_NULL
+    st, code = rs.rs_get_device_error(None, 0)
+    assert st == rs.RS_ERR_NULL
+    rs.rs_destroy_cache(None)
+
+
+def test_status_strings():
+    for s in range(9):
+        assert rs.rs_status_string(s) and rs.rs_status_string(s) != "unknown status"
+    assert rs.rs_status_string(42) == "unknown status"

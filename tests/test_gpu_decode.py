@@ -1,0 +1,143 @@
+"""GPU parity of the standard decode step (non-flush and flush bodies) against the oracle.
+
+Every case runs through the C ABI (ReplayCache -> libreplayssm.so).  Outputs
+and checkpoints are compared elementwise within 2e-4 * max(|ref|, 1e-3);
+cursors, flush flags and the Mamba-2 ring contents bit-exactly.
+"""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from tests.harness import Pair, assert_close
+from workloads import configs
+from workloads.configs import GDN, MAMBA2, LayerShape
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_decode(pair: Pair, steps: int, check_every_ckpt=True):
+    flushes = 0
+    for t in range(steps):
+        y, ref = pair.decode(t)
+        assert_close(y, ref, f"step {t} output")
+        pair.check_cursor(f"step {t} cursor")
+        if pair.cursor_gpu()[:, 2].any():
+            flushes += 1
+            if check_every_ckpt:
+                pair.check_ckpt(f"step {t} checkpoint")
+    assert pair.cache.device_error() == 0
+    return flushes
+
+
+def test_config0_tiny_mamba2_64_steps_16_flushes():
+    pair = Pair(configs.config0())
+    assert _run_decode(pair, 64) == 16
+
+
+def test_config0_ring_contents_bit_exact():
+    """Mamba-2 ring slots hold bf16 copies of the buffered inputs, at (head + j) mod C."""
+    wl = configs.config0()
+    pair = Pair(wl)
+    hist = []
+    for t in range(11):
+        pair.decode(t)
+        hist.append(wl.step(t))
+        ring = pair.cache.ring_views()
+        cur = pair.cache.cursor.cpu().numpy()
+        for b in range(wl.shape.batch):
+            head, count = cur[b, 0], cur[b, 1]
+            for j in range(count):
+                src = hist[len(hist) - count + j]
+                slot = (head + j) % pair.cache.C
+                got = ring["x"][b, :, slot].view(torch.int16).cpu().numpy().view(np.uint16)
+                np.testing.assert_array_equal(got, src["x"][b])
+                got_b = ring["B"][b, :, slot].view(torch.int16).cpu().numpy().view(np.uint16)
+                np.testing.assert_array_equal(got_b, src["B"][b])
+
+
+def test_mamba2_multi_tile_ragged():
+    """Several heads per group, odd window, steps not a multiple of L, larger tile."""
+    shape = LayerShape(MAMBA2, batch=3, n_heads=6, n_groups=3, d_head=32, d_state=64, ring_len=5)
+    wl = configs.Mamba2Workload(shape, seed=11, s0_std=0.1)
+    pair = Pair(wl)
+    assert _run_decode(pair, 23) == 4
+
+
+def test_mamba2_window_of_one_flushes_every_step():
+    shape = LayerShape(MAMBA2, batch=2, n_heads=2, n_groups=1, d_head=16, d_state=16, ring_len=1)
+    pair = Pair(configs.Mamba2Workload(shape, seed=12, s0_std=0.1))
+    assert _run_decode(pair, 5) == 5
+
+
+def test_gdn_small_64_steps():
+    shape = LayerShape(GDN, batch=2, n_heads=4, n_groups=2, d_head=16, d_state=16, ring_len=4)
+    pair = Pair(configs.GdnWorkload(shape, seed=13, s0_std=0.05))
+    assert _run_decode(pair, 64) == 16
+
+
+def test_gdn_multi_tile_ragged():
+    shape = LayerShape(GDN, batch=3, n_heads=4, n_groups=2, d_head=64, d_state=128, ring_len=6)
+    pair = Pair(configs.GdnWorkload(shape, seed=14, s0_std=0.05))
+    assert _run_decode(pair, 20) == 3
+
+
+@pytest.mark.parametrize("N,P", [(32, 32), (128, 128), (16, 128), (128, 16)])
+def test_shapes_sweep(N, P):
+    for kind in (MAMBA2, GDN):
+        shape = LayerShape(kind, batch=2, n_heads=4, n_groups=2, d_head=P, d_state=N, ring_len=3)
+        wl = configs.workload(shape, seed=15, s0_std=0.1)
+        assert _run_decode(Pair(wl), 7) == 2
+
+
+def test_config1_full_batch_sampled_sequences():
+    """Config 1 (B=256, H=128, P=64, N=128, G=8, L=16), 160 steps, the launch the bench
+    times; the oracle follows three sequences, cursors checked for all 256."""
+    wl = configs.config1()
+    pair = Pair(wl, seqs=[0, 137, 255])
+    for t in range(160):
+        y, ref = pair.decode(t)
+        assert_close(y, ref, f"step {t} output")
+        cur = pair.cache.cursor.cpu().numpy()
+        assert (cur[:, 1] == (t + 1) % 16).all() and (cur[:, 0] == ((t + 1) // 16 * 16) % 16).all()
+        if (t + 1) % 16 == 0:
+            assert cur[:, 2].all()
+            pair.check_ckpt(f"step {t} checkpoint")
+    assert pair.cache.device_error() == 0
+
+
+def test_config2_full_batch_sampled_sequences():
+    """Config 2 (GDN, B=256, Hv=32, Hk=16, d=128, L=16), 160 steps."""
+    wl = configs.config2()
+    pair = Pair(wl, seqs=[3, 200])
+    for t in range(160):
+        y, ref = pair.decode(t)
+        assert_close(y, ref, f"step {t} output")
+        pair.check_cursor(f"step {t}")
+        if (t + 1) % 16 == 0:
+            pair.check_ckpt(f"step {t} checkpoint")
+    assert pair.cache.device_error() == 0
+
+
+def test_flush_with_mask_and_export():
+    """rs_flush folds only the masked sequences; afterwards their checkpoint is the full state."""
+    shape = LayerShape(MAMBA2, batch=4, n_heads=4, n_groups=2, d_head=16, d_state=32, ring_len=8)
+    wl = configs.Mamba2Workload(shape, seed=16, s0_std=0.1)
+    pair = Pair(wl)
+    for t in range(5):
+        pair.decode(t)
+    mask = np.array([1, 0, 1, 0], dtype=np.uint8)
+    pair.cache.flush(torch.from_numpy(mask).cuda())
+    pair.oracle.flush(mask)
+    pair.check_cursor("after masked flush")
+    pair.check_ckpt("after masked flush")
+    for t in range(5, 12):
+        y, ref = pair.decode(t)
+        assert_close(y, ref, f"step {t}")
+        pair.check_cursor(f"step {t}")
+    pair.cache.flush()
+    pair.oracle.flush()
+    pair.check_ckpt("after full flush")
+    assert pair.cache.device_error() == 0

@@ -1,0 +1,94 @@
+"""GPU parity of speculative verification (chunkwise form) and pointer-advance commit.
+
+Drafts are appended after the committed records, outputs of every draft
+position are compared with the oracle's token-by-token drafts, and commit
+advances the cursor by the accepted prefix (folding when the ring fills).
+Cursors and flush flags are compared bit-exactly after every call.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from tests.harness import Pair, assert_close
+from workloads import configs
+from workloads.configs import GDN, MAMBA2, LayerShape
+
+pytestmark = pytest.mark.gpu
+
+
+def _spec_session(pair: Pair, rounds: int, T: int, decode_between=True, check_ckpt=True):
+    t = 0
+    for s in range(rounds):
+        y, ref = pair.verify(s, T)
+        assert_close(y, ref, f"verify {s}")
+        pair.check_cursor(f"after verify {s}")
+        pair.commit(s, T)
+        pair.check_cursor(f"after commit {s}")
+        if check_ckpt and pair.cursor_gpu()[:, 2].any():
+            pair.check_ckpt(f"after commit {s}")
+        if decode_between and s % 3 == 2:
+            y, ref = pair.decode(1000 + t)
+            t += 1
+            assert_close(y, ref, f"decode after round {s}")
+            pair.check_cursor(f"decode after round {s}")
+    assert pair.cache.device_error() == 0
+
+
+@pytest.mark.parametrize("T", [1, 2, 4])
+def test_mamba2_small_spec_session(T):
+    shape = LayerShape(MAMBA2, batch=3, n_heads=4, n_groups=2, d_head=16, d_state=32, ring_len=5, max_draft=4)
+    pair = Pair(configs.Mamba2Workload(shape, seed=21, s0_std=0.1))
+    _spec_session(pair, 12, T)
+
+
+@pytest.mark.parametrize("T", [1, 3, 4])
+def test_gdn_small_spec_session(T):
+    shape = LayerShape(GDN, batch=3, n_heads=4, n_groups=2, d_head=32, d_state=16, ring_len=5, max_draft=4)
+    pair = Pair(configs.GdnWorkload(shape, seed=22, s0_std=0.05))
+    _spec_session(pair, 12, T)
+
+
+def test_all_accepted_and_none_accepted():
+    shape = LayerShape(MAMBA2, batch=2, n_heads=2, n_groups=1, d_head=16, d_state=16, ring_len=4, max_draft=3)
+    pair = Pair(configs.Mamba2Workload(shape, seed=23, s0_std=0.1))
+    for s, acc in enumerate([[3, 0], [3, 0], [0, 0], [1, 3], [3, 3]]):
+        y, ref = pair.verify(s, 3)
+        assert_close(y, ref, f"verify {s}")
+        pair.commit(s, 3, accepted=acc)
+        pair.check_cursor(f"commit {s}")
+        pair.check_ckpt(f"commit {s}")
+
+
+def test_drafts_land_after_committed_records():
+    """Draft records occupy slots (head + count + tau) mod C; the cursor does not move at verify."""
+    shape = LayerShape(MAMBA2, batch=2, n_heads=2, n_groups=1, d_head=16, d_state=16, ring_len=4, max_draft=2)
+    wl = configs.Mamba2Workload(shape, seed=24, s0_std=0.1)
+    pair = Pair(wl)
+    pair.decode(0)
+    before = pair.cache.cursor.cpu().numpy().copy()
+    pair.verify(0, 2)
+    after = pair.cache.cursor.cpu().numpy()
+    np.testing.assert_array_equal(before[:, :2], after[:, :2])
+    ring = pair.cache.ring_views()
+    drafts = wl.draft(0, 2)
+    for b in range(2):
+        for tau in range(2):
+            slot = (after[b, 0] + after[b, 1] + tau) % pair.cache.C
+            got = ring["x"][b, :, slot].view(torch.int16).cpu().numpy().view(np.uint16)
+            np.testing.assert_array_equal(got, drafts["x"][b, tau])
+
+
+@pytest.mark.parametrize("kind", ["mamba2", "gdn"])
+def test_config3_full_batch_sampled(kind):
+    """Config 3: B=512, T=4, L=16, 64 verify steps with accepted counts U{0..4}."""
+    wl = configs.config3_mamba2() if kind == "mamba2" else configs.config3_gdn()
+    pair = Pair(wl, seqs=[1, 511])
+    for s in range(64):
+        y, ref = pair.verify(s, 4)
+        assert_close(y, ref, f"verify {s}")
+        acc = pair.commit(s, 4)
+        pair.check_cursor(f"commit {s}")
+        if pair.cursor_gpu()[:, 2].any():
+            pair.check_ckpt(f"commit {s}")
+    assert pair.cache.device_error() == 0
