@@ -83,23 +83,25 @@ class ReplayCache:
         return self._mem[2][: 16 * self.B].view(torch.int32).view(self.B, 4)
 
     def ring_views(self) -> dict:
+        """Views of the ring sections; per-head scalar rows have Cp = C rounded up to 8 slots."""
         B, H, G, P, N, C = self.B, self.H, self.G, self.P, self.N, self.C
+        Cp = (C + 7) // 8 * 8
         m = self._mem[1]
         if self.kind == _lib.RS_MAMBA2:
             o1 = _a256(B * H * C * P * 2)
-            o2 = o1 + _a256(B * H * C * 2)
-            o3 = o2 + _a256(B * H * C * 4)
+            o2 = o1 + _a256(B * H * Cp * 2)
+            o3 = o2 + _a256(B * H * Cp * 4)
             return {
                 "x": m[0:B * H * C * P * 2].view(torch.bfloat16).view(B, H, C, P),
-                "dt": m[o1:o1 + B * H * C * 2].view(torch.bfloat16).view(B, H, C),
-                "la": m[o2:o2 + B * H * C * 4].view(torch.float32).view(B, H, C),
+                "dt": m[o1:o1 + B * H * Cp * 2].view(torch.bfloat16).view(B, H, Cp),
+                "la": m[o2:o2 + B * H * Cp * 4].view(torch.float32).view(B, H, Cp),
                 "B": m[o3:o3 + B * G * C * N * 2].view(torch.bfloat16).view(B, G, C, N),
             }
         o1 = _a256(B * H * C * P * 4)
-        o2 = o1 + _a256(B * H * C * 4)
+        o2 = o1 + _a256(B * H * Cp * 4)
         return {
             "u": m[0:B * H * C * P * 4].view(torch.float32).view(B, H, C, P),
-            "g": m[o1:o1 + B * H * C * 4].view(torch.float32).view(B, H, C),
+            "g": m[o1:o1 + B * H * Cp * 4].view(torch.float32).view(B, H, Cp),
             "k": m[o2:o2 + B * G * C * N * 2].view(torch.bfloat16).view(B, G, C, N),
         }
 

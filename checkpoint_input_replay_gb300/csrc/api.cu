@@ -61,17 +61,18 @@ Layout layout_of(const rs_config& c) {
   Layout L{};
   const size_t B = c.batch, H = c.n_heads, G = c.n_groups, P = c.d_head, N = c.d_state;
   const size_t C = static_cast<size_t>(c.ring_len) + c.max_draft;
+  const size_t Cp = (C + 7) & ~static_cast<size_t>(7);
   L.ckpt = B * H * P * N * 4;
   if (c.kind == RS_MAMBA2) {
     L.r0 = 0;                                   // x  bf16 [B][H][C][P]
-    L.r1 = L.r0 + align256(B * H * C * P * 2);  // dt bf16 [B][H][C]
-    L.r2 = L.r1 + align256(B * H * C * 2);      // la f32  [B][H][C]
-    L.r3 = L.r2 + align256(B * H * C * 4);      // B  bf16 [B][G][C][N]
+    L.r1 = L.r0 + align256(B * H * C * P * 2);  // dt bf16 [B][H][Cp]
+    L.r2 = L.r1 + align256(B * H * Cp * 2);     // la f32  [B][H][Cp]
+    L.r3 = L.r2 + align256(B * H * Cp * 4);     // B  bf16 [B][G][C][N]
     L.ring = L.r3 + align256(B * G * C * N * 2);
   } else {
     L.r0 = 0;                                   // u f32  [B][H][C][P]
-    L.r1 = L.r0 + align256(B * H * C * P * 4);  // g f32  [B][H][C]
-    L.r2 = L.r1 + align256(B * H * C * 4);      // k bf16 [B][G][C][N]
+    L.r1 = L.r0 + align256(B * H * C * P * 4);  // g f32  [B][H][Cp]
+    L.r2 = L.r1 + align256(B * H * Cp * 4);     // k bf16 [B][G][C][N]
     L.r3 = L.r2;
     L.ring = L.r2 + align256(B * G * C * N * 2);
   }
@@ -189,7 +190,15 @@ rs_status rs_create_cache(const rs_config* cfg, const rs_buffers* bufs, rs_cache
   d.L = cfg->ring_len;
   d.T_max = cfg->max_draft;
   d.C = cfg->ring_len + cfg->max_draft;
+  d.Cp = (d.C + 7) & ~7;
   d.read_mode = cfg->read_mode;
+  {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return RS_ERR_CUDA;
+    d.num_sms = sms;
+  }
   d.ckpt = static_cast<float*>(bufs->ckpt);
   char* ring = static_cast<char*>(bufs->ring);
   if (cfg->kind == RS_MAMBA2) {
@@ -238,7 +247,6 @@ rs_status rs_decode_step(rs_cache* h, const rs_inputs* in, float* y, rs_stream s
   if (st != RS_OK) return st;
   if (!aligned16(y)) return RS_ERR_ALIGN;
   if (h->pending) return RS_ERR_STATE;
-  if (h->cfg.read_mode != RS_READ_NONE) return RS_ERR_UNSUPPORTED;
   return from_cuda(rs::launch_decode(h->dev, token_in(in), y, reinterpret_cast<cudaStream_t>(stream)));
 }
 

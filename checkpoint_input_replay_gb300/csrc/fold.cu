@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const LayerDev d, const 
       sK[i] = bf(rk[static_cast<size_t>(ring_slot(head, j, C)) * N + e]);
     }
     if (t < n) {
-      const size_t s = static_cast<size_t>(bh) * C + ring_slot(head, t, C);
+      const size_t s = static_cast<size_t>(bh) * d.Cp + ring_slot(head, t, C);
       if (KIND == 0) {
         sla[t] = d.r_la[s];
         sdt[t] = bf(d.r_dt[s]);

@@ -17,15 +17,17 @@ enum FoldMode : int { FOLD_COMMIT = 0, FOLD_FLUSH = 1 };
 
 struct LayerDev {
   int kind, B, H, G, P, N, L, C, T_max, read_mode;
+  int Cp;                      // ring row stride of the per-head scalars: C rounded up to 8
+  int num_sms;                 // SMs of the device (persistent grid size)
   float* ckpt;                 // [B][H][P][N]
   // Mamba-2 ring
   uint16_t* r_x;               // bf16 [B][H][C][P]
-  uint16_t* r_dt;              // bf16 [B][H][C]
-  float* r_la;                 // f32  [B][H][C]   log decay dt*A
+  uint16_t* r_dt;              // bf16 [B][H][Cp]
+  float* r_la;                 // f32  [B][H][Cp]  log decay dt*A
   uint16_t* r_B;               // bf16 [B][G][C][N]
   // GDN ring
   float* r_u;                  // f32  [B][H][C][P] delta u
-  float* r_g;                  // f32  [B][H][C]    log decay g
+  float* r_g;                  // f32  [B][H][Cp]   log decay g
   uint16_t* r_k;               // bf16 [B][G][C][N]
   // cursor and bookkeeping
   int* cursor;                 // [B][4] head, count, last_flush, 0

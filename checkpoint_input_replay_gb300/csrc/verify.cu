@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kThreads) m2_verify_kernel(const LayerDev d, c
   }
   if (t < nr) {
     if (t < n) {
-      const size_t s = static_cast<size_t>(bh) * C + ring_slot(head, t, C);
+      const size_t s = static_cast<size_t>(bh) * d.Cp + ring_slot(head, t, C);
       sla[t] = d.r_la[s];
       sdt[t] = bf(d.r_dt[s]);
     } else {
@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kThreads) m2_verify_kernel(const LayerDev d, c
     return;
   }
   if (!tile_ok) return;
+  if (h == 0 && t == 0) d.cursor[4 * b + 2] = 0;  // verify folds nothing
 
   // O[tau][r] = D[tau] (S_ckpt q_tau)[r] + sum_j W[j][tau] (k_j . q_tau) v_j[r]
   const int c4 = t % SEG;
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(kThreads) m2_verify_kernel(const LayerDev d, c
         in.x[((static_cast<size_t>(b) * T + tau) * H + h) * P + r];
   }
   if (t < T) {
-    const size_t s = static_cast<size_t>(bh) * C + ring_slot(head, n + t, C);
+    const size_t s = static_cast<size_t>(bh) * d.Cp + ring_slot(head, n + t, C);
     d.r_dt[s] = in.dt[(static_cast<size_t>(b) * T + t) * H + h];
     d.r_la[s] = sla[n + t];
   }
@@ -250,7 +251,7 @@ __global__ void __launch_bounds__(kThreads) gdn_verify_kernel(const LayerDev d, 
   }
   if (t < nr) {
     if (t < n) {
-      sla[t] = d.r_g[static_cast<size_t>(bh) * C + ring_slot(head, t, C)];
+      sla[t] = d.r_g[static_cast<size_t>(bh) * d.Cp + ring_slot(head, t, C)];
     } else {
       const size_t s = (static_cast<size_t>(b) * T + (t - n)) * H + h;
       sla[t] = in.g[s];
@@ -308,6 +309,7 @@ __global__ void __launch_bounds__(kThreads) gdn_verify_kernel(const LayerDev d, 
     return;
   }
   if (!tile_ok) return;
+  if (h == 0 && t == 0) d.cursor[4 * b + 2] = 0;  // verify folds nothing
 
   const int c4 = t % SEG;
   float4 k4[kTMax], q4[kTMax];
@@ -358,7 +360,7 @@ __global__ void __launch_bounds__(kThreads) gdn_verify_kernel(const LayerDev d, 
     }
   }
   if (t < T) {
-    d.r_g[static_cast<size_t>(bh) * C + ring_slot(head, n + t, C)] = sla[n + t];
+    d.r_g[static_cast<size_t>(bh) * d.Cp + ring_slot(head, n + t, C)] = sla[n + t];
   }
   if (h % hpg == 0) {
     for (int i = t; i < T * N; i += kThreads) {

@@ -38,7 +38,8 @@
  * Notation: B batch, H heads (Mamba-2 nheads | GDN value heads), G groups
  * (Mamba-2 ngroups | GDN key heads), P = d_head (Mamba-2 headdim | GDN d_v),
  * N = d_state (Mamba-2 dstate | GDN d_k), L ring_len, T_max max_draft,
- * C = L + T_max ring capacity.  Head h uses group h / (H / G).
+ * C = L + T_max ring capacity, Cp = C rounded up to a multiple of 8.
+ * Head h uses group h / (H / G).
  */
 #ifndef REPLAYSSM_H
 #define REPLAYSSM_H
@@ -91,7 +92,7 @@ typedef struct {
   int32_t d_state;   /* N in {16, 32, 64, 128}; P * N * 4 <= 65536         */
   int32_t ring_len;  /* L >= 1                                             */
   int32_t max_draft; /* T_max >= 0 (0: standard decode only), L+T_max<=32  */
-  int32_t read_mode; /* rs_read_mode; NVFP4 needs N % 16 == 0, P*N <= 8192 */
+  int32_t read_mode; /* rs_read_mode (Mamba-2 only)                      */
 } rs_config;
 
 /*
@@ -102,10 +103,10 @@ typedef struct {
  * ring       the input-record ring, C slots per sequence; record j since the
  *            last flush lives in slot (head + j) mod C.  Sections, each
  *            starting on a 256-byte boundary:
- *              Mamba-2: x bf16 [B][H][C][P] | dt bf16 [B][H][C] |
- *                       log a = dt*A f32 [B][H][C] | B bf16 [B][G][C][N]
+ *              Mamba-2: x bf16 [B][H][C][P] | dt bf16 [B][H][Cp] |
+ *                       log a = dt*A f32 [B][H][Cp] | B bf16 [B][G][C][N]
  *              GDN:     u f32 [B][H][C][P] (delta u = b (v - a S_{t-1} k)) |
- *                       g f32 [B][H][C] | k bf16 [B][G][C][N]
+ *                       g f32 [B][H][Cp] | k bf16 [B][G][C][N]
  * cursor     int32 [B][4] = {head, count, last_flush, 0} followed by the
  *            device error word int32 [4] = {code, sequence, 0, 0}.
  *            last_flush is 1 if the last call folded that sequence.
@@ -129,7 +130,10 @@ typedef struct {
  *            A f32 [H], Bm bf16 [..][G][N], Cm bf16 [..][G][N]
  *   GDN:     q bf16 [..][G][N], k bf16 [..][G][N], v bf16 [..][H][P],
  *            g f32 [..][H] (log decay), beta f32 [..][H]
- * Pointers of the other kind are ignored and may be NULL.
+ * Pointers of the other kind are ignored and may be NULL.  The decode kernel
+ * stages the per-head scalars (dt, A, g, beta) in 16-byte blocks, so each of
+ * those arrays must stay readable up to the next 16-byte boundary after its
+ * last element (every cudaMalloc or PyTorch allocation is).
  */
 typedef struct {
   const void *x, *dt;

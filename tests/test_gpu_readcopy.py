@@ -1,0 +1,106 @@
+"""GPU parity of the low-precision read copy (FP8 per-row, NVFP4).
+
+* The copy quantised from an initial checkpoint is compared code by code with
+  the oracle's codecs (both sides take the rounding decisions in float32).
+* Decode outputs with the copy are compared with the oracle's quantised-read
+  output (the copy replaces S_ckpt only in the decayed S_ckpt q term) and,
+  per window, with the exact FP32-recurrence output: rel-L2 must stay below
+  1% (FP8) / 6% (NVFP4) from the second window on and must not grow with the
+  window index, because the copy never feeds the recurrence.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import codecs
+from tests.harness import Pair, assert_close
+from workloads import configs
+from workloads.configs import MAMBA2, LayerShape
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_initial_copy(pair, mode, seqs):
+    S0 = pair.wl.S0()[seqs]
+    v = pair.cache.read_copy_views()
+    if mode == "fp8":
+        codes, sc = codecs.fp8_rows_quantize(S0)
+        np.testing.assert_array_equal(v["codes"][seqs].cpu().numpy(), codes)
+        np.testing.assert_array_equal(v["row_scale"][seqs].cpu().numpy(), sc)
+    else:
+        packed, bs, s = codecs.nvfp4_quantize(S0)
+        np.testing.assert_array_equal(v["matrix_scale"][seqs].cpu().numpy(), s)
+        np.testing.assert_array_equal(v["block_scale"][seqs].cpu().numpy(), bs)
+        np.testing.assert_array_equal(v["codes"][seqs].cpu().numpy(), packed)
+
+
+@pytest.mark.parametrize("mode", ["fp8", "nvfp4"])
+@pytest.mark.parametrize("P,N", [(16, 16), (32, 64), (64, 128)])
+def test_initial_quantisation_bit_exact(mode, P, N):
+    shape = LayerShape(MAMBA2, batch=3, n_heads=4, n_groups=2, d_head=P, d_state=N, ring_len=4)
+    pair = Pair(configs.Mamba2Workload(shape, seed=41, s0_std=0.1), read_mode=mode)
+    _check_initial_copy(pair, mode, [0, 1, 2])
+    assert pair.cache.device_error() == 0
+
+
+def _rel_l2(a, b):
+    return float(np.sqrt(np.sum((a - b) ** 2) / np.sum(b ** 2)))
+
+
+@pytest.mark.parametrize("mode", ["fp8", "nvfp4"])
+def test_small_read_copy_decode_matches_oracle(mode):
+    shape = LayerShape(MAMBA2, batch=2, n_heads=4, n_groups=2, d_head=16, d_state=32, ring_len=4)
+    pair = Pair(configs.Mamba2Workload(shape, seed=42, s0_std=0.1), read_mode=mode)
+    for t in range(20):
+        y, ref = pair.decode(t)
+        yq = pair.oracle.last_read_out
+        if t < 3:
+            # first window: the copy was quantised from the exact initial state on both sides
+            assert_close(y, yq, f"{mode} step {t}")
+        else:
+            assert _rel_l2(y, yq) < 2e-3, (t, _rel_l2(y, yq))
+        pair.check_cursor(f"step {t}")
+        if pair.cursor_gpu()[:, 2].any():
+            assert_close(y, ref, f"{mode} flush step {t} reads the FP32 checkpoint")
+            pair.check_ckpt(f"step {t}")
+    assert pair.cache.device_error() == 0
+
+
+def _config4_windows(mode, steps, seqs):
+    wl = configs.config4()
+    pair = Pair(wl, seqs=seqs, read_mode=mode)
+    _check_initial_copy(pair, mode, seqs)
+    L = wl.shape.ring_len
+    num = np.zeros(steps // L)
+    den = np.zeros(steps // L)
+    num_q = np.zeros(steps // L)
+    for t in range(steps):
+        y, ref = pair.decode(t)
+        w = t // L
+        num[w] += np.sum((y - ref) ** 2)
+        den[w] += np.sum(ref ** 2)
+        num_q[w] += np.sum((y - pair.oracle.last_read_out) ** 2)
+    assert pair.cache.device_error() == 0
+    return np.sqrt(num / den), np.sqrt(num_q / den), float(np.sqrt(num.sum() / den.sum()))
+
+
+@pytest.mark.parametrize("mode,bound", [("fp8", 0.01), ("nvfp4", 0.06)])
+def test_config4_error_per_window(mode, bound):
+    """Config-4 shape (B=256, H=128, P=64, N=128, G=8, L=16), 512 steps = 32 windows,
+    oracle on two sampled sequences."""
+    per_window, vs_quantised_oracle, aggregate = _config4_windows(mode, 512, [0, 255])
+    assert np.all(per_window[1:] <= bound), per_window
+    assert aggregate <= bound
+    # the copy never feeds the recurrence: no growth with the window index
+    assert per_window[-8:].mean() <= 1.1 * per_window[1:9].mean(), per_window
+    assert np.all(vs_quantised_oracle <= 2e-3), vs_quantised_oracle
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("mode,bound", [("fp8", 0.01), ("nvfp4", 0.06)])
+def test_config4_full_4096_steps(mode, bound):
+    per_window, _, aggregate = _config4_windows(mode, 4096, [0])
+    assert np.all(per_window[1:] <= bound)
+    assert aggregate <= bound
+    assert per_window[-32:].mean() <= 1.1 * per_window[1:33].mean()
