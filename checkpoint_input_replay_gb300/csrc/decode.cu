@@ -25,8 +25,13 @@
 //  * all warps compute unit i from shared memory while units i+1.. load: the
 //    per-group key dot products once per group, the decay weights with a warp
 //    scan, the buffered term per row, then one pass over the matrix;
-//  * a flush unit folds the records into the matrix in shared memory and a bulk
-//    store writes the checkpoint back once; a non-flush unit stores no state.
+//  * a dedicated producer warp issues the copies; the eight computing warps
+//    release a stage through an mbarrier when they are done with it;
+//  * for d_state = 128 a unit is computed warp-locally: warp w owns rows
+//    w, w+8, ..; lanes split the buffered records four per row and the row
+//    sums use a transpose-reduce over 8 rows (9 shuffles);
+//  * a flush unit folds the records in registers and writes the checkpoint
+//    back once; a non-flush unit stores no state.
 #include "common.cuh"
 #include "readcopy.cuh"
 
@@ -92,8 +97,8 @@ __host__ __device__ __forceinline__ Persist persist_layout(int P, int N, int C) 
   p.coef = o;   o += C * P;      // flush coefficients [C][P]
   p.red = o;    o += kThreads / 32;
   p.misc = o;   o += 4;
-  p.bars = (o + 3) & ~3;         // 16-byte aligned, up to 8 mbarriers (u64)
-  o = p.bars + 2 * 8;
+  p.bars = (o + 3) & ~3;         // 16-byte aligned: 8 full + 8 empty mbarriers (u64)
+  o = p.bars + 2 * 16;
   p.seq = o;    o += 3 * kMaxSeq;  // cached cursors: head, count, ok
   p.size_floats = o;
   return p;
@@ -108,21 +113,6 @@ __device__ __forceinline__ int ring_slot(int head, int j, int C) {
 __device__ __forceinline__ void copy_in(unsigned char* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   if (bytes) bulk_g2s(dst, src, bytes, bar);
 }
-
-__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
-               "r"(bytes)
-               : "memory");
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 struct UnitInfo {
   int u, b, h, g, k;  // unit, sequence, head, group, cached-sequence index
@@ -224,10 +214,64 @@ __device__ __forceinline__ void rc_rows_nvfp4(const unsigned char* sC, const uns
 // ---------------------------------------------------------------------------
 // The kernel (KIND 0: Mamba-2, 1: Gated DeltaNet)
 // ---------------------------------------------------------------------------
+constexpr int kDecodeThreads = kThreads + 32;  // 8 computing warps + 1 producer warp
+
+__device__ __forceinline__ bool compute_sync_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "n"(kThreads)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Sum each of v[0..7] over the 32 lanes of the warp (transpose-reduce: 9
+// shuffles).  Lane L returns the total of v[(L >> 2) & 7].
+__device__ __forceinline__ float reduce8(const float v[8], int lane) {
+  const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
+  float w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = b4 ? v[i] : v[i + 4];
+    const float keep = b4 ? v[i + 4] : v[i];
+    w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+  float x[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = b3 ? w[i] : w[i + 2];
+    const float keep = b3 ? w[i + 2] : w[i];
+    x[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  float z = (b2 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, b2 ? x[0] : x[1], 4);
+  z += __shfl_xor_sync(0xffffffffu, z, 2);
+  z += __shfl_xor_sync(0xffffffffu, z, 1);
+  return z;
+}
+
+// Inclusive suffix sum over lanes 0..last of one value per lane (lanes past
+// `last` contribute nothing).
+__device__ __forceinline__ float suffix_sum(float v, int lane, int last) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float w = __shfl_down_sync(0xffffffffu, v, o);
+    if (lane + o <= last) v += w;
+  }
+  return v;
+}
+
 template <int KIND, int N, int READ>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const LayerDev d, const TokenIn in,
-                                                             float* __restrict__ y, const int units_per_cta,
-                                                             const int stages) {
+__global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const LayerDev d, const TokenIn in,
+                                                                   float* __restrict__ y, const int units_per_cta,
+                                                                   const int stages) {
   constexpr int SEG = N / 4;  // lanes per state row, one float4 each
   extern __shared__ __align__(1024) unsigned char smem[];
 
@@ -247,7 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const LayerDev d, c
   float* srow2 = pf + PL.row2;
   float* scoef = pf + PL.coef;
   float* sred = pf + PL.red;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(pf + PL.bars);
+  volatile int* smisc = reinterpret_cast<volatile int*>(pf + PL.misc);  // [0] abort, [1] issued
+  uint64_t* full = reinterpret_cast<uint64_t*>(pf + PL.bars);
+  uint64_t* empty = full + 8;
   int* sseq = reinterpret_cast<int*>(pf + PL.seq);
 
   const int total_units = d.B * H;
@@ -284,8 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const LayerDev d, c
       }
     }
   }
-  if (t == 0) {
-    for (int s = 0; s < stages; ++s) mbar_init(bars + s, 1);
+  if (t == kThreads) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    smisc[0] = 0;
+    smisc[1] = 0;
   }
   __syncthreads();
 
@@ -305,100 +356,111 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const LayerDev d, c
     return ui;
   };
 
-  // --- producer: stage the inputs of unit i (thread 0 only) ---
-  auto issue = [&](int i) {
-    const UnitInfo ui = unit_info(i);
-    unsigned char* st = smem + static_cast<size_t>(SL.size) * (i % stages);
-    uint64_t* bar = bars + (i % stages);
-    const size_t u = static_cast<size_t>(ui.u);
-    const size_t bg = static_cast<size_t>(ui.b) * G + ui.g;
-    const int n = ui.n;
-    const int seg1 = min(n, C - ui.head), seg2 = n - seg1;
-    const int resz = KIND == 0 ? 2 : 4;  // record element size
-    uint32_t tb0 = 0, tb1 = 0;
-    if (READ == READ_NONE || ui.flush) {
-      tb0 = tile * 4;
-    } else if (READ == READ_FP8) {
-      tb0 = tile;
-      tb1 = P * 4;
-    } else {
-      tb0 = tile / 2;
-      tb1 = tile / 16;
+  // =========================== producer warp ===============================
+  if (warp == kThreads / 32) {
+    if (lane != 0) return;
+    for (int i = 0; i < nunits; ++i) {
+      const int s = i % stages;
+      if (i >= stages && !mbar_wait_bounded(empty + s, static_cast<uint32_t>(((i / stages) - 1) & 1))) break;
+      if (smisc[0]) break;
+      const UnitInfo ui = unit_info(i);
+      unsigned char* st = smem + static_cast<size_t>(SL.size) * s;
+      uint64_t* bar = full + s;
+      const size_t u = static_cast<size_t>(ui.u);
+      const size_t bg = static_cast<size_t>(ui.b) * G + ui.g;
+      const int n = ui.n;
+      const int seg1 = min(n, C - ui.head), seg2 = n - seg1;
+      const int resz = KIND == 0 ? 2 : 4;  // record element size
+      uint32_t tb0 = 0, tb1 = 0;
+      if (READ == READ_NONE || ui.flush) {
+        tb0 = tile * 4;
+      } else if (READ == READ_FP8) {
+        tb0 = tile;
+        tb1 = P * 4;
+      } else {
+        tb0 = tile / 2;
+        tb1 = tile / 16;
+      }
+      uint32_t bytes = tb0 + tb1;
+      bytes += static_cast<uint32_t>(n) * P * resz;                        // buffered records
+      bytes += KIND == 0 ? P * 2 : a16(P * 2);                              // current x / v
+      if (ui.first_of_group) bytes += static_cast<uint32_t>(n + 1) * N * 2 + N * 2;  // keys + q
+      bytes += Cp * 4 + (KIND == 0 ? a16(Cp * 2) : 0) + 48;               // log decays, dt, chunks
+      mbar_expect_tx(bar, bytes);
+      if (READ == READ_NONE || ui.flush) {
+        copy_in(st + SL.tile, d.ckpt + u * tile, tb0, bar);
+      } else if (READ == READ_FP8) {
+        copy_in(st + SL.tile, d.rc_codes + u * tile, tb0, bar);
+        copy_in(st + SL.tile + tile, d.rc_rowscale + u * P, tb1, bar);
+      } else {
+        copy_in(st + SL.tile, d.rc_codes + u * (tile / 2), tb0, bar);
+        copy_in(st + SL.tile + tile / 2, d.rc_blkscale + u * (tile / 16), tb1, bar);
+      }
+      if (KIND == 0) {
+        const uint16_t* rx = d.r_x + u * C * P;
+        copy_in(st + SL.rec, rx + static_cast<size_t>(ui.head) * P, seg1 * P * 2, bar);
+        copy_in(st + SL.rec + seg1 * P * 2, rx, seg2 * P * 2, bar);
+        copy_in(st + SL.rec + n * P * 2, in.x + u * P, P * 2, bar);
+      } else {
+        const float* ru = d.r_u + u * C * P;
+        copy_in(st + SL.rec, ru + static_cast<size_t>(ui.head) * P, seg1 * P * 4, bar);
+        copy_in(st + SL.rec + seg1 * P * 4, ru, seg2 * P * 4, bar);
+        copy_in(st + SL.v, in.v + u * P, a16(P * 2), bar);
+      }
+      if (ui.first_of_group) {
+        const uint16_t* rk = (KIND == 0 ? d.r_B : d.r_k) + bg * C * N;
+        copy_in(st + SL.key, rk + static_cast<size_t>(ui.head) * N, seg1 * N * 2, bar);
+        copy_in(st + SL.key + seg1 * N * 2, rk, seg2 * N * 2, bar);
+        copy_in(st + SL.key + n * N * 2, (KIND == 0 ? in.Bm : in.k) + bg * N, N * 2, bar);
+        copy_in(st + SL.q, (KIND == 0 ? in.Cm : in.q) + bg * N, N * 2, bar);
+      }
+      if (KIND == 0) {
+        copy_in(st + SL.la, d.r_la + u * Cp, Cp * 4, bar);
+        copy_in(st + SL.dt, d.r_dt + u * Cp, a16(Cp * 2), bar);
+        copy_in(st + SL.chunk, in.dt + (u & ~static_cast<size_t>(7)), 16, bar);
+        copy_in(st + SL.chunk + 16, in.A + (ui.h & ~3), 16, bar);
+        if (READ == READ_NVFP4)
+          copy_in(st + SL.chunk + 32, d.rc_matscale + (u & ~static_cast<size_t>(3)), 16, bar);
+        else
+          copy_in(st + SL.chunk + 32, in.A + (ui.h & ~3), 16, bar);
+      } else {
+        copy_in(st + SL.la, d.r_g + u * Cp, Cp * 4, bar);
+        copy_in(st + SL.chunk, in.g + (u & ~static_cast<size_t>(3)), 16, bar);
+        copy_in(st + SL.chunk + 16, in.beta + (u & ~static_cast<size_t>(3)), 16, bar);
+        copy_in(st + SL.chunk + 32, in.g + (u & ~static_cast<size_t>(3)), 16, bar);
+      }
+      smisc[1] = i + 1;
     }
-    uint32_t bytes = tb0 + tb1;
-    bytes += static_cast<uint32_t>(n) * P * resz;                        // buffered records
-    bytes += KIND == 0 ? P * 2 : a16(P * 2);                              // current x / v
-    if (ui.first_of_group) bytes += static_cast<uint32_t>(n + 1) * N * 2 + N * 2;  // keys + q
-    bytes += Cp * 4 + (KIND == 0 ? a16(Cp * 2) : 0) + 48;               // log decays, dt, chunks
-    mbar_expect_tx(bar, bytes);
-    if (READ == READ_NONE || ui.flush) {
-      copy_in(st + SL.tile, d.ckpt + u * tile, tb0, bar);
-    } else if (READ == READ_FP8) {
-      copy_in(st + SL.tile, d.rc_codes + u * tile, tb0, bar);
-      copy_in(st + SL.tile + tile, d.rc_rowscale + u * P, tb1, bar);
-    } else {
-      copy_in(st + SL.tile, d.rc_codes + u * (tile / 2), tb0, bar);
-      copy_in(st + SL.tile + tile / 2, d.rc_blkscale + u * (tile / 16), tb1, bar);
-    }
-    if (KIND == 0) {
-      const uint16_t* rx = d.r_x + u * C * P;
-      copy_in(st + SL.rec, rx + static_cast<size_t>(ui.head) * P, seg1 * P * 2, bar);
-      copy_in(st + SL.rec + seg1 * P * 2, rx, seg2 * P * 2, bar);
-      copy_in(st + SL.rec + n * P * 2, in.x + u * P, P * 2, bar);
-    } else {
-      const float* ru = d.r_u + u * C * P;
-      copy_in(st + SL.rec, ru + static_cast<size_t>(ui.head) * P, seg1 * P * 4, bar);
-      copy_in(st + SL.rec + seg1 * P * 4, ru, seg2 * P * 4, bar);
-      copy_in(st + SL.v, in.v + u * P, a16(P * 2), bar);
-    }
-    if (ui.first_of_group) {
-      const uint16_t* rk = (KIND == 0 ? d.r_B : d.r_k) + bg * C * N;
-      copy_in(st + SL.key, rk + static_cast<size_t>(ui.head) * N, seg1 * N * 2, bar);
-      copy_in(st + SL.key + seg1 * N * 2, rk, seg2 * N * 2, bar);
-      copy_in(st + SL.key + n * N * 2, (KIND == 0 ? in.Bm : in.k) + bg * N, N * 2, bar);
-      copy_in(st + SL.q, (KIND == 0 ? in.Cm : in.q) + bg * N, N * 2, bar);
-    }
-    if (KIND == 0) {
-      copy_in(st + SL.la, d.r_la + u * Cp, Cp * 4, bar);
-      copy_in(st + SL.dt, d.r_dt + u * Cp, a16(Cp * 2), bar);
-      copy_in(st + SL.chunk, in.dt + (u & ~static_cast<size_t>(7)), 16, bar);
-      copy_in(st + SL.chunk + 16, in.A + (ui.h & ~3), 16, bar);
-      if (READ == READ_NVFP4)
-        copy_in(st + SL.chunk + 32, d.rc_matscale + (u & ~static_cast<size_t>(3)), 16, bar);
-      else
-        copy_in(st + SL.chunk + 32, in.A + (ui.h & ~3), 16, bar);
-    } else {
-      copy_in(st + SL.la, d.r_g + u * Cp, Cp * 4, bar);
-      copy_in(st + SL.chunk, in.g + (u & ~static_cast<size_t>(3)), 16, bar);
-      copy_in(st + SL.chunk + 16, in.beta + (u & ~static_cast<size_t>(3)), 16, bar);
-      copy_in(st + SL.chunk + 32, in.g + (u & ~static_cast<size_t>(3)), 16, bar);
-    }
-  };
-
-  if (t == 0) {
-    for (int i = 0; i < min(stages, nunits); ++i) issue(i);
+    return;
   }
 
+  // =========================== computing warps ==============================
   const int c4 = t % SEG;
+  int consumed = 0;
   for (int i = 0; i < nunits; ++i) {
     const UnitInfo ui = unit_info(i);
-    unsigned char* st = smem + static_cast<size_t>(SL.size) * (i % stages);
+    const int s = i % stages;
+    unsigned char* st = smem + static_cast<size_t>(SL.size) * s;
     const uint32_t parity = static_cast<uint32_t>((i / stages) & 1);
-    const bool arrived = __syncthreads_and(mbar_wait_bounded(bars + (i % stages), parity) ? 1 : 0) != 0;
+    const bool arrived = compute_sync_and(mbar_wait_bounded(full + s, parity));
     if (!arrived) {
       if (t == 0) {
         report_error(d.err, DEVERR_TIMEOUT, ui.b);
-        // wait (bounded) for every copy already issued, then stop
-        for (int j = i; j < min(i + stages, nunits); ++j)
-          mbar_wait_bounded(bars + (j % stages), static_cast<uint32_t>((j / stages) & 1));
+        smisc[0] = 1;
       }
-      __syncthreads();
       break;
     }
+    consumed = i + 1;
     const size_t u = static_cast<size_t>(ui.u);
     const int n = ui.n;
     const int slot = ring_slot(ui.head, n, C);
     const int slot_lane = lane < n ? ring_slot(ui.head, lane, C) : 0;
+    const float* la_slot = reinterpret_cast<const float*>(st + SL.la);
+    const float* chunk = reinterpret_cast<const float*>(st + SL.chunk);
+    float* yrow = y + u * P;
+    float4* sT4 = reinterpret_cast<float4*>(st + SL.tile);
+    float4* gS4 = reinterpret_cast<float4*>(d.ckpt + u * tile);
+    const int nf4 = tile / 4;
 
     // ---- per group: keys, query and their dot products (once per group) ----
     if (ui.first_of_group) {
@@ -406,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const LayerDev d, c
       const uint16_t* qb = reinterpret_cast<const uint16_t*>(st + SL.q);
       for (int e = t; e < (n + 1) * N; e += kThreads) sK[e] = bf(kb[e]);
       for (int e = t; e < N; e += kThreads) sq[e] = bf(qb[e]);
-      __syncthreads();
+      compute_sync();
       for (int j = warp; j <= n; j += kThreads / 32) {  // one warp per record
         float aq = 0.f, ak = 0.f;
         for (int e = lane; e < N; e += 32) {
@@ -421,87 +483,205 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const LayerDev d, c
           if (KIND == 1) sdot2[j] = ak;
         }
       }
+      compute_sync();
     }
 
-    // ---- decay weights (warp 0): suffix sums of log decays ----
-    const float* la_slot = reinterpret_cast<const float*>(st + SL.la);
-    const float* chunk = reinterpret_cast<const float*>(st + SL.chunk);
-    if (warp == 0) {
+    const bool fast = (N == 128) && (READ == READ_NONE || ui.flush);
+    if (fast && ui.ok) {
+      // ======== warp-local unit: warp w owns rows w, w+8, ...; lane = column chunk ========
+      const int RW = P / 8;  // rows per warp
       if (KIND == 0) {
-        // records 0..n (current at n): w_j = exp(sum_{i=j+1..n} la_i), gamma = exp(sum_{i<=n} la_i)
+        const uint16_t* xb = reinterpret_cast<const uint16_t*>(st + SL.rec);
+        const uint16_t* dtr = reinterpret_cast<const uint16_t*>(st + SL.dt);
         const uint16_t* dtc = reinterpret_cast<const uint16_t*>(st + SL.chunk);
         const float dt_cur = bf(dtc[u & 7]);
         const float la_cur = dt_cur * chunk[4 + (ui.h & 3)];
-        float v = lane < n ? la_slot[slot_lane] : (lane == n ? la_cur : 0.f);
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float w = __shfl_down_sync(0xffffffffu, v, o);
-          if (lane + o <= n) v += w;
-        }
+        // records 0..n (current at n): w_j = exp(sum_{i=j+1..n} la_i), gamma = exp(sum_{i<=n} la_i)
+        const float v = suffix_sum(lane < n ? la_slot[slot_lane] : (lane == n ? la_cur : 0.f), lane, n);
         const float excl = __shfl_down_sync(0xffffffffu, v, 1);
-        if (lane <= n) sW[lane] = expf(lane < n ? excl : 0.f);
-        if (lane == 0) {
-          sW[C] = expf(v);
-          sW[C + 1] = dt_cur;
-          sW[C + 2] = la_cur;
+        const float Wl = lane <= n ? expf(lane < n ? excl : 0.f) : 0.f;
+        const float gamma = expf(__shfl_sync(0xffffffffu, v, 0));
+        const float dtl = lane < n ? bf(dtr[slot_lane]) : (lane == n ? dt_cur : 0.f);
+        const float cy = lane <= n ? Wl * dtl * sdot[lane] : 0.f;  // output coefficient on x_j[r]
+        const float cf = Wl * dtl;                                 // fold coefficient on x_j[r]
+        const float4 q4 = reinterpret_cast<const float4*>(sq)[lane];
+        const int kq = (lane >> 2) & 7, jl = lane & 3;
+        for (int r0 = 0; r0 < RW; r0 += 8) {
+          // buffered term of row slot kq: lanes 4kq..4kq+3 split the records
+          const int Rq = warp + 8 * (r0 + kq);
+          const bool vq = r0 + kq < RW;
+          float ry = 0.f;
+          for (int j0 = 0; j0 <= n; j0 += 4) {
+            const int j = j0 + jl;
+            const float c = __shfl_sync(0xffffffffu, cy, j & 31);
+            if (j <= n && vq) ry = fmaf(c, bf(xb[j * P + Rq]), ry);
+          }
+          ry += __shfl_xor_sync(0xffffffffu, ry, 1);
+          ry += __shfl_xor_sync(0xffffffffu, ry, 2);
+          float4 s4[8];
+          float part[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const bool vk = r0 + k < RW;
+            s4[k] = vk ? sT4[(warp + 8 * (r0 + k)) * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+            part[k] = dot4(s4[k], q4);
+          }
+          const float tot = reduce8(part, lane);
+          if (jl == 0 && vq) yrow[Rq] = fmaf(gamma, tot, ry);
+          if (ui.flush) {
+            float4 acc[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] = scale4(gamma, s4[k]);
+            for (int j = 0; j <= n; ++j) {
+              const float4 k4 = reinterpret_cast<const float4*>(sK + j * N)[lane];
+              const float c = __shfl_sync(0xffffffffu, cf, j);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const int R = warp + 8 * (r0 + k);
+                if (r0 + k < RW) acc[k] = axpy4(c * bf(xb[j * P + R]), k4, acc[k]);
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              if (r0 + k < RW) {
+                const int f = (warp + 8 * (r0 + k)) * 32 + lane;
+                __stcs(gS4 + f, acc[k]);
+                if (READ != READ_NONE) sT4[f] = acc[k];
+              }
+            }
+          }
         }
       } else {
+        const float* ub = reinterpret_cast<const float*>(st + SL.rec);
+        const uint16_t* vb = reinterpret_cast<const uint16_t*>(st + SL.v);
         // buffered records 0..n-1: w_j = exp(sum_{i=j+1..n-1} g_i), gamma = exp(sum_{i<n} g_i)
-        float v = lane < n ? la_slot[slot_lane] : 0.f;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float w = __shfl_down_sync(0xffffffffu, v, o);
-          if (lane + o < n) v += w;
-        }
+        const float v = suffix_sum(lane < n ? la_slot[slot_lane] : 0.f, lane, n - 1);
         const float excl = __shfl_down_sync(0xffffffffu, v, 1);
-        if (lane < n) sW[lane] = expf(lane + 1 < n ? excl : 0.f);
-        if (lane == 0) {
-          sW[C] = n > 0 ? expf(v) : 1.f;
-          sW[C + 1] = expf(chunk[u & 3]);
-          sW[C + 2] = chunk[4 + (u & 3)];
+        const float Wl = lane < n ? expf(lane + 1 < n ? excl : 0.f) : 0.f;
+        const float gamma = n > 0 ? expf(__shfl_sync(0xffffffffu, v, 0)) : 1.f;
+        const float a = expf(chunk[u & 3]);
+        const float beta = chunk[4 + (u & 3)];
+        const float kq_dot = sdot[n];
+        const float ck = lane < n ? Wl * sdot2[lane] : 0.f;   // coefficient of u_j[r] in S k
+        const float cq = lane < n ? Wl * sdot[lane] : 0.f;    // coefficient of u_j[r] in S q
+        const float cf = a * Wl;                              // fold coefficient of u_j[r]
+        const float4 q4 = reinterpret_cast<const float4*>(sq)[lane];
+        const float4 k4c = reinterpret_cast<const float4*>(sK + n * N)[lane];
+        float* urow = d.r_u + (u * C + slot) * P;
+        const int kq = (lane >> 2) & 7, jl = lane & 3;
+        for (int r0 = 0; r0 < RW; r0 += 8) {
+          const int Rq = warp + 8 * (r0 + kq);
+          const bool vq = r0 + kq < RW;
+          float rk = 0.f, rq = 0.f;
+          for (int j0 = 0; j0 < n; j0 += 4) {
+            const int j = j0 + jl;
+            const float c1 = __shfl_sync(0xffffffffu, ck, j & 31);
+            const float c2 = __shfl_sync(0xffffffffu, cq, j & 31);
+            if (j < n && vq) {
+              const float uj = ub[j * P + Rq];
+              rk = fmaf(c1, uj, rk);
+              rq = fmaf(c2, uj, rq);
+            }
+          }
+          rk += __shfl_xor_sync(0xffffffffu, rk, 1);
+          rk += __shfl_xor_sync(0xffffffffu, rk, 2);
+          rq += __shfl_xor_sync(0xffffffffu, rq, 1);
+          rq += __shfl_xor_sync(0xffffffffu, rq, 2);
+          float4 s4[8];
+          float pk[8], pq[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const bool vk = r0 + k < RW;
+            s4[k] = vk ? sT4[(warp + 8 * (r0 + k)) * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+            pk[k] = dot4(s4[k], k4c);
+            pq[k] = dot4(s4[k], q4);
+          }
+          const float Sk = fmaf(gamma, reduce8(pk, lane), rk);
+          const float Sq = fmaf(gamma, reduce8(pq, lane), rq);
+          const float uu = vq ? beta * (bf(vb[Rq]) - a * Sk) : 0.f;
+          if (jl == 0 && vq) {
+            yrow[Rq] = fmaf(a, Sq, uu * kq_dot);
+            if (!ui.flush) urow[Rq] = uu;
+          }
+          if (ui.flush) {
+            float4 acc[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              acc[k] = axpy4(__shfl_sync(0xffffffffu, uu, 4 * k), k4c, scale4(a * gamma, s4[k]));
+            for (int j = 0; j < n; ++j) {
+              const float4 k4 = reinterpret_cast<const float4*>(sK + j * N)[lane];
+              const float c = __shfl_sync(0xffffffffu, cf, j);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const int R = warp + 8 * (r0 + k);
+                if (r0 + k < RW) acc[k] = axpy4(c * ub[j * P + R], k4, acc[k]);
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              if (r0 + k < RW) __stcs(gS4 + (warp + 8 * (r0 + k)) * 32 + lane, acc[k]);
+            }
+          }
         }
       }
-    }
-    __syncthreads();
-
-    // ---- per-row buffered terms; fold coefficients on flush units ----
-    if (KIND == 0) {
-      const uint16_t* xb = reinterpret_cast<const uint16_t*>(st + SL.rec);
-      const uint16_t* dtr = reinterpret_cast<const uint16_t*>(st + SL.dt);
-      const float dt_cur = sW[C + 1];
-      for (int r = t; r < P; r += kThreads) {
-        float acc = 0.f;
-        for (int j = 0; j <= n; ++j) {
-          const float dtj = j < n ? bf(dtr[ring_slot(ui.head, j, C)]) : dt_cur;
-          const float v = dtj * bf(xb[j * P + r]);
-          acc = fmaf(sW[j] * sdot[j], v, acc);
-          if (ui.flush) scoef[j * P + r] = sW[j] * v;
+    } else if (ui.ok) {
+      // ======== shared-memory path (d_state < 128, or a read-copy non-flush unit) ========
+      if (warp == 0) {
+        if (KIND == 0) {
+          const uint16_t* dtc = reinterpret_cast<const uint16_t*>(st + SL.chunk);
+          const float dt_cur = bf(dtc[u & 7]);
+          const float la_cur = dt_cur * chunk[4 + (ui.h & 3)];
+          const float v = suffix_sum(lane < n ? la_slot[slot_lane] : (lane == n ? la_cur : 0.f), lane, n);
+          const float excl = __shfl_down_sync(0xffffffffu, v, 1);
+          if (lane <= n) sW[lane] = expf(lane < n ? excl : 0.f);
+          if (lane == 0) {
+            sW[C] = expf(v);
+            sW[C + 1] = dt_cur;
+            sW[C + 2] = la_cur;
+          }
+        } else {
+          const float v = suffix_sum(lane < n ? la_slot[slot_lane] : 0.f, lane, n - 1);
+          const float excl = __shfl_down_sync(0xffffffffu, v, 1);
+          if (lane < n) sW[lane] = expf(lane + 1 < n ? excl : 0.f);
+          if (lane == 0) {
+            sW[C] = n > 0 ? expf(v) : 1.f;
+            sW[C + 1] = expf(chunk[u & 3]);
+            sW[C + 2] = chunk[4 + (u & 3)];
+          }
         }
-        srow[r] = acc;
       }
-    } else {
-      const float* ub = reinterpret_cast<const float*>(st + SL.rec);
-      const float a = sW[C + 1];
-      for (int r = t; r < P; r += kThreads) {
-        float ak = 0.f, aq = 0.f;
-        for (int j = 0; j < n; ++j) {
-          const float wu = sW[j] * ub[j * P + r];
-          ak = fmaf(wu, sdot2[j], ak);
-          aq = fmaf(wu, sdot[j], aq);
-          if (ui.flush) scoef[j * P + r] = a * wu;
+      compute_sync();
+      if (KIND == 0) {
+        const uint16_t* xb = reinterpret_cast<const uint16_t*>(st + SL.rec);
+        const uint16_t* dtr = reinterpret_cast<const uint16_t*>(st + SL.dt);
+        const float dt_cur = sW[C + 1];
+        for (int r = t; r < P; r += kThreads) {
+          float acc = 0.f;
+          for (int j = 0; j <= n; ++j) {
+            const float dtj = j < n ? bf(dtr[ring_slot(ui.head, j, C)]) : dt_cur;
+            const float v = dtj * bf(xb[j * P + r]);
+            acc = fmaf(sW[j] * sdot[j], v, acc);
+            if (ui.flush) scoef[j * P + r] = sW[j] * v;
+          }
+          srow[r] = acc;
         }
-        srow[r] = ak;
-        srow2[r] = aq;
+      } else {
+        const float* ub = reinterpret_cast<const float*>(st + SL.rec);
+        const float a = sW[C + 1];
+        for (int r = t; r < P; r += kThreads) {
+          float ak = 0.f, aq = 0.f;
+          for (int j = 0; j < n; ++j) {
+            const float wu = sW[j] * ub[j * P + r];
+            ak = fmaf(wu, sdot2[j], ak);
+            aq = fmaf(wu, sdot[j], aq);
+            if (ui.flush) scoef[j * P + r] = a * wu;
+          }
+          srow[r] = ak;
+          srow2[r] = aq;
+        }
       }
-    }
-    __syncthreads();
-
-    // ---- one pass over the state matrix ----
-    float* yrow = y + u * P;
-    float4* sT4 = reinterpret_cast<float4*>(st + SL.tile);
-    const int nf4 = tile / 4;
-    const float gamma = sW[C];
-    if (ui.ok) {
+      compute_sync();
+      const float gamma = sW[C];
       if (KIND == 0) {
         const float4 q4 = reinterpret_cast<const float4*>(sq)[c4];
         if (!ui.flush && READ == READ_FP8) {
@@ -524,6 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const LayerDev d, c
             float4 acc = scale4(gamma, s4);
             for (int j = 0; j <= n; ++j)
               acc = axpy4(scoef[j * P + r], reinterpret_cast<const float4*>(sK + j * N)[c4], acc);
+            __stcs(gS4 + f, acc);
             sT4[f] = acc;
           }
         }
@@ -549,19 +730,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const LayerDev d, c
             float4 acc = axpy4(uu, k4, scale4(a * gamma, s4));
             for (int j = 0; j < n; ++j)
               acc = axpy4(scoef[j * P + r], reinterpret_cast<const float4*>(sK + j * N)[c4], acc);
-            sT4[f] = acc;
+            __stcs(gS4 + f, acc);
           }
         }
       }
     }
 
-    // ---- flush: write the folded matrix back once (bulk store), refresh the read copy ----
-    if (ui.ok && ui.flush) {
-      fence_proxy_async();
-      __syncthreads();
-      if (t == 0) bulk_s2g(d.ckpt + u * tile, st + SL.tile, static_cast<uint32_t>(tile) * 4u);
-      if (READ != READ_NONE)
-        write_read_copy<N, READ>(d, static_cast<int>(u), reinterpret_cast<const float*>(st + SL.tile), sred);
+    // ---- flush: refresh the read copy from the folded matrix in shared memory ----
+    if (READ != READ_NONE && ui.ok && ui.flush) {
+      compute_sync();
+      write_read_copy<N, READ>(d, static_cast<int>(u), reinterpret_cast<const float*>(st + SL.tile), sred);
     }
 
     // ---- append this token's record (non-flush units) ----
@@ -572,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const LayerDev d, c
         if (t == 0) {
           const uint16_t* dtc = reinterpret_cast<const uint16_t*>(st + SL.chunk);
           d.r_dt[u * Cp + slot] = dtc[u & 7];
-          d.r_la[u * Cp + slot] = sW[C + 2];
+          d.r_la[u * Cp + slot] = bf(dtc[u & 7]) * chunk[4 + (ui.h & 3)];
         }
       } else {
         if (t == 0) d.r_g[u * Cp + slot] = chunk[u & 3];
@@ -585,13 +763,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const LayerDev d, c
       }
     }
 
-    __syncthreads();  // stage i % stages is free
-    if (t == 0 && i + stages < nunits) {
-      if (ui.ok && ui.flush) bulk_wait_read_all();  // the bulk store has read the stage
-      issue(i + stages);
-    }
+    compute_sync();  // every computing thread is done with stage s
+    if (t == 0) mbar_arrive(empty + s);
   }
-  if (t == 0) bulk_wait_all();
+  // after an abort: let the copies already issued land before the CTA exits
+  if (smisc[0] && t == 0) {
+    const uint64_t t0 = global_ns();
+    while (smisc[1] < min(consumed + stages, nunits) && global_ns() - t0 < 1000000000ull) {
+    }
+    const int issued = smisc[1];
+    for (int j = consumed; j < issued; ++j)
+      mbar_wait_bounded(full + (j % stages), static_cast<uint32_t>((j / stages) & 1));
+  }
 }
 
 int stages_for(const LayerDev& d) {
@@ -622,7 +805,7 @@ cudaError_t launch_one(const LayerDev& d, const TokenIn& in, float* y, cudaStrea
   auto kernel = decode_kernel<KIND, N, READ>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kThreads, smem, s>>>(d, in, y, per, stages);
+  kernel<<<grid, kDecodeThreads, smem, s>>>(d, in, y, per, stages);
   return cudaGetLastError();
 }
 

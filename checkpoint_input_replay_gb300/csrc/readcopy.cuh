@@ -17,8 +17,12 @@
 
 namespace rs {
 
+// Barrier among the kThreads threads that compute (named barrier 1): the
+// decode kernel adds a producer warp that does not take part.
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
 // sT: folded matrix [P][N] f32 in shared memory; sred: kThreads/32 floats.
-// Called by all threads of the CTA.
+// Called by the kThreads computing threads (threads 0..kThreads-1) of the CTA.
 template <int N, int READ>
 __device__ __forceinline__ void write_read_copy(const LayerDev& d, int bh, const float* sT, float* sred) {
   constexpr int SEG = N / 4;
@@ -53,7 +57,7 @@ __device__ __forceinline__ void write_read_copy(const LayerDev& d, int bh, const
     }
     m = seg_max<32>(m);
     if ((t & 31) == 0) sred[t >> 5] = m;
-    __syncthreads();
+    compute_sync();
     float amax = 0.0f;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) amax = fmaxf(amax, sred[w]);
