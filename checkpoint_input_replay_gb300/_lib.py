@@ -34,7 +34,7 @@ RS_DEVERR_CURSOR = 2
 RS_DEVERR_TIMEOUT = 3
 
 EXPORTED = ("rs_query_sizes", "rs_create_cache", "rs_destroy_cache", "rs_decode_step", "rs_verify",
-            "rs_commit", "rs_flush", "rs_get_device_error", "rs_status_string")
+            "rs_commit", "rs_flush", "rs_get_device_error", "rs_status_string", "rs_decode_step_noalloc")
 
 
 class rs_config(ctypes.Structure):
@@ -77,6 +77,8 @@ def load() -> ctypes.CDLL:
         lib.rs_commit.argtypes = [vp, vp, vp]
         lib.rs_flush.argtypes = [vp, vp, vp]
         lib.rs_get_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
+        lib.rs_decode_step_noalloc.argtypes = [ctypes.POINTER(rs_config), ctypes.POINTER(rs_buffers),
+                                               ctypes.POINTER(rs_inputs), vp, vp]
         lib.rs_status_string.argtypes = [ctypes.c_int]
         lib.rs_status_string.restype = ctypes.c_char_p
         for name in EXPORTED:
@@ -140,3 +142,9 @@ def rs_get_device_error(handle, stream: int):
 
 def rs_status_string(status: int) -> str:
     return status_string(status)
+
+
+def rs_decode_step_noalloc(cfg: rs_config, bufs: rs_buffers, inputs: rs_inputs, y_ptr: int, stream: int) -> int:
+    """Decode step with the library's fixed arrival-counter array (no handle, no scratch buffer)."""
+    return load().rs_decode_step_noalloc(ctypes.byref(cfg), ctypes.byref(bufs), ctypes.byref(inputs),
+                                         ctypes.c_void_p(y_ptr), ctypes.c_void_p(stream))

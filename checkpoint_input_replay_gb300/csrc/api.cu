@@ -152,6 +152,82 @@ cudaError_t set_smem_limit(const void* func, size_t bytes) {
   return cudaSuccess;
 }
 
+// Layer descriptor for caller buffers, validated like rs_create_cache but
+// without a handle and without touching device memory.  The arrival counters
+// are left unset when needs_scratch is false (the caller supplies them).
+rs_status bind_layer(const rs_config* cfg, const rs_buffers* bufs, bool needs_scratch, LayerDev* out) {
+  if (!cfg || !bufs || !out) return RS_ERR_NULL;
+  const rs_status st = validate(cfg);
+  if (st != RS_OK) return st;
+  if (!bufs->ckpt || !bufs->ring || !bufs->cursor || (needs_scratch && !bufs->scratch)) return RS_ERR_NULL;
+  if (cfg->read_mode != RS_READ_NONE && !bufs->read_copy) return RS_ERR_NULL;
+  if (!aligned16(bufs->ckpt) || !aligned16(bufs->ring) || !aligned16(bufs->cursor) ||
+      (needs_scratch && !aligned16(bufs->scratch)) || (bufs->read_copy && !aligned16(bufs->read_copy)))
+    return RS_ERR_ALIGN;
+  const Layout L = layout_of(*cfg);
+  LayerDev d{};
+  d.kind = cfg->kind;
+  d.B = cfg->batch;
+  d.H = cfg->n_heads;
+  d.G = cfg->n_groups;
+  d.P = cfg->d_head;
+  d.N = cfg->d_state;
+  d.L = cfg->ring_len;
+  d.T_max = cfg->max_draft;
+  d.C = cfg->ring_len + cfg->max_draft;
+  d.Cp = (d.C + 7) & ~7;
+  d.read_mode = cfg->read_mode;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return RS_ERR_CUDA;
+  d.num_sms = sms;
+  d.ckpt = static_cast<float*>(bufs->ckpt);
+  char* ring = static_cast<char*>(bufs->ring);
+  if (cfg->kind == RS_MAMBA2) {
+    d.r_x = reinterpret_cast<uint16_t*>(ring + L.r0);
+    d.r_dt = reinterpret_cast<uint16_t*>(ring + L.r1);
+    d.r_la = reinterpret_cast<float*>(ring + L.r2);
+    d.r_B = reinterpret_cast<uint16_t*>(ring + L.r3);
+  } else {
+    d.r_u = reinterpret_cast<float*>(ring + L.r0);
+    d.r_g = reinterpret_cast<float*>(ring + L.r1);
+    d.r_k = reinterpret_cast<uint16_t*>(ring + L.r2);
+  }
+  d.cursor = static_cast<int*>(bufs->cursor);
+  d.err = d.cursor + 4 * d.B;
+  d.arrive = needs_scratch ? static_cast<int*>(bufs->scratch) : nullptr;
+  if (cfg->read_mode != RS_READ_NONE) {
+    char* rc = static_cast<char*>(bufs->read_copy);
+    d.rc_codes = reinterpret_cast<uint8_t*>(rc + L.c0);
+    if (cfg->read_mode == RS_READ_FP8_ROW) {
+      d.rc_rowscale = reinterpret_cast<float*>(rc + L.c1);
+    } else {
+      d.rc_blkscale = reinterpret_cast<uint8_t*>(rc + L.c1);
+      d.rc_matscale = reinterpret_cast<float*>(rc + L.c2);
+    }
+  }
+  *out = d;
+  return RS_OK;
+}
+
+// Token inputs of one call, checked for the layer kind (NULL / alignment).
+rs_status bind_inputs(int kind, const rs_inputs* in, TokenIn* out) {
+  if (!in || !out) return RS_ERR_NULL;
+  const void* p[5];
+  if (kind == RS_MAMBA2) {
+    p[0] = in->x; p[1] = in->dt; p[2] = in->A; p[3] = in->Bm; p[4] = in->Cm;
+  } else {
+    p[0] = in->q; p[1] = in->k; p[2] = in->v; p[3] = in->g; p[4] = in->beta;
+  }
+  for (const void* q : p)
+    if (!q) return RS_ERR_NULL;
+  for (const void* q : p)
+    if (!aligned16(q)) return RS_ERR_ALIGN;
+  *out = token_in(in);
+  return RS_OK;
+}
+
 }  // namespace rs
 
 extern "C" {

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "replayssm.h"
+
 namespace rs {
 
 constexpr int kThreads = 256;          // threads per CTA of every hot-path kernel
@@ -52,6 +54,10 @@ cudaError_t launch_decode(const LayerDev& d, const TokenIn& in, float* y, cudaSt
 cudaError_t launch_verify(const LayerDev& d, const TokenIn& in, int T, float* y, cudaStream_t s);
 cudaError_t launch_fold(const LayerDev& d, int mode, const int* accepted, const uint8_t* mask,
                         int T_pending, cudaStream_t s);
+
+// Host helpers of api.cu shared with other entry points.
+rs_status bind_layer(const rs_config* cfg, const rs_buffers* bufs, bool needs_scratch, LayerDev* out);
+rs_status bind_inputs(int kind, const rs_inputs* in, TokenIn* out);
 
 // Raise a kernel's dynamic shared-memory limit (once per kernel and size).
 cudaError_t set_smem_limit(const void* func, size_t bytes);

@@ -206,6 +206,26 @@ rs_status rs_flush(rs_cache *cache, const uint8_t *seq_mask, rs_stream stream);
  * sticky; a cache with a device error should be re-created. */
 rs_status rs_get_device_error(rs_cache *cache, rs_stream stream, int32_t *code);
 
+/* Standard decode step, as rs_decode_step, for callers that cannot allocate
+ * device memory -- for example code running inside a server or plugin whose
+ * device memory is owned and pre-allocated by someone else.  It takes the
+ * config and the caller's buffers directly (no rs_cache handle; bufs->scratch
+ * is ignored and may be NULL) and keeps the per-sequence arrival counters in
+ * a fixed array of this library (64 KiB on every GPU that loads the library,
+ * held until the process exits).  It calls no cudaMalloc, no cudaFree and no
+ * allocating library routine.  The paper has no counterpart of this call.
+ *   - batch must be <= 16384, else RS_ERR_UNSUPPORTED.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call clears the counters it uses on `stream`, then launches.  All
+ *     calls on a device share the array: calls that overlap on the GPU (other
+ *     streams, other caches, other threads) race and must be ordered by the
+ *     caller.
+ *   - No drafts may be pending on these buffers (rs_verify without rs_commit);
+ *     without a handle this call cannot check that. */
+rs_status rs_decode_step_noalloc(const rs_config *cfg, const rs_buffers *bufs, const rs_inputs *in, float *y,
+                                 rs_stream stream);
+
 /* Static description of a status code. */
 const char *rs_status_string(rs_status status);
 
