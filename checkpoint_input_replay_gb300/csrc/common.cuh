@@ -24,6 +24,12 @@ __device__ __forceinline__ void bf8(const uint4 raw, float out[8]) {
   }
 }
 
+// 4 bf16 packed in a uint2 -> float4
+__device__ __forceinline__ float4 bf4(const uint2 raw) {
+  return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                     __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
+}
+
 // Sum over aligned groups of SEG lanes (SEG a power of two <= 32); every lane
 // of the group receives the total.
 template <int SEG>
@@ -50,6 +56,24 @@ __device__ __forceinline__ float4 axpy4(float a, const float4 x, float4 y) {
   y.z = fmaf(a, x.z, y.z);
   y.w = fmaf(a, x.w, y.w);
   return y;
+}
+
+// y += a * x with packed two-lane FP32 FMAs (fma.rn.f32x2: two IEEE fmaf)
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float4 axpy4x2(float a, const float4 x, const float4 y) {
+  const float2 lo = fma2(make_float2(a, a), make_float2(x.x, x.y), make_float2(y.x, y.y));
+  const float2 hi = fma2(make_float2(a, a), make_float2(x.z, x.w), make_float2(y.z, y.w));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
 __device__ __forceinline__ float4 scale4(float a, const float4 x) {

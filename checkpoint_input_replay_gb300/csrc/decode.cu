@@ -53,6 +53,7 @@ struct Stage {
   int la;     // f32 [Cp] log decays in slot order
   int dt;     // Mamba-2: dt bf16 [Cp] in slot order
   int chunk;  // three 16-byte chunks: Mamba-2 dt_cur, A, matrix scale; GDN g_cur, beta, -
+  int scal;   // f32 [3C + 2P + 8]: per-record coefficients, per-row buffered terms, scalars
   int size;
 };
 
@@ -75,6 +76,8 @@ __host__ __device__ __forceinline__ Stage stage_layout(int kind, int P, int N, i
   o += kind == 0 ? a16(Cp * 2) : 0;
   s.chunk = o;
   o += 48;
+  s.scal = o;
+  o += (3 * C + 2 * P + 8) * 4;
   s.size = a128(o);
   return s;
 }
@@ -97,8 +100,8 @@ __host__ __device__ __forceinline__ Persist persist_layout(int P, int N, int C) 
   p.coef = o;   o += C * P;      // flush coefficients [C][P]
   p.red = o;    o += kThreads / 32;
   p.misc = o;   o += 4;
-  p.bars = (o + 3) & ~3;         // 16-byte aligned: 8 full + 8 empty mbarriers (u64)
-  o = p.bars + 2 * 16;
+  p.bars = (o + 3) & ~3;         // 16-byte aligned: 8 full + 8 empty + 8 ready mbarriers (u64)
+  o = p.bars + 2 * 24;
   p.seq = o;    o += 3 * kMaxSeq;  // cached cursors: head, count, ok
   p.size_floats = o;
   return p;
@@ -214,7 +217,11 @@ __device__ __forceinline__ void rc_rows_nvfp4(const unsigned char* sC, const uns
 // ---------------------------------------------------------------------------
 // The kernel (KIND 0: Mamba-2, 1: Gated DeltaNet)
 // ---------------------------------------------------------------------------
-constexpr int kDecodeThreads = kThreads + 32;  // 8 computing warps + 1 producer warp
+// 8 computing warps + 1 producer warp, + 1 prologue warp on the warp-local path
+template <int N, int READ>
+constexpr int decode_threads() {
+  return kThreads + ((N == 128 && READ == READ_NONE) ? 64 : 32);
+}
 
 __device__ __forceinline__ bool compute_sync_and(bool v) {
   uint32_t r;
@@ -269,10 +276,12 @@ __device__ __forceinline__ float suffix_sum(float v, int lane, int last) {
 }
 
 template <int KIND, int N, int READ>
-__global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const LayerDev d, const TokenIn in,
+__global__ void __launch_bounds__(decode_threads<N, READ>(), 1) decode_kernel(const LayerDev d, const TokenIn in,
                                                                    float* __restrict__ y, const int units_per_cta,
                                                                    const int stages) {
   constexpr int SEG = N / 4;  // lanes per state row, one float4 each
+  // d_state 128 without a read copy: every warp computes its rows of a unit on its own
+  constexpr bool kWarpLocal = (N == 128 && READ == READ_NONE);
   extern __shared__ __align__(1024) unsigned char smem[];
 
   const int P = d.P, H = d.H, G = d.G, C = d.C, L = d.L, Cp = d.Cp;
@@ -291,9 +300,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const LayerDe
   float* srow2 = pf + PL.row2;
   float* scoef = pf + PL.coef;
   float* sred = pf + PL.red;
-  volatile int* smisc = reinterpret_cast<volatile int*>(pf + PL.misc);  // [0] abort, [1] issued
+  volatile int* smisc = reinterpret_cast<volatile int*>(pf + PL.misc);  // abort, issued, producer done
   uint64_t* full = reinterpret_cast<uint64_t*>(pf + PL.bars);
   uint64_t* empty = full + 8;
+  uint64_t* ready = full + 16;
   int* sseq = reinterpret_cast<int*>(pf + PL.seq);
 
   const int total_units = d.B * H;
@@ -333,10 +343,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const LayerDe
   if (t == kThreads) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(full + s, 1);
-      mbar_init(empty + s, 1);
+      mbar_init(empty + s, kWarpLocal ? kThreads / 32 : 1);
+      mbar_init(ready + s, 1);
     }
-    smisc[0] = 0;
-    smisc[1] = 0;
+    smisc[0] = 0;  // abort
+    smisc[1] = 0;  // units issued
+    smisc[2] = 0;  // producer finished
   }
   __syncthreads();
 
@@ -357,7 +369,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const LayerDe
   };
 
   // =========================== producer warp ===============================
-  if (warp == kThreads / 32) {
+  if (warp == kThreads / 32 + (kWarpLocal ? 1 : 0)) {
     if (lane != 0) return;
     for (int i = 0; i < nunits; ++i) {
       const int s = i % stages;
@@ -384,7 +396,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const LayerDe
       uint32_t bytes = tb0 + tb1;
       bytes += static_cast<uint32_t>(n) * P * resz;                        // buffered records
       bytes += KIND == 0 ? P * 2 : a16(P * 2);                              // current x / v
-      if (ui.first_of_group) bytes += static_cast<uint32_t>(n + 1) * N * 2 + N * 2;  // keys + q
+      // all buffered keys for the first unit of a group (dot products) and for a
+      // fold; the current key and q for every unit on the warp-local path
+      const bool all_keys = ui.first_of_group || (kWarpLocal && ui.flush);
+      const bool cur_key = kWarpLocal || all_keys;
+      if (all_keys) bytes += static_cast<uint32_t>(n) * N * 2;
+      if (cur_key) bytes += 2 * N * 2;
       bytes += Cp * 4 + (KIND == 0 ? a16(Cp * 2) : 0) + 48;               // log decays, dt, chunks
       mbar_expect_tx(bar, bytes);
       if (READ == READ_NONE || ui.flush) {
@@ -407,10 +424,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const LayerDe
         copy_in(st + SL.rec + seg1 * P * 4, ru, seg2 * P * 4, bar);
         copy_in(st + SL.v, in.v + u * P, a16(P * 2), bar);
       }
-      if (ui.first_of_group) {
+      if (all_keys) {
         const uint16_t* rk = (KIND == 0 ? d.r_B : d.r_k) + bg * C * N;
         copy_in(st + SL.key, rk + static_cast<size_t>(ui.head) * N, seg1 * N * 2, bar);
         copy_in(st + SL.key + seg1 * N * 2, rk, seg2 * N * 2, bar);
+      }
+      if (cur_key) {
         copy_in(st + SL.key + n * N * 2, (KIND == 0 ? in.Bm : in.k) + bg * N, N * 2, bar);
         copy_in(st + SL.q, (KIND == 0 ? in.Cm : in.q) + bg * N, N * 2, bar);
       }
@@ -431,10 +450,271 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const LayerDe
       }
       smisc[1] = i + 1;
     }
+    smisc[2] = 1;
     return;
   }
 
   // =========================== computing warps ==============================
+  if constexpr (kWarpLocal) {
+    const int RW = P / 8;  // rows per computing warp
+    const int kq = (lane >> 2) & 7, jl = lane & 3;
+    // ===================== prologue warp =====================
+    // Runs ahead of the computing warps: per unit it turns the staged records
+    // into scalars -- key dot products (once per group, kept in registers),
+    // decay weights, per-record coefficients and the buffered term of every
+    // row -- writes them into the stage and signals `ready`.
+    if (warp == kThreads / 32) {
+      float dq = 0.f, dk = 0.f;  // lane j: k_j . q, k_j . k_cur of the current group
+      int consumed = 0;
+      for (int i = 0; i < nunits; ++i) {
+        if (smisc[0]) break;
+        const int s = i % stages;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(full + s, static_cast<uint32_t>((i / stages) & 1)))) {
+          if (lane == 0) {
+            report_error(d.err, DEVERR_TIMEOUT, (u0 + i) / H);
+            smisc[0] = 1;
+          }
+          break;
+        }
+        consumed = i + 1;
+        const UnitInfo ui = unit_info(i);
+        unsigned char* st = smem + static_cast<size_t>(SL.size) * s;
+        float* sc = reinterpret_cast<float*>(st + SL.scal);
+        if (ui.ok) {
+          const size_t u = static_cast<size_t>(ui.u);
+          const int n = ui.n;
+          const int slot_lane = lane < n ? ring_slot(ui.head, lane, C) : 0;
+          const float* la_slot = reinterpret_cast<const float*>(st + SL.la);
+          const float* chunk = reinterpret_cast<const float*>(st + SL.chunk);
+          if (ui.first_of_group) {
+            const uint16_t* kb = reinterpret_cast<const uint16_t*>(st + SL.key);
+            const float4 q4 = bf4(reinterpret_cast<const uint2*>(st + SL.q)[lane]);
+            const float4 kc4 = bf4(reinterpret_cast<const uint2*>(kb + n * N)[lane]);
+            for (int j0 = 0; j0 <= n; j0 += 8) {
+              float pq[8], pk[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const int j = j0 + k;
+                const float4 kj = j <= n ? bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane])
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                pq[k] = dot4(kj, q4);
+                pk[k] = KIND == 1 ? dot4(kj, kc4) : 0.f;
+              }
+              const float tq = __shfl_sync(0xffffffffu, reduce8(pq, lane), 4 * (lane & 7));
+              if ((lane >> 3) == (j0 >> 3)) dq = tq;
+              if (KIND == 1) {
+                const float tk = __shfl_sync(0xffffffffu, reduce8(pk, lane), 4 * (lane & 7));
+                if ((lane >> 3) == (j0 >> 3)) dk = tk;
+              }
+            }
+          }
+          if (KIND == 0) {
+            const uint16_t* dtr = reinterpret_cast<const uint16_t*>(st + SL.dt);
+            const uint16_t* dtc = reinterpret_cast<const uint16_t*>(st + SL.chunk);
+            const float dt_cur = bf(dtc[u & 7]);
+            const float la_cur = dt_cur * chunk[4 + (ui.h & 3)];
+            // records 0..n (current at n): w_j = exp(sum_{i=j+1..n} la_i), gamma = exp(sum_{i<=n} la_i)
+            const float v = suffix_sum(lane < n ? la_slot[slot_lane] : (lane == n ? la_cur : 0.f), lane, n);
+            const float excl = __shfl_down_sync(0xffffffffu, v, 1);
+            const float Wl = lane <= n ? expf(lane < n ? excl : 0.f) : 0.f;
+            const float dtl = lane < n ? bf(dtr[slot_lane]) : (lane == n ? dt_cur : 0.f);
+            if (lane <= n) {
+              sc[lane] = Wl * dtl * dq;     // output coefficient on x_j[r]
+              sc[2 * C + lane] = Wl * dtl;  // fold coefficient on x_j[r]
+            }
+            if (lane == 0) {
+              sc[3 * C + 2 * P] = expf(v);
+              sc[3 * C + 2 * P + 4] = la_cur;
+            }
+          } else {
+            // buffered records 0..n-1: w_j = exp(sum_{i=j+1..n-1} g_i), gamma = exp(sum_{i<n} g_i)
+            const float v = suffix_sum(lane < n ? la_slot[slot_lane] : 0.f, lane, n - 1);
+            const float excl = __shfl_down_sync(0xffffffffu, v, 1);
+            const float Wl = lane < n ? expf(lane + 1 < n ? excl : 0.f) : 0.f;
+            const float a = expf(chunk[u & 3]);
+            if (lane < n) {
+              sc[lane] = Wl * dk;          // coefficient of u_j[r] in S k
+              sc[C + lane] = Wl * dq;      // coefficient of u_j[r] in S q
+              sc[2 * C + lane] = a * Wl;   // fold coefficient of u_j[r]
+            }
+            const float kq_dot = __shfl_sync(0xffffffffu, dq, n);
+            if (lane == 0) {
+              sc[3 * C + 2 * P] = n > 0 ? expf(v) : 1.f;
+              sc[3 * C + 2 * P + 1] = a;
+              sc[3 * C + 2 * P + 2] = chunk[4 + (u & 3)];
+              sc[3 * C + 2 * P + 3] = kq_dot;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ready + s);
+      }
+      // after an abort: let the copies already issued land before the CTA exits
+      if (smisc[0] && lane == 0) {
+        const uint64_t t0 = global_ns();
+        while (!smisc[2] && global_ns() - t0 < 2000000000ull) {
+        }
+        const int issued = smisc[1];
+        for (int j = consumed; j < issued; ++j)
+          mbar_wait_bounded(full + (j % stages), static_cast<uint32_t>((j / stages) & 1));
+      }
+      return;
+    }
+    // ===================== computing warps =====================
+    // warp w owns rows w, w+8, ..; lane = column chunk; no barrier across warps
+    for (int i = 0; i < nunits; ++i) {
+      if (smisc[0]) break;
+      const int s = i % stages;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(ready + s, static_cast<uint32_t>((i / stages) & 1)))) {
+        if (lane == 0) {
+          report_error(d.err, DEVERR_TIMEOUT, (u0 + i) / H);
+          smisc[0] = 1;
+        }
+        break;
+      }
+      const UnitInfo ui = unit_info(i);
+      unsigned char* st = smem + static_cast<size_t>(SL.size) * s;
+      const float* sc = reinterpret_cast<const float*>(st + SL.scal);
+      if (ui.ok) {
+        const size_t u = static_cast<size_t>(ui.u);
+        const int n = ui.n;
+        const int slot = ring_slot(ui.head, n, C);
+        const uint16_t* kb = reinterpret_cast<const uint16_t*>(st + SL.key);
+        float* yrow = y + u * P;
+        const float4* sT4 = reinterpret_cast<const float4*>(st + SL.tile);
+        float4* gS4 = reinterpret_cast<float4*>(d.ckpt + u * tile);
+        const float4 q4 = bf4(reinterpret_cast<const uint2*>(st + SL.q)[lane]);
+        const float4 kc4 = bf4(reinterpret_cast<const uint2*>(kb + n * N)[lane]);
+        const float gamma = sc[3 * C + 2 * P];
+        if (KIND == 0) {
+          const uint16_t* xb = reinterpret_cast<const uint16_t*>(st + SL.rec);
+          for (int r0 = 0; r0 < RW; r0 += 8) {
+            const int Rq = warp + 8 * (r0 + kq);
+            const bool vq = r0 + kq < RW;
+            // buffered term of row slot kq: lanes 4kq..4kq+3 split the records
+            float ry = 0.f;
+            for (int j0 = 0; j0 <= n; j0 += 4) {
+              const int j = j0 + jl;
+              if (j <= n && vq) ry = fmaf(sc[j], bf(xb[j * P + Rq]), ry);
+            }
+            ry += __shfl_xor_sync(0xffffffffu, ry, 1);
+            ry += __shfl_xor_sync(0xffffffffu, ry, 2);
+            float4 s4[8];
+            float part[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              s4[k] = r0 + k < RW ? sT4[(warp + 8 * (r0 + k)) * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+              part[k] = dot4(s4[k], q4);
+            }
+            const float tot = reduce8(part, lane);
+            if (jl == 0 && vq) {
+              yrow[Rq] = fmaf(gamma, tot, ry);
+              if (!ui.flush) d.r_x[(u * C + slot) * P + Rq] = xb[n * P + Rq];
+            }
+            if (ui.flush) {
+              float4 acc[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) acc[k] = scale4(gamma, s4[k]);
+              for (int j = 0; j <= n; ++j) {
+                const float4 k4 = bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane]);
+                const float c = sc[2 * C + j];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                  if (r0 + k < RW) acc[k] = axpy4x2(c * bf(xb[j * P + warp + 8 * (r0 + k)]), k4, acc[k]);
+              }
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                if (r0 + k < RW) __stcs(gS4 + (warp + 8 * (r0 + k)) * 32 + lane, acc[k]);
+            }
+          }
+          if (!ui.flush && warp == 0) {
+            if (lane == 0) {
+              const uint16_t* dtc = reinterpret_cast<const uint16_t*>(st + SL.chunk);
+              d.r_dt[u * Cp + slot] = dtc[u & 7];
+              d.r_la[u * Cp + slot] = sc[3 * C + 2 * P + 4];
+            }
+            if (ui.h % hpg == 0) {
+              const size_t bg = static_cast<size_t>(ui.b) * G + ui.g;
+              reinterpret_cast<uint2*>(d.r_B + (bg * C + slot) * N)[lane] =
+                  reinterpret_cast<const uint2*>(kb + n * N)[lane];
+            }
+          }
+        } else {
+          const float* ub = reinterpret_cast<const float*>(st + SL.rec);
+          const uint16_t* vb = reinterpret_cast<const uint16_t*>(st + SL.v);
+          const float a = sc[3 * C + 2 * P + 1], beta = sc[3 * C + 2 * P + 2];
+          const float kq_dot = sc[3 * C + 2 * P + 3];
+          float* urow = d.r_u + (u * C + slot) * P;
+          for (int r0 = 0; r0 < RW; r0 += 8) {
+            const int Rq = warp + 8 * (r0 + kq);
+            const bool vq = r0 + kq < RW;
+            float rk = 0.f, rq = 0.f;
+            for (int j0 = 0; j0 < n; j0 += 4) {
+              const int j = j0 + jl;
+              if (j < n && vq) {
+                const float uj = ub[j * P + Rq];
+                rk = fmaf(sc[j], uj, rk);
+                rq = fmaf(sc[C + j], uj, rq);
+              }
+            }
+            rk += __shfl_xor_sync(0xffffffffu, rk, 1);
+            rk += __shfl_xor_sync(0xffffffffu, rk, 2);
+            rq += __shfl_xor_sync(0xffffffffu, rq, 1);
+            rq += __shfl_xor_sync(0xffffffffu, rq, 2);
+            float4 s4[8];
+            float pk[8], pq[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              s4[k] = r0 + k < RW ? sT4[(warp + 8 * (r0 + k)) * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+              pk[k] = dot4(s4[k], kc4);
+              pq[k] = dot4(s4[k], q4);
+            }
+            const float tk = reduce8(pk, lane);
+            const float tq = reduce8(pq, lane);
+            float uu = 0.f;
+            if (vq) {
+              const float Sk = fmaf(gamma, tk, rk);
+              const float Sq = fmaf(gamma, tq, rq);
+              uu = beta * (bf(vb[Rq]) - a * Sk);
+              if (jl == 0) {
+                yrow[Rq] = fmaf(a, Sq, uu * kq_dot);
+                if (!ui.flush) urow[Rq] = uu;
+              }
+            }
+            if (ui.flush) {
+              float4 acc[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                acc[k] = axpy4(__shfl_sync(0xffffffffu, uu, 4 * k), kc4, scale4(a * gamma, s4[k]));
+              for (int j = 0; j < n; ++j) {
+                const float4 k4 = bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane]);
+                const float c = sc[2 * C + j];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                  if (r0 + k < RW) acc[k] = axpy4x2(c * ub[j * P + warp + 8 * (r0 + k)], k4, acc[k]);
+              }
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                if (r0 + k < RW) __stcs(gS4 + (warp + 8 * (r0 + k)) * 32 + lane, acc[k]);
+            }
+          }
+          if (!ui.flush && warp == 0) {
+            const float* chunk = reinterpret_cast<const float*>(st + SL.chunk);
+            if (lane == 0) d.r_g[u * Cp + slot] = chunk[u & 3];
+            if (ui.h % hpg == 0) {
+              const size_t bg = static_cast<size_t>(ui.b) * G + ui.g;
+              reinterpret_cast<uint2*>(d.r_k + (bg * C + slot) * N)[lane] =
+                  reinterpret_cast<const uint2*>(kb + n * N)[lane];
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
+    }
+    return;
+  }
+
   const int c4 = t % SEG;
   int consumed = 0;
   for (int i = 0; i < nunits; ++i) {
@@ -805,7 +1085,7 @@ cudaError_t launch_one(const LayerDev& d, const TokenIn& in, float* y, cudaStrea
   auto kernel = decode_kernel<KIND, N, READ>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kDecodeThreads, smem, s>>>(d, in, y, per, stages);
+  kernel<<<grid, decode_threads<N, READ>(), smem, s>>>(d, in, y, per, stages);
   return cudaGetLastError();
 }
 
