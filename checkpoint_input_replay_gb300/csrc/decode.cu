@@ -223,23 +223,6 @@ constexpr int decode_threads() {
   return kThreads + ((N == 128 && READ == READ_NONE) ? 64 : 32);
 }
 
-__device__ __forceinline__ bool compute_sync_and(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, %2, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(v)), "n"(kThreads)
-      : "memory");
-  return r != 0;
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 // Sum each of v[0..7] over the 32 lanes of the warp (transpose-reduce: 9
 // shuffles).  Lane L returns the total of v[(L >> 2) & 7].
 __device__ __forceinline__ float reduce8(const float v[8], int lane) {
@@ -262,17 +245,6 @@ __device__ __forceinline__ float reduce8(const float v[8], int lane) {
   z += __shfl_xor_sync(0xffffffffu, z, 2);
   z += __shfl_xor_sync(0xffffffffu, z, 1);
   return z;
-}
-
-// Inclusive suffix sum over lanes 0..last of one value per lane (lanes past
-// `last` contribute nothing).
-__device__ __forceinline__ float suffix_sum(float v, int lane, int last) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float w = __shfl_down_sync(0xffffffffu, v, o);
-    if (lane + o <= last) v += w;
-  }
-  return v;
 }
 
 template <int KIND, int N, int READ>
@@ -612,15 +584,28 @@ __global__ void __launch_bounds__(decode_threads<N, READ>(), 1) decode_kernel(co
               if (!ui.flush) d.r_x[(u * C + slot) * P + Rq] = xb[n * P + Rq];
             }
             if (ui.flush) {
+              // lane (kq, jl) holds m_j[Rq] = w_j dt_j x_j[Rq] for records j = 4 jc + jl
+              float mreg[kMaxRec / 4];
+#pragma unroll
+              for (int jc = 0; jc < kMaxRec / 4; ++jc) {
+                const int j = 4 * jc + jl;
+                mreg[jc] = (j <= n && vq) ? sc[2 * C + j] * bf(xb[j * P + Rq]) : 0.f;
+              }
               float4 acc[8];
 #pragma unroll
               for (int k = 0; k < 8; ++k) acc[k] = scale4(gamma, s4[k]);
-              for (int j = 0; j <= n; ++j) {
-                const float4 k4 = bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane]);
-                const float c = sc[2 * C + j];
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                  if (r0 + k < RW) acc[k] = axpy4x2(c * bf(xb[j * P + warp + 8 * (r0 + k)]), k4, acc[k]);
+              for (int jc = 0; jc < kMaxRec / 4; ++jc) {
+                if (4 * jc > n) break;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                  const int j = 4 * jc + jj;
+                  if (j > n) break;
+                  const float4 k4 = bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane]);
+#pragma unroll
+                  for (int k = 0; k < 8; ++k)
+                    acc[k] = axpy4x2(__shfl_sync(0xffffffffu, mreg[jc], 4 * k + jj), k4, acc[k]);
+                }
               }
 #pragma unroll
               for (int k = 0; k < 8; ++k)
@@ -682,16 +667,29 @@ __global__ void __launch_bounds__(decode_threads<N, READ>(), 1) decode_kernel(co
               }
             }
             if (ui.flush) {
+              // lane (kq, jl) holds m_j[Rq] = a w_j u_j[Rq] for records j = 4 jc + jl
+              float mreg[kMaxRec / 4];
+#pragma unroll
+              for (int jc = 0; jc < kMaxRec / 4; ++jc) {
+                const int j = 4 * jc + jl;
+                mreg[jc] = (j < n && vq) ? sc[2 * C + j] * ub[j * P + Rq] : 0.f;
+              }
               float4 acc[8];
 #pragma unroll
               for (int k = 0; k < 8; ++k)
                 acc[k] = axpy4(__shfl_sync(0xffffffffu, uu, 4 * k), kc4, scale4(a * gamma, s4[k]));
-              for (int j = 0; j < n; ++j) {
-                const float4 k4 = bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane]);
-                const float c = sc[2 * C + j];
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                  if (r0 + k < RW) acc[k] = axpy4x2(c * ub[j * P + warp + 8 * (r0 + k)], k4, acc[k]);
+              for (int jc = 0; jc < kMaxRec / 4; ++jc) {
+                if (4 * jc >= n) break;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                  const int j = 4 * jc + jj;
+                  if (j >= n) break;
+                  const float4 k4 = bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane]);
+#pragma unroll
+                  for (int k = 0; k < 8; ++k)
+                    acc[k] = axpy4x2(__shfl_sync(0xffffffffu, mreg[jc], 4 * k + jj), k4, acc[k]);
+                }
               }
 #pragma unroll
               for (int k = 0; k < 8; ++k)
