@@ -46,6 +46,17 @@ __device__ __forceinline__ float seg_max(float v) {
   return v;
 }
 
+// Inclusive suffix sum over lanes 0..last of one value per lane (lanes past
+// `last` contribute nothing).
+__device__ __forceinline__ float suffix_sum(float v, int lane, int last) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float w = __shfl_down_sync(0xffffffffu, v, o);
+    if (lane + o <= last) v += w;
+  }
+  return v;
+}
+
 __device__ __forceinline__ float dot4(const float4 a, const float4 b) {
   return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, a.x * b.x)));
 }
@@ -99,6 +110,25 @@ __device__ __forceinline__ bool arrive_last(int* arrive, int b, int nctas) {
   return false;
 }
 
+// ---- barriers among the kThreads computing threads (named barrier 1) ---------
+// Kernels with a producer warp keep it out of these.
+
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
+// Barrier that also returns whether `v` held in every computing thread.
+__device__ __forceinline__ bool compute_sync_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "n"(kThreads)
+      : "memory");
+  return r != 0;
+}
+
 // ---- mbarrier + bulk copy (cp.async.bulk, the untiled TMA path) -------------
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -108,6 +138,10 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {

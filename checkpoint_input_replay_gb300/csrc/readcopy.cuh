@@ -17,10 +17,6 @@
 
 namespace rs {
 
-// Barrier among the kThreads threads that compute (named barrier 1): the
-// decode kernel adds a producer warp that does not take part.
-__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
-
 // sT: folded matrix [P][N] f32 in shared memory; sred: kThreads/32 floats.
 // Called by the kThreads computing threads (threads 0..kThreads-1) of the CTA.
 template <int N, int READ>
