@@ -100,8 +100,8 @@ __host__ __device__ __forceinline__ Persist persist_layout(int P, int N, int C) 
   p.coef = o;   o += C * P;      // flush coefficients [C][P]
   p.red = o;    o += kThreads / 32;
   p.misc = o;   o += 4;
-  p.bars = (o + 3) & ~3;         // 16-byte aligned: 8 full + 8 empty + 8 ready mbarriers (u64)
-  o = p.bars + 2 * 24;
+  p.bars = (o + 3) & ~3;         // 16-byte aligned: 8 full, empty, ready, amax mbarriers (u64)
+  o = p.bars + 2 * 32;
   p.seq = o;    o += 3 * kMaxSeq;  // cached cursors: head, count, ok
   p.size_floats = o;
   return p;
@@ -220,7 +220,7 @@ __device__ __forceinline__ void rc_rows_nvfp4(const unsigned char* sC, const uns
 // 8 computing warps + 1 producer warp, + 1 prologue warp on the warp-local path
 template <int N, int READ>
 constexpr int decode_threads() {
-  return kThreads + ((N == 128 && READ == READ_NONE) ? 64 : 32);
+  return kThreads + (N == 128 ? 64 : 32);
 }
 
 // Sum each of v[0..7] over the 32 lanes of the warp (transpose-reduce: 9
@@ -252,8 +252,8 @@ __global__ void __launch_bounds__(decode_threads<N, READ>(), 1) decode_kernel(co
                                                                    float* __restrict__ y, const int units_per_cta,
                                                                    const int stages) {
   constexpr int SEG = N / 4;  // lanes per state row, one float4 each
-  // d_state 128 without a read copy: every warp computes its rows of a unit on its own
-  constexpr bool kWarpLocal = (N == 128 && READ == READ_NONE);
+  // d_state 128: every warp computes its rows of a unit on its own
+  constexpr bool kWarpLocal = (N == 128);
   extern __shared__ __align__(1024) unsigned char smem[];
 
   const int P = d.P, H = d.H, G = d.G, C = d.C, L = d.L, Cp = d.Cp;
@@ -276,6 +276,7 @@ __global__ void __launch_bounds__(decode_threads<N, READ>(), 1) decode_kernel(co
   uint64_t* full = reinterpret_cast<uint64_t*>(pf + PL.bars);
   uint64_t* empty = full + 8;
   uint64_t* ready = full + 16;
+  uint64_t* amaxbar = full + 24;  // NVFP4 flush units: the eight computing warps exchange the matrix amax
   int* sseq = reinterpret_cast<int*>(pf + PL.seq);
 
   const int total_units = d.B * H;
@@ -317,6 +318,7 @@ __global__ void __launch_bounds__(decode_threads<N, READ>(), 1) decode_kernel(co
       mbar_init(full + s, 1);
       mbar_init(empty + s, kWarpLocal ? kThreads / 32 : 1);
       mbar_init(ready + s, 1);
+      mbar_init(amaxbar + s, kThreads / 32);
     }
     smisc[0] = 0;  // abort
     smisc[1] = 0;  // units issued
@@ -518,6 +520,7 @@ __global__ void __launch_bounds__(decode_threads<N, READ>(), 1) decode_kernel(co
             }
           }
         }
+        if (lane == 0) reinterpret_cast<int*>(sc)[3 * C + 2 * P + 6] = 0;  // NVFP4 matrix amax slot
         __syncwarp();
         if (lane == 0) mbar_arrive(ready + s);
       }
@@ -534,6 +537,8 @@ __global__ void __launch_bounds__(decode_threads<N, READ>(), 1) decode_kernel(co
     }
     // ===================== computing warps =====================
     // warp w owns rows w, w+8, ..; lane = column chunk; no barrier across warps
+    // (an NVFP4 flush unit exchanges its matrix amax through a bounded mbarrier)
+    uint32_t amax_phase = 0;
     for (int i = 0; i < nunits; ++i) {
       if (smisc[0]) break;
       const int s = i % stages;
@@ -553,7 +558,7 @@ __global__ void __launch_bounds__(decode_threads<N, READ>(), 1) decode_kernel(co
         const int slot = ring_slot(ui.head, n, C);
         const uint16_t* kb = reinterpret_cast<const uint16_t*>(st + SL.key);
         float* yrow = y + u * P;
-        const float4* sT4 = reinterpret_cast<const float4*>(st + SL.tile);
+        float4* sT4 = reinterpret_cast<float4*>(st + SL.tile);
         float4* gS4 = reinterpret_cast<float4*>(d.ckpt + u * tile);
         const float4 q4 = bf4(reinterpret_cast<const uint2*>(st + SL.q)[lane]);
         const float4 kc4 = bf4(reinterpret_cast<const uint2*>(kb + n * N)[lane]);
@@ -573,14 +578,46 @@ __global__ void __launch_bounds__(decode_threads<N, READ>(), 1) decode_kernel(co
             ry += __shfl_xor_sync(0xffffffffu, ry, 2);
             float4 s4[8];
             float part[8];
+            float row_scale = 1.f;  // read-copy scale of row slot kq
+            if (READ != READ_NONE && !ui.flush) {
+              // non-flush: the checkpoint term from the low-precision copy
+              const unsigned char* cb = st + SL.tile;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              s4[k] = r0 + k < RW ? sT4[(warp + 8 * (r0 + k)) * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-              part[k] = dot4(s4[k], q4);
+              for (int k = 0; k < 8; ++k) {
+                const int R = warp + 8 * (r0 + k);
+                float pv = 0.f;
+                if (r0 + k < RW) {
+                  if (READ == READ_FP8) {
+                    const uint32_t w = reinterpret_cast<const uint32_t*>(cb + R * N)[lane];
+                    const float2 lo = e4m3x2_to_f32x2(static_cast<uint16_t>(w & 0xFFFFu));
+                    const float2 hi = e4m3x2_to_f32x2(static_cast<uint16_t>(w >> 16));
+                    pv = dot4(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
+                  } else {
+                    const uint32_t w = reinterpret_cast<const uint16_t*>(cb + R * (N / 2))[lane];
+                    const float2 lo = e2m1x2_to_f32x2(w & 0xFFu);
+                    const float2 hi = e2m1x2_to_f32x2(w >> 8);
+                    const float bs = e4m3_to_f32(cb[P * (N / 2) + R * (N / 16) + (lane >> 2)]);
+                    pv = bs * dot4(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
+                  }
+                }
+                part[k] = pv;
+              }
+              if (vq) {
+                if (READ == READ_FP8)
+                  row_scale = reinterpret_cast<const float*>(cb + P * N)[Rq];
+                else
+                  row_scale = reinterpret_cast<const float*>(st + SL.chunk)[8 + (u & 3)];
+              }
+            } else {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                s4[k] = r0 + k < RW ? sT4[(warp + 8 * (r0 + k)) * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+                part[k] = dot4(s4[k], q4);
+              }
             }
             const float tot = reduce8(part, lane);
             if (jl == 0 && vq) {
-              yrow[Rq] = fmaf(gamma, tot, ry);
+              yrow[Rq] = fmaf(gamma * row_scale, tot, ry);
               if (!ui.flush) d.r_x[(u * C + slot) * P + Rq] = xb[n * P + Rq];
             }
             if (ui.flush) {
@@ -608,8 +645,79 @@ __global__ void __launch_bounds__(decode_threads<N, READ>(), 1) decode_kernel(co
                 }
               }
 #pragma unroll
-              for (int k = 0; k < 8; ++k)
-                if (r0 + k < RW) __stcs(gS4 + (warp + 8 * (r0 + k)) * 32 + lane, acc[k]);
+              for (int k = 0; k < 8; ++k) {
+                if (r0 + k < RW) {
+                  __stcs(gS4 + (warp + 8 * (r0 + k)) * 32 + lane, acc[k]);
+                  if (READ != READ_NONE) sT4[(warp + 8 * (r0 + k)) * 32 + lane] = acc[k];
+                }
+              }
+            }
+          }
+          if (READ != READ_NONE && ui.flush) {
+            // refresh the read copy of this warp's rows from the folded rows in shared memory
+            if (READ == READ_FP8) {
+              uint32_t* codes = reinterpret_cast<uint32_t*>(d.rc_codes + u * tile);
+              for (int m = 0; m < RW; ++m) {
+                const int R = warp + 8 * m;
+                const float4 v4 = sT4[R * 32 + lane];
+                float mx = fmaxf(fmaxf(fabsf(v4.x), fabsf(v4.y)), fmaxf(fabsf(v4.z), fabsf(v4.w)));
+                mx = seg_max<32>(mx);
+                const float scale = __fdiv_rn(mx, 448.0f);
+                uint32_t packed = 0;
+                if (scale != 0.0f) {
+                  const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(v4.x, scale), __fdiv_rn(v4.y, scale));
+                  const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(v4.z, scale), __fdiv_rn(v4.w, scale));
+                  packed = lo | (hi << 16);
+                }
+                codes[R * 32 + lane] = packed;
+                if (lane == 0) d.rc_rowscale[u * P + R] = scale;
+              }
+            } else {
+              float mloc = 0.f;
+              for (int m = 0; m < RW; ++m) {
+                const float4 v4 = sT4[(warp + 8 * m) * 32 + lane];
+                mloc = fmaxf(mloc, fmaxf(fmaxf(fabsf(v4.x), fabsf(v4.y)), fmaxf(fabsf(v4.z), fabsf(v4.w))));
+              }
+              mloc = seg_max<32>(mloc);
+              volatile int* slot_amax = reinterpret_cast<volatile int*>(
+                  reinterpret_cast<int*>(st + SL.scal) + 3 * C + 2 * P + 6);
+              if (lane == 0) {
+                atomicMax(const_cast<int*>(slot_amax), __float_as_int(mloc));  // non-negative floats order as ints
+                __threadfence_block();
+              }
+              __syncwarp();
+              if (lane == 0) mbar_arrive(amaxbar + s);
+              const bool got = __all_sync(0xffffffffu,
+                                          mbar_wait_bounded(amaxbar + s, (amax_phase >> s) & 1u));
+              amax_phase ^= 1u << s;
+              if (!got) {
+                if (lane == 0) {
+                  report_error(d.err, DEVERR_TIMEOUT, ui.b);
+                  smisc[0] = 1;
+                }
+              } else {
+                const float amax = __int_as_float(*slot_amax);
+                const float smat = __fdiv_rn(amax, 2688.0f);  // 448 * 6
+                const float six_s = __fmul_rn(6.0f, smat);
+                uint16_t* codes = reinterpret_cast<uint16_t*>(d.rc_codes + u * (tile / 2));
+                uint8_t* blk = d.rc_blkscale + u * (tile / 16);
+                for (int m = 0; m < RW; ++m) {
+                  const int R = warp + 8 * m;
+                  const float4 v4 = sT4[R * 32 + lane];
+                  float mb = fmaxf(fmaxf(fabsf(v4.x), fabsf(v4.y)), fmaxf(fabsf(v4.z), fabsf(v4.w)));
+                  mb = seg_max<4>(mb);  // 4 lanes = one 16-element block
+                  uint32_t bcode = 0;
+                  if (six_s != 0.0f) bcode = f32x2_to_e4m3x2(__fdiv_rn(mb, six_s), 0.0f) & 0xFFu;
+                  const float dd = __fmul_rn(e4m3_to_f32(bcode), smat);
+                  uint32_t q = 0;
+                  if (dd != 0.0f)
+                    q = f32x4_to_e2m1x4(__fdiv_rn(v4.x, dd), __fdiv_rn(v4.y, dd), __fdiv_rn(v4.z, dd),
+                                        __fdiv_rn(v4.w, dd));
+                  codes[R * 32 + lane] = static_cast<uint16_t>(q);
+                  if ((lane & 3) == 0) blk[R * (N / 16) + (lane >> 2)] = static_cast<uint8_t>(bcode);
+                }
+                if (warp == 0 && lane == 0) d.rc_matscale[u] = smat;
+              }
             }
           }
           if (!ui.flush && warp == 0) {
