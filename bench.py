@@ -52,7 +52,7 @@ def peaks():
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
-    for f in ("decode.cu", "common.cuh", "internal.h"):
+    for f in ("decode128.cu", "common.cuh", "internal.h"):
         h.update(open(os.path.join(ROOT, "checkpoint_input_replay_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 

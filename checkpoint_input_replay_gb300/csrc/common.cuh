@@ -234,4 +234,28 @@ __device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
   return __half22float2(hv);
 }
 
+// Sum each of v[0..7] over the 32 lanes of the warp (transpose-reduce: 9
+// shuffles).  Lane L returns the total of v[(L >> 2) & 7].
+__device__ __forceinline__ float reduce8(const float v[8], int lane) {
+  const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
+  float w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = b4 ? v[i] : v[i + 4];
+    const float keep = b4 ? v[i + 4] : v[i];
+    w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+  float x[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = b3 ? w[i] : w[i + 2];
+    const float keep = b3 ? w[i + 2] : w[i];
+    x[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  float z = (b2 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, b2 ? x[0] : x[1], 4);
+  z += __shfl_xor_sync(0xffffffffu, z, 2);
+  z += __shfl_xor_sync(0xffffffffu, z, 1);
+  return z;
+}
+
 }  // namespace rs

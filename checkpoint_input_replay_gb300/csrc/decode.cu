@@ -223,30 +223,6 @@ constexpr int decode_threads() {
   return kThreads + (N == 128 ? 64 : 32);
 }
 
-// Sum each of v[0..7] over the 32 lanes of the warp (transpose-reduce: 9
-// shuffles).  Lane L returns the total of v[(L >> 2) & 7].
-__device__ __forceinline__ float reduce8(const float v[8], int lane) {
-  const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
-  float w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float send = b4 ? v[i] : v[i + 4];
-    const float keep = b4 ? v[i + 4] : v[i];
-    w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-  }
-  float x[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float send = b3 ? w[i] : w[i + 2];
-    const float keep = b3 ? w[i + 2] : w[i];
-    x[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-  }
-  float z = (b2 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, b2 ? x[0] : x[1], 4);
-  z += __shfl_xor_sync(0xffffffffu, z, 2);
-  z += __shfl_xor_sync(0xffffffffu, z, 1);
-  return z;
-}
-
 template <int KIND, int N, int READ>
 __global__ void __launch_bounds__(decode_threads<N, READ>(), 1) decode_kernel(const LayerDev d, const TokenIn in,
                                                                    float* __restrict__ y, const int units_per_cta,
@@ -1211,6 +1187,8 @@ size_t decode_smem_bytes(const LayerDev& d) {
 }
 
 cudaError_t launch_decode(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s) {
+  // d_state 128 with a group buffer that fits: the grouped kernel (decode128.cu)
+  if (d.N == 128 && decode128_smem_bytes(d) <= 227u * 1024) return launch_decode128(d, in, y, s);
   if (d.kind == 0) {
     switch (d.N) {
       case 16: return launch_kn<0, 16>(d, in, y, s);
