@@ -1187,8 +1187,8 @@ size_t decode_smem_bytes(const LayerDev& d) {
 }
 
 cudaError_t launch_decode(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s) {
-  // d_state 128 with a group buffer that fits: the grouped kernel (decode128.cu)
-  if (d.N == 128 && decode128_smem_bytes(d) <= 227u * 1024) return launch_decode128(d, in, y, s);
+  // d_state 128, d_head 64 or 128: the grouped kernel (decode128.cu)
+  if (decode128_supports(d)) return launch_decode128(d, in, y, s);
   if (d.kind == 0) {
     switch (d.N) {
       case 16: return launch_kn<0, 16>(d, in, y, s);

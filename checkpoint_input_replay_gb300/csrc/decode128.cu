@@ -1,21 +1,23 @@
-// Standard decode step for d_state = 128 (every configuration the workloads
-// measure): the output-only non-flush body and the flush body, per sequence,
-// in one persistent launch.  Same arithmetic as decode.cu (the unrolled
-// checkpoint-plus-buffer form of "ReplaySSM caches SSM inputs instead of
-// state" (richland.au), "What shipped"); this file differs in how the work is
-// fed and split:
+// Standard decode step for d_state = 128 and d_head 64 or 128 (the layer
+// shapes the workloads use): the output-only non-flush body and the flush
+// body, per sequence, in one persistent launch.  Same arithmetic as decode.cu
+// (the unrolled checkpoint-plus-buffer form of "ReplaySSM caches SSM inputs
+// instead of state" (richland.au), "What shipped"); this file differs in how
+// the work is fed and split, so that the computing warps do little besides the
+// pass over the state matrix:
 //
 //  * a work unit is one (sequence, head) state matrix [P][128]; CTA c owns a
 //    contiguous range of units, so it meets each group (and sequence) once;
 //  * a producer warp stages each unit with two bulk copies (cp.async.bulk):
 //    the state matrix (or its read copy) and the buffered records of that
-//    head.  Everything the heads of a group share or that is small -- the
-//    group's keys and query, the current tokens of all its heads, the ring's
-//    per-head decay rows, the current per-head scalars, the read-copy scales --
-//    is staged once per group into one of two group buffers;
-//  * a prologue warp turns each unit into scalars (key dot products once per
-//    group, the decay suffix scan, per-record coefficients) and signals
-//    `ready`;
+//    head.  What the heads of a group share, or what is small -- the group's
+//    keys and query, the current tokens of all its heads, the ring's per-head
+//    decay rows, the current per-head scalars, the read-copy scales -- is
+//    staged once per group into one of two group buffers;
+//  * a prologue warp, once per group, computes the key dot products, each
+//    head's decay suffix scan and its per-record coefficient table (into the
+//    group buffer), and appends the group's current token to the ring; per
+//    unit it only publishes a 16-byte descriptor and signals `ready`;
 //  * eight computing warps each own rows w, w+8, .. of every unit: lane = 4
 //    columns, 4 lanes per row split the buffered records, an 8-row
 //    transpose-reduce forms the row sums.  A flush unit folds in registers
@@ -31,17 +33,21 @@ constexpr int N = 128;               // d_state of this kernel
 constexpr int SEG = N / 4;           // lanes per state row (one float4 each)
 constexpr int kMaxSeq128 = 64;       // sequences one CTA may cover
 constexpr int kThreads128 = kThreads + 64;  // 8 computing warps, prologue warp, producer warp
+constexpr int kPrologueWarp = kThreads / 32;
+constexpr int kProducerWarp = kThreads / 32 + 1;
 
 __host__ __device__ __forceinline__ int al16(int x) { return (x + 15) & ~15; }
 __host__ __device__ __forceinline__ int al128(int x) { return (x + 127) & ~127; }
+// floats per head in a coefficient table: 3 rows of C record coefficients, 8 scalars
+__host__ __device__ __forceinline__ int coef_stride(int C) { return (3 * C + 8 + 3) & ~3; }
+
+// per-head scalars after the 3C record coefficients
+enum : int { CO_GAMMA = 0, CO_A = 1, CO_BETA = 2, CO_KQ = 3, CO_MATSCALE = 4 };
 
 // Shared-memory layout (bytes): [stages][2 group buffers][persistent].
 struct Lay128 {
-  // stage
-  int st_tile, st_rec, st_scal, st_size;
-  // group buffer
-  int gb_key, gb_q, gb_cur, gb_la, gb_dt, gb_s1, gb_s2, gb_rs, gb_ms, gb_size;
-  // persistent
+  int st_tile, st_rec, st_meta, st_size;
+  int gb_key, gb_q, gb_cur, gb_la, gb_dt, gb_s1, gb_s2, gb_rs, gb_ms, gb_qf, gb_kf, gb_coef, gb_size;
   int pe_A, pe_bars, pe_seq, pe_misc, pe_size;
 };
 
@@ -50,7 +56,7 @@ __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int
   int o = 0;
   l.st_tile = o;  o += P * N * 4;
   l.st_rec = o;   o += kind == 0 ? al16(C * P * 2) : C * P * 4;
-  l.st_scal = o;  o += al16((3 * C + 2 * P + 8) * 4);
+  l.st_meta = o;  o += 32;              // int4 descriptor, NVFP4 amax word
   l.st_size = al128(o);
   o = 0;
   const int span = al16(hpg * 4) + 16;
@@ -63,6 +69,9 @@ __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int
   l.gb_s2 = o;    o += kind == 0 ? 0 : span;
   l.gb_rs = o;    o += read == READ_FP8 ? hpg * P * 4 : (read == READ_NVFP4 ? hpg * P * (N / 16) : 0);
   l.gb_ms = o;    o += read == READ_NVFP4 ? span : 0;
+  l.gb_qf = o;    o += N * 4;
+  l.gb_kf = o;    o += kind == 0 ? 0 : N * 4;
+  l.gb_coef = o;  o += hpg * coef_stride(C) * 4;
   l.gb_size = al128(o);
   o = 0;
   l.pe_A = o;     o += al16(H * 4);
@@ -78,19 +87,42 @@ __device__ __forceinline__ int ring_slot(int head, int j, int C) {
   return s >= C ? s - C : s;
 }
 
-struct Unit {
-  int u, b, h, g, hh, k, head, n;
-  bool ok, flush, first;
+// Position of a unit in (sequence, head, group, head-in-group), advanced one
+// unit at a time so that no role divides per unit.
+struct Walk {
+  int u, b, h, g, hh;
+  __device__ __forceinline__ void start(int u0, int H, int hpg) {
+    u = u0;
+    b = u0 / H;
+    h = u0 - b * H;
+    g = h / hpg;
+    hh = h - g * hpg;
+  }
+  __device__ __forceinline__ void next(int H, int hpg) {
+    ++u;
+    ++h;
+    if (++hh == hpg) {
+      hh = 0;
+      ++g;
+    }
+    if (h == H) {
+      h = 0;
+      g = 0;
+      ++b;
+    }
+  }
 };
 
-template <int KIND, int READ>
+template <int KIND, int READ, int P>
 __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDev d, const TokenIn in,
                                                                    float* __restrict__ y, const int units_per_cta,
                                                                    const int stages) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  const int P = d.P, H = d.H, G = d.G, C = d.C, L = d.L, Cp = d.Cp;
+  constexpr int RW = P / 8;  // rows per computing warp
+  constexpr int tile = P * N;
+  const int H = d.H, G = d.G, C = d.C, L = d.L, Cp = d.Cp;
   const int hpg = H / G;
-  const int tile = P * N;
+  const int CS = coef_stride(C);
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const Lay128 LY = lay128(KIND, READ, P, C, Cp, H, hpg);
   unsigned char* gbase = smem + static_cast<size_t>(LY.st_size) * stages;
@@ -117,8 +149,8 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     const int head = d.cursor[4 * b], cnt = d.cursor[4 * b + 1];
     const bool ok = static_cast<unsigned>(head) < static_cast<unsigned>(C) &&
                     static_cast<unsigned>(cnt) < static_cast<unsigned>(L);
-    sseq[3 * t] = head;
-    sseq[3 * t + 1] = cnt;
+    sseq[3 * t] = ok ? head : 0;  // a rejected cursor stages nothing from the ring
+    sseq[3 * t + 1] = ok ? cnt : 0;
     sseq[3 * t + 2] = ok ? 1 : 0;
     const int lo = max(u0, b * H), hi = min(u1, (b + 1) * H);
     __threadfence();
@@ -150,52 +182,39 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   }
   __syncthreads();
 
-  auto unit_of = [&](int i) {
-    Unit v;
-    v.u = u0 + i;
-    v.b = v.u / H;
-    v.h = v.u - v.b * H;
-    v.g = v.h / hpg;
-    v.hh = v.h - v.g * hpg;
-    v.k = v.b - b0;
-    v.ok = sseq[3 * v.k + 2] != 0;
-    v.head = v.ok ? sseq[3 * v.k] : 0;  // a rejected cursor stages nothing from the ring
-    const int cnt = sseq[3 * v.k + 1];
-    v.n = v.ok ? cnt : 0;
-    v.flush = v.ok && (cnt + 1 == L);
-    v.first = (i == 0) || (v.hh == 0);
-    return v;
-  };
   // first element of the 16-byte block holding element e, for 2-byte / 4-byte arrays
   auto blk2 = [](size_t e) { return e & ~static_cast<size_t>(7); };
   auto blk4 = [](size_t e) { return e & ~static_cast<size_t>(3); };
 
   // =============================== producer warp ===============================
-  if (warp == kThreads / 32 + 1) {
+  if (warp == kProducerWarp) {
     if (lane != 0) return;
+    Walk w;
+    w.start(u0, H, hpg);
     int gi = -1;
-    for (int i = 0; i < nunits; ++i) {
+    for (int i = 0; i < nunits; ++i, w.next(H, hpg)) {
       const int s = i % stages;
       if (i >= stages && !mbar_wait_bounded(empty + s, static_cast<uint32_t>(((i / stages) - 1) & 1))) break;
       if (smisc[0]) break;
-      const Unit v = unit_of(i);
-      if (v.first) ++gi;
+      const bool first = i == 0 || w.hh == 0;
+      if (first) ++gi;
+      const int k = w.b - b0;
+      const int head = sseq[3 * k], n = sseq[3 * k + 1];
+      const bool flush = sseq[3 * k + 2] != 0 && n + 1 == L;
       unsigned char* st = smem + static_cast<size_t>(LY.st_size) * s;
       unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * (gi & 1);
       uint64_t* bar = full + s;
-      const size_t u = static_cast<size_t>(v.u);
-      const int n = v.n;
-      const int seg1 = min(n, C - v.head), seg2 = n - seg1;
-      const int esz = KIND == 0 ? 2 : 4;
-      const uint32_t tb = (READ == READ_NONE || v.flush) ? tile * 4 : (READ == READ_FP8 ? tile : tile / 2);
+      const size_t u = static_cast<size_t>(w.u);
+      const int seg1 = min(n, C - head), seg2 = n - seg1;
+      constexpr int esz = KIND == 0 ? 2 : 4;
+      const uint32_t tb = (READ == READ_NONE || flush) ? tile * 4 : (READ == READ_FP8 ? tile : tile / 2);
       uint32_t bytes = tb + static_cast<uint32_t>(n) * P * esz;
-      // group data (first unit of a group in this CTA)
-      const size_t ug = static_cast<size_t>(v.b) * H + static_cast<size_t>(v.g) * hpg;  // first unit of the group
-      const size_t bg = static_cast<size_t>(v.b) * G + v.g;
+      const size_t ug = static_cast<size_t>(w.b) * H + static_cast<size_t>(w.g) * hpg;  // first unit of the group
+      const size_t bg = static_cast<size_t>(w.b) * G + w.g;
       const uint32_t s1b = KIND == 0 ? static_cast<uint32_t>((blk2(ug + hpg + 7) - blk2(ug)) * 2)
                                      : static_cast<uint32_t>((blk4(ug + hpg + 3) - blk4(ug)) * 4);
       const uint32_t s4b = static_cast<uint32_t>((blk4(ug + hpg + 3) - blk4(ug)) * 4);
-      if (v.first) {
+      if (first) {
         bytes += static_cast<uint32_t>(n + 1) * N * 2 + N * 2 + hpg * P * 2 + hpg * Cp * 4 + s1b;
         if (KIND == 0) bytes += hpg * Cp * 2;
         else bytes += s4b;
@@ -205,17 +224,17 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       if (KIND == 0 && i == 0) bytes += al16(H * 4);  // A (Mamba-2 only)
       mbar_expect_tx(bar, bytes);
       // the unit: state matrix (or read copy) and this head's buffered records
-      if (READ == READ_NONE || v.flush) bulk_g2s(st + LY.st_tile, d.ckpt + u * tile, tb, bar);
+      if (READ == READ_NONE || flush) bulk_g2s(st + LY.st_tile, d.ckpt + u * tile, tb, bar);
       else bulk_g2s(st + LY.st_tile, d.rc_codes + u * tb, tb, bar);
       const unsigned char* rsrc = KIND == 0 ? reinterpret_cast<const unsigned char*>(d.r_x)
                                             : reinterpret_cast<const unsigned char*>(d.r_u);
-      const size_t rrow = static_cast<size_t>(P) * esz;
-      if (seg1) bulk_g2s(st + LY.st_rec, rsrc + (u * C + v.head) * rrow, seg1 * rrow, bar);
+      constexpr size_t rrow = static_cast<size_t>(P) * esz;
+      if (seg1) bulk_g2s(st + LY.st_rec, rsrc + (u * C + head) * rrow, seg1 * rrow, bar);
       if (seg2) bulk_g2s(st + LY.st_rec + seg1 * rrow, rsrc + u * C * rrow, seg2 * rrow, bar);
       // the group: keys and query, current tokens, decay rows, scalars, scales
-      if (v.first) {
+      if (first) {
         const uint16_t* rk = (KIND == 0 ? d.r_B : d.r_k) + bg * C * N;
-        if (seg1) bulk_g2s(gb + LY.gb_key, rk + static_cast<size_t>(v.head) * N, seg1 * N * 2, bar);
+        if (seg1) bulk_g2s(gb + LY.gb_key, rk + static_cast<size_t>(head) * N, seg1 * N * 2, bar);
         if (seg2) bulk_g2s(gb + LY.gb_key + seg1 * N * 2, rk, seg2 * N * 2, bar);
         bulk_g2s(gb + LY.gb_key + n * N * 2, (KIND == 0 ? in.Bm : in.k) + bg * N, N * 2, bar);
         bulk_g2s(gb + LY.gb_q, (KIND == 0 ? in.Cm : in.q) + bg * N, N * 2, bar);
@@ -242,99 +261,131 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     return;
   }
 
-  const int RW = P / 8;  // rows per computing warp
   const int kq = (lane >> 2) & 7, jl = lane & 3;
 
   // =============================== prologue warp ===============================
-  if (warp == kThreads / 32) {
-    float dq = 0.f, dk = 0.f;  // lane j: k_j . q, k_j . k_cur of the current group
+  if (warp == kPrologueWarp) {
+    Walk w;
+    w.start(u0, H, hpg);
     int gi = -1, consumed = 0;
-    for (int i = 0; i < nunits; ++i) {
+    for (int i = 0; i < nunits; ++i, w.next(H, hpg)) {
       if (smisc[0]) break;
       const int s = i % stages;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(full + s, static_cast<uint32_t>((i / stages) & 1)))) {
         if (lane == 0) {
-          report_error(d.err, DEVERR_TIMEOUT, (u0 + i) / H);
+          report_error(d.err, DEVERR_TIMEOUT, w.b);
           smisc[0] = 1;
         }
         break;
       }
       consumed = i + 1;
-      const Unit v = unit_of(i);
-      if (v.first) ++gi;
-      unsigned char* st = smem + static_cast<size_t>(LY.st_size) * s;
-      const unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * (gi & 1);
-      float* sc = reinterpret_cast<float*>(st + LY.st_scal);
-      if (v.ok) {
-        const int n = v.n;
-        const int slot_lane = lane < n ? ring_slot(v.head, lane, C) : 0;
-        const float* la_row = reinterpret_cast<const float*>(gb + LY.gb_la) + v.hh * Cp;
-        const size_t ug = static_cast<size_t>(v.b) * H + static_cast<size_t>(v.g) * hpg;
-        if (v.first) {
-          const uint16_t* kb = reinterpret_cast<const uint16_t*>(gb + LY.gb_key);
-          const float4 q4 = bf4(reinterpret_cast<const uint2*>(gb + LY.gb_q)[lane]);
-          const float4 kc4 = bf4(reinterpret_cast<const uint2*>(kb + n * N)[lane]);
-          for (int j0 = 0; j0 <= n; j0 += 8) {
-            float pq[8], pk[8];
+      const bool first = i == 0 || w.hh == 0;
+      if (first) ++gi;
+      const int k = w.b - b0;
+      const int head = sseq[3 * k], n = sseq[3 * k + 1];
+      const bool ok = sseq[3 * k + 2] != 0;
+      const bool flush = ok && n + 1 == L;
+      const int slot = ring_slot(head, n, C);
+      unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * (gi & 1);
+      if (first && ok) {
+        // ---- once per group: dot products, coefficient tables, ring appends ----
+        const size_t ug = static_cast<size_t>(w.b) * H + static_cast<size_t>(w.g) * hpg;
+        const uint16_t* kb = reinterpret_cast<const uint16_t*>(gb + LY.gb_key);
+        const float4 q4 = bf4(reinterpret_cast<const uint2*>(gb + LY.gb_q)[lane]);
+        const float4 kc4 = bf4(reinterpret_cast<const uint2*>(kb + n * N)[lane]);
+        reinterpret_cast<float4*>(gb + LY.gb_qf)[lane] = q4;
+        if (KIND == 1) reinterpret_cast<float4*>(gb + LY.gb_kf)[lane] = kc4;
+        float dq = 0.f, dk = 0.f;  // lane j: k_j . q, k_j . k_cur
+        for (int j0 = 0; j0 <= n; j0 += 8) {
+          float pq[8], pk[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int j = j0 + k;
-              const float4 kj = j <= n ? bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane])
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-              pq[k] = dot4(kj, q4);
-              pk[k] = KIND == 1 ? dot4(kj, kc4) : 0.f;
+          for (int e = 0; e < 8; ++e) {
+            const int j = j0 + e;
+            const float4 kj = j <= n ? bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane])
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+            pq[e] = dot4(kj, q4);
+            pk[e] = KIND == 1 ? dot4(kj, kc4) : 0.f;
+          }
+          const float tq = __shfl_sync(0xffffffffu, reduce8(pq, lane), 4 * (lane & 7));
+          if ((lane >> 3) == (j0 >> 3)) dq = tq;
+          if (KIND == 1) {
+            const float tk = __shfl_sync(0xffffffffu, reduce8(pk, lane), 4 * (lane & 7));
+            if ((lane >> 3) == (j0 >> 3)) dk = tk;
+          }
+        }
+        const int slot_lane = lane < n ? ring_slot(head, lane, C) : 0;
+        const int hh_hi = min(hpg, w.hh + (nunits - i));  // heads of this group in this CTA
+        for (int e = w.hh; e < hh_hi; ++e) {
+          float* co = reinterpret_cast<float*>(gb + LY.gb_coef) + e * CS;
+          const float* la_row = reinterpret_cast<const float*>(gb + LY.gb_la) + e * Cp;
+          const size_t ue = ug + e;
+          if (KIND == 0) {
+            const uint16_t* dt_row = reinterpret_cast<const uint16_t*>(gb + LY.gb_dt) + e * Cp;
+            const uint16_t dt_bits = reinterpret_cast<const uint16_t*>(gb + LY.gb_s1)[(ug & 7) + e];
+            const float dt_cur = bf(dt_bits);
+            const float la_cur = dt_cur * sA[w.g * hpg + e];
+            // records 0..n (current at n): w_j = exp(sum_{i=j+1..n} la_i), gamma = exp(sum_{i<=n} la_i)
+            const float sv = suffix_sum(lane < n ? la_row[slot_lane] : (lane == n ? la_cur : 0.f), lane, n);
+            const float excl = __shfl_down_sync(0xffffffffu, sv, 1);
+            const float Wl = lane <= n ? expf(lane < n ? excl : 0.f) : 0.f;
+            const float dtl = lane < n ? bf(dt_row[slot_lane]) : (lane == n ? dt_cur : 0.f);
+            if (lane <= n) {
+              co[lane] = Wl * dtl * dq;     // output coefficient on x_j[r]
+              co[2 * C + lane] = Wl * dtl;  // fold coefficient on x_j[r]
             }
-            const float tq = __shfl_sync(0xffffffffu, reduce8(pq, lane), 4 * (lane & 7));
-            if ((lane >> 3) == (j0 >> 3)) dq = tq;
-            if (KIND == 1) {
-              const float tk = __shfl_sync(0xffffffffu, reduce8(pk, lane), 4 * (lane & 7));
-              if ((lane >> 3) == (j0 >> 3)) dk = tk;
+            if (lane == 0) {
+              co[3 * C + CO_GAMMA] = expf(sv);
+              if (READ == READ_NVFP4)
+                co[3 * C + CO_MATSCALE] = reinterpret_cast<const float*>(gb + LY.gb_ms)[(ug & 3) + e];
+            }
+            if (!flush) {
+              // append the current token of head e: x row, dt, log decay
+              const uint16_t* xc = reinterpret_cast<const uint16_t*>(gb + LY.gb_cur) + e * P;
+              uint16_t* dst = d.r_x + (ue * C + slot) * P;
+              if (P == 64)
+                reinterpret_cast<uint32_t*>(dst)[lane] = reinterpret_cast<const uint32_t*>(xc)[lane];
+              else
+                reinterpret_cast<uint2*>(dst)[lane] = reinterpret_cast<const uint2*>(xc)[lane];
+              if (lane == 0) {
+                d.r_dt[ue * Cp + slot] = dt_bits;
+                d.r_la[ue * Cp + slot] = la_cur;
+              }
+            }
+          } else {
+            // buffered records 0..n-1: w_j = exp(sum_{i=j+1..n-1} g_i), gamma = exp(sum_{i<n} g_i)
+            const float sv = suffix_sum(lane < n ? la_row[slot_lane] : 0.f, lane, n - 1);
+            const float excl = __shfl_down_sync(0xffffffffu, sv, 1);
+            const float Wl = lane < n ? expf(lane + 1 < n ? excl : 0.f) : 0.f;
+            const float g_cur = reinterpret_cast<const float*>(gb + LY.gb_s1)[(ug & 3) + e];
+            const float a = expf(g_cur);
+            if (lane < n) {
+              co[lane] = Wl * dk;         // coefficient of u_j[r] in S k
+              co[C + lane] = Wl * dq;     // coefficient of u_j[r] in S q
+              co[2 * C + lane] = a * Wl;  // fold coefficient of u_j[r]
+            }
+            const float kq_dot = __shfl_sync(0xffffffffu, dq, n);
+            if (lane == 0) {
+              co[3 * C + CO_GAMMA] = n > 0 ? expf(sv) : 1.f;
+              co[3 * C + CO_A] = a;
+              co[3 * C + CO_BETA] = reinterpret_cast<const float*>(gb + LY.gb_s2)[(ug & 3) + e];
+              co[3 * C + CO_KQ] = kq_dot;
+              if (!flush) d.r_g[ue * Cp + slot] = g_cur;
             }
           }
         }
-        if (KIND == 0) {
-          const uint16_t* dt_row = reinterpret_cast<const uint16_t*>(gb + LY.gb_dt) + v.hh * Cp;
-          const uint16_t* s1 = reinterpret_cast<const uint16_t*>(gb + LY.gb_s1);
-          const float dt_cur = bf(s1[(ug & 7) + v.hh]);
-          const float la_cur = dt_cur * sA[v.h];
-          // records 0..n (current at n): w_j = exp(sum_{i=j+1..n} la_i), gamma = exp(sum_{i<=n} la_i)
-          const float sv = suffix_sum(lane < n ? la_row[slot_lane] : (lane == n ? la_cur : 0.f), lane, n);
-          const float excl = __shfl_down_sync(0xffffffffu, sv, 1);
-          const float Wl = lane <= n ? expf(lane < n ? excl : 0.f) : 0.f;
-          const float dtl = lane < n ? bf(dt_row[slot_lane]) : (lane == n ? dt_cur : 0.f);
-          if (lane <= n) {
-            sc[lane] = Wl * dtl * dq;     // output coefficient on x_j[r]
-            sc[2 * C + lane] = Wl * dtl;  // fold coefficient on x_j[r]
-          }
-          if (lane == 0) {
-            sc[3 * C + 2 * P] = expf(sv);
-            sc[3 * C + 2 * P + 4] = la_cur;
-          }
-        } else {
-          const float* s1 = reinterpret_cast<const float*>(gb + LY.gb_s1);
-          const float* s2 = reinterpret_cast<const float*>(gb + LY.gb_s2);
-          // buffered records 0..n-1: w_j = exp(sum_{i=j+1..n-1} g_i), gamma = exp(sum_{i<n} g_i)
-          const float sv = suffix_sum(lane < n ? la_row[slot_lane] : 0.f, lane, n - 1);
-          const float excl = __shfl_down_sync(0xffffffffu, sv, 1);
-          const float Wl = lane < n ? expf(lane + 1 < n ? excl : 0.f) : 0.f;
-          const float g_cur = s1[(ug & 3) + v.hh];
-          const float a = expf(g_cur);
-          if (lane < n) {
-            sc[lane] = Wl * dk;         // coefficient of u_j[r] in S k
-            sc[C + lane] = Wl * dq;     // coefficient of u_j[r] in S q
-            sc[2 * C + lane] = a * Wl;  // fold coefficient of u_j[r]
-          }
-          const float kq_dot = __shfl_sync(0xffffffffu, dq, n);
-          if (lane == 0) {
-            sc[3 * C + 2 * P] = n > 0 ? expf(sv) : 1.f;
-            sc[3 * C + 2 * P + 1] = a;
-            sc[3 * C + 2 * P + 2] = s2[(ug & 3) + v.hh];
-            sc[3 * C + 2 * P + 3] = kq_dot;
-            sc[3 * C + 2 * P + 4] = g_cur;
-          }
+        if (!flush && w.hh == 0) {
+          // the group's key row: appended by the CTA that holds the group's first head
+          const size_t bg = static_cast<size_t>(w.b) * G + w.g;
+          reinterpret_cast<uint2*>((KIND == 0 ? d.r_B : d.r_k) + (bg * C + slot) * N)[lane] =
+              reinterpret_cast<const uint2*>(kb + n * N)[lane];
         }
       }
-      if (lane == 0) reinterpret_cast<int*>(sc)[3 * C + 2 * P + 6] = 0;  // NVFP4 matrix amax slot
+      if (lane == 0) {
+        unsigned char* st = smem + static_cast<size_t>(LY.st_size) * s;
+        *reinterpret_cast<int4*>(st + LY.st_meta) =
+            make_int4(w.u, n | (flush ? 0x100 : 0) | (ok ? 0x200 : 0), slot, w.hh | ((gi & 1) << 16));
+        reinterpret_cast<int*>(st + LY.st_meta)[4] = 0;  // NVFP4 matrix amax
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(ready + s);
     }
@@ -352,7 +403,6 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
 
   // =============================== computing warps ===============================
   uint32_t amax_phase = 0;
-  int gi = -1;
   for (int i = 0; i < nunits; ++i) {
     if (smisc[0]) break;
     const int s = i % stages;
@@ -363,93 +413,77 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       }
       break;
     }
-    const Unit v = unit_of(i);
-    if (v.first) ++gi;
     unsigned char* st = smem + static_cast<size_t>(LY.st_size) * s;
-    const unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * (gi & 1);
-    const float* sc = reinterpret_cast<const float*>(st + LY.st_scal);
-    if (v.ok) {
-      const size_t u = static_cast<size_t>(v.u);
-      const int n = v.n;
-      const int slot = ring_slot(v.head, n, C);
-      const size_t ug = static_cast<size_t>(v.b) * H + static_cast<size_t>(v.g) * hpg;
+    const int4 meta = *reinterpret_cast<const int4*>(st + LY.st_meta);
+    if (meta.y & 0x200) {
+      const size_t u = static_cast<size_t>(meta.x);
+      const int n = meta.y & 0xFF;
+      const bool flush = (meta.y & 0x100) != 0;
+      const int slot = meta.z;
+      const int hh = meta.w & 0xFFFF;
+      const unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * (meta.w >> 16);
+      const float* co = reinterpret_cast<const float*>(gb + LY.gb_coef) + hh * CS;
       const uint16_t* kb = reinterpret_cast<const uint16_t*>(gb + LY.gb_key);
-      const uint16_t* cur = reinterpret_cast<const uint16_t*>(gb + LY.gb_cur) + v.hh * P;  // x or v of this head
+      const uint16_t* cur = reinterpret_cast<const uint16_t*>(gb + LY.gb_cur) + hh * P;  // x or v of this head
       float* yrow = y + u * P;
       float4* sT4 = reinterpret_cast<float4*>(st + LY.st_tile);
       float4* gS4 = reinterpret_cast<float4*>(d.ckpt + u * tile);
-      const float4 q4 = bf4(reinterpret_cast<const uint2*>(gb + LY.gb_q)[lane]);
-      const float4 kc4 = bf4(reinterpret_cast<const uint2*>(kb + n * N)[lane]);
-      const float gamma = sc[3 * C + 2 * P];
+      const float4 q4 = reinterpret_cast<const float4*>(gb + LY.gb_qf)[lane];
+      const float gamma = co[3 * C + CO_GAMMA];
       if (KIND == 0) {
         const uint16_t* xb = reinterpret_cast<const uint16_t*>(st + LY.st_rec);
+#pragma unroll
         for (int r0 = 0; r0 < RW; r0 += 8) {
           const int Rq = warp + 8 * (r0 + kq);
-          const bool vq = r0 + kq < RW;
-          // buffered term of row slot kq: lanes 4kq..4kq+3 split the records 0..n
-          float ry = 0.f;
-          for (int j0 = 0; j0 <= n; j0 += 4) {
-            const int j = j0 + jl;
-            if (j <= n && vq) ry = fmaf(sc[j], bf(j < n ? xb[j * P + Rq] : cur[Rq]), ry);
-          }
+          // buffered term of row Rq: lanes 4kq..4kq+3 split the records 0..n-1, lane jl = 0 adds record n
+          float ry = jl == 0 ? co[n] * bf(cur[Rq]) : 0.f;
+          for (int j = jl; j < n; j += 4) ry = fmaf(co[j], bf(xb[j * P + Rq]), ry);
           ry += __shfl_xor_sync(0xffffffffu, ry, 1);
           ry += __shfl_xor_sync(0xffffffffu, ry, 2);
           float4 s4[8];
           float part[8];
           float row_scale = 1.f;
-          if (READ != READ_NONE && !v.flush) {
+          if (READ != READ_NONE && !flush) {
             // non-flush: the checkpoint term from the low-precision copy
             const unsigned char* cb = st + LY.st_tile;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int R = warp + 8 * (r0 + k);
-              float pv = 0.f;
-              if (r0 + k < RW) {
-                if (READ == READ_FP8) {
-                  const uint32_t w = reinterpret_cast<const uint32_t*>(cb + R * N)[lane];
-                  const float2 lo = e4m3x2_to_f32x2(static_cast<uint16_t>(w & 0xFFFFu));
-                  const float2 hi = e4m3x2_to_f32x2(static_cast<uint16_t>(w >> 16));
-                  pv = dot4(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
-                } else {
-                  const uint32_t w = reinterpret_cast<const uint16_t*>(cb + R * (N / 2))[lane];
-                  const float2 lo = e2m1x2_to_f32x2(w & 0xFFu);
-                  const float2 hi = e2m1x2_to_f32x2(w >> 8);
-                  const float bs =
-                      e4m3_to_f32(gb[LY.gb_rs + (v.hh * P + R) * (N / 16) + (lane >> 2)]);
-                  pv = bs * dot4(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
-                }
+            for (int e = 0; e < 8; ++e) {
+              const int R = warp + 8 * (r0 + e);
+              if (READ == READ_FP8) {
+                const uint32_t wd = reinterpret_cast<const uint32_t*>(cb + R * N)[lane];
+                const float2 lo = e4m3x2_to_f32x2(static_cast<uint16_t>(wd & 0xFFFFu));
+                const float2 hi = e4m3x2_to_f32x2(static_cast<uint16_t>(wd >> 16));
+                part[e] = dot4(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
+              } else {
+                const uint32_t wd = reinterpret_cast<const uint16_t*>(cb + R * (N / 2))[lane];
+                const float2 lo = e2m1x2_to_f32x2(wd & 0xFFu);
+                const float2 hi = e2m1x2_to_f32x2(wd >> 8);
+                const float bs = e4m3_to_f32(gb[LY.gb_rs + (hh * P + R) * (N / 16) + (lane >> 2)]);
+                part[e] = bs * dot4(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
               }
-              part[k] = pv;
             }
-            if (vq) {
-              if (READ == READ_FP8)
-                row_scale = reinterpret_cast<const float*>(gb + LY.gb_rs)[v.hh * P + Rq];
-              else
-                row_scale = reinterpret_cast<const float*>(gb + LY.gb_ms)[(ug & 3) + v.hh];
-            }
+            row_scale = READ == READ_FP8 ? reinterpret_cast<const float*>(gb + LY.gb_rs)[hh * P + Rq]
+                                         : co[3 * C + CO_MATSCALE];
           } else {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              s4[k] = r0 + k < RW ? sT4[(warp + 8 * (r0 + k)) * SEG + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-              part[k] = dot4(s4[k], q4);
+            for (int e = 0; e < 8; ++e) {
+              s4[e] = sT4[(warp + 8 * (r0 + e)) * SEG + lane];
+              part[e] = dot4(s4[e], q4);
             }
           }
           const float tot = reduce8(part, lane);
-          if (jl == 0 && vq) {
-            yrow[Rq] = fmaf(gamma * row_scale, tot, ry);
-            if (!v.flush) d.r_x[(u * C + slot) * P + Rq] = cur[Rq];
-          }
-          if (v.flush) {
+          if (jl == 0) yrow[Rq] = fmaf(gamma * row_scale, tot, ry);
+          if (flush) {
             // lane (kq, jl) holds m_j[Rq] = w_j dt_j x_j[Rq] for records j = 4 jc + jl
             float mreg[kMaxRec / 4];
 #pragma unroll
             for (int jc = 0; jc < kMaxRec / 4; ++jc) {
               const int j = 4 * jc + jl;
-              mreg[jc] = (j <= n && vq) ? sc[2 * C + j] * bf(j < n ? xb[j * P + Rq] : cur[Rq]) : 0.f;
+              mreg[jc] = j <= n ? co[2 * C + j] * bf(j < n ? xb[j * P + Rq] : cur[Rq]) : 0.f;
             }
             float4 acc[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) acc[k] = scale4(gamma, s4[k]);
+            for (int e = 0; e < 8; ++e) acc[e] = scale4(gamma, s4[e]);
 #pragma unroll
             for (int jc = 0; jc < kMaxRec / 4; ++jc) {
               if (4 * jc > n) break;
@@ -459,23 +493,22 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
                 if (j > n) break;
                 const float4 k4 = bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane]);
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                  acc[k] = axpy4x2(__shfl_sync(0xffffffffu, mreg[jc], 4 * k + jj), k4, acc[k]);
+                for (int e = 0; e < 8; ++e)
+                  acc[e] = axpy4x2(__shfl_sync(0xffffffffu, mreg[jc], 4 * e + jj), k4, acc[e]);
               }
             }
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              if (r0 + k < RW) {
-                __stcs(gS4 + (warp + 8 * (r0 + k)) * SEG + lane, acc[k]);
-                if (READ != READ_NONE) sT4[(warp + 8 * (r0 + k)) * SEG + lane] = acc[k];
-              }
+            for (int e = 0; e < 8; ++e) {
+              __stcs(gS4 + (warp + 8 * (r0 + e)) * SEG + lane, acc[e]);
+              if (READ != READ_NONE) sT4[(warp + 8 * (r0 + e)) * SEG + lane] = acc[e];
             }
           }
         }
-        if (READ != READ_NONE && v.flush) {
+        if (READ != READ_NONE && flush) {
           // refresh the read copy of this warp's rows from the folded rows in shared memory
           if (READ == READ_FP8) {
             uint32_t* codes = reinterpret_cast<uint32_t*>(d.rc_codes + u * tile);
+#pragma unroll
             for (int m = 0; m < RW; ++m) {
               const int R = warp + 8 * m;
               const float4 v4 = sT4[R * SEG + lane];
@@ -493,21 +526,21 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
             }
           } else {
             float mloc = 0.f;
+#pragma unroll
             for (int m = 0; m < RW; ++m) {
               const float4 v4 = sT4[(warp + 8 * m) * SEG + lane];
               mloc = fmaxf(mloc, fmaxf(fmaxf(fabsf(v4.x), fabsf(v4.y)), fmaxf(fabsf(v4.z), fabsf(v4.w))));
             }
             mloc = seg_max<32>(mloc);
-            int* slot_amax = reinterpret_cast<int*>(st + LY.st_scal) + 3 * C + 2 * P + 6;
+            int* slot_amax = reinterpret_cast<int*>(st + LY.st_meta) + 4;
             if (lane == 0) atomicMax(slot_amax, __float_as_int(mloc));  // non-negative floats order as ints
             __syncwarp();
             if (lane == 0) mbar_arrive(amaxbar + s);
-            const bool got =
-                __all_sync(0xffffffffu, mbar_wait_bounded(amaxbar + s, (amax_phase >> s) & 1u));
+            const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(amaxbar + s, (amax_phase >> s) & 1u));
             amax_phase ^= 1u << s;
             if (!got) {
               if (lane == 0) {
-                report_error(d.err, DEVERR_TIMEOUT, v.b);
+                report_error(d.err, DEVERR_TIMEOUT, static_cast<int>(u / H));
                 smisc[0] = 1;
               }
             } else {
@@ -516,6 +549,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
               const float six_s = __fmul_rn(6.0f, smat);
               uint16_t* codes = reinterpret_cast<uint16_t*>(d.rc_codes + u * (tile / 2));
               uint8_t* blk = d.rc_blkscale + u * (tile / 16);
+#pragma unroll
               for (int m = 0; m < RW; ++m) {
                 const int R = warp + 8 * m;
                 const float4 v4 = sT4[R * SEG + lane];
@@ -524,45 +558,31 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
                 uint32_t bcode = 0;
                 if (six_s != 0.0f) bcode = f32x2_to_e4m3x2(__fdiv_rn(mb, six_s), 0.0f) & 0xFFu;
                 const float dd = __fmul_rn(e4m3_to_f32(bcode), smat);
-                uint32_t q = 0;
+                uint32_t qv = 0;
                 if (dd != 0.0f)
-                  q = f32x4_to_e2m1x4(__fdiv_rn(v4.x, dd), __fdiv_rn(v4.y, dd), __fdiv_rn(v4.z, dd),
-                                      __fdiv_rn(v4.w, dd));
-                codes[R * SEG + lane] = static_cast<uint16_t>(q);
+                  qv = f32x4_to_e2m1x4(__fdiv_rn(v4.x, dd), __fdiv_rn(v4.y, dd), __fdiv_rn(v4.z, dd),
+                                       __fdiv_rn(v4.w, dd));
+                codes[R * SEG + lane] = static_cast<uint16_t>(qv);
                 if ((lane & 3) == 0) blk[R * (N / 16) + (lane >> 2)] = static_cast<uint8_t>(bcode);
               }
               if (warp == 0 && lane == 0) d.rc_matscale[u] = smat;
             }
           }
         }
-        if (!v.flush && warp == 0) {
-          if (lane == 0) {
-            const uint16_t* s1 = reinterpret_cast<const uint16_t*>(gb + LY.gb_s1);
-            d.r_dt[u * Cp + slot] = s1[(ug & 7) + v.hh];
-            d.r_la[u * Cp + slot] = sc[3 * C + 2 * P + 4];
-          }
-          if (v.hh == 0) {
-            const size_t bg = static_cast<size_t>(v.b) * G + v.g;
-            reinterpret_cast<uint2*>(d.r_B + (bg * C + slot) * N)[lane] =
-                reinterpret_cast<const uint2*>(kb + n * N)[lane];
-          }
-        }
       } else {
         const float* ub = reinterpret_cast<const float*>(st + LY.st_rec);
-        const float a = sc[3 * C + 2 * P + 1], beta = sc[3 * C + 2 * P + 2];
-        const float kq_dot = sc[3 * C + 2 * P + 3];
+        const float4 kc4 = reinterpret_cast<const float4*>(gb + LY.gb_kf)[lane];
+        const float a = co[3 * C + CO_A], beta = co[3 * C + CO_BETA];
+        const float kq_dot = co[3 * C + CO_KQ];
         float* urow = d.r_u + (u * C + slot) * P;
+#pragma unroll
         for (int r0 = 0; r0 < RW; r0 += 8) {
           const int Rq = warp + 8 * (r0 + kq);
-          const bool vq = r0 + kq < RW;
           float rk = 0.f, rq = 0.f;
-          for (int j0 = 0; j0 < n; j0 += 4) {
-            const int j = j0 + jl;
-            if (j < n && vq) {
-              const float uj = ub[j * P + Rq];
-              rk = fmaf(sc[j], uj, rk);
-              rq = fmaf(sc[C + j], uj, rq);
-            }
+          for (int j = jl; j < n; j += 4) {
+            const float uj = ub[j * P + Rq];
+            rk = fmaf(co[j], uj, rk);
+            rq = fmaf(co[C + j], uj, rq);
           }
           rk += __shfl_xor_sync(0xffffffffu, rk, 1);
           rk += __shfl_xor_sync(0xffffffffu, rk, 2);
@@ -571,35 +591,32 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
           float4 s4[8];
           float pk[8], pq[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            s4[k] = r0 + k < RW ? sT4[(warp + 8 * (r0 + k)) * SEG + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-            pk[k] = dot4(s4[k], kc4);
-            pq[k] = dot4(s4[k], q4);
+          for (int e = 0; e < 8; ++e) {
+            s4[e] = sT4[(warp + 8 * (r0 + e)) * SEG + lane];
+            pk[e] = dot4(s4[e], kc4);
+            pq[e] = dot4(s4[e], q4);
           }
           const float tk = reduce8(pk, lane);
           const float tq = reduce8(pq, lane);
-          float uu = 0.f;
-          if (vq) {
-            const float Sk = fmaf(gamma, tk, rk);
-            const float Sq = fmaf(gamma, tq, rq);
-            uu = beta * (bf(cur[Rq]) - a * Sk);
-            if (jl == 0) {
-              yrow[Rq] = fmaf(a, Sq, uu * kq_dot);
-              if (!v.flush) urow[Rq] = uu;
-            }
+          const float Sk = fmaf(gamma, tk, rk);
+          const float Sq = fmaf(gamma, tq, rq);
+          const float uu = beta * (bf(cur[Rq]) - a * Sk);
+          if (jl == 0) {
+            yrow[Rq] = fmaf(a, Sq, uu * kq_dot);
+            if (!flush) urow[Rq] = uu;
           }
-          if (v.flush) {
+          if (flush) {
             // lane (kq, jl) holds m_j[Rq] = a w_j u_j[Rq] for records j = 4 jc + jl
             float mreg[kMaxRec / 4];
 #pragma unroll
             for (int jc = 0; jc < kMaxRec / 4; ++jc) {
               const int j = 4 * jc + jl;
-              mreg[jc] = (j < n && vq) ? sc[2 * C + j] * ub[j * P + Rq] : 0.f;
+              mreg[jc] = j < n ? co[2 * C + j] * ub[j * P + Rq] : 0.f;
             }
             float4 acc[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              acc[k] = axpy4(__shfl_sync(0xffffffffu, uu, 4 * k), kc4, scale4(a * gamma, s4[k]));
+            for (int e = 0; e < 8; ++e)
+              acc[e] = axpy4(__shfl_sync(0xffffffffu, uu, 4 * e), kc4, scale4(a * gamma, s4[e]));
 #pragma unroll
             for (int jc = 0; jc < kMaxRec / 4; ++jc) {
               if (4 * jc >= n) break;
@@ -609,21 +626,12 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
                 if (j >= n) break;
                 const float4 k4 = bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane]);
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                  acc[k] = axpy4x2(__shfl_sync(0xffffffffu, mreg[jc], 4 * k + jj), k4, acc[k]);
+                for (int e = 0; e < 8; ++e)
+                  acc[e] = axpy4x2(__shfl_sync(0xffffffffu, mreg[jc], 4 * e + jj), k4, acc[e]);
               }
             }
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              if (r0 + k < RW) __stcs(gS4 + (warp + 8 * (r0 + k)) * SEG + lane, acc[k]);
-          }
-        }
-        if (!v.flush && warp == 0) {
-          if (lane == 0) d.r_g[u * Cp + slot] = sc[3 * C + 2 * P + 4];
-          if (v.hh == 0) {
-            const size_t bg = static_cast<size_t>(v.b) * G + v.g;
-            reinterpret_cast<uint2*>(d.r_k + (bg * C + slot) * N)[lane] =
-                reinterpret_cast<const uint2*>(kb + n * N)[lane];
+            for (int e = 0; e < 8; ++e) __stcs(gS4 + (warp + 8 * (r0 + e)) * SEG + lane, acc[e]);
           }
         }
       }
@@ -633,10 +641,10 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   }
 }
 
-template <int KIND, int READ>
+template <int KIND, int READ, int P>
 cudaError_t launch128(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s) {
   const int hpg = d.H / d.G;
-  const Lay128 LY = lay128(KIND, READ, d.P, d.C, d.Cp, d.H, hpg);
+  const Lay128 LY = lay128(KIND, READ, P, d.C, d.Cp, d.H, hpg);
   const long budget = 227L * 1024 - 2L * LY.gb_size - LY.pe_size;
   long stages = budget / LY.st_size;
   if (stages > 8) stages = 8;
@@ -654,28 +662,34 @@ cudaError_t launch128(const LayerDev& d, const TokenIn& in, float* y, cudaStream
     per = (total + grid - 1) / grid;
   }
   grid = (total + per - 1) / per;
-  auto kernel = decode128_kernel<KIND, READ>;
+  auto kernel = decode128_kernel<KIND, READ, P>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
   kernel<<<grid, kThreads128, smem, s>>>(d, in, y, per, static_cast<int>(stages));
   return cudaGetLastError();
 }
 
+template <int P>
+cudaError_t launch128_p(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s) {
+  if (d.kind == 0) {
+    if (d.read_mode == READ_FP8) return launch128<0, READ_FP8, P>(d, in, y, s);
+    if (d.read_mode == READ_NVFP4) return launch128<0, READ_NVFP4, P>(d, in, y, s);
+    return launch128<0, READ_NONE, P>(d, in, y, s);
+  }
+  return launch128<1, READ_NONE, P>(d, in, y, s);
+}
+
 }  // namespace
 
-size_t decode128_smem_bytes(const LayerDev& d) {
+bool decode128_supports(const LayerDev& d) {
+  if (d.N != N || (d.P != 64 && d.P != 128)) return false;
   const Lay128 LY = lay128(d.kind, d.read_mode, d.P, d.C, d.Cp, d.H, d.H / d.G);
-  return static_cast<size_t>(LY.st_size) + 2u * LY.gb_size + LY.pe_size;
+  return static_cast<long>(LY.st_size) + 2L * LY.gb_size + LY.pe_size <= 227L * 1024;
 }
 
 cudaError_t launch_decode128(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s) {
-  if (d.N != N) return cudaErrorInvalidValue;
-  if (d.kind == 0) {
-    if (d.read_mode == READ_FP8) return launch128<0, READ_FP8>(d, in, y, s);
-    if (d.read_mode == READ_NVFP4) return launch128<0, READ_NVFP4>(d, in, y, s);
-    return launch128<0, READ_NONE>(d, in, y, s);
-  }
-  return launch128<1, READ_NONE>(d, in, y, s);
+  if (!decode128_supports(d)) return cudaErrorInvalidValue;
+  return d.P == 64 ? launch128_p<64>(d, in, y, s) : launch128_p<128>(d, in, y, s);
 }
 
 }  // namespace rs

@@ -64,8 +64,9 @@ cudaError_t set_smem_limit(const void* func, size_t bytes);
 
 // Dynamic shared memory the decode kernel needs for this layer.
 size_t decode_smem_bytes(const LayerDev& d);
-// grouped decode kernel for d_state 128 (one stage + both group buffers)
-size_t decode128_smem_bytes(const LayerDev& d);
+// grouped decode kernel for d_state 128, d_head 64 or 128, when one stage and
+// both group buffers fit in shared memory
+bool decode128_supports(const LayerDev& d);
 cudaError_t launch_decode128(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s);
 
 }  // namespace rs
