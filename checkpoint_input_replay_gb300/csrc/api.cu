@@ -10,9 +10,11 @@
 #include "replayssm.h"
 
 struct rs_cache {
+  CUtensorMap ckpt_map;  // the checkpoint as a TMA tensor (when the tcgen05 verify kernel serves the shape)
   rs_config cfg;
   rs::LayerDev dev;
-  int pending;  // drafts appended by the last rs_verify and not yet committed
+  int pending;    // drafts appended by the last rs_verify and not yet committed
+  bool map_ok;
 };
 
 namespace {
@@ -311,6 +313,7 @@ rs_status rs_create_cache(const rs_config* cfg, const rs_buffers* bufs, rs_cache
   h->cfg = *cfg;
   h->dev = d;
   h->pending = 0;
+  h->map_ok = rs::verify128_supports(d) && rs::make_ckpt_tmap(d, &h->ckpt_map) == cudaSuccess;
   *out = h;
   return RS_OK;
 }
@@ -333,7 +336,9 @@ rs_status rs_verify(rs_cache* h, int32_t T, const rs_inputs* in, float* y, rs_st
   if (st != RS_OK) return st;
   if (!aligned16(y)) return RS_ERR_ALIGN;
   if (h->pending) return RS_ERR_STATE;
-  const cudaError_t e = rs::launch_verify(h->dev, token_in(in), T, y, reinterpret_cast<cudaStream_t>(stream));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = h->map_ok ? rs::launch_verify128(h->dev, h->ckpt_map, token_in(in), T, y, s)
+                                  : rs::launch_verify(h->dev, token_in(in), T, y, s);
   if (e != cudaSuccess) return RS_ERR_CUDA;
   h->pending = T;
   return RS_OK;

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <cuda.h>
+
 #include "replayssm.h"
 
 namespace rs {
@@ -68,5 +70,12 @@ size_t decode_smem_bytes(const LayerDev& d);
 // both group buffers fit in shared memory
 bool decode128_supports(const LayerDev& d);
 cudaError_t launch_decode128(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s);
+
+// verify kernel on tcgen05 for d_state 128, d_head 64 or 128 (verify128.cu); it
+// reads the checkpoint through a TMA tensor map made once per cache
+bool verify128_supports(const LayerDev& d);
+cudaError_t make_ckpt_tmap(const LayerDev& d, CUtensorMap* out);
+cudaError_t launch_verify128(const LayerDev& d, const CUtensorMap& tmap, const TokenIn& in, int T, float* y,
+                             cudaStream_t s);
 
 }  // namespace rs

@@ -92,3 +92,33 @@ def test_config3_full_batch_sampled(kind):
         if pair.cursor_gpu()[:, 2].any():
             pair.check_ckpt(f"commit {s}")
     assert pair.cache.device_error() == 0
+
+
+# d_state 128 with d_head 64 or 128: the tcgen05 verify kernel (128-row units:
+# two heads of d_head 64 or one of d_head 128), in small shapes that the oracle
+# checks element by element.
+@pytest.mark.parametrize("kind,P,H,G,T", [
+    ("mamba2", 64, 4, 2, 1), ("mamba2", 64, 4, 2, 4), ("mamba2", 128, 4, 1, 3),
+    ("gdn", 128, 4, 2, 1), ("gdn", 128, 4, 2, 4), ("gdn", 64, 4, 2, 2),
+])
+def test_tensor_core_verify_small(kind, P, H, G, T):
+    k = MAMBA2 if kind == "mamba2" else GDN
+    shape = LayerShape(k, batch=3, n_heads=H, n_groups=G, d_head=P, d_state=128, ring_len=5, max_draft=4)
+    wl = configs.workload(shape, seed=31 + P + T, s0_std=0.1 if k == MAMBA2 else 0.05)
+    _spec_session(Pair(wl), 10, T)
+
+
+@pytest.mark.parametrize("kind", ["mamba2", "gdn"])
+def test_tensor_core_verify_many_units_per_cta(kind):
+    """Several units per CTA; groups split across CTA boundaries; the ring wraps."""
+    if kind == "mamba2":
+        shape = LayerShape(MAMBA2, batch=24, n_heads=32, n_groups=2, d_head=64, d_state=128, ring_len=16,
+                           max_draft=4)
+        wl = configs.Mamba2Workload(shape, seed=41, s0_std=0.1)
+        seqs = [0, 11, 23]
+    else:
+        shape = LayerShape(GDN, batch=40, n_heads=32, n_groups=16, d_head=128, d_state=128, ring_len=16,
+                           max_draft=4)
+        wl = configs.GdnWorkload(shape, seed=42, s0_std=0.05)
+        seqs = [0, 19, 39]
+    _spec_session(Pair(wl, seqs=seqs), 20, 4)
