@@ -425,6 +425,9 @@ def main(argv=None):
                     help="sequences per GPU of the Mamba-2 decode leg (the metric is quoted at 256)")
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the Mamba-2 decode leg (a small profiling case with --batch)")
+    ap.add_argument("--verify-only", choices=["mamba2", "gdn"],
+                    help="time only one verify + commit leg, at --verify-batch sequences (a profiling case)")
+    ap.add_argument("--verify-batch", type=int, default=512)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -438,6 +441,12 @@ def main(argv=None):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.verify_only:
+        wl = (configs.config3_mamba2 if args.verify_only == "mamba2" else configs.config3_gdn)(args.verify_batch)
+        res = verify_leg(wl, dev, args.steps, args.warmup, lambda: None)
+        if rank == 0:
+            print(json.dumps({"verify": res}))
+        return 0
     if world > 1:
         import torch.distributed as dist
         barrier = lambda: dist.barrier()

@@ -30,7 +30,8 @@
 //  * MMA thread: the two passes into one of two accumulators;
 //  * four epilogue warps: once per group the key dot products K^T Q (and
 //    K^T K_draft); per unit the decay weights and coefficient tables of its
-//    heads (one suffix scan per head), then the accumulator rows back from
+//    heads (one suffix scan per head and draft position, spread over the
+//    warps), then the accumulator rows back from
 //    tensor memory, the buffered-record terms, the triangular solve (Gated
 //    DeltaNet), outputs and the drafts' u records.
 // Every wait is bounded; on a timeout the CTA records an error and drains its
@@ -542,101 +543,68 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         }
       }
       epi_sync();
-      if (ok && ew < HPU) {
-        // decay weights and coefficient table of head hh0 + ew, from one suffix scan
-        // F(m) = sum of the log decays of records m..nr-1:
-        //   prod_{i=j+1..m-1} a_i = exp(F(j+1) - F(m))
-        const int hh = hh0 + ew, h = h0 + ew;
-        float* co = reinterpret_cast<float*>(gb + LY.g_coef) + hh * HS;
-        const float* la_row = reinterpret_cast<const float*>(gb + LY.g_la) + hh * Cp;
+      if (ok) {
+        // decay weights and coefficient tables, one (head, draft position) item per warp
+        // at a time; each item is a suffix scan over the records 0..n+tau (FP32, as in
+        // the decode kernels), lane j holding record j
         const int slot_lane = lane < n ? ring_slot(head, lane, C) : 0;
         const int sigma = lane - n;
         const bool is_draft = sigma >= 0 && sigma < T;
-        const size_t i0s = is_draft ? (static_cast<size_t>(b) * T + sigma) * H + static_cast<size_t>(h - hh) : 0;
-        const float4 dq4 = lane < nr ? reinterpret_cast<const float4*>(dqt)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float dq[kT] = {dq4.x, dq4.y, dq4.z, dq4.w};
-        float lj, dtj = 0.f, g_d = 0.f, beta_d = 0.f;
-        if (KIND == 0) {
-          const uint16_t dt_bits =
-              is_draft ? reinterpret_cast<const uint16_t*>(gb + LY.g_s1 + sigma * LY.span)[(i0s & 7) + hh] : 0;
-          const uint16_t* dtr = reinterpret_cast<const uint16_t*>(gb + LY.g_dt) + hh * Cp;
-          lj = lane < n ? la_row[slot_lane] : (is_draft ? bf(dt_bits) * sA[h] : 0.f);
-          dtj = lane < n ? bf(dtr[slot_lane]) : (is_draft ? bf(dt_bits) : 0.f);
-        } else {
-          if (is_draft) {
-            g_d = reinterpret_cast<const float*>(gb + LY.g_s1 + sigma * LY.span)[(i0s & 3) + hh];
-            beta_d = reinterpret_cast<const float*>(gb + LY.g_s2 + sigma * LY.span)[(i0s & 3) + hh];
-          }
-          lj = lane < n ? la_row[slot_lane] : g_d;
-        }
-        // F in FP64: the weights come from differences of these sums
-        double F = lane < nr ? static_cast<double>(lj) : 0.0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const double w = __shfl_down_sync(0xffffffffu, F, o);
-          if (lane + o <= nr - 1) F += w;
-        }
-        const double Fd = __shfl_down_sync(0xffffffffu, F, 1);
-        const double Fx = lane + 1 < nr ? Fd : 0.0;  // F(lane + 1)
-        const double F0 = __shfl_sync(0xffffffffu, F, 0);
-        auto F_at = [&](int m) {  // F(m), m uniform over the warp, 0 <= m <= nr
-          const double v = __shfl_sync(0xffffffffu, F, m < 32 ? m : 31);
-          return m < nr ? v : 0.0;
-        };
-        if (KIND == 0) {
-          float c1[kT], Dv[kT];
-#pragma unroll
-          for (int tau = 0; tau < kT; ++tau) {
-            c1[tau] = Dv[tau] = 0.f;
-            if (tau < T) {
-              const double E = F_at(n + tau + 1);
-              c1[tau] = lane <= n + tau ? expf(static_cast<float>(Fx - E)) * dq[tau] * dtj : 0.f;
-              Dv[tau] = expf(static_cast<float>(F0 - E));
+        for (int it = ew; it < HPU * T; it += 4) {
+          const int hu_t = it / T, tau = it - hu_t * T;
+          const int hh = hh0 + hu_t, h = h0 + hu_t;
+          float* co = reinterpret_cast<float*>(gb + LY.g_coef) + hh * HS;
+          const float* la_row = reinterpret_cast<const float*>(gb + LY.g_la) + hh * Cp;
+          const size_t i0s = is_draft ? (static_cast<size_t>(b) * T + sigma) * H + static_cast<size_t>(h - hh) : 0;
+          const int m = n + tau;  // draft tau is record m
+          const float dqj = lane < nr ? dqt[lane * 4 + tau] : 0.f;
+          if (KIND == 0) {
+            const uint16_t dt_bits =
+                is_draft ? reinterpret_cast<const uint16_t*>(gb + LY.g_s1 + sigma * LY.span)[(i0s & 7) + hh] : 0;
+            const uint16_t* dtr = reinterpret_cast<const uint16_t*>(gb + LY.g_dt) + hh * Cp;
+            const float lj = lane < n ? la_row[slot_lane] : (is_draft ? bf(dt_bits) * sA[h] : 0.f);
+            const float dtj = lane < n ? bf(dtr[slot_lane]) : (is_draft ? bf(dt_bits) : 0.f);
+            // w_j = prod_{i=j+1..m} a_i, D = prod_{i<=m} a_i
+            const float v = suffix_sum(lane <= m ? lj : 0.f, lane, m);
+            const float ex = __shfl_down_sync(0xffffffffu, v, 1);
+            const float W = lane <= m ? expf(lane < m ? ex : 0.f) : 0.f;
+            if (lane < nr) co[lane * 4 + tau] = W * dqj * dtj;
+            if (lane == 0) co[4 * C + tau] = expf(v);
+          } else {
+            float g_d = 0.f, beta_d = 0.f;
+            if (is_draft) {
+              g_d = reinterpret_cast<const float*>(gb + LY.g_s1 + sigma * LY.span)[(i0s & 3) + hh];
+              beta_d = reinterpret_cast<const float*>(gb + LY.g_s2 + sigma * LY.span)[(i0s & 3) + hh];
             }
-          }
-          if (lane < nr) reinterpret_cast<float4*>(co)[lane] = make_float4(c1[0], c1[1], c1[2], c1[3]);
-          if (lane == 0) reinterpret_cast<float4*>(co)[C] = make_float4(Dv[0], Dv[1], Dv[2], Dv[3]);
-        } else {
-          const float4 dk4 = lane < nr ? reinterpret_cast<const float4*>(dkt)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-          const float dk[kT] = {dk4.x, dk4.y, dk4.z, dk4.w};
-          float c1[kT], c2[kT], G1[kT], G2[kT], a_t[kT], b_t[kT], Mrow[kT], Qrow[kT];
-#pragma unroll
-          for (int tau = 0; tau < kT; ++tau) {
-            c1[tau] = c2[tau] = G1[tau] = G2[tau] = a_t[tau] = b_t[tau] = Mrow[tau] = Qrow[tau] = 0.f;
-            if (tau < T) {
-              const int m = n + tau;  // draft tau is record m
-              a_t[tau] = expf(__shfl_sync(0xffffffffu, g_d, m));
-              b_t[tau] = __shfl_sync(0xffffffffu, beta_d, m);
-              const double E1 = F_at(m + 1), E0 = F_at(m);
-              const float tW = lane <= m ? expf(static_cast<float>(Fx - E1)) : 0.f;   // prod_{i=lane+1..m} a_i
-              const float tWk = lane < m ? expf(static_cast<float>(Fx - E0)) : 0.f;   // prod_{i=lane+1..m-1} a_i
-              G2[tau] = expf(static_cast<float>(F0 - E1));
-              G1[tau] = expf(static_cast<float>(F0 - E0));
-              c1[tau] = lane < n ? tWk * dk[tau] : 0.f;  // coefficient of u_j[r] in S k_tau
-              c2[tau] = lane < n ? tW * dq[tau] : 0.f;   // coefficient of u_j[r] in S q_tau
-              Mrow[tau] = (is_draft && sigma < tau) ? b_t[tau] * a_t[tau] * tWk * dk[tau] : 0.f;
-              Qrow[tau] = (is_draft && sigma <= tau) ? tW * dq[tau] : 0.f;
+            const float lj = lane < n ? la_row[slot_lane] : g_d;
+            const float dkj = lane < nr ? dkt[lane * 4 + tau] : 0.f;
+            // tW_j = prod_{i=j+1..m} a_i (j <= m), tWk_j = prod_{i=j+1..m-1} a_i (j < m)
+            const float vq = suffix_sum(lane <= m ? lj : 0.f, lane, m);
+            const float exq = __shfl_down_sync(0xffffffffu, vq, 1);
+            const float tW = lane <= m ? expf(lane < m ? exq : 0.f) : 0.f;
+            const float vk = suffix_sum(lane < m ? lj : 0.f, lane, m - 1);
+            const float exk = __shfl_down_sync(0xffffffffu, vk, 1);
+            const float tWk = lane < m ? expf(lane + 1 < m ? exk : 0.f) : 0.f;
+            const float a_t = expf(__shfl_sync(0xffffffffu, g_d, m));
+            const float b_t = __shfl_sync(0xffffffffu, beta_d, m);
+            if (lane < n) {
+              co[lane * 4 + tau] = tWk * dkj;        // coefficient of u_j[r] in S k_tau
+              co[(C + lane) * 4 + tau] = tW * dqj;   // coefficient of u_j[r] in S q_tau
             }
-          }
-          if (lane < n) {
-            reinterpret_cast<float4*>(co)[lane] = make_float4(c1[0], c1[1], c1[2], c1[3]);
-            reinterpret_cast<float4*>(co)[C + lane] = make_float4(c2[0], c2[1], c2[2], c2[3]);
-          }
-          float* sc = co + 8 * C;
-          if (lane == 0) {
-            reinterpret_cast<float4*>(sc)[0] = make_float4(G2[0], G2[1], G2[2], G2[3]);
-            reinterpret_cast<float4*>(sc)[1] = make_float4(G1[0], G1[1], G1[2], G1[3]);
-            reinterpret_cast<float4*>(sc)[2] = make_float4(a_t[0], a_t[1], a_t[2], a_t[3]);
-            reinterpret_cast<float4*>(sc)[3] = make_float4(b_t[0], b_t[1], b_t[2], b_t[3]);
-          }
-          // M[tau][s] and Qd[tau][s] for s = lane < 4, gathered from lane n + s
-#pragma unroll
-          for (int tau = 0; tau < kT; ++tau) {
-            const float mv = __shfl_sync(0xffffffffu, Mrow[tau], min(n + (lane & 3), 31));
-            const float qv = __shfl_sync(0xffffffffu, Qrow[tau], min(n + (lane & 3), 31));
-            if (lane < kT) {
-              sc[16 + tau * 4 + lane] = lane < T ? mv : 0.f;
-              sc[32 + tau * 4 + lane] = lane < T ? qv : 0.f;
+            float* sc = co + 8 * C;
+            if (lane == 0) {
+              sc[tau] = expf(vq);                   // G2
+              sc[4 + tau] = m > 0 ? expf(vk) : 1.f;  // G1
+              sc[8 + tau] = a_t;
+              sc[12 + tau] = b_t;
+            }
+            if (is_draft) {  // lane n + s: M[tau][s] (s < tau), Qd[tau][s] (s <= tau)
+              sc[16 + tau * 4 + sigma] = sigma < tau ? b_t * a_t * tWk * dkj : 0.f;
+              sc[32 + tau * 4 + sigma] = sigma <= tau ? tW * dqj : 0.f;
+            }
+            if (lane >= T && lane < kT) {  // unused draft slots of the T x T tables
+              sc[16 + tau * 4 + lane] = 0.f;
+              sc[32 + tau * 4 + lane] = 0.f;
             }
           }
         }
@@ -659,6 +627,7 @@ __global__ void __launch_bounds__(kThreadsV, 1)
           const uint16_t* xr = reinterpret_cast<const uint16_t*>(rec) + hu * C * P + p;
           const uint16_t* xd = reinterpret_cast<const uint16_t*>(gb + LY.g_dx) + hh * P + p;
           float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 4
           for (int j = 0; j < n; ++j) {
             const float4 c = co4[j];
             const float xv = bf(xr[j * P]);
@@ -684,6 +653,7 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         } else {
           const float* ur = reinterpret_cast<const float*>(rec) + hu * C * P + p;
           float rk[kT] = {0.f, 0.f, 0.f, 0.f}, rq[kT] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
           for (int j = 0; j < n; ++j) {
             const float4 c1 = co4[j], c2 = co4[C + j];
             const float uj = ur[j * P];
