@@ -27,6 +27,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Layout {
   size_t ckpt, ring, cursor, read_copy, scratch;
+  size_t s1;  // scratch: offset of the verify coefficient tables (0 when there are none)
   // ring section offsets (bytes)
   size_t r0, r1, r2, r3;
   // read-copy section offsets
@@ -90,6 +91,11 @@ Layout layout_of(const rs_config& c) {
     L.read_copy = L.c2 + align256(B * H * 4);
   }
   L.scratch = B * 4;
+  if (c.max_draft > 0) {
+    // per-head coefficient tables of the tensor-core verify kernel
+    L.s1 = align256(B * 4);
+    L.scratch = L.s1 + B * H * static_cast<size_t>(rs::verify_table_stride(c.kind, static_cast<int>(C))) * 4;
+  }
   return L;
 }
 
@@ -292,6 +298,7 @@ rs_status rs_create_cache(const rs_config* cfg, const rs_buffers* bufs, rs_cache
   d.cursor = static_cast<int*>(bufs->cursor);
   d.err = d.cursor + 4 * d.B;
   d.arrive = static_cast<int*>(bufs->scratch);
+  d.vtab = L.s1 ? reinterpret_cast<float*>(static_cast<char*>(bufs->scratch) + L.s1) : nullptr;
   if (cfg->read_mode != RS_READ_NONE) {
     char* rc = static_cast<char*>(bufs->read_copy);
     d.rc_codes = reinterpret_cast<uint8_t*>(rc + L.c0);

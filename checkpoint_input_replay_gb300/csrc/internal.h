@@ -42,6 +42,8 @@ struct LayerDev {
   float* rc_rowscale;          // FP8: [B][H][P]
   uint8_t* rc_blkscale;        // NVFP4: [B][H][P][N/16]
   float* rc_matscale;          // NVFP4: [B][H]
+  // verify coefficient tables (scratch): f32 [B][H][verify_table_stride]
+  float* vtab;
 };
 
 struct TokenIn {
@@ -74,6 +76,7 @@ cudaError_t launch_decode128(const LayerDev& d, const TokenIn& in, float* y, cud
 // verify kernel on tcgen05 for d_state 128, d_head 64 or 128 (verify128.cu); it
 // reads the checkpoint through a TMA tensor map made once per cache
 bool verify128_supports(const LayerDev& d);
+int verify_table_stride(int kind, int C);
 cudaError_t make_ckpt_tmap(const LayerDev& d, CUtensorMap* out);
 cudaError_t launch_verify128(const LayerDev& d, const CUtensorMap& tmap, const TokenIn& in, int T, float* y,
                              cudaStream_t s);

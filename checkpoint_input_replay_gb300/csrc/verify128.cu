@@ -5,37 +5,46 @@
 // shipped", the paragraph on the second benefit), with the Gated DeltaNet
 // drafts obtained by forward substitution of the unit lower-triangular T x T
 // system (same arithmetic and notation as verify.cu, which serves the other
-// shapes).
+// shapes).  Two launches:
 //
-// A work unit is 128 consecutive state rows of one group: two heads of d_head
-// 64, or one head of d_head 128, so one tcgen05 MMA with M = 128 covers it.
-// The dense part S_ckpt [128][128] x [K_draft | Q] [128][16] runs on the
-// tensor cores in kind::tf32 with FP32 accumulation in tensor memory.  The FP32
-// state is split exactly: kind::tf32 reads an FP32 operand with its low 13
-// mantissa bits ignored, so the first pass takes the raw state as loaded by
-// TMA (128-byte swizzle, the layout the MMA reads directly), and the second
-// pass takes lo = S - trunc(S), computed in registers and stored to tensor
-// memory, as its A operand.  The drafts' queries and keys are bf16, which TF32
-// holds exactly.
+// 1. verify_prep_kernel, one CTA per (sequence, group): K^T Q (and K^T K_draft)
+//    once for the group, then per head the decay weights W, D (and for Gated
+//    DeltaNet the T x T system) folded into a coefficient table in scratch
+//    memory, and the drafts' keys and per-head scalars into the ring.  This is
+//    the latency-bound scalar part; thousands of independent groups hide its
+//    latency.
 //
-// Roles (11 warps, one persistent CTA per SM):
-//  * producer (1 thread): per unit, the state tile by four 2D TMA loads into
-//    one of two tile stages, and the unit's committed records by bulk copies
-//    into one of up to three record stages; once per group, the group's keys,
-//    draft queries, draft values, per-head scalars and ring decay rows into
-//    one of two group buffers;
-//  * prologue warp: once per group, the MMA B operand and the drafts' ring
-//    appends; per unit a descriptor;
-//  * four split warps: lo = S - trunc(S), row r to tensor-memory lane r;
-//  * MMA thread: the two passes into one of two accumulators;
-//  * four epilogue warps: once per group the key dot products K^T Q (and
-//    K^T K_draft); per unit the decay weights and coefficient tables of its
-//    heads (one suffix scan per head and draft position, spread over the
-//    warps), then the accumulator rows back from
-//    tensor memory, the buffered-record terms, the triangular solve (Gated
-//    DeltaNet), outputs and the drafts' u records.
-// Every wait is bounded; on a timeout the CTA records an error and drains its
-// copies and MMAs before it frees tensor memory and exits.
+// 2. verify128_kernel, the pass over the state.  A work unit is 128
+//    consecutive state rows of one group: two heads of d_head 64, or one head
+//    of d_head 128, so one tcgen05 MMA with M = 128 covers it.  The dense part
+//    S_ckpt [128][128] x [K_draft | Q] [128][16] runs on the tensor cores in
+//    kind::tf32 with FP32 accumulation in tensor memory.  The FP32 state is
+//    split exactly: kind::tf32 reads an FP32 operand with its low 13 mantissa
+//    bits ignored, so one pass takes the raw state and a second pass takes
+//    lo = S - trunc(S).  Both A operands are read from tensor memory (an MMA
+//    with A in shared memory costs about 1.7x one with A in tensor memory at
+//    these shapes): the split warps copy each 32-column block of the state
+//    rows, raw and lo, into a ring of tensor-memory chunks that the MMA thread
+//    consumes block by block.  The drafts' queries and keys are bf16, which
+//    TF32 holds exactly.  Roles (15 warps, one persistent CTA per SM):
+//     * producer (1 thread): per unit, the state tile by four 2D TMA loads
+//       into one of two tile stages, and the unit's committed records and
+//       coefficient tables by bulk copies into one of up to three record
+//       stages; once per group, the draft keys, queries and values into one
+//       of two group buffers;
+//     * prologue warp: once per group, the MMA B operand; per unit a
+//       descriptor;
+//     * eight split warps (two per tensor-memory lane quarter, one for the
+//       even and one for the odd 32-column blocks): per block, the raw rows
+//       and lo = S - trunc(S) into a tensor-memory chunk (row r to lane r);
+//       the shared-memory tile is released once it has been read;
+//     * MMA thread: per chunk, four MMAs on the raw part and four on lo, into
+//       one of two accumulators;
+//     * four epilogue warps: accumulator rows back from tensor memory, the
+//       buffered-record terms, the triangular solve (Gated DeltaNet), outputs
+//       and the drafts' x (Mamba-2) or u (Gated DeltaNet) records.
+//    Every wait is bounded; on a timeout the CTA records an error and drains
+//    its copies and MMAs before it frees tensor memory and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -53,63 +62,294 @@ constexpr int kMaxSeqV = 64;      // sequences one CTA may cover
 constexpr int kNT = 2;            // tile stages
 constexpr int kMaxNR = 3;         // record stages, at most
 constexpr uint32_t kTileBytes = kRows * N * 4;
-constexpr int kWarpPro = 8, kWarpProd = 9, kWarpMma = 10;
-constexpr int kThreadsV = 11 * 32;
-// tensor memory: two lo operands (128 columns each), then two accumulators
+constexpr int kSplitWarps = 8;  // two per tensor-memory lane quarter: one for the even, one for the odd blocks
+constexpr int kWarpEpi = 8;      // epilogue warps 8..11
+constexpr int kWarpPro = 12, kWarpProd = 13, kWarpMma = 14;
+constexpr int kThreadsV = 15 * 32;
+constexpr int kPrepThreads = 128;
+// tensor memory: a ring of six A-operand chunks, each the 32 K-columns of one
+// 128-byte block of the state rows as [raw (32 columns) | lo (32 columns)],
+// then two accumulators
+constexpr int kSlots = 6;
+constexpr uint32_t kSlotCols = 64;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kLoCol = 0, kAccCol = 256;
+constexpr uint32_t kAccCol = kSlots * kSlotCols;
 
 __host__ __device__ __forceinline__ int al16(int x) { return (x + 15) & ~15; }
 __host__ __device__ __forceinline__ int al128(int x) { return (x + 127) & ~127; }
 
-// floats per head in a coefficient table
-//   Mamba-2: C1[C][4], then D[4]
-//   GDN:     C1[C][4], C2[C][4], then G2[4] G1[4] a[4] beta[4] M[4][4] Qd[4][4]
+// floats per head in a coefficient table (a multiple of 4)
+//   Mamba-2: C1[C][4] (output coefficient of x_j for draft position tau), D[4]
+//   GDN:     C1[C][4] (coefficient of u_j in S k_tau), C2[C][4] (in S q_tau),
+//            then G2[4] G1[4] a[4] beta[4] M[4][4] Qd[4][4]
 __host__ __device__ __forceinline__ int head_stride(int kind, int C) { return kind == 0 ? 4 * C + 4 : 8 * C + 48; }
 
+__device__ __forceinline__ int ring_slot(int head, int j, int C) {
+  int s = head + j;
+  return s >= C ? s - C : s;
+}
+
+// ============================================================================
+// prep kernel
+// ============================================================================
+// One CTA of four warps per (sequence, group).  Its work is a short chain of
+// dependent global loads, so every load is issued up front: the cursor, then
+// the keys and queries together with the per-head ring scalars (up to four
+// heads per warp per batch, held in registers) before any arithmetic.
+constexpr int kPrepWarps = kPrepThreads / 32;
+constexpr int kHB = 4;  // heads per warp per batch
+
+template <int KIND>
+__global__ void __launch_bounds__(kPrepThreads, 6) verify_prep_kernel(const LayerDev d, const TokenIn in, const int T) {
+  const int H = d.H, G = d.G, C = d.C, L = d.L, Cp = d.Cp;
+  const int hpg = H / G, HS = head_stride(KIND, C);
+  const int bg = blockIdx.x, b = bg / G, g = bg - b * G;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  __shared__ uint2 skey[kMaxRec][N / 4];  // keys of records 0..n+T-1 (committed, then drafts)
+  __shared__ uint2 sq[kT][N / 4];         // draft queries
+  __shared__ float sdq[kMaxRec][kT];      // k_j . q_tau
+  __shared__ float sdk[kMaxRec][kT];      // k_j . k_{n+tau} (GDN)
+
+  const int head = d.cursor[4 * b], cnt = d.cursor[4 * b + 1];
+  const bool ok = static_cast<unsigned>(head) < static_cast<unsigned>(C) &&
+                  static_cast<unsigned>(cnt) < static_cast<unsigned>(L) && cnt + T <= C;
+  if (!ok) {
+    if (g == 0 && t == 0) report_error(d.err, DEVERR_CURSOR, b);
+    return;
+  }
+  if (g == 0 && t == 0) d.cursor[4 * b + 2] = 0;  // verify folds nothing
+  const int n = cnt, nr = n + T;
+  const int slot_lane = lane < n ? ring_slot(head, lane, C) : 0;
+  const int sigma = lane - n;  // draft index of record `lane`
+  const bool is_draft = sigma >= 0 && sigma < T;
+
+  // per-head scalars of record `lane`: log decay, and dt (Mamba-2) or beta (GDN)
+  float pl[kHB], px[kHB];
+  auto load_heads = [&](int batch) {
+#pragma unroll
+    for (int hb = 0; hb < kHB; ++hb) {
+      const int e = batch * (kHB * kPrepWarps) + hb * kPrepWarps + warp;
+      pl[hb] = 0.f;
+      px[hb] = 0.f;
+      if (e < hpg) {
+        const int h = g * hpg + e;
+        const size_t bh = static_cast<size_t>(b) * H + h;
+        const size_t idx_d = is_draft ? (static_cast<size_t>(b) * T + sigma) * H + h : 0;
+        if (KIND == 0) {
+          if (lane < n) {
+            pl[hb] = d.r_la[bh * Cp + slot_lane];
+            px[hb] = bf(d.r_dt[bh * Cp + slot_lane]);
+          } else if (is_draft) {
+            const float dt = bf(in.dt[idx_d]);
+            pl[hb] = dt * in.A[h];
+            px[hb] = dt;
+          }
+        } else {
+          if (lane < n) {
+            pl[hb] = d.r_g[bh * Cp + slot_lane];
+          } else if (is_draft) {
+            pl[hb] = in.g[idx_d];
+            px[hb] = in.beta[idx_d];
+          }
+        }
+      }
+    }
+  };
+
+  uint16_t* rk = (KIND == 0 ? d.r_B : d.r_k) + static_cast<size_t>(bg) * C * N;
+  const uint16_t* kin = KIND == 0 ? in.Bm : in.k;
+  const uint16_t* qin = KIND == 0 ? in.Cm : in.q;
+  for (int e = t; e < nr * (N / 4); e += kPrepThreads) {
+    const int j = e / (N / 4), c = e - j * (N / 4);
+    const uint16_t* src = j < n ? rk + static_cast<size_t>(ring_slot(head, j, C)) * N
+                                : kin + ((static_cast<size_t>(b) * T + (j - n)) * G + g) * N;
+    skey[j][c] = reinterpret_cast<const uint2*>(src)[c];
+  }
+  for (int e = t; e < T * (N / 4); e += kPrepThreads) {
+    const int tau = e / (N / 4), c = e - tau * (N / 4);
+    sq[tau][c] = reinterpret_cast<const uint2*>(qin + ((static_cast<size_t>(b) * T + tau) * G + g) * N)[c];
+  }
+  load_heads(0);
+  __syncthreads();
+  // the drafts' keys into the ring, after the committed records
+  for (int e = t; e < T * (N / 4); e += kPrepThreads) {
+    const int tau = e / (N / 4), c = e - tau * (N / 4);
+    reinterpret_cast<uint2*>(rk + static_cast<size_t>(ring_slot(head, n + tau, C)) * N)[c] = skey[n + tau][c];
+  }
+  // key dot products: item = (8 records, one column), one warp per item
+  {
+    const int ncol = KIND == 0 ? T : 2 * T;
+    const int nblk = (nr + 7) >> 3;
+    for (int it = warp; it < nblk * ncol; it += kPrepWarps) {
+      const int jb = it / ncol, c = it - jb * ncol;
+      const float4 o4 = bf4(c < T ? sq[c][lane] : skey[n + c - T][lane]);
+      float part[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int j = 8 * jb + e;
+        part[e] = j < nr ? dot4(bf4(skey[j][lane]), o4) : 0.f;
+      }
+      const float tot = reduce8(part, lane);
+      const int j = 8 * jb + (lane >> 2);
+      if ((lane & 3) == 0 && j < nr) {
+        if (c < T) sdq[j][c] = tot;
+        else sdk[j][c - T] = tot;
+      }
+    }
+  }
+  __syncthreads();
+  float dq[kT], dk[kT];
+#pragma unroll
+  for (int tau = 0; tau < kT; ++tau) {
+    dq[tau] = (lane < nr && tau < T) ? sdq[lane][tau] : 0.f;
+    dk[tau] = (KIND == 1 && lane < nr && tau < T) ? sdk[lane][tau] : 0.f;
+  }
+  // per head: decay weights and the coefficient table (all draft positions in one
+  // warp, T interleaved suffix scans over the records 0..n+tau), the drafts' appends
+  const int nbatch = (hpg + kHB * kPrepWarps - 1) / (kHB * kPrepWarps);
+  for (int batch = 0; batch < nbatch; ++batch) {
+    if (batch > 0) load_heads(batch);
+#pragma unroll
+    for (int hb = 0; hb < kHB; ++hb) {
+      const int e = batch * (kHB * kPrepWarps) + hb * kPrepWarps + warp;
+      if (e >= hpg) continue;
+      const int h = g * hpg + e;
+      const size_t bh = static_cast<size_t>(b) * H + h;
+      float* co = d.vtab + bh * HS;
+      const float lj = pl[hb];
+      if (KIND == 0) {
+        const float dtj = px[hb];
+        float v[kT];
+#pragma unroll
+        for (int tau = 0; tau < kT; ++tau) v[tau] = lane <= n + tau ? lj : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+          for (int tau = 0; tau < kT; ++tau) {
+            const float w = __shfl_down_sync(0xffffffffu, v[tau], o);
+            if (lane + o <= n + tau) v[tau] += w;
+          }
+        }
+        float c1[kT], Dv[kT];
+#pragma unroll
+        for (int tau = 0; tau < kT; ++tau) {
+          // w_j = prod_{i=j+1..n+tau} a_i, D = prod_{i<=n+tau} a_i
+          const float ex = __shfl_down_sync(0xffffffffu, v[tau], 1);
+          const float W = lane <= n + tau ? expf(lane < n + tau ? ex : 0.f) : 0.f;
+          c1[tau] = tau < T ? W * dq[tau] * dtj : 0.f;
+          Dv[tau] = tau < T ? expf(__shfl_sync(0xffffffffu, v[tau], 0)) : 0.f;
+        }
+        if (lane < nr) reinterpret_cast<float4*>(co)[lane] = make_float4(c1[0], c1[1], c1[2], c1[3]);
+        if (lane == 0) reinterpret_cast<float4*>(co)[C] = make_float4(Dv[0], Dv[1], Dv[2], Dv[3]);
+        // the drafts into the ring: dt and log decay (the x rows are appended by
+        // the main kernel, which stages them anyway)
+        if (is_draft) {
+          d.r_dt[bh * Cp + ring_slot(head, lane, C)] = static_cast<uint16_t>(__float_as_uint(dtj) >> 16);
+          d.r_la[bh * Cp + ring_slot(head, lane, C)] = lj;
+        }
+      } else {
+        const float g_d = is_draft ? lj : 0.f;
+        const float beta_d = px[hb];
+        float vq[kT], vk[kT];
+#pragma unroll
+        for (int tau = 0; tau < kT; ++tau) {
+          vq[tau] = lane <= n + tau ? lj : 0.f;
+          vk[tau] = lane < n + tau ? lj : 0.f;
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+          for (int tau = 0; tau < kT; ++tau) {
+            const float wq = __shfl_down_sync(0xffffffffu, vq[tau], o);
+            const float wk = __shfl_down_sync(0xffffffffu, vk[tau], o);
+            if (lane + o <= n + tau) vq[tau] += wq;
+            if (lane + o <= n + tau - 1) vk[tau] += wk;
+          }
+        }
+        float c1[kT], c2[kT], G1[kT], G2[kT], a_t[kT], b_t[kT], Mv[kT], Qv[kT];
+#pragma unroll
+        for (int tau = 0; tau < kT; ++tau) {
+          const int m = n + tau;  // draft tau is record m
+          // tW_j = prod_{i=j+1..m} a_i (j <= m), tWk_j = prod_{i=j+1..m-1} a_i (j < m)
+          const float exq = __shfl_down_sync(0xffffffffu, vq[tau], 1);
+          const float exk = __shfl_down_sync(0xffffffffu, vk[tau], 1);
+          const float tW = lane <= m ? expf(lane < m ? exq : 0.f) : 0.f;
+          const float tWk = lane < m ? expf(lane + 1 < m ? exk : 0.f) : 0.f;
+          const float v0q = __shfl_sync(0xffffffffu, vq[tau], 0), v0k = __shfl_sync(0xffffffffu, vk[tau], 0);
+          const float gm = __shfl_sync(0xffffffffu, g_d, m < 32 ? m : 31);
+          const float bm = __shfl_sync(0xffffffffu, beta_d, m < 32 ? m : 31);
+          const bool live = tau < T;
+          G2[tau] = live ? expf(v0q) : 0.f;
+          G1[tau] = live ? (m > 0 ? expf(v0k) : 1.f) : 0.f;
+          a_t[tau] = live ? expf(gm) : 0.f;
+          b_t[tau] = live ? bm : 0.f;
+          c1[tau] = (live && lane < n) ? tWk * dk[tau] : 0.f;  // coefficient of u_j[r] in S k_tau
+          c2[tau] = (live && lane < n) ? tW * dq[tau] : 0.f;   // coefficient of u_j[r] in S q_tau
+          // lane n + s: M[tau][s] (s < tau), Qd[tau][s] (s <= tau)
+          Mv[tau] = (live && is_draft && sigma < tau) ? b_t[tau] * a_t[tau] * tWk * dk[tau] : 0.f;
+          Qv[tau] = (live && is_draft && sigma <= tau) ? tW * dq[tau] : 0.f;
+        }
+        if (lane < n) {
+          reinterpret_cast<float4*>(co)[lane] = make_float4(c1[0], c1[1], c1[2], c1[3]);
+          reinterpret_cast<float4*>(co)[C + lane] = make_float4(c2[0], c2[1], c2[2], c2[3]);
+        }
+        float* sc = co + 8 * C;
+        if (lane == 0) {
+          reinterpret_cast<float4*>(sc)[0] = make_float4(G2[0], G2[1], G2[2], G2[3]);
+          reinterpret_cast<float4*>(sc)[1] = make_float4(G1[0], G1[1], G1[2], G1[3]);
+          reinterpret_cast<float4*>(sc)[2] = make_float4(a_t[0], a_t[1], a_t[2], a_t[3]);
+          reinterpret_cast<float4*>(sc)[3] = make_float4(b_t[0], b_t[1], b_t[2], b_t[3]);
+        }
+        if (is_draft) {
+#pragma unroll
+          for (int tau = 0; tau < kT; ++tau) {
+            sc[16 + tau * 4 + sigma] = Mv[tau];
+            sc[32 + tau * 4 + sigma] = Qv[tau];
+          }
+          d.r_g[bh * Cp + ring_slot(head, lane, C)] = g_d;
+        }
+      }
+    }
+  }
+}
+
+// ============================================================================
+// main kernel
+// ============================================================================
 struct VL {
-  int tile, rec, rec_size, rec_meta;
+  int tile, rec, rec_size, rec_tab, rec_meta;
   int gb, gb_size;
-  int g_key, g_q, g_B, g_dx, g_s1, g_s2, g_la, g_dt, g_dq, g_dk, g_coef;
-  int span;  // bytes of one per-draft scalar span
-  int bars, seq, A, misc;
+  int g_key, g_q, g_B, g_dx;
+  int bars, seq, misc;
   int total;
 };
 
-__host__ __device__ __forceinline__ VL vlayout(int kind, int C, int Cp, int H, int hpg, int P, int NR) {
+__host__ __device__ __forceinline__ VL vlayout(int kind, int C, int hpg, int P, int NR) {
+  const int HPU = kRows / P;
   VL l;
   int o = 0;
   l.tile = o;     o += kNT * static_cast<int>(kTileBytes);
   l.rec = o;
-  l.rec_meta = kind == 0 ? 256 * C : 512 * C;  // records of the unit's 128 rows, then 32 bytes of descriptor
-  l.rec_size = al128(l.rec_meta + 32);
+  l.rec_tab = kind == 0 ? 256 * C : 512 * C;                 // records of the unit's 128 rows
+  l.rec_meta = l.rec_tab + HPU * head_stride(kind, C) * 4;   // coefficient tables of its heads
+  l.rec_size = al128(l.rec_meta + 32);                       // 32 bytes of descriptor
   o += NR * l.rec_size;
-  l.span = al16(hpg * 4) + 16;
   int g = 0;
   l.g_B = g;      g += kNmma * N * 4;
-  l.g_key = g;    g += C * N * 2;
-  l.g_q = g;      g += kT * N * 2;
+  l.g_key = g;    g += kT * N * 2;  // draft keys
+  l.g_q = g;      g += kT * N * 2;  // draft queries
   l.g_dx = g;     g += al16(kT * hpg * P * 2);
-  l.g_s1 = g;     g += kT * l.span;
-  l.g_s2 = g;     g += kind == 0 ? 0 : kT * l.span;
-  l.g_la = g;     g += hpg * Cp * 4;
-  l.g_dt = g;     g += kind == 0 ? al16(hpg * Cp * 2) : 0;
-  l.g_dq = g;     g += C * 16;
-  l.g_dk = g;     g += kind == 0 ? 0 : C * 16;
-  l.g_coef = g;   g += hpg * head_stride(kind, C) * 4;
   l.gb_size = al128(g);
   l.gb = o;       o += 2 * l.gb_size;
   l.bars = o;     o += 32 * 8;
   l.seq = o;      o += 3 * kMaxSeqV * 4;
-  l.A = o;        o += al16(H * 4);
   l.misc = o;     o += 16;
   l.total = al128(o) + 1024;  // + slack to align the base to 1024 bytes
   return l;
 }
 
-// Barrier among the four epilogue warps (named barrier 2, 128 threads); the
-// _and form also returns whether `v` held in all of them.
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+// Barrier among the four epilogue warps (named barrier 2, 128 threads) that
+// also returns whether `v` held in all of them.
 __device__ __forceinline__ bool epi_sync_and(bool v) {
   uint32_t r;
   asm volatile(
@@ -121,11 +361,6 @@ __device__ __forceinline__ bool epi_sync_and(bool v) {
       : "r"(static_cast<uint32_t>(v))
       : "memory");
   return r != 0;
-}
-
-__device__ __forceinline__ int ring_slot(int head, int j, int C) {
-  int s = head + j;
-  return s >= C ? s - C : s;
 }
 
 // Unit position (sequence, first head, group, head-in-group of the first head),
@@ -162,25 +397,24 @@ __global__ void __launch_bounds__(kThreadsV, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int H = d.H, G = d.G, C = d.C, L = d.L, Cp = d.Cp;
+  const int H = d.H, G = d.G, C = d.C, L = d.L;
   const int hpg = H / G;
   const int UPH = H / HPU;
   const int HS = head_stride(KIND, C);
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const VL LY = vlayout(KIND, C, Cp, H, hpg, P, NR);
+  const VL LY = vlayout(KIND, C, hpg, P, NR);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY.bars);
   uint64_t* tile_full = bars;        // [2]
   uint64_t* tile_empty = bars + 2;   // [2]
-  uint64_t* lo_ready = bars + 4;     // [2]
-  uint64_t* lo_free = bars + 6;      // [2]
-  uint64_t* acc_full = bars + 8;     // [2]
-  uint64_t* acc_empty = bars + 10;   // [2]
-  uint64_t* drain = bars + 12;       // [1]
-  uint64_t* rec_full = bars + 16;    // [NR]
-  uint64_t* rec_empty = bars + 20;   // [NR]
-  uint64_t* ready = bars + 24;       // [NR]
+  uint64_t* acc_full = bars + 4;     // [2]
+  uint64_t* acc_empty = bars + 6;    // [2]
+  uint64_t* drain = bars + 8;        // [1]
+  uint64_t* chunk_full = bars + 10;  // [6]
+  uint64_t* chunk_free = bars + 16;  // [6]
+  uint64_t* rec_full = bars + 22;    // [NR]
+  uint64_t* rec_empty = bars + 25;   // [NR]
+  uint64_t* ready = bars + 28;       // [NR]
   int* sseq = reinterpret_cast<int*>(smem + LY.seq);
-  const float* sA = reinterpret_cast<const float*>(smem + LY.A);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + LY.misc);
   volatile int* smisc = reinterpret_cast<volatile int*>(smem + LY.misc + 4);  // abort, tiles issued, records issued
 
@@ -204,13 +438,15 @@ __global__ void __launch_bounds__(kThreadsV, 1)
   if (t == 0) {
     for (int s = 0; s < kNT; ++s) {
       mbar_init(tile_full + s, 1);
-      mbar_init(tile_empty + s, 1);
+      mbar_init(tile_empty + s, kSplitWarps);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(lo_ready + s, 4);
-      mbar_init(lo_free + s, 1);
       mbar_init(acc_full + s, 1);
       mbar_init(acc_empty + s, 4);
+    }
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(chunk_full + s, 4);
+      mbar_init(chunk_free + s, 1);
     }
     mbar_init(drain, 1);
     for (int s = 0; s < NR; ++s) {
@@ -235,9 +471,6 @@ __global__ void __launch_bounds__(kThreadsV, 1)
   auto tile_at = [&](int ts) { return smem + LY.tile + ts * kTileBytes; };
   auto rec_at = [&](int rs) { return smem + LY.rec + rs * LY.rec_size; };
   auto gb_at = [&](int gs) { return smem + LY.gb + gs * LY.gb_size; };
-  // first element of the 16-byte block holding element e, for 2-byte / 4-byte arrays
-  auto blk2 = [](size_t e) { return e & ~static_cast<size_t>(7); };
-  auto blk4 = [](size_t e) { return e & ~static_cast<size_t>(3); };
 
   if (warp == kWarpProd) {
     // ================================ producer ================================
@@ -256,7 +489,8 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         if (smisc[0]) break;
         mbar_expect_tx(tile_full + ts, kTileBytes);
         const int row0 = (w.b * H + w.h0) * P;
-        for (int kb = 0; kb < 4; ++kb) tma_load_2d(tile_at(ts) + kb * (kTileBytes / 4), &tmap, kb * 32, row0, tile_full + ts);
+        for (int kb = 0; kb < 4; ++kb)
+          tma_load_2d(tile_at(ts) + kb * (kTileBytes / 4), &tmap, kb * 32, row0, tile_full + ts);
         smisc[1] = i + 1;
         if (i >= NR && !mbar_wait_bounded(rec_empty + rs, static_cast<uint32_t>(((i / NR) - 1) & 1))) {
           abort_with(w.b);
@@ -270,25 +504,11 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         unsigned char* gb = gb_at(gi & 1);
         uint64_t* bar = rec_full + rs;
         const size_t bh0 = static_cast<size_t>(w.b) * H + w.h0;
-        const size_t ug = static_cast<size_t>(w.b) * H + static_cast<size_t>(w.g) * hpg;  // first head of the group
-        const size_t bg = static_cast<size_t>(w.b) * G + w.g;
         constexpr int esz = KIND == 0 ? 2 : 4;
-        uint32_t bytes = static_cast<uint32_t>(HPU * n * P * esz);
-        if (first) {
-          bytes += static_cast<uint32_t>((n + T) * N * 2 + T * N * 2 + T * hpg * P * 2 + hpg * Cp * 4);
-          for (int tau = 0; tau < T; ++tau) {
-            const size_t i0 = (static_cast<size_t>(w.b) * T + tau) * H + static_cast<size_t>(w.g) * hpg;
-            if (KIND == 0) {
-              bytes += static_cast<uint32_t>((blk2(i0 + hpg + 7) - blk2(i0)) * 2);
-            } else {
-              bytes += 2u * static_cast<uint32_t>((blk4(i0 + hpg + 3) - blk4(i0)) * 4);
-            }
-          }
-          if (KIND == 0) bytes += static_cast<uint32_t>(hpg * Cp * 2);
-        }
-        if (KIND == 0 && i == 0) bytes += al16(H * 4);
+        uint32_t bytes = static_cast<uint32_t>(HPU * n * P * esz + HPU * HS * 4);
+        if (first) bytes += static_cast<uint32_t>(2 * T * N * 2 + T * hpg * P * 2);
         mbar_expect_tx(bar, bytes);
-        // committed records of the unit's rows
+        // committed records of the unit's rows, the coefficient tables of its heads
         for (int hu = 0; hu < HPU; ++hu) {
           const size_t base = (bh0 + hu) * C;
           unsigned char* dst = rec + static_cast<size_t>(hu) * C * P * esz;
@@ -297,34 +517,17 @@ __global__ void __launch_bounds__(kThreadsV, 1)
           if (seg1) bulk_g2s(dst, src + (base + head) * P * esz, seg1 * P * esz, bar);
           if (seg2) bulk_g2s(dst + static_cast<size_t>(seg1) * P * esz, src + base * P * esz, seg2 * P * esz, bar);
         }
+        bulk_g2s(rec + LY.rec_tab, d.vtab + bh0 * HS, HPU * HS * 4, bar);
         if (first) {
-          const uint16_t* rk = (KIND == 0 ? d.r_B : d.r_k) + bg * C * N;
-          if (seg1) bulk_g2s(gb + LY.g_key, rk + static_cast<size_t>(head) * N, seg1 * N * 2, bar);
-          if (seg2) bulk_g2s(gb + LY.g_key + seg1 * N * 2, rk, seg2 * N * 2, bar);
           for (int tau = 0; tau < T; ++tau) {
             const size_t bt = static_cast<size_t>(w.b) * T + tau;
             const size_t kq = (bt * G + w.g) * N;
-            bulk_g2s(gb + LY.g_key + (n + tau) * N * 2, (KIND == 0 ? in.Bm : in.k) + kq, N * 2, bar);
+            bulk_g2s(gb + LY.g_key + tau * N * 2, (KIND == 0 ? in.Bm : in.k) + kq, N * 2, bar);
             bulk_g2s(gb + LY.g_q + tau * N * 2, (KIND == 0 ? in.Cm : in.q) + kq, N * 2, bar);
             const size_t i0 = bt * H + static_cast<size_t>(w.g) * hpg;
             bulk_g2s(gb + LY.g_dx + tau * hpg * P * 2, (KIND == 0 ? in.x : in.v) + i0 * P, hpg * P * 2, bar);
-            if (KIND == 0) {
-              bulk_g2s(gb + LY.g_s1 + tau * LY.span, in.dt + blk2(i0),
-                       static_cast<uint32_t>((blk2(i0 + hpg + 7) - blk2(i0)) * 2), bar);
-            } else {
-              const uint32_t sb = static_cast<uint32_t>((blk4(i0 + hpg + 3) - blk4(i0)) * 4);
-              bulk_g2s(gb + LY.g_s1 + tau * LY.span, in.g + blk4(i0), sb, bar);
-              bulk_g2s(gb + LY.g_s2 + tau * LY.span, in.beta + blk4(i0), sb, bar);
-            }
-          }
-          if (KIND == 0) {
-            bulk_g2s(gb + LY.g_la, d.r_la + ug * Cp, hpg * Cp * 4, bar);
-            bulk_g2s(gb + LY.g_dt, d.r_dt + ug * Cp, hpg * Cp * 2, bar);
-          } else {
-            bulk_g2s(gb + LY.g_la, d.r_g + ug * Cp, hpg * Cp * 4, bar);
           }
         }
-        if (KIND == 0 && i == 0) bulk_g2s(smem + LY.A, in.A, al16(H * 4), bar);
         smisc[2] = i + 1;
       }
       // after an abort: the copies already issued land before the CTA frees its memory
@@ -355,9 +558,9 @@ __global__ void __launch_bounds__(kThreadsV, 1)
       const bool ok = sseq[3 * k + 2] != 0;
       unsigned char* gb = gb_at(gi & 1);
       if (first && ok) {
+        // the MMA B operand, canonical K-major: rows = [K_draft | Q] (GDN) or [Q] (Mamba-2)
         const uint16_t* kb = reinterpret_cast<const uint16_t*>(gb + LY.g_key);
         const uint16_t* qb = reinterpret_cast<const uint16_t*>(gb + LY.g_q);
-        // ---- the MMA B operand, canonical K-major: rows = [K_draft | Q] (GDN) or [Q] (Mamba-2) ----
         float* Bs = reinterpret_cast<float*>(gb + LY.g_B);
         for (int it = 0; it < kNmma * N / 4 / 32; ++it) {
           const int rho = (it >> 3) * 8 + (lane & 7);
@@ -366,57 +569,16 @@ __global__ void __launch_bounds__(kThreadsV, 1)
           if (KIND == 0) {
             if (rho < T) src = qb + rho * N;
           } else {
-            if (rho < T) src = kb + (n + rho) * N;
+            if (rho < T) src = kb + rho * N;
             else if (rho < 2 * T) src = qb + (rho - T) * N;
           }
           const float4 v = src ? bf4(reinterpret_cast<const uint2*>(src)[c]) : make_float4(0.f, 0.f, 0.f, 0.f);
           *reinterpret_cast<float4*>(Bs + canon_offset(rho, 4 * c, N)) = v;
         }
-        // ---- the drafts into the ring after the committed records ----
-        const int sigma = lane - n;  // draft index of record `lane`
-        const bool is_draft = sigma >= 0 && sigma < T;
-        const size_t i0s = is_draft ? (static_cast<size_t>(w.b) * T + sigma) * H + static_cast<size_t>(w.g) * hpg : 0;
-        const int hh_hi = min(hpg, w.hh0 + (nunits - i) * HPU);  // heads of this group in this CTA
-        for (int e = w.hh0; e < hh_hi; ++e) {
-          const int h = w.g * hpg + e;
-          const size_t bhe = static_cast<size_t>(w.b) * H + h;
-          if (KIND == 0) {
-            for (int tau = 0; tau < T; ++tau) {
-              const uint16_t* xs = reinterpret_cast<const uint16_t*>(gb + LY.g_dx) + (tau * hpg + e) * P;
-              uint16_t* xd = d.r_x + (bhe * C + ring_slot(head, n + tau, C)) * P;
-              if (P == 64)
-                reinterpret_cast<uint32_t*>(xd)[lane] = reinterpret_cast<const uint32_t*>(xs)[lane];
-              else
-                reinterpret_cast<uint2*>(xd)[lane] = reinterpret_cast<const uint2*>(xs)[lane];
-            }
-            if (is_draft) {
-              const uint16_t dt_bits = reinterpret_cast<const uint16_t*>(gb + LY.g_s1 + sigma * LY.span)[(i0s & 7) + e];
-              const int sl = ring_slot(head, lane, C);
-              d.r_dt[bhe * Cp + sl] = dt_bits;
-              d.r_la[bhe * Cp + sl] = bf(dt_bits) * sA[h];
-            }
-          } else if (is_draft) {
-            d.r_g[bhe * Cp + ring_slot(head, lane, C)] =
-                reinterpret_cast<const float*>(gb + LY.g_s1 + sigma * LY.span)[(i0s & 3) + e];
-          }
-        }
-        if (w.hh0 == 0) {
-          // the drafts' key rows: appended by the CTA that holds the group's first head
-          const size_t bg = static_cast<size_t>(w.b) * G + w.g;
-          uint16_t* rk = KIND == 0 ? d.r_B : d.r_k;
-          for (int tau = 0; tau < T; ++tau)
-            reinterpret_cast<uint2*>(rk + (bg * C + ring_slot(head, n + tau, C)) * N)[lane] =
-                reinterpret_cast<const uint2*>(kb + (n + tau) * N)[lane];
-        }
       }
       if (lane == 0) {
-        if (w.h0 == 0) {
-          if (ok) d.cursor[4 * w.b + 2] = 0;  // verify folds nothing
-          else report_error(d.err, DEVERR_CURSOR, w.b);
-        }
         int* meta = reinterpret_cast<int*>(rec_at(rs) + LY.rec_meta);
-        *reinterpret_cast<int4*>(meta) =
-            make_int4(w.b, w.h0, n | (ok ? 0x100 : 0) | (first ? 0x200 : 0), w.hh0 | ((gi & 1) << 16));
+        *reinterpret_cast<int4*>(meta) = make_int4(w.b, w.h0, n | (ok ? 0x100 : 0), w.hh0 | ((gi & 1) << 16));
         meta[4] = head;
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // B operand -> tensor cores
@@ -430,9 +592,8 @@ __global__ void __launch_bounds__(kThreadsV, 1)
       int issued = 0;
       for (int i = 0; i < nunits; ++i) {
         if (smisc[0]) break;
-        const int ts = i % kNT, rs = i % NR, ab = i & 1, lb = i & 1;
-        bool okw = mbar_wait_bounded(tile_full + ts, static_cast<uint32_t>((i / kNT) & 1));
-        okw = okw && mbar_wait_bounded(ready + rs, static_cast<uint32_t>((i / NR) & 1));
+        const int rs = i % NR, ab = i & 1;
+        bool okw = mbar_wait_bounded(ready + rs, static_cast<uint32_t>((i / NR) & 1));
         if (i >= 2) okw = okw && mbar_wait_bounded(acc_empty + ab, static_cast<uint32_t>(((i / 2) - 1) & 1));
         if (!okw) {
           abort_with((u0 + i) / UPH);
@@ -440,186 +601,107 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         }
         const int4 meta = *reinterpret_cast<const int4*>(rec_at(rs) + LY.rec_meta);
         const uint32_t bsm = smem_u32(gb_at(meta.w >> 16) + LY.g_B);
-        const uint32_t asm_ = smem_u32(tile_at(ts));
         const uint32_t dacc = tmem + kAccCol + ab * 32;
-        tc_fence_after();
-        for (int ks = 0; ks < N / 8; ++ks)
-          mma_tf32(dacc, umma_desc_sw128(asm_ + (ks >> 2) * (kTileBytes / 4) + (ks & 3) * 32, 1024),
-                   umma_desc(bsm + ks * 256, 128, (N / 4) * 128), idesc, ks > 0);
-        issued = i + 1;
-        if (!mbar_wait_bounded(lo_ready + lb, static_cast<uint32_t>((i / 2) & 1))) {
+        bool okc = true;
+        for (int kb = 0; kb < 4; ++kb) {
+          const int q = 4 * i + kb, slot = q % kSlots;
+          if (!mbar_wait_bounded(chunk_full + slot, static_cast<uint32_t>((q / kSlots) & 1))) {
+            okc = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = tmem + slot * kSlotCols;
+          for (int kk = 0; kk < 4; ++kk)  // raw part
+            mma_tf32_ta(dacc, a0 + kk * 8, umma_desc(bsm + (4 * kb + kk) * 256, 128, (N / 4) * 128), idesc,
+                        kb > 0 || kk > 0);
+          for (int kk = 0; kk < 4; ++kk)  // lo part
+            mma_tf32_ta(dacc, a0 + 32 + kk * 8, umma_desc(bsm + (4 * kb + kk) * 256, 128, (N / 4) * 128), idesc, true);
+          mma_commit(chunk_free + slot);
+          issued = i + 1;
+        }
+        if (!okc) {
           abort_with((u0 + i) / UPH);
           break;
         }
-        tc_fence_after();
-        for (int ks = 0; ks < N / 8; ++ks)
-          mma_tf32_ta(dacc, tmem + kLoCol + lb * 128 + ks * 8, umma_desc(bsm + ks * 256, 128, (N / 4) * 128), idesc,
-                      true);
         mma_commit(acc_full + ab);
-        mma_commit(tile_empty + ts);
-        mma_commit(lo_free + lb);
       }
       // every MMA issued has completed before tensor memory is freed
       mma_commit(drain);
       if (issued > 0 || smisc[0]) mbar_wait_bounded(drain, 0);
     }
-  } else if (warp < 4) {
+  } else if (warp < kSplitWarps) {
     // ================================ split warps ================================
-    const int r = warp * 32 + lane;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;
     for (int i = 0; i < nunits; ++i) {
       if (smisc[0]) break;
-      const int ts = i % kNT, lb = i & 1;
-      bool okw = mbar_wait_bounded(tile_full + ts, static_cast<uint32_t>((i / kNT) & 1));
-      if (i >= 2) okw = okw && mbar_wait_bounded(lo_free + lb, static_cast<uint32_t>(((i / 2) - 1) & 1));
-      if (!__all_sync(0xffffffffu, okw)) {
+      const int ts = i % kNT;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(tile_full + ts, static_cast<uint32_t>((i / kNT) & 1)))) {
         if (lane == 0) abort_with((u0 + i) / UPH);
         break;
       }
       const unsigned char* tl = tile_at(ts) + r * 128;
-#pragma unroll
-      for (int kb = 0; kb < 4; ++kb) {
-        uint32_t v[32];
+      bool okc = true;
+#pragma unroll 1
+      for (int kb = half; kb < 4; kb += 2) {
+        const int q = 4 * i + kb, slot = q % kSlots;
+        if (q >= kSlots &&
+            !__all_sync(0xffffffffu, mbar_wait_bounded(chunk_free + slot, static_cast<uint32_t>(((q / kSlots) - 1) & 1)))) {
+          okc = false;
+          break;
+        }
+        uint32_t hi[32], lo[32];
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
           const float4 x = *reinterpret_cast<const float4*>(tl + kb * (kTileBytes / 4) + ((cc ^ (r & 7)) << 4));
-          v[4 * cc + 0] = __float_as_uint(x.x - __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u));
-          v[4 * cc + 1] = __float_as_uint(x.y - __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u));
-          v[4 * cc + 2] = __float_as_uint(x.z - __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u));
-          v[4 * cc + 3] = __float_as_uint(x.w - __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u));
+          const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hi[4 * cc + e] = __float_as_uint(xs[e]);
+            lo[4 * cc + e] = __float_as_uint(xs[e] - __uint_as_float(__float_as_uint(xs[e]) & 0xFFFFE000u));
+          }
         }
-        tmem_st32(tmem + kLoCol + lb * 128 + (static_cast<uint32_t>(warp * 32) << 16) + kb * 32, v);
+        const uint32_t ta = tmem + slot * kSlotCols + (static_cast<uint32_t>(quarter * 32) << 16);
+        tmem_st32(ta, hi);
+        tmem_st32(ta + 32, lo);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(chunk_full + slot);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(lo_ready + lb);
+      if (!okc) {
+        if (lane == 0) abort_with((u0 + i) / UPH);
+        break;
+      }
+      // the tile has been read: the producer may refill the stage
+      if (lane == 0) mbar_arrive(tile_empty + ts);
     }
   } else {
     // ================================ epilogue warps ================================
     // The four warps decide together (named barrier 2) whether to go on, so
     // that none of them is left waiting at the barrier.
-    const int ew = warp - 4;  // also the tensor-memory lane quarter
+    const int ew = warp - kWarpEpi;  // also the tensor-memory lane quarter
     const int r = ew * 32 + lane;
     const int hu = r / P, p = r - hu * P;
     for (int i = 0; i < nunits; ++i) {
       const int rs = i % NR, ab = i & 1;
-      const bool got = mbar_wait_bounded(ready + rs, static_cast<uint32_t>((i / NR) & 1));
+      bool got = mbar_wait_bounded(ready + rs, static_cast<uint32_t>((i / NR) & 1));
+      got = got && mbar_wait_bounded(acc_full + ab, static_cast<uint32_t>((i / 2) & 1));
       if (!epi_sync_and(got)) {
         if (ew == 0 && lane == 0) abort_with((u0 + i) / UPH);
-        break;
-      }
-      const unsigned char* rec = rec_at(rs);
-      const int* meta = reinterpret_cast<const int*>(rec + LY.rec_meta);
-      const int b = meta[0], h0 = meta[1], n = meta[2] & 0xFF;
-      const bool ok = (meta[2] & 0x100) != 0, first = (meta[2] & 0x200) != 0;
-      const int hh0 = meta[3] & 0xFFFF;
-      const int head = meta[4];
-      unsigned char* gb = gb_at(meta[3] >> 16);
-      const int nr = n + T;
-      float* dqt = reinterpret_cast<float*>(gb + LY.g_dq);  // [C][4]: k_j . q_tau
-      float* dkt = reinterpret_cast<float*>(gb + LY.g_dk);  // [C][4]: k_j . k_{n+tau} (GDN)
-      const uint16_t* kb = reinterpret_cast<const uint16_t*>(gb + LY.g_key);
-      if (ok && first) {
-        // key dot products of the group, shared by its heads; item = (8 records, one column)
-        const uint16_t* qb = reinterpret_cast<const uint16_t*>(gb + LY.g_q);
-        const int ncol = KIND == 0 ? T : 2 * T;
-        const int nblk = (nr + 7) >> 3;
-        for (int it = ew; it < nblk * ncol; it += 4) {
-          const int jb = it / ncol, c = it - jb * ncol;
-          const uint16_t* other = c < T ? qb + c * N : kb + (n + c - T) * N;
-          const float4 o4 = bf4(reinterpret_cast<const uint2*>(other)[lane]);
-          float part[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = 8 * jb + e;
-            part[e] = j < nr ? dot4(bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane]), o4) : 0.f;
-          }
-          const float tot = reduce8(part, lane);
-          const int j = 8 * jb + (lane >> 2);
-          if ((lane & 3) == 0 && j < nr) {
-            if (c < T) dqt[j * 4 + c] = tot;
-            else dkt[j * 4 + c - T] = tot;
-          }
-        }
-      }
-      epi_sync();
-      if (ok) {
-        // decay weights and coefficient tables, one (head, draft position) item per warp
-        // at a time; each item is a suffix scan over the records 0..n+tau (FP32, as in
-        // the decode kernels), lane j holding record j
-        const int slot_lane = lane < n ? ring_slot(head, lane, C) : 0;
-        const int sigma = lane - n;
-        const bool is_draft = sigma >= 0 && sigma < T;
-        for (int it = ew; it < HPU * T; it += 4) {
-          const int hu_t = it / T, tau = it - hu_t * T;
-          const int hh = hh0 + hu_t, h = h0 + hu_t;
-          float* co = reinterpret_cast<float*>(gb + LY.g_coef) + hh * HS;
-          const float* la_row = reinterpret_cast<const float*>(gb + LY.g_la) + hh * Cp;
-          const size_t i0s = is_draft ? (static_cast<size_t>(b) * T + sigma) * H + static_cast<size_t>(h - hh) : 0;
-          const int m = n + tau;  // draft tau is record m
-          const float dqj = lane < nr ? dqt[lane * 4 + tau] : 0.f;
-          if (KIND == 0) {
-            const uint16_t dt_bits =
-                is_draft ? reinterpret_cast<const uint16_t*>(gb + LY.g_s1 + sigma * LY.span)[(i0s & 7) + hh] : 0;
-            const uint16_t* dtr = reinterpret_cast<const uint16_t*>(gb + LY.g_dt) + hh * Cp;
-            const float lj = lane < n ? la_row[slot_lane] : (is_draft ? bf(dt_bits) * sA[h] : 0.f);
-            const float dtj = lane < n ? bf(dtr[slot_lane]) : (is_draft ? bf(dt_bits) : 0.f);
-            // w_j = prod_{i=j+1..m} a_i, D = prod_{i<=m} a_i
-            const float v = suffix_sum(lane <= m ? lj : 0.f, lane, m);
-            const float ex = __shfl_down_sync(0xffffffffu, v, 1);
-            const float W = lane <= m ? expf(lane < m ? ex : 0.f) : 0.f;
-            if (lane < nr) co[lane * 4 + tau] = W * dqj * dtj;
-            if (lane == 0) co[4 * C + tau] = expf(v);
-          } else {
-            float g_d = 0.f, beta_d = 0.f;
-            if (is_draft) {
-              g_d = reinterpret_cast<const float*>(gb + LY.g_s1 + sigma * LY.span)[(i0s & 3) + hh];
-              beta_d = reinterpret_cast<const float*>(gb + LY.g_s2 + sigma * LY.span)[(i0s & 3) + hh];
-            }
-            const float lj = lane < n ? la_row[slot_lane] : g_d;
-            const float dkj = lane < nr ? dkt[lane * 4 + tau] : 0.f;
-            // tW_j = prod_{i=j+1..m} a_i (j <= m), tWk_j = prod_{i=j+1..m-1} a_i (j < m)
-            const float vq = suffix_sum(lane <= m ? lj : 0.f, lane, m);
-            const float exq = __shfl_down_sync(0xffffffffu, vq, 1);
-            const float tW = lane <= m ? expf(lane < m ? exq : 0.f) : 0.f;
-            const float vk = suffix_sum(lane < m ? lj : 0.f, lane, m - 1);
-            const float exk = __shfl_down_sync(0xffffffffu, vk, 1);
-            const float tWk = lane < m ? expf(lane + 1 < m ? exk : 0.f) : 0.f;
-            const float a_t = expf(__shfl_sync(0xffffffffu, g_d, m));
-            const float b_t = __shfl_sync(0xffffffffu, beta_d, m);
-            if (lane < n) {
-              co[lane * 4 + tau] = tWk * dkj;        // coefficient of u_j[r] in S k_tau
-              co[(C + lane) * 4 + tau] = tW * dqj;   // coefficient of u_j[r] in S q_tau
-            }
-            float* sc = co + 8 * C;
-            if (lane == 0) {
-              sc[tau] = expf(vq);                   // G2
-              sc[4 + tau] = m > 0 ? expf(vk) : 1.f;  // G1
-              sc[8 + tau] = a_t;
-              sc[12 + tau] = b_t;
-            }
-            if (is_draft) {  // lane n + s: M[tau][s] (s < tau), Qd[tau][s] (s <= tau)
-              sc[16 + tau * 4 + sigma] = sigma < tau ? b_t * a_t * tWk * dkj : 0.f;
-              sc[32 + tau * 4 + sigma] = sigma <= tau ? tW * dqj : 0.f;
-            }
-            if (lane >= T && lane < kT) {  // unused draft slots of the T x T tables
-              sc[16 + tau * 4 + lane] = 0.f;
-              sc[32 + tau * 4 + lane] = 0.f;
-            }
-          }
-        }
-      }
-      // the tables are complete; the accumulator of this unit is needed next
-      const bool acc_ok = mbar_wait_bounded(acc_full + ab, static_cast<uint32_t>((i / 2) & 1));
-      if (!epi_sync_and(acc_ok)) {
-        if (ew == 0 && lane == 0) abort_with(b);
         break;
       }
       tc_fence_after();
       float acc[8];
       tmem_ld8(tmem + kAccCol + ab * 32 + (static_cast<uint32_t>(ew * 32) << 16), acc);
-      const int hh = hh0 + hu;
-      const float* co = reinterpret_cast<const float*>(gb + LY.g_coef) + hh * HS;
+      const unsigned char* rec = rec_at(rs);
+      const int* meta = reinterpret_cast<const int*>(rec + LY.rec_meta);
+      const int b = meta[0], h0 = meta[1], n = meta[2] & 0xFF;
+      const bool ok = (meta[2] & 0x100) != 0;
+      const int hh = (meta[3] & 0xFFFF) + hu;
+      const int head = meta[4];
+      const unsigned char* gb = gb_at(meta[3] >> 16);
+      const float* co = reinterpret_cast<const float*>(rec + LY.rec_tab) + hu * HS;
       const float4* co4 = reinterpret_cast<const float4*>(co);
       const int h = h0 + hu;
       if (ok) {
@@ -636,9 +718,12 @@ __global__ void __launch_bounds__(kThreadsV, 1)
             a2 = fmaf(c.z, xv, a2);
             a3 = fmaf(c.w, xv, a3);
           }
+          uint16_t* xring = d.r_x + (static_cast<size_t>(b) * H + h) * C * P + p;
           for (int s = 0; s < T; ++s) {
             const float4 c = co4[n + s];
-            const float xv = bf(xd[s * hpg * P]);
+            const uint16_t xbits = xd[s * hpg * P];
+            xring[static_cast<size_t>(ring_slot(head, n + s, C)) * P] = xbits;  // the draft into the ring
+            const float xv = bf(xbits);
             a0 = fmaf(c.x, xv, a0);
             a1 = fmaf(c.y, xv, a1);
             a2 = fmaf(c.z, xv, a2);
@@ -720,8 +805,11 @@ cudaError_t launch_v128(const LayerDev& d, const CUtensorMap& tmap, const TokenI
   const int hpg = d.H / d.G;
   const int U = hpg / HPU;  // units per group
   const int NR = U + 1 < kMaxNR ? U + 1 : kMaxNR;
-  const VL LY = vlayout(KIND, d.C, d.Cp, d.H, hpg, P, NR);
+  const VL LY = vlayout(KIND, d.C, hpg, P, NR);
   if (LY.total > 227 * 1024) return cudaErrorInvalidConfiguration;
+  verify_prep_kernel<KIND><<<d.B * d.G, kPrepThreads, 0, s>>>(d, in, T);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   const int UPH = d.H / HPU;
   const int total = d.B * UPH;
   int grid = d.num_sms > 0 ? d.num_sms : 1;
@@ -733,7 +821,7 @@ cudaError_t launch_v128(const LayerDev& d, const CUtensorMap& tmap, const TokenI
   }
   grid = (total + per - 1) / per;
   auto kernel = verify128_kernel<KIND, P>;
-  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kernel), LY.total);
+  e = set_smem_limit(reinterpret_cast<const void*>(kernel), LY.total);
   if (e != cudaSuccess) return e;
   kernel<<<grid, kThreadsV, LY.total, s>>>(tmap, d, in, T, y, per, NR);
   return cudaGetLastError();
@@ -741,13 +829,15 @@ cudaError_t launch_v128(const LayerDev& d, const CUtensorMap& tmap, const TokenI
 
 }  // namespace
 
+int verify_table_stride(int kind, int C) { return head_stride(kind, C); }
+
 bool verify128_supports(const LayerDev& d) {
-  if (d.N != N || (d.P != 64 && d.P != 128) || d.T_max > kT || d.C > kMaxRec) return false;
+  if (d.N != N || (d.P != 64 && d.P != 128) || d.T_max > kT || d.C > kMaxRec || !d.vtab) return false;
   const int HPU = kRows / d.P, hpg = d.H / d.G;
   if (hpg % HPU != 0) return false;
   const int U = hpg / HPU;
   const int NR = U + 1 < kMaxNR ? U + 1 : kMaxNR;
-  return vlayout(d.kind, d.C, d.Cp, d.H, hpg, d.P, NR).total <= 227 * 1024;
+  return vlayout(d.kind, d.C, hpg, d.P, NR).total <= 227 * 1024;
 }
 
 cudaError_t make_ckpt_tmap(const LayerDev& d, CUtensorMap* out) {
@@ -773,7 +863,8 @@ cudaError_t make_ckpt_tmap(const LayerDev& d, CUtensorMap* out) {
 cudaError_t launch_verify128(const LayerDev& d, const CUtensorMap& tmap, const TokenIn& in, int T, float* y,
                              cudaStream_t s) {
   if (!verify128_supports(d) || T < 1 || T > kT) return cudaErrorInvalidValue;
-  if (d.kind == 0) return d.P == 64 ? launch_v128<0, 64>(d, tmap, in, T, y, s) : launch_v128<0, 128>(d, tmap, in, T, y, s);
+  if (d.kind == 0)
+    return d.P == 64 ? launch_v128<0, 64>(d, tmap, in, T, y, s) : launch_v128<0, 128>(d, tmap, in, T, y, s);
   return d.P == 64 ? launch_v128<1, 64>(d, tmap, in, T, y, s) : launch_v128<1, 128>(d, tmap, in, T, y, s);
 }
 

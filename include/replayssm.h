@@ -117,7 +117,12 @@ typedef struct {
  *                       matrix scale f32 [B][H]
  * scratch    int32 [B] per-sequence arrival counters (the last CTA of a
  *            sequence to finish a launch advances its cursor).  Zeroed by
- *            rs_create_cache; every launch leaves it zero again.
+ *            rs_create_cache; every launch leaves it zero again.  When
+ *            max_draft > 0 a second section follows on a 256-byte boundary:
+ *            f32 [B][H][S] per-head coefficient tables that rs_verify writes
+ *            and reads within one call (decay weights times key dot products
+ *            of the chunkwise form), S = 4C + 4 for Mamba-2 and 8C + 48 for
+ *            Gated DeltaNet.
  */
 typedef struct {
   void *ckpt, *ring, *cursor, *read_copy, *scratch;

@@ -42,6 +42,15 @@ def test_query_sizes_config1_and_config2():
     assert st == rs.RS_OK and sz[3] == 256 * 128 * 64 * 64 + 256 * 128 * 64 * 8 + 256 * 128 * 4
 
 
+def test_query_sizes_scratch_with_drafts():
+    """max_draft > 0 adds the verify coefficient tables after the arrival counters."""
+    st, sz = rs.rs_query_sizes(rs.rs_config(0, 512, 128, 8, 64, 128, 16, 4, 0))
+    C = 16 + 4
+    assert st == rs.RS_OK and sz[4] == 512 * 4 + 512 * 128 * (4 * C + 4) * 4
+    st, sz = rs.rs_query_sizes(rs.rs_config(1, 3, 32, 16, 128, 128, 16, 4, 0))
+    assert st == rs.RS_OK and sz[4] == 256 + 3 * 32 * (8 * C + 48) * 4
+
+
 @pytest.mark.parametrize("fields,status", [
     ((2, 1, 4, 1, 16, 16, 4, 0, 0), rs.RS_ERR_RANGE),        # kind
     ((0, 1, 4, 1, 16, 16, 4, 0, 7), rs.RS_ERR_RANGE),        # read mode
