@@ -76,6 +76,10 @@ cudaError_t launch_decode128(const LayerDev& d, const TokenIn& in, float* y, cud
 // verify kernel on tcgen05 for d_state 128, d_head 64 or 128 (verify128.cu); it
 // reads the checkpoint through a TMA tensor map made once per cache
 bool verify128_supports(const LayerDev& d);
+// commit / flush for d_state 128, d_head 64 or 128 (fold128.cu)
+bool fold128_supports(const LayerDev& d);
+cudaError_t launch_fold128(const LayerDev& d, int mode, const int* accepted, const uint8_t* mask, int T_pending,
+                           cudaStream_t s);
 int verify_table_stride(int kind, int C);
 cudaError_t make_ckpt_tmap(const LayerDev& d, CUtensorMap* out);
 cudaError_t launch_verify128(const LayerDev& d, const CUtensorMap& tmap, const TokenIn& in, int T, float* y,
