@@ -34,7 +34,8 @@ RS_DEVERR_CURSOR = 2
 RS_DEVERR_TIMEOUT = 3
 
 EXPORTED = ("rs_query_sizes", "rs_create_cache", "rs_destroy_cache", "rs_decode_step", "rs_verify",
-            "rs_commit", "rs_flush", "rs_get_device_error", "rs_status_string", "rs_decode_step_noalloc")
+            "rs_commit", "rs_flush", "rs_get_device_error", "rs_status_string", "rs_decode_step_noalloc",
+            "rs_selftest_wait_timeout")
 
 
 class rs_config(ctypes.Structure):
@@ -77,6 +78,7 @@ def load() -> ctypes.CDLL:
         lib.rs_commit.argtypes = [vp, vp, vp]
         lib.rs_flush.argtypes = [vp, vp, vp]
         lib.rs_get_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
+        lib.rs_selftest_wait_timeout.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), vp]
         lib.rs_decode_step_noalloc.argtypes = [ctypes.POINTER(rs_config), ctypes.POINTER(rs_buffers),
                                                ctypes.POINTER(rs_inputs), vp, vp]
         lib.rs_status_string.argtypes = [ctypes.c_int]
@@ -148,3 +150,10 @@ def rs_decode_step_noalloc(cfg: rs_config, bufs: rs_buffers, inputs: rs_inputs, 
     """Decode step with the library's fixed arrival-counter array (no handle, no scratch buffer)."""
     return load().rs_decode_step_noalloc(ctypes.byref(cfg), ctypes.byref(bufs), ctypes.byref(inputs),
                                          ctypes.c_void_p(y_ptr), ctypes.c_void_p(stream))
+
+
+def rs_selftest_wait_timeout(limit_us: int, stream: int):
+    """Returns (status, device code); see the header."""
+    code = ctypes.c_int32(-1)
+    st = load().rs_selftest_wait_timeout(ctypes.c_int32(limit_us), ctypes.byref(code), ctypes.c_void_p(stream))
+    return st, code.value

@@ -20,10 +20,12 @@
 //    unit it only publishes a 16-byte descriptor and signals `ready`;
 //  * eight computing warps each own rows w, w+8, .. of every unit: lane = 4
 //    columns, 4 lanes per row split the buffered records, an 8-row
-//    transpose-reduce forms the row sums.  A flush unit folds in registers
-//    (register-held coefficients, shuffles, packed fma.rn.f32x2) and stores the
-//    checkpoint once.  No barrier spans the warps, except an NVFP4 flush unit,
-//    whose matrix amax is exchanged through a bounded mbarrier.
+//    transpose-reduce forms the row sums.  A flush unit folds in registers:
+//    each warp writes the fold coefficients of its 8 rows into a small table
+//    in shared memory, reads them back four records at a time by broadcast,
+//    and accumulates with packed fma.rn.f32x2; it stores the checkpoint once.
+//    No barrier spans the warps, except an NVFP4 flush unit, whose matrix
+//    amax is exchanged through a bounded mbarrier.
 #include "common.cuh"
 
 namespace rs {
@@ -35,6 +37,9 @@ constexpr int kMaxSeq128 = 64;       // sequences one CTA may cover
 constexpr int kThreads128 = kThreads + 64;  // 8 computing warps, prologue warp, producer warp
 constexpr int kPrologueWarp = kThreads / 32;
 constexpr int kProducerWarp = kThreads / 32 + 1;
+// row stride (floats) of a warp's fold-coefficient table: kMaxRec padded so the
+// 32 lanes' stores (8 rows x 4 records) fall in 32 different banks
+constexpr int kMtabRow = kMaxRec + 4;
 
 __host__ __device__ __forceinline__ int al16(int x) { return (x + 15) & ~15; }
 __host__ __device__ __forceinline__ int al128(int x) { return (x + 127) & ~127; }
@@ -48,7 +53,7 @@ enum : int { CO_GAMMA = 0, CO_A = 1, CO_BETA = 2, CO_KQ = 3, CO_MATSCALE = 4 };
 struct Lay128 {
   int st_tile, st_rec, st_meta, st_size;
   int gb_key, gb_q, gb_cur, gb_la, gb_dt, gb_s1, gb_s2, gb_rs, gb_ms, gb_qf, gb_kf, gb_coef, gb_size;
-  int pe_A, pe_bars, pe_seq, pe_misc, pe_size;
+  int pe_A, pe_bars, pe_seq, pe_misc, pe_mtab, pe_size;
 };
 
 __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int C, int Cp, int H, int hpg) {
@@ -78,6 +83,7 @@ __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int
   l.pe_bars = o;  o += 4 * 8 * 8;       // full, empty, ready, amax x 8 stages
   l.pe_seq = o;   o += 3 * kMaxSeq128 * 4;
   l.pe_misc = o;  o += 16;
+  l.pe_mtab = o;  o += (kThreads / 32) * 8 * kMtabRow * 4;  // per computing warp: fold coefficients [8 rows][records]
   l.pe_size = al128(o);
   return l;
 }
@@ -134,6 +140,8 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   uint64_t* amaxbar = full + 24;
   int* sseq = reinterpret_cast<int*>(pbase + LY.pe_seq);
   volatile int* smisc = reinterpret_cast<volatile int*>(pbase + LY.pe_misc);  // abort, issued, producer done
+  // this warp's fold-coefficient table (computing warps)
+  float* mt = reinterpret_cast<float*>(pbase + LY.pe_mtab) + (warp < kThreads / 32 ? warp : 0) * 8 * kMtabRow;
 
   const int total_units = d.B * H;
   const int u0 = blockIdx.x * units_per_cta;
@@ -474,29 +482,33 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
           const float tot = reduce8(part, lane);
           if (jl == 0) yrow[Rq] = fmaf(gamma * row_scale, tot, ry);
           if (flush) {
-            // lane (kq, jl) holds m_j[Rq] = w_j dt_j x_j[Rq] for records j = 4 jc + jl
-            float mreg[kMaxRec / 4];
-#pragma unroll
-            for (int jc = 0; jc < kMaxRec / 4; ++jc) {
+            // m_j[row] = w_j dt_j x_j[row] for records j = 0..n (current at n) into this warp's
+            // table (lane (kq, jl) writes records jl, jl + 4, .. of row slot kq; zero past n to
+            // the end of the last quad), then four records per broadcast read
+            for (int jc = 0; 4 * jc <= n; ++jc) {
               const int j = 4 * jc + jl;
-              mreg[jc] = j <= n ? co[2 * C + j] * bf(j < n ? xb[j * P + Rq] : cur[Rq]) : 0.f;
+              mt[kq * kMtabRow + j] = j <= n ? co[2 * C + j] * bf(j < n ? xb[j * P + Rq] : cur[Rq]) : 0.f;
             }
+            __syncwarp();
             float4 acc[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] = scale4(gamma, s4[e]);
+            for (int jq = 0; 4 * jq <= n; ++jq) {
+              float4 k4[4];
 #pragma unroll
-            for (int jc = 0; jc < kMaxRec / 4; ++jc) {
-              if (4 * jc > n) break;
+              for (int i = 0; i < 4; ++i)
+                k4[i] = 4 * jq + i <= n ? bf4(reinterpret_cast<const uint2*>(kb + (4 * jq + i) * N)[lane])
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-              for (int jj = 0; jj < 4; ++jj) {
-                const int j = 4 * jc + jj;
-                if (j > n) break;
-                const float4 k4 = bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                  acc[e] = axpy4x2(__shfl_sync(0xffffffffu, mreg[jc], 4 * e + jj), k4, acc[e]);
+              for (int e = 0; e < 8; ++e) {
+                const float4 m4 = *reinterpret_cast<const float4*>(mt + e * kMtabRow + 4 * jq);
+                acc[e] = axpy4x2(m4.x, k4[0], acc[e]);
+                acc[e] = axpy4x2(m4.y, k4[1], acc[e]);
+                acc[e] = axpy4x2(m4.z, k4[2], acc[e]);
+                acc[e] = axpy4x2(m4.w, k4[3], acc[e]);
               }
             }
+            __syncwarp();
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               __stcs(gS4 + (warp + 8 * (r0 + e)) * SEG + lane, acc[e]);
@@ -606,30 +618,33 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
             if (!flush) urow[Rq] = uu;
           }
           if (flush) {
-            // lane (kq, jl) holds m_j[Rq] = a w_j u_j[Rq] for records j = 4 jc + jl
-            float mreg[kMaxRec / 4];
-#pragma unroll
-            for (int jc = 0; jc < kMaxRec / 4; ++jc) {
+            // m_j[row] = a w_j u_j[row] for records j < n into this warp's table (zero past n to
+            // the end of the last quad), then four records per broadcast read
+            for (int jc = 0; 4 * jc < n; ++jc) {
               const int j = 4 * jc + jl;
-              mreg[jc] = j < n ? co[2 * C + j] * ub[j * P + Rq] : 0.f;
+              mt[kq * kMtabRow + j] = j < n ? co[2 * C + j] * ub[j * P + Rq] : 0.f;
             }
+            __syncwarp();
             float4 acc[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
               acc[e] = axpy4(__shfl_sync(0xffffffffu, uu, 4 * e), kc4, scale4(a * gamma, s4[e]));
+            for (int jq = 0; 4 * jq < n; ++jq) {
+              float4 k4[4];
 #pragma unroll
-            for (int jc = 0; jc < kMaxRec / 4; ++jc) {
-              if (4 * jc >= n) break;
+              for (int i = 0; i < 4; ++i)
+                k4[i] = 4 * jq + i < n ? bf4(reinterpret_cast<const uint2*>(kb + (4 * jq + i) * N)[lane])
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-              for (int jj = 0; jj < 4; ++jj) {
-                const int j = 4 * jc + jj;
-                if (j >= n) break;
-                const float4 k4 = bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                  acc[e] = axpy4x2(__shfl_sync(0xffffffffu, mreg[jc], 4 * e + jj), k4, acc[e]);
+              for (int e = 0; e < 8; ++e) {
+                const float4 m4 = *reinterpret_cast<const float4*>(mt + e * kMtabRow + 4 * jq);
+                acc[e] = axpy4x2(m4.x, k4[0], acc[e]);
+                acc[e] = axpy4x2(m4.y, k4[1], acc[e]);
+                acc[e] = axpy4x2(m4.z, k4[2], acc[e]);
+                acc[e] = axpy4x2(m4.w, k4[3], acc[e]);
               }
             }
+            __syncwarp();
 #pragma unroll
             for (int e = 0; e < 8; ++e) __stcs(gS4 + (warp + 8 * (r0 + e)) * SEG + lane, acc[e]);
           }

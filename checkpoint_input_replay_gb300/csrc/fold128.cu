@@ -18,9 +18,10 @@
 // warp stages each folding unit (the state matrix and its records) with bulk
 // copies and, once per group, the group's keys and ring decay rows; the
 // prologue warp computes, once per group, each head's fold weights from one
-// suffix scan; eight computing warps fold in registers (register-held
-// coefficients, shuffles, packed fma.rn.f32x2), store the checkpoint once and
-// refresh the low-precision read copy where there is one.
+// suffix scan; eight computing warps fold in registers (fold coefficients from
+// a per-warp shared-memory table, four records per broadcast read, packed
+// fma.rn.f32x2), store the checkpoint once and refresh the low-precision read
+// copy where there is one.
 #include "common.cuh"
 
 namespace rs {
@@ -32,6 +33,9 @@ constexpr int kMaxSeqF = 64;
 constexpr int kThreadsF = kThreads + 64;  // 8 computing warps, prologue warp, producer warp
 constexpr int kPrologueWarp = kThreads / 32;
 constexpr int kProducerWarp = kThreads / 32 + 1;
+// row stride (floats) of a warp's fold-coefficient table: kMaxRec padded so the
+// 32 lanes' stores (8 rows x 4 records) fall in 32 different banks
+constexpr int kMtabRow = kMaxRec + 4;
 
 __host__ __device__ __forceinline__ int al16(int x) { return (x + 15) & ~15; }
 __host__ __device__ __forceinline__ int al128(int x) { return (x + 127) & ~127; }
@@ -41,7 +45,7 @@ __host__ __device__ __forceinline__ int fold_stride(int C) { return (C + 4 + 3) 
 struct LayF {
   int st_tile, st_rec, st_meta, st_size;
   int gb_key, gb_la, gb_dt, gb_coef, gb_size;
-  int pe_bars, pe_seq, pe_misc, pe_cnt, pe_size;
+  int pe_bars, pe_seq, pe_misc, pe_cnt, pe_mtab, pe_size;
 };
 
 __host__ __device__ __forceinline__ LayF layf(int kind, int P, int C, int Cp, int hpg) {
@@ -62,6 +66,7 @@ __host__ __device__ __forceinline__ LayF layf(int kind, int P, int C, int Cp, in
   l.pe_seq = o;   o += 3 * kMaxSeqF * 4;
   l.pe_misc = o;  o += 16;
   l.pe_cnt = o;   o += al16((kThreadsF / 32 + 1) * 4);  // per-warp counts of the sequence scan, last-CTA flag
+  l.pe_mtab = o;  o += (kThreads / 32) * 8 * kMtabRow * 4;  // per computing warp: fold coefficients [8 rows][records]
   l.pe_size = al128(o);
   return l;
 }
@@ -115,6 +120,8 @@ __global__ void __launch_bounds__(kThreadsF, 1)
   uint64_t* amaxbar = full + 24;
   int* sseq = reinterpret_cast<int*>(pbase + LY.pe_seq);
   volatile int* smisc = reinterpret_cast<volatile int*>(pbase + LY.pe_misc);  // abort, issued, producer done
+  // this warp's fold-coefficient table (computing warps)
+  float* mt = reinterpret_cast<float*>(pbase + LY.pe_mtab) + (warp < kThreads / 32 ? warp : 0) * 8 * kMtabRow;
 
   // --- the folding sequences, numbered in order (every CTA computes the same list) ---
   int* s_cnt = reinterpret_cast<int*>(pbase + LY.pe_cnt);
@@ -361,34 +368,38 @@ __global__ void __launch_bounds__(kThreadsF, 1)
 #pragma unroll
       for (int r0 = 0; r0 < RW; r0 += 8) {
         const int Rq = warp + 8 * (r0 + kq);
-        // lane (kq, jl) holds m_j[Rq] = coefficient * record j for records j = 4 jc + jl
-        float mreg[kMaxRec / 4];
-#pragma unroll
-        for (int jc = 0; jc < kMaxRec / 4; ++jc) {
+        // m_j[row] = coefficient * record j (j < n) into this warp's table, lane (kq, jl)
+        // writing records jl, jl + 4, .. of row slot kq (zero past n to the end of the
+        // last quad); then four records per broadcast read
+        for (int jc = 0; 4 * jc < n; ++jc) {
           const int j = 4 * jc + jl;
           float rv = 0.f;
           if (j < n) {
             if (KIND == 0) rv = bf(reinterpret_cast<const uint16_t*>(st + LY.st_rec)[j * P + Rq]);
             else rv = reinterpret_cast<const float*>(st + LY.st_rec)[j * P + Rq];
           }
-          mreg[jc] = j < n ? co[j] * rv : 0.f;
+          mt[kq * kMtabRow + j] = j < n ? co[j] * rv : 0.f;
         }
+        __syncwarp();
         float4 acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = scale4(gamma, sT4[(warp + 8 * (r0 + e)) * SEG + lane]);
+        for (int jq = 0; 4 * jq < n; ++jq) {
+          float4 k4[4];
 #pragma unroll
-        for (int jc = 0; jc < kMaxRec / 4; ++jc) {
-          if (4 * jc >= n) break;
+          for (int i = 0; i < 4; ++i)
+            k4[i] = 4 * jq + i < n ? bf4(reinterpret_cast<const uint2*>(kb + (4 * jq + i) * N)[lane])
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int j = 4 * jc + jj;
-            if (j >= n) break;
-            const float4 k4 = bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane]);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              acc[e] = axpy4x2(__shfl_sync(0xffffffffu, mreg[jc], 4 * e + jj), k4, acc[e]);
+          for (int e = 0; e < 8; ++e) {
+            const float4 m4 = *reinterpret_cast<const float4*>(mt + e * kMtabRow + 4 * jq);
+            acc[e] = axpy4x2(m4.x, k4[0], acc[e]);
+            acc[e] = axpy4x2(m4.y, k4[1], acc[e]);
+            acc[e] = axpy4x2(m4.z, k4[2], acc[e]);
+            acc[e] = axpy4x2(m4.w, k4[3], acc[e]);
           }
         }
+        __syncwarp();
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           __stcs(gS4 + (warp + 8 * (r0 + e)) * SEG + lane, acc[e]);

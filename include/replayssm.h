@@ -231,6 +231,16 @@ rs_status rs_get_device_error(rs_cache *cache, rs_stream stream, int32_t *code);
 rs_status rs_decode_step_noalloc(const rs_config *cfg, const rs_buffers *bufs, const rs_inputs *in, float *y,
                                  rs_stream stream);
 
+/* Self-test of the bounded wait every kernel uses on its mbarriers: one GPU
+ * thread waits on an mbarrier that nothing completes, giving up after
+ * limit_us microseconds (1..1000000), with the same primitive and the same
+ * give-up rule (time limit or 2^22 polls) as the hot-path kernels.  Writes the
+ * outcome to *code_out: RS_DEVERR_TIMEOUT when the wait gave up (the expected
+ * result), RS_DEVERR_NONE if the barrier was somehow seen complete.  No GPU
+ * fault is involved and the context stays usable.  Synchronises `stream`.
+ * RS_ERR_NULL / RS_ERR_RANGE for bad arguments, RS_ERR_CUDA on a CUDA error. */
+rs_status rs_selftest_wait_timeout(int32_t limit_us, int32_t *code_out, rs_stream stream);
+
 /* Static description of a status code. */
 const char *rs_status_string(rs_status status);
 

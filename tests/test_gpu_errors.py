@@ -7,7 +7,8 @@ import pytest
 import torch
 
 import checkpoint_input_replay_gb300 as rs
-from tests.harness import Pair
+from checkpoint_input_replay_gb300 import _lib
+from tests.harness import Pair, assert_close
 from workloads import configs
 from workloads.configs import MAMBA2, LayerShape
 
@@ -66,3 +67,21 @@ def test_corrupt_cursor_sets_error():
     assert pair.cache.device_error() == rs._lib.RS_DEVERR_CURSOR
     after = pair.cache.cursor.cpu().numpy()
     assert after[1, 1] == 99 and after[0, 1] == 2 and after[2, 1] == 2
+
+
+def test_bounded_wait_gives_up_without_a_fault():
+    """The bounded mbarrier wait of the kernels, on a barrier nothing completes:
+    it gives up after the limit, reports RS_DEVERR_TIMEOUT, and the context
+    stays usable (a decode step afterwards still matches the oracle)."""
+    import time
+    stream = torch.cuda.current_stream().cuda_stream
+    t0 = time.perf_counter()
+    st, code = _lib.rs_selftest_wait_timeout(2000, stream)
+    dt = time.perf_counter() - t0
+    assert st == _lib.RS_OK and code == _lib.RS_DEVERR_TIMEOUT
+    assert 0.002 <= dt < 1.0
+    assert _lib.rs_selftest_wait_timeout(0, stream)[0] == _lib.RS_ERR_RANGE
+    pair = Pair(configs.config0())
+    y, ref = pair.decode(0)
+    assert_close(y, ref, "decode after the timeout self-test")
+    assert pair.cache.device_error() == 0
