@@ -428,6 +428,8 @@ def main(argv=None):
     ap.add_argument("--verify-only", choices=["mamba2", "gdn"],
                     help="time only one verify + commit leg, at --verify-batch sequences (a profiling case)")
     ap.add_argument("--verify-batch", type=int, default=512)
+    ap.add_argument("--read-copy-only", choices=["fp8", "nvfp4"],
+                    help="time only the non-flush decode with a read copy, at --batch sequences (a profiling case)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -446,6 +448,11 @@ def main(argv=None):
         res = verify_leg(wl, dev, args.steps, args.warmup, lambda: None)
         if rank == 0:
             print(json.dumps({"verify": res}))
+        return 0
+    if args.read_copy_only:
+        res = read_copy_leg(configs.config1(batch=args.batch), dev, args.read_copy_only, args.steps, args.warmup)
+        if rank == 0:
+            print(json.dumps({"read_copy": res}))
         return 0
     if world > 1:
         import torch.distributed as dist

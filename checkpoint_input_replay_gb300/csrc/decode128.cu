@@ -14,10 +14,14 @@
 //    keys and query, the current tokens of all its heads, the ring's per-head
 //    decay rows, the current per-head scalars, the read-copy scales -- is
 //    staged once per group into one of two group buffers;
-//  * a prologue warp, once per group, computes the key dot products, each
-//    head's decay suffix scan and its per-record coefficient table (into the
-//    group buffer), and appends the group's current token to the ring; per
-//    unit it only publishes a 16-byte descriptor and signals `ready`;
+//  * a prologue warp, once per group, converts the query (and current key) to
+//    FP32 and appends the group's current tokens to the ring; per unit it
+//    publishes a 16-byte descriptor and signals `ready`;
+//  * at the first unit of a group the eight computing warps build the group's
+//    key dot products (records shared out over the warps) and then the
+//    per-head coefficient tables (one decay suffix scan per head, heads shared
+//    out over the warps) in the group buffer, the two phases ordered by
+//    bounded mbarriers;
 //  * eight computing warps each own rows w, w+8, .. of every unit: lane = 4
 //    columns, 4 lanes per row split the buffered records, an 8-row
 //    transpose-reduce forms the row sums.  A flush unit folds in registers:
@@ -52,7 +56,7 @@ enum : int { CO_GAMMA = 0, CO_A = 1, CO_BETA = 2, CO_KQ = 3, CO_MATSCALE = 4 };
 // Shared-memory layout (bytes): [stages][2 group buffers][persistent].
 struct Lay128 {
   int st_tile, st_rec, st_meta, st_size;
-  int gb_key, gb_q, gb_cur, gb_la, gb_dt, gb_s1, gb_s2, gb_rs, gb_ms, gb_qf, gb_kf, gb_coef, gb_size;
+  int gb_key, gb_q, gb_cur, gb_la, gb_dt, gb_s1, gb_s2, gb_rs, gb_ms, gb_qf, gb_kf, gb_dq, gb_coef, gb_size;
   int pe_A, pe_bars, pe_seq, pe_misc, pe_mtab, pe_size;
 };
 
@@ -76,11 +80,12 @@ __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int
   l.gb_ms = o;    o += read == READ_NVFP4 ? span : 0;
   l.gb_qf = o;    o += N * 4;
   l.gb_kf = o;    o += kind == 0 ? 0 : N * 4;
+  l.gb_dq = o;    o += al16(C * 4) * 2;  // k_j . q, then (GDN) k_j . k_cur
   l.gb_coef = o;  o += hpg * coef_stride(C) * 4;
   l.gb_size = al128(o);
   o = 0;
   l.pe_A = o;     o += al16(H * 4);
-  l.pe_bars = o;  o += 4 * 8 * 8;       // full, empty, ready, amax x 8 stages
+  l.pe_bars = o;  o += 4 * 8 * 8 + 16;  // full, empty, ready, amax x 8 stages; group dots, group tables
   l.pe_seq = o;   o += 3 * kMaxSeq128 * 4;
   l.pe_misc = o;  o += 16;
   l.pe_mtab = o;  o += (kThreads / 32) * 8 * kMtabRow * 4;  // per computing warp: fold coefficients [8 rows][records]
@@ -138,6 +143,8 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   uint64_t* empty = full + 8;
   uint64_t* ready = full + 16;
   uint64_t* amaxbar = full + 24;
+  uint64_t* dots_bar = full + 32;  // computing warps: the group's key dot products are in place
+  uint64_t* tab_bar = full + 33;   // computing warps: the group's coefficient tables are in place
   int* sseq = reinterpret_cast<int*>(pbase + LY.pe_seq);
   volatile int* smisc = reinterpret_cast<volatile int*>(pbase + LY.pe_misc);  // abort, issued, producer done
   // this warp's fold-coefficient table (computing warps)
@@ -184,6 +191,8 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       mbar_init(ready + s, 1);
       mbar_init(amaxbar + s, kThreads / 32);
     }
+    mbar_init(dots_bar, kThreads / 32);
+    mbar_init(tab_bar, kThreads / 32);
     smisc[0] = 0;
     smisc[1] = 0;
     smisc[2] = 0;
@@ -296,58 +305,19 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       const int slot = ring_slot(head, n, C);
       unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * (gi & 1);
       if (first && ok) {
-        // ---- once per group: dot products, coefficient tables, ring appends ----
+        // ---- once per group: the query (and current key) in FP32, ring appends ----
         const size_t ug = static_cast<size_t>(w.b) * H + static_cast<size_t>(w.g) * hpg;
         const uint16_t* kb = reinterpret_cast<const uint16_t*>(gb + LY.gb_key);
         const float4 q4 = bf4(reinterpret_cast<const uint2*>(gb + LY.gb_q)[lane]);
         const float4 kc4 = bf4(reinterpret_cast<const uint2*>(kb + n * N)[lane]);
         reinterpret_cast<float4*>(gb + LY.gb_qf)[lane] = q4;
         if (KIND == 1) reinterpret_cast<float4*>(gb + LY.gb_kf)[lane] = kc4;
-        float dq = 0.f, dk = 0.f;  // lane j: k_j . q, k_j . k_cur
-        for (int j0 = 0; j0 <= n; j0 += 8) {
-          float pq[8], pk[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = j0 + e;
-            const float4 kj = j <= n ? bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane])
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-            pq[e] = dot4(kj, q4);
-            pk[e] = KIND == 1 ? dot4(kj, kc4) : 0.f;
-          }
-          const float tq = __shfl_sync(0xffffffffu, reduce8(pq, lane), 4 * (lane & 7));
-          if ((lane >> 3) == (j0 >> 3)) dq = tq;
-          if (KIND == 1) {
-            const float tk = __shfl_sync(0xffffffffu, reduce8(pk, lane), 4 * (lane & 7));
-            if ((lane >> 3) == (j0 >> 3)) dk = tk;
-          }
-        }
-        const int slot_lane = lane < n ? ring_slot(head, lane, C) : 0;
         const int hh_hi = min(hpg, w.hh + (nunits - i));  // heads of this group in this CTA
-        for (int e = w.hh; e < hh_hi; ++e) {
-          float* co = reinterpret_cast<float*>(gb + LY.gb_coef) + e * CS;
-          const float* la_row = reinterpret_cast<const float*>(gb + LY.gb_la) + e * Cp;
-          const size_t ue = ug + e;
-          if (KIND == 0) {
-            const uint16_t* dt_row = reinterpret_cast<const uint16_t*>(gb + LY.gb_dt) + e * Cp;
-            const uint16_t dt_bits = reinterpret_cast<const uint16_t*>(gb + LY.gb_s1)[(ug & 7) + e];
-            const float dt_cur = bf(dt_bits);
-            const float la_cur = dt_cur * sA[w.g * hpg + e];
-            // records 0..n (current at n): w_j = exp(sum_{i=j+1..n} la_i), gamma = exp(sum_{i<=n} la_i)
-            const float sv = suffix_sum(lane < n ? la_row[slot_lane] : (lane == n ? la_cur : 0.f), lane, n);
-            const float excl = __shfl_down_sync(0xffffffffu, sv, 1);
-            const float Wl = lane <= n ? expf(lane < n ? excl : 0.f) : 0.f;
-            const float dtl = lane < n ? bf(dt_row[slot_lane]) : (lane == n ? dt_cur : 0.f);
-            if (lane <= n) {
-              co[lane] = Wl * dtl * dq;     // output coefficient on x_j[r]
-              co[2 * C + lane] = Wl * dtl;  // fold coefficient on x_j[r]
-            }
-            if (lane == 0) {
-              co[3 * C + CO_GAMMA] = expf(sv);
-              if (READ == READ_NVFP4)
-                co[3 * C + CO_MATSCALE] = reinterpret_cast<const float*>(gb + LY.gb_ms)[(ug & 3) + e];
-            }
-            if (!flush) {
-              // append the current token of head e: x row, dt, log decay
+        if (!flush) {
+          // append the current tokens of the group's heads in this CTA to the ring
+          for (int e = w.hh; e < hh_hi; ++e) {
+            const size_t ue = ug + e;
+            if (KIND == 0) {
               const uint16_t* xc = reinterpret_cast<const uint16_t*>(gb + LY.gb_cur) + e * P;
               uint16_t* dst = d.r_x + (ue * C + slot) * P;
               if (P == 64)
@@ -355,29 +325,12 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
               else
                 reinterpret_cast<uint2*>(dst)[lane] = reinterpret_cast<const uint2*>(xc)[lane];
               if (lane == 0) {
+                const uint16_t dt_bits = reinterpret_cast<const uint16_t*>(gb + LY.gb_s1)[(ug & 7) + e];
                 d.r_dt[ue * Cp + slot] = dt_bits;
-                d.r_la[ue * Cp + slot] = la_cur;
+                d.r_la[ue * Cp + slot] = bf(dt_bits) * sA[w.g * hpg + e];
               }
-            }
-          } else {
-            // buffered records 0..n-1: w_j = exp(sum_{i=j+1..n-1} g_i), gamma = exp(sum_{i<n} g_i)
-            const float sv = suffix_sum(lane < n ? la_row[slot_lane] : 0.f, lane, n - 1);
-            const float excl = __shfl_down_sync(0xffffffffu, sv, 1);
-            const float Wl = lane < n ? expf(lane + 1 < n ? excl : 0.f) : 0.f;
-            const float g_cur = reinterpret_cast<const float*>(gb + LY.gb_s1)[(ug & 3) + e];
-            const float a = expf(g_cur);
-            if (lane < n) {
-              co[lane] = Wl * dk;         // coefficient of u_j[r] in S k
-              co[C + lane] = Wl * dq;     // coefficient of u_j[r] in S q
-              co[2 * C + lane] = a * Wl;  // fold coefficient of u_j[r]
-            }
-            const float kq_dot = __shfl_sync(0xffffffffu, dq, n);
-            if (lane == 0) {
-              co[3 * C + CO_GAMMA] = n > 0 ? expf(sv) : 1.f;
-              co[3 * C + CO_A] = a;
-              co[3 * C + CO_BETA] = reinterpret_cast<const float*>(gb + LY.gb_s2)[(ug & 3) + e];
-              co[3 * C + CO_KQ] = kq_dot;
-              if (!flush) d.r_g[ue * Cp + slot] = g_cur;
+            } else if (lane == 0) {
+              d.r_g[ue * Cp + slot] = reinterpret_cast<const float*>(gb + LY.gb_s1)[(ug & 3) + e];
             }
           }
         }
@@ -390,8 +343,8 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       }
       if (lane == 0) {
         unsigned char* st = smem + static_cast<size_t>(LY.st_size) * s;
-        *reinterpret_cast<int4*>(st + LY.st_meta) =
-            make_int4(w.u, n | (flush ? 0x100 : 0) | (ok ? 0x200 : 0), slot, w.hh | ((gi & 1) << 16));
+        *reinterpret_cast<int4*>(st + LY.st_meta) = make_int4(
+            w.u, n | (flush ? 0x100 : 0) | (ok ? 0x200 : 0) | (first ? 0x400 : 0), slot, w.hh | ((gi & 1) << 16));
         reinterpret_cast<int*>(st + LY.st_meta)[4] = 0;  // NVFP4 matrix amax
       }
       __syncwarp();
@@ -411,6 +364,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
 
   // =============================== computing warps ===============================
   uint32_t amax_phase = 0;
+  int groups = 0;  // groups whose tables these warps have built
   for (int i = 0; i < nunits; ++i) {
     if (smisc[0]) break;
     const int s = i % stages;
@@ -423,6 +377,98 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     }
     unsigned char* st = smem + static_cast<size_t>(LY.st_size) * s;
     const int4 meta = *reinterpret_cast<const int4*>(st + LY.st_meta);
+    // ---- first unit of a group in this CTA: the group's key dot products and the
+    // coefficient tables of its heads, shared out over the eight warps (two bounded
+    // mbarriers order the phases) ----
+    if ((meta.y & 0x600) == 0x600) {
+      const int n = meta.y & 0xFF;
+      const int hh_lo = meta.w & 0xFFFF;
+      const size_t ug = static_cast<size_t>(meta.x) - hh_lo;  // first unit of the group
+      unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * (meta.w >> 16);
+      const uint16_t* kb = reinterpret_cast<const uint16_t*>(gb + LY.gb_key);
+      float* gdq = reinterpret_cast<float*>(gb + LY.gb_dq);
+      float* gdk = gdq + al16(C * 4) / 4;
+      const float4 q4 = reinterpret_cast<const float4*>(gb + LY.gb_qf)[lane];
+      const float4 kc4 =
+          KIND == 1 ? reinterpret_cast<const float4*>(gb + LY.gb_kf)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = warp; j <= n; j += kThreads / 32) {
+        const float4 kj = bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane]);
+        float pq = dot4(kj, q4), pk = KIND == 1 ? dot4(kj, kc4) : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          pq += __shfl_xor_sync(0xffffffffu, pq, o);
+          if (KIND == 1) pk += __shfl_xor_sync(0xffffffffu, pk, o);
+        }
+        if (lane == 0) {
+          gdq[j] = pq;
+          if (KIND == 1) gdk[j] = pk;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dots_bar);
+      bool okg = __all_sync(0xffffffffu, mbar_wait_bounded(dots_bar, static_cast<uint32_t>(groups & 1)));
+      if (okg) {
+        const float dq = lane <= n ? gdq[lane] : 0.f;  // lane j: k_j . q
+        const float dk = (KIND == 1 && lane <= n) ? gdk[lane] : 0.f;  // lane j: k_j . k_cur
+        const int head = meta.z - n < 0 ? meta.z - n + C : meta.z - n;
+        const int slot_lane = lane < n ? ring_slot(head, lane, C) : 0;
+        const int hh_hi = min(hpg, hh_lo + (nunits - i));  // heads of this group in this CTA
+        for (int e = hh_lo + warp; e < hh_hi; e += kThreads / 32) {
+          float* co = reinterpret_cast<float*>(gb + LY.gb_coef) + e * CS;
+          const float* la_row = reinterpret_cast<const float*>(gb + LY.gb_la) + e * Cp;
+          if (KIND == 0) {
+            const uint16_t* dt_row = reinterpret_cast<const uint16_t*>(gb + LY.gb_dt) + e * Cp;
+            const uint16_t dt_bits = reinterpret_cast<const uint16_t*>(gb + LY.gb_s1)[(ug & 7) + e];
+            const float dt_cur = bf(dt_bits);
+            const float la_cur = dt_cur * sA[static_cast<int>(ug % H) + e];
+            // records 0..n (current at n): w_j = exp(sum_{i=j+1..n} la_i), gamma = exp(sum_{i<=n} la_i)
+            const float sv = suffix_sum(lane < n ? la_row[slot_lane] : (lane == n ? la_cur : 0.f), lane, n);
+            const float excl = __shfl_down_sync(0xffffffffu, sv, 1);
+            const float Wl = lane <= n ? expf(lane < n ? excl : 0.f) : 0.f;
+            const float dtl = lane < n ? bf(dt_row[slot_lane]) : (lane == n ? dt_cur : 0.f);
+            if (lane <= n) {
+              co[lane] = Wl * dtl * dq;     // output coefficient on x_j[r]
+              co[2 * C + lane] = Wl * dtl;  // fold coefficient on x_j[r]
+            }
+            if (lane == 0) {
+              co[3 * C + CO_GAMMA] = expf(sv);
+              if (READ == READ_NVFP4)
+                co[3 * C + CO_MATSCALE] = reinterpret_cast<const float*>(gb + LY.gb_ms)[(ug & 3) + e];
+            }
+          } else {
+            // buffered records 0..n-1: w_j = exp(sum_{i=j+1..n-1} g_i), gamma = exp(sum_{i<n} g_i)
+            const float sv = suffix_sum(lane < n ? la_row[slot_lane] : 0.f, lane, n - 1);
+            const float excl = __shfl_down_sync(0xffffffffu, sv, 1);
+            const float Wl = lane < n ? expf(lane + 1 < n ? excl : 0.f) : 0.f;
+            const float g_cur = reinterpret_cast<const float*>(gb + LY.gb_s1)[(ug & 3) + e];
+            const float a = expf(g_cur);
+            if (lane < n) {
+              co[lane] = Wl * dk;         // coefficient of u_j[r] in S k
+              co[C + lane] = Wl * dq;     // coefficient of u_j[r] in S q
+              co[2 * C + lane] = a * Wl;  // fold coefficient of u_j[r]
+            }
+            const float kq_dot = __shfl_sync(0xffffffffu, dq, n);
+            if (lane == 0) {
+              co[3 * C + CO_GAMMA] = n > 0 ? expf(sv) : 1.f;
+              co[3 * C + CO_A] = a;
+              co[3 * C + CO_BETA] = reinterpret_cast<const float*>(gb + LY.gb_s2)[(ug & 3) + e];
+              co[3 * C + CO_KQ] = kq_dot;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tab_bar);
+        okg = __all_sync(0xffffffffu, mbar_wait_bounded(tab_bar, static_cast<uint32_t>(groups & 1)));
+      }
+      ++groups;
+      if (!okg) {
+        if (lane == 0) {
+          report_error(d.err, DEVERR_TIMEOUT, (u0 + i) / H);
+          smisc[0] = 1;
+        }
+        break;
+      }
+    }
     if (meta.y & 0x200) {
       const size_t u = static_cast<size_t>(meta.x);
       const int n = meta.y & 0xFF;
