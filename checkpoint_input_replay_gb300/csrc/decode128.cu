@@ -6,7 +6,9 @@
 // the work is fed and split, so that the computing warps do little besides the
 // pass over the state matrix:
 //
-//  * a work unit is one (sequence, head) state matrix [P][128]; CTA c owns a
+//  * a work unit is one (sequence, head) state matrix [P][128] -- on a layer
+//    with a low-precision read copy, the non-flush units hold four heads of a
+//    group, whose codes fit where one FP32 matrix goes -- and CTA c owns a
 //    contiguous range of units, so it meets each group (and sequence) once;
 //  * a producer warp stages each unit with two bulk copies (cp.async.bulk):
 //    the state matrix (or its read copy) and the buffered records of that
@@ -60,11 +62,15 @@ struct Lay128 {
   int pe_A, pe_bars, pe_seq, pe_misc, pe_mtab, pe_size;
 };
 
+// heads in a non-flush unit of a read-copy layer: 4 heads' codes fit where one
+// FP32 matrix goes, and the unit's fixed costs are shared by 4 heads
+__host__ __device__ __forceinline__ int read_heads(int read) { return read == READ_NONE ? 1 : 4; }
+
 __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int C, int Cp, int H, int hpg) {
   Lay128 l;
   int o = 0;
   l.st_tile = o;  o += P * N * 4;
-  l.st_rec = o;   o += kind == 0 ? al16(C * P * 2) : C * P * 4;
+  l.st_rec = o;   o += kind == 0 ? read_heads(read) * al16(C * P * 2) : C * P * 4;
   l.st_meta = o;  o += 32;              // int4 descriptor, NVFP4 amax word
   l.st_size = al128(o);
   o = 0;
@@ -109,10 +115,13 @@ struct Walk {
     g = h / hpg;
     hh = h - g * hpg;
   }
-  __device__ __forceinline__ void next(int H, int hpg) {
-    ++u;
-    ++h;
-    if (++hh == hpg) {
+  // advance by `step` heads (1, or HR for a non-flush read-copy unit; HR divides
+  // heads-per-group and H)
+  __device__ __forceinline__ void next(int H, int hpg, int step) {
+    u += step;
+    h += step;
+    hh += step;
+    if (hh == hpg) {
       hh = 0;
       ++g;
     }
@@ -131,6 +140,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int RW = P / 8;  // rows per computing warp
   constexpr int tile = P * N;
+  constexpr int HR = READ == READ_NONE ? 1 : 4;  // heads of a non-flush unit
   const int H = d.H, G = d.G, C = d.C, L = d.L, Cp = d.Cp;
   const int hpg = H / G;
   const int CS = coef_stride(C);
@@ -154,7 +164,6 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   const int u0 = blockIdx.x * units_per_cta;
   const int u1 = min(u0 + units_per_cta, total_units);
   if (u0 >= u1) return;
-  const int nunits = u1 - u0;
   const int b0 = u0 / H, b1 = (u1 - 1) / H;
   const int nseq = b1 - b0 + 1;
 
@@ -199,6 +208,11 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   }
   __syncthreads();
 
+  // heads in the unit that starts at sequence b: HR unless b flushes this step
+  auto step_of = [&](int b) {
+    const int k = b - b0;
+    return (HR > 1 && !(sseq[3 * k + 2] != 0 && sseq[3 * k + 1] + 1 == L)) ? HR : 1;
+  };
   // first element of the 16-byte block holding element e, for 2-byte / 4-byte arrays
   auto blk2 = [](size_t e) { return e & ~static_cast<size_t>(7); };
   auto blk4 = [](size_t e) { return e & ~static_cast<size_t>(3); };
@@ -209,7 +223,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     Walk w;
     w.start(u0, H, hpg);
     int gi = -1;
-    for (int i = 0; i < nunits; ++i, w.next(H, hpg)) {
+    for (int i = 0; w.u < u1; ++i, w.next(H, hpg, step_of(w.b))) {
       const int s = i % stages;
       if (i >= stages && !mbar_wait_bounded(empty + s, static_cast<uint32_t>(((i / stages) - 1) & 1))) break;
       if (smisc[0]) break;
@@ -224,8 +238,9 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       const size_t u = static_cast<size_t>(w.u);
       const int seg1 = min(n, C - head), seg2 = n - seg1;
       constexpr int esz = KIND == 0 ? 2 : 4;
+      const int nh = step_of(w.b);  // heads in this unit
       const uint32_t tb = (READ == READ_NONE || flush) ? tile * 4 : (READ == READ_FP8 ? tile : tile / 2);
-      uint32_t bytes = tb + static_cast<uint32_t>(n) * P * esz;
+      uint32_t bytes = nh * (tb + static_cast<uint32_t>(n) * P * esz);
       const size_t ug = static_cast<size_t>(w.b) * H + static_cast<size_t>(w.g) * hpg;  // first unit of the group
       const size_t bg = static_cast<size_t>(w.b) * G + w.g;
       const uint32_t s1b = KIND == 0 ? static_cast<uint32_t>((blk2(ug + hpg + 7) - blk2(ug)) * 2)
@@ -242,12 +257,16 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       mbar_expect_tx(bar, bytes);
       // the unit: state matrix (or read copy) and this head's buffered records
       if (READ == READ_NONE || flush) bulk_g2s(st + LY.st_tile, d.ckpt + u * tile, tb, bar);
-      else bulk_g2s(st + LY.st_tile, d.rc_codes + u * tb, tb, bar);
+      else bulk_g2s(st + LY.st_tile, d.rc_codes + u * tb, nh * tb, bar);  // nh consecutive heads
       const unsigned char* rsrc = KIND == 0 ? reinterpret_cast<const unsigned char*>(d.r_x)
                                             : reinterpret_cast<const unsigned char*>(d.r_u);
       constexpr size_t rrow = static_cast<size_t>(P) * esz;
-      if (seg1) bulk_g2s(st + LY.st_rec, rsrc + (u * C + head) * rrow, seg1 * rrow, bar);
-      if (seg2) bulk_g2s(st + LY.st_rec + seg1 * rrow, rsrc + u * C * rrow, seg2 * rrow, bar);
+      for (int hu = 0; hu < nh; ++hu) {
+        unsigned char* rdst = st + LY.st_rec + static_cast<size_t>(hu) * al16(C * P * 2);
+        const size_t uh = u + hu;
+        if (seg1) bulk_g2s(rdst, rsrc + (uh * C + head) * rrow, seg1 * rrow, bar);
+        if (seg2) bulk_g2s(rdst + seg1 * rrow, rsrc + uh * C * rrow, seg2 * rrow, bar);
+      }
       // the group: keys and query, current tokens, decay rows, scalars, scales
       if (first) {
         const uint16_t* rk = (KIND == 0 ? d.r_B : d.r_k) + bg * C * N;
@@ -285,7 +304,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     Walk w;
     w.start(u0, H, hpg);
     int gi = -1, consumed = 0;
-    for (int i = 0; i < nunits; ++i, w.next(H, hpg)) {
+    for (int i = 0; w.u < u1; ++i, w.next(H, hpg, step_of(w.b))) {
       if (smisc[0]) break;
       const int s = i % stages;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(full + s, static_cast<uint32_t>((i / stages) & 1)))) {
@@ -312,7 +331,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
         const float4 kc4 = bf4(reinterpret_cast<const uint2*>(kb + n * N)[lane]);
         reinterpret_cast<float4*>(gb + LY.gb_qf)[lane] = q4;
         if (KIND == 1) reinterpret_cast<float4*>(gb + LY.gb_kf)[lane] = kc4;
-        const int hh_hi = min(hpg, w.hh + (nunits - i));  // heads of this group in this CTA
+        const int hh_hi = min(hpg, w.hh + (u1 - w.u));  // heads of this group in this CTA
         if (!flush) {
           // append the current tokens of the group's heads in this CTA to the ring
           for (int e = w.hh; e < hh_hi; ++e) {
@@ -365,7 +384,9 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   // =============================== computing warps ===============================
   uint32_t amax_phase = 0;
   int groups = 0;  // groups whose tables these warps have built
-  for (int i = 0; i < nunits; ++i) {
+  Walk wc;
+  wc.start(u0, H, hpg);
+  for (int i = 0; wc.u < u1; ++i, wc.next(H, hpg, step_of(wc.b))) {
     if (smisc[0]) break;
     const int s = i % stages;
     if (!__all_sync(0xffffffffu, mbar_wait_bounded(ready + s, static_cast<uint32_t>((i / stages) & 1)))) {
@@ -412,7 +433,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
         const float dk = (KIND == 1 && lane <= n) ? gdk[lane] : 0.f;  // lane j: k_j . k_cur
         const int head = meta.z - n < 0 ? meta.z - n + C : meta.z - n;
         const int slot_lane = lane < n ? ring_slot(head, lane, C) : 0;
-        const int hh_hi = min(hpg, hh_lo + (nunits - i));  // heads of this group in this CTA
+        const int hh_hi = min(hpg, hh_lo + (u1 - meta.x));  // heads of this group in this CTA
         for (int e = hh_lo + warp; e < hh_hi; e += kThreads / 32) {
           float* co = reinterpret_cast<float*>(gb + LY.gb_coef) + e * CS;
           const float* la_row = reinterpret_cast<const float*>(gb + LY.gb_la) + e * Cp;
@@ -469,12 +490,75 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
         break;
       }
     }
-    if (meta.y & 0x200) {
-      const size_t u = static_cast<size_t>(meta.x);
+    const int nh_unit = (READ != READ_NONE && !(meta.y & 0x100)) ? HR : 1;  // heads of this unit
+    if (KIND == 0 && READ != READ_NONE && nh_unit == HR && (meta.y & 0x200)) {
+      // non-flush unit of a read-copy layer: HR heads, their chains interleaved
+      // (record terms, code decoding and row reductions of the heads are independent)
+      const int n = meta.y & 0xFF;
+      const int hh0 = meta.w & 0xFFFF;
+      const size_t uh0 = static_cast<size_t>(meta.x);
+      const unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * (meta.w >> 16);
+      const float* cob = reinterpret_cast<const float*>(gb + LY.gb_coef);
+      const uint16_t* curb = reinterpret_cast<const uint16_t*>(gb + LY.gb_cur);
+      const float4 q4 = reinterpret_cast<const float4*>(gb + LY.gb_qf)[lane];
+      constexpr int TBH = READ == READ_FP8 ? tile : tile / 2;  // code bytes per head
+      const int recH = al16(C * P * 2) / 2;                   // record elements per head
+      const uint16_t* xb = reinterpret_cast<const uint16_t*>(st + LY.st_rec);
+#pragma unroll
+      for (int r0 = 0; r0 < RW; r0 += 8) {
+        const int Rq = warp + 8 * (r0 + kq);
+        float ry[HR], gsc[HR], part[HR][8];
+#pragma unroll
+        for (int hu = 0; hu < HR; ++hu) {
+          const float* co = cob + (hh0 + hu) * CS;
+          ry[hu] = jl == 0 ? co[n] * bf(curb[(hh0 + hu) * P + Rq]) : 0.f;
+          gsc[hu] = co[3 * C + CO_GAMMA] * (READ == READ_FP8
+                                                ? reinterpret_cast<const float*>(gb + LY.gb_rs)[(hh0 + hu) * P + Rq]
+                                                : co[3 * C + CO_MATSCALE]);
+        }
+        // buffered terms: lanes 4kq..4kq+3 split the records 0..n-1 (lane jl = 0 took record n)
+        for (int j = jl; j < n; j += 4) {
+#pragma unroll
+          for (int hu = 0; hu < HR; ++hu)
+            ry[hu] = fmaf(cob[(hh0 + hu) * CS + j], bf(xb[hu * recH + j * P + Rq]), ry[hu]);
+        }
+        // the checkpoint term from the low-precision copies
+#pragma unroll
+        for (int hu = 0; hu < HR; ++hu) {
+          const unsigned char* cb = st + LY.st_tile + hu * TBH;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int R = warp + 8 * (r0 + e);
+            if (READ == READ_FP8) {
+              const uint32_t wd = reinterpret_cast<const uint32_t*>(cb + R * N)[lane];
+              const float2 lo = e4m3x2_to_f32x2(static_cast<uint16_t>(wd & 0xFFFFu));
+              const float2 hi = e4m3x2_to_f32x2(static_cast<uint16_t>(wd >> 16));
+              part[hu][e] = dot4(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
+            } else {
+              const uint32_t wd = reinterpret_cast<const uint16_t*>(cb + R * (N / 2))[lane];
+              const float2 lo = e2m1x2_to_f32x2(wd & 0xFFu);
+              const float2 hi = e2m1x2_to_f32x2(wd >> 8);
+              const float bs = e4m3_to_f32(gb[LY.gb_rs + ((hh0 + hu) * P + R) * (N / 16) + (lane >> 2)]);
+              part[hu][e] = bs * dot4(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
+            }
+          }
+        }
+#pragma unroll
+        for (int hu = 0; hu < HR; ++hu) {
+          float r = ry[hu];
+          r += __shfl_xor_sync(0xffffffffu, r, 1);
+          r += __shfl_xor_sync(0xffffffffu, r, 2);
+          const float tot = reduce8(part[hu], lane);
+          if (jl == 0) y[(uh0 + hu) * P + Rq] = fmaf(gsc[hu], tot, r);
+        }
+      }
+    }
+    for (int hu = 0; hu < 1 && nh_unit == 1 && (meta.y & 0x200); ++hu) {
+      const size_t u = static_cast<size_t>(meta.x) + hu;
       const int n = meta.y & 0xFF;
       const bool flush = (meta.y & 0x100) != 0;
       const int slot = meta.z;
-      const int hh = meta.w & 0xFFFF;
+      const int hh = (meta.w & 0xFFFF) + hu;
       const unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * (meta.w >> 16);
       const float* co = reinterpret_cast<const float*>(gb + LY.gb_coef) + hh * CS;
       const uint16_t* kb = reinterpret_cast<const uint16_t*>(gb + LY.gb_key);
@@ -485,7 +569,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       const float4 q4 = reinterpret_cast<const float4*>(gb + LY.gb_qf)[lane];
       const float gamma = co[3 * C + CO_GAMMA];
       if (KIND == 0) {
-        const uint16_t* xb = reinterpret_cast<const uint16_t*>(st + LY.st_rec);
+        const uint16_t* xb = reinterpret_cast<const uint16_t*>(st + LY.st_rec + static_cast<size_t>(hu) * al16(C * P * 2));
 #pragma unroll
         for (int r0 = 0; r0 < RW; r0 += 8) {
           const int Rq = warp + 8 * (r0 + kq);
@@ -498,8 +582,8 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
           float part[8];
           float row_scale = 1.f;
           if (READ != READ_NONE && !flush) {
-            // non-flush: the checkpoint term from the low-precision copy
-            const unsigned char* cb = st + LY.st_tile;
+            // non-flush: the checkpoint term from the low-precision copy of head hu of the unit
+            const unsigned char* cb = st + LY.st_tile + hu * (READ == READ_FP8 ? tile : tile / 2);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const int R = warp + 8 * (r0 + e);
@@ -710,17 +794,21 @@ cudaError_t launch128(const LayerDev& d, const TokenIn& in, float* y, cudaStream
   long stages = budget / LY.st_size;
   if (stages > 8) stages = 8;
   // a group buffer is rewritten two groups later: every unit of that earlier
-  // group must have left the pipeline, which holds when stages <= hpg + 1
-  if (stages > hpg + 1) stages = hpg + 1;
+  // group must have left the pipeline, which holds when stages <= (units per
+  // group) + 1; a non-flush read-copy unit holds read_heads(READ) heads
+  const int upg = hpg / read_heads(READ);
+  if (stages > upg + 1) stages = upg + 1;
   if (stages < 1) return cudaErrorInvalidConfiguration;
   const size_t smem = static_cast<size_t>(LY.st_size) * stages + 2u * LY.gb_size + LY.pe_size;
+  // each CTA takes a contiguous range of heads, a multiple of read_heads(READ)
+  const int hr = read_heads(READ);
   const int total = d.B * d.H;
   int grid = d.num_sms > 0 ? d.num_sms : 1;
-  if (grid > total) grid = total;
-  int per = (total + grid - 1) / grid;
+  if (grid > total / hr) grid = total / hr;
+  int per = ((total + grid - 1) / grid + hr - 1) / hr * hr;
   while (per / d.H + 2 > kMaxSeq128) {
     grid *= 2;
-    per = (total + grid - 1) / grid;
+    per = ((total + grid - 1) / grid + hr - 1) / hr * hr;
   }
   grid = (total + per - 1) / per;
   auto kernel = decode128_kernel<KIND, READ, P>;
@@ -744,6 +832,8 @@ cudaError_t launch128_p(const LayerDev& d, const TokenIn& in, float* y, cudaStre
 
 bool decode128_supports(const LayerDev& d) {
   if (d.N != N || (d.P != 64 && d.P != 128)) return false;
+  // a read-copy layer's non-flush units span read_heads heads of one group
+  if (d.H % read_heads(d.read_mode) != 0 || (d.H / d.G) % read_heads(d.read_mode) != 0) return false;
   const Lay128 LY = lay128(d.kind, d.read_mode, d.P, d.C, d.Cp, d.H, d.H / d.G);
   return static_cast<long>(LY.st_size) + 2L * LY.gb_size + LY.pe_size <= 227L * 1024;
 }

@@ -107,3 +107,39 @@ def test_config4_full_4096_steps(mode, bound):
     assert np.all(per_window[1:] <= bound)
     assert aggregate <= bound
     assert per_window[-32:].mean() <= 1.1 * per_window[1:33].mean()
+
+
+@pytest.mark.parametrize("mode", ["fp8", "nvfp4"])
+def test_read_copy_d128_mixed_window_positions(mode):
+    """d_state 128, heads-per-group a multiple of four: the non-flush units of a
+    read-copy layer hold four heads, flush units one.  Verify + commit rounds with
+    per-sequence accepted counts put the sequences at different window positions,
+    so single decode launches mix both kinds of unit.  Flushing sequences must
+    match the FP32 recurrence, the others the oracle's quantised-read output."""
+    shape = LayerShape(MAMBA2, batch=5, n_heads=16, n_groups=2, d_head=64, d_state=128, ring_len=4, max_draft=2)
+    pair = Pair(configs.Mamba2Workload(shape, seed=43, s0_std=0.1), read_mode=mode)
+    _check_initial_copy(pair, mode, list(range(5)))
+    for t in range(2):  # first window: the copy and the oracle's copy come from the same state
+        y, ref = pair.decode(t)
+        assert_close(y, pair.oracle.last_read_out, f"{mode} step {t}")
+    for s, acc in enumerate([[0, 1, 2, 1, 0], [2, 0, 1, 2, 1], [1, 2, 0, 0, 2]]):
+        y, ref = pair.verify(s, 2)
+        assert_close(y, ref, f"{mode} verify {s}")
+        pair.commit(s, 2, accepted=acc)
+        pair.check_cursor(f"{mode} commit {s}")
+    mixed = 0
+    for t in range(2, 26):
+        y, ref = pair.decode(t)
+        yq = pair.oracle.last_read_out
+        flushed = pair.cursor_gpu()[:, 2].astype(bool)
+        mixed += int(0 < flushed.sum() < len(flushed))
+        for b in range(5):
+            if flushed[b]:
+                assert_close(y[b], ref[b], f"{mode} step {t} seq {b} (flush reads the FP32 checkpoint)")
+            else:
+                assert _rel_l2(y[b], yq[b]) < 2e-3, (t, b, _rel_l2(y[b], yq[b]))
+        pair.check_cursor(f"{mode} step {t}")
+        if flushed.any():
+            pair.check_ckpt(f"{mode} step {t}")
+    assert mixed > 0  # some launches had flush and non-flush sequences together
+    assert pair.cache.device_error() == 0
