@@ -428,6 +428,8 @@ def main(argv=None):
     ap.add_argument("--verify-only", choices=["mamba2", "gdn"],
                     help="time only one verify + commit leg, at --verify-batch sequences (a profiling case)")
     ap.add_argument("--verify-batch", type=int, default=512)
+    ap.add_argument("--gdn-decode-only", action="store_true",
+                    help="time only the GDN decode leg, at --batch sequences (a profiling case)")
     ap.add_argument("--read-copy-only", choices=["fp8", "nvfp4"],
                     help="time only the non-flush decode with a read copy, at --batch sequences (a profiling case)")
     args = ap.parse_args(argv)
@@ -448,6 +450,13 @@ def main(argv=None):
         res = verify_leg(wl, dev, args.steps, args.warmup, lambda: None)
         if rank == 0:
             print(json.dumps({"verify": res}))
+        return 0
+    if args.gdn_decode_only:
+        wl = configs.config2(batch=args.batch)
+        r = decode_leg(wl, dev, args.steps, args.warmup, 16, gdn_bytes, lambda: None)
+        if rank == 0:
+            print(json.dumps({"gdn": {"batch": args.batch, "nonflush_us": r["nonflush_us"], "flush_us": r["flush_us"],
+                                      "nonflush_gbs": r["nonflush_gbs"], "launches": r["launches"]}}))
         return 0
     if args.read_copy_only:
         res = read_copy_leg(configs.config1(batch=args.batch), dev, args.read_copy_only, args.steps, args.warmup)

@@ -66,11 +66,16 @@ struct Lay128 {
 // FP32 matrix goes, and the unit's fixed costs are shared by 4 heads
 __host__ __device__ __forceinline__ int read_heads(int read) { return read == READ_NONE ? 1 : 4; }
 
+// units per head: a Gated DeltaNet head of d_head 128 is two units of 64 rows,
+// so that a stage holds 32 KB of state and five stages fit
+__host__ __device__ __forceinline__ int splits(int kind, int P) { return (kind == 1 && P == 128) ? 2 : 1; }
+
 __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int C, int Cp, int H, int hpg) {
   Lay128 l;
   int o = 0;
-  l.st_tile = o;  o += P * N * 4;
-  l.st_rec = o;   o += kind == 0 ? read_heads(read) * al16(C * P * 2) : C * P * 4;
+  const int rpu = P / splits(kind, P);  // state rows per unit
+  l.st_tile = o;  o += rpu * N * 4;
+  l.st_rec = o;   o += kind == 0 ? read_heads(read) * al16(C * P * 2) : C * rpu * 4;
   l.st_meta = o;  o += 32;              // int4 descriptor, NVFP4 amax word
   l.st_size = al128(o);
   o = 0;
@@ -91,7 +96,7 @@ __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int
   l.gb_size = al128(o);
   o = 0;
   l.pe_A = o;     o += al16(H * 4);
-  l.pe_bars = o;  o += 4 * 8 * 8 + 16;  // full, empty, ready, amax x 8 stages; group dots, group tables
+  l.pe_bars = o;  o += 48 * 8;  // full, empty, ready x 8 stages; amax x 2 teams x 8 stages; dots, tables x 2 teams; group tables x 2 buffers
   l.pe_seq = o;   o += 3 * kMaxSeq128 * 4;
   l.pe_misc = o;  o += 16;
   l.pe_mtab = o;  o += (kThreads / 32) * 8 * kMtabRow * 4;  // per computing warp: fold coefficients [8 rows][records]
@@ -104,20 +109,32 @@ __device__ __forceinline__ int ring_slot(int head, int j, int C) {
   return s >= C ? s - C : s;
 }
 
-// Position of a unit in (sequence, head, group, head-in-group), advanced one
-// unit at a time so that no role divides per unit.
+// Position of a unit: its index ui, sequence b, head (u = b H + h), group g,
+// head-in-group hh and part sp of a split head; advanced one unit at a time so
+// that no role divides per unit.
 struct Walk {
-  int u, b, h, g, hh;
-  __device__ __forceinline__ void start(int u0, int H, int hpg) {
-    u = u0;
-    b = u0 / H;
-    h = u0 - b * H;
+  int ui, u, b, h, g, hh, sp;
+  __device__ __forceinline__ void start(int u0, int H, int hpg, int spl) {
+    ui = u0;
+    b = u0 / (H * spl);
+    const int r = u0 - b * H * spl;
+    h = r / spl;
+    sp = r - h * spl;
+    u = b * H + h;
     g = h / hpg;
     hh = h - g * hpg;
   }
-  // advance by `step` heads (1, or HR for a non-flush read-copy unit; HR divides
-  // heads-per-group and H)
-  __device__ __forceinline__ void next(int H, int hpg, int step) {
+  // advance one unit: the next part of a split head, or `step` heads (1, or HR
+  // for a non-flush read-copy unit; HR divides heads-per-group and H)
+  __device__ __forceinline__ void next(int H, int hpg, int step, int spl) {
+    if (spl > 1) {
+      ++ui;
+      if (++sp < spl) return;
+      sp = 0;
+      step = 1;
+    } else {
+      ui += step;
+    }
     u += step;
     h += step;
     hh += step;
@@ -133,14 +150,22 @@ struct Walk {
   }
 };
 
-template <int KIND, int READ, int P>
+// TEAMS: the eight computing warps form TEAMS teams of 8 / TEAMS warps; team t
+// takes units t, t + TEAMS, ..., so that TEAMS units are computed at once
+template <int KIND, int READ, int P, int TEAMS>
 __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDev d, const TokenIn in,
                                                                    float* __restrict__ y, const int units_per_cta,
                                                                    const int stages) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  constexpr int RW = P / 8;  // rows per computing warp
-  constexpr int tile = P * N;
-  constexpr int HR = READ == READ_NONE ? 1 : 4;  // heads of a non-flush unit
+  constexpr int SPL = (KIND == 1 && P == 128) ? 2 : 1;  // units per head
+  constexpr int RPU = P / SPL;                          // state rows per unit
+  constexpr int TW = 8 / TEAMS;                         // warps of a team
+  // Gated DeltaNet: the prologue warp builds each group's key dots and coefficient
+  // tables (two heads a group, little else to do there); Mamba-2: the computing warps
+  constexpr bool PRO = KIND == 1;
+  constexpr int RW = RPU / TW;                          // rows per computing warp and unit
+  constexpr int tile = P * N;                           // floats of one head's state
+  constexpr int HR = READ == READ_NONE ? 1 : 4;         // heads of a non-flush read-copy unit
   const int H = d.H, G = d.G, C = d.C, L = d.L, Cp = d.Cp;
   const int hpg = H / G;
   const int CS = coef_stride(C);
@@ -152,19 +177,21 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   uint64_t* full = reinterpret_cast<uint64_t*>(pbase + LY.pe_bars);
   uint64_t* empty = full + 8;
   uint64_t* ready = full + 16;
-  uint64_t* amaxbar = full + 24;
-  uint64_t* dots_bar = full + 32;  // computing warps: the group's key dot products are in place
-  uint64_t* tab_bar = full + 33;   // computing warps: the group's coefficient tables are in place
+  uint64_t* amaxbar = full + 24;   // [team][stage]: NVFP4 matrix amax of a flushed unit
+  uint64_t* dots_bar = full + 40;  // [team]: the group's key dot products are in place
+  uint64_t* tab_bar = full + 42;   // [team]: the group's coefficient tables are in place
+  uint64_t* grp_bar = full + 44;   // [group buffer]: its tables are in place (for the other teams)
   int* sseq = reinterpret_cast<int*>(pbase + LY.pe_seq);
   volatile int* smisc = reinterpret_cast<volatile int*>(pbase + LY.pe_misc);  // abort, issued, producer done
   // this warp's fold-coefficient table (computing warps)
   float* mt = reinterpret_cast<float*>(pbase + LY.pe_mtab) + (warp < kThreads / 32 ? warp : 0) * 8 * kMtabRow;
 
-  const int total_units = d.B * H;
+  const int upseq = H * SPL;  // units of a sequence
+  const int total_units = d.B * upseq;
   const int u0 = blockIdx.x * units_per_cta;
   const int u1 = min(u0 + units_per_cta, total_units);
   if (u0 >= u1) return;
-  const int b0 = u0 / H, b1 = (u1 - 1) / H;
+  const int b0 = u0 / upseq, b1 = (u1 - 1) / upseq;
   const int nseq = b1 - b0 + 1;
 
   // --- cursors of the covered sequences; arrival; new cursors by the last arriver ---
@@ -176,10 +203,10 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     sseq[3 * t] = ok ? head : 0;  // a rejected cursor stages nothing from the ring
     sseq[3 * t + 1] = ok ? cnt : 0;
     sseq[3 * t + 2] = ok ? 1 : 0;
-    const int lo = max(u0, b * H), hi = min(u1, (b + 1) * H);
+    const int lo = max(u0, b * upseq), hi = min(u1, (b + 1) * upseq);
     __threadfence();
     const int prev = atomicAdd(d.arrive + b, hi - lo);
-    if (prev + (hi - lo) == H) {  // every CTA of this sequence has read its cursor
+    if (prev + (hi - lo) == upseq) {  // every CTA of this sequence has read its cursor
       atomicExch(d.arrive + b, 0);
       if (!ok) {
         report_error(d.err, DEVERR_CURSOR, b);
@@ -196,12 +223,15 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   if (t == kThreads) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(full + s, 1);
-      mbar_init(empty + s, kThreads / 32);
+      mbar_init(empty + s, TW);
       mbar_init(ready + s, 1);
-      mbar_init(amaxbar + s, kThreads / 32);
+      for (int k = 0; k < TEAMS; ++k) mbar_init(amaxbar + 8 * k + s, TW);
     }
-    mbar_init(dots_bar, kThreads / 32);
-    mbar_init(tab_bar, kThreads / 32);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(dots_bar + k, TW);
+      mbar_init(tab_bar + k, TW);
+      mbar_init(grp_bar + k, TW);
+    }
     smisc[0] = 0;
     smisc[1] = 0;
     smisc[2] = 0;
@@ -213,6 +243,52 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     const int k = b - b0;
     return (HR > 1 && !(sseq[3 * k + 2] != 0 && sseq[3 * k + 1] + 1 == L)) ? HR : 1;
   };
+  // coefficient table of head-in-group e of the group in buffer gb (one warp): record
+  // coefficients and per-head scalars; lane j holds dq = k_j . q, dk = k_j . k_cur and
+  // the ring slot of record j
+  auto head_table = [&](unsigned char* gb, size_t ug, int e, int n, float dq, float dk, int slot_lane) {
+    float* co = reinterpret_cast<float*>(gb + LY.gb_coef) + e * CS;
+    const float* la_row = reinterpret_cast<const float*>(gb + LY.gb_la) + e * Cp;
+    if (KIND == 0) {
+      const uint16_t* dt_row = reinterpret_cast<const uint16_t*>(gb + LY.gb_dt) + e * Cp;
+      const uint16_t dt_bits = reinterpret_cast<const uint16_t*>(gb + LY.gb_s1)[(ug & 7) + e];
+      const float dt_cur = bf(dt_bits);
+      const float la_cur = dt_cur * sA[static_cast<int>(ug % H) + e];
+      // records 0..n (current at n): w_j = exp(sum_{i=j+1..n} la_i), gamma = exp(sum_{i<=n} la_i)
+      const float sv = suffix_sum(lane < n ? la_row[slot_lane] : (lane == n ? la_cur : 0.f), lane, n);
+      const float excl = __shfl_down_sync(0xffffffffu, sv, 1);
+      const float Wl = lane <= n ? expf(lane < n ? excl : 0.f) : 0.f;
+      const float dtl = lane < n ? bf(dt_row[slot_lane]) : (lane == n ? dt_cur : 0.f);
+      if (lane <= n) {
+        co[lane] = Wl * dtl * dq;     // output coefficient on x_j[r]
+        co[2 * C + lane] = Wl * dtl;  // fold coefficient on x_j[r]
+      }
+      if (lane == 0) {
+        co[3 * C + CO_GAMMA] = expf(sv);
+        if (READ == READ_NVFP4)
+          co[3 * C + CO_MATSCALE] = reinterpret_cast<const float*>(gb + LY.gb_ms)[(ug & 3) + e];
+      }
+    } else {
+      // buffered records 0..n-1: w_j = exp(sum_{i=j+1..n-1} g_i), gamma = exp(sum_{i<n} g_i)
+      const float sv = suffix_sum(lane < n ? la_row[slot_lane] : 0.f, lane, n - 1);
+      const float excl = __shfl_down_sync(0xffffffffu, sv, 1);
+      const float Wl = lane < n ? expf(lane + 1 < n ? excl : 0.f) : 0.f;
+      const float g_cur = reinterpret_cast<const float*>(gb + LY.gb_s1)[(ug & 3) + e];
+      const float a = expf(g_cur);
+      if (lane < n) {
+        co[lane] = Wl * dk;         // coefficient of u_j[r] in S k
+        co[C + lane] = Wl * dq;     // coefficient of u_j[r] in S q
+        co[2 * C + lane] = a * Wl;  // fold coefficient of u_j[r]
+      }
+      const float kq_dot = __shfl_sync(0xffffffffu, dq, n);
+      if (lane == 0) {
+        co[3 * C + CO_GAMMA] = n > 0 ? expf(sv) : 1.f;
+        co[3 * C + CO_A] = a;
+        co[3 * C + CO_BETA] = reinterpret_cast<const float*>(gb + LY.gb_s2)[(ug & 3) + e];
+        co[3 * C + CO_KQ] = kq_dot;
+      }
+    }
+  };
   // first element of the 16-byte block holding element e, for 2-byte / 4-byte arrays
   auto blk2 = [](size_t e) { return e & ~static_cast<size_t>(7); };
   auto blk4 = [](size_t e) { return e & ~static_cast<size_t>(3); };
@@ -221,13 +297,13 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   if (warp == kProducerWarp) {
     if (lane != 0) return;
     Walk w;
-    w.start(u0, H, hpg);
+    w.start(u0, H, hpg, SPL);
     int gi = -1;
-    for (int i = 0; w.u < u1; ++i, w.next(H, hpg, step_of(w.b))) {
+    for (int i = 0; w.ui < u1; ++i, w.next(H, hpg, step_of(w.b), SPL)) {
       const int s = i % stages;
       if (i >= stages && !mbar_wait_bounded(empty + s, static_cast<uint32_t>(((i / stages) - 1) & 1))) break;
       if (smisc[0]) break;
-      const bool first = i == 0 || w.hh == 0;
+      const bool first = i == 0 || (w.hh == 0 && w.sp == 0);
       if (first) ++gi;
       const int k = w.b - b0;
       const int head = sseq[3 * k], n = sseq[3 * k + 1];
@@ -239,8 +315,8 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       const int seg1 = min(n, C - head), seg2 = n - seg1;
       constexpr int esz = KIND == 0 ? 2 : 4;
       const int nh = step_of(w.b);  // heads in this unit
-      const uint32_t tb = (READ == READ_NONE || flush) ? tile * 4 : (READ == READ_FP8 ? tile : tile / 2);
-      uint32_t bytes = nh * (tb + static_cast<uint32_t>(n) * P * esz);
+      const uint32_t tb = (READ == READ_NONE || flush) ? RPU * N * 4 : (READ == READ_FP8 ? tile : tile / 2);
+      uint32_t bytes = nh * (tb + static_cast<uint32_t>(n) * RPU * esz);
       const size_t ug = static_cast<size_t>(w.b) * H + static_cast<size_t>(w.g) * hpg;  // first unit of the group
       const size_t bg = static_cast<size_t>(w.b) * G + w.g;
       const uint32_t s1b = KIND == 0 ? static_cast<uint32_t>((blk2(ug + hpg + 7) - blk2(ug)) * 2)
@@ -256,16 +332,24 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       if (KIND == 0 && i == 0) bytes += al16(H * 4);  // A (Mamba-2 only)
       mbar_expect_tx(bar, bytes);
       // the unit: state matrix (or read copy) and this head's buffered records
-      if (READ == READ_NONE || flush) bulk_g2s(st + LY.st_tile, d.ckpt + u * tile, tb, bar);
+      if (READ == READ_NONE || flush) bulk_g2s(st + LY.st_tile, d.ckpt + u * tile + w.sp * RPU * N, tb, bar);
       else bulk_g2s(st + LY.st_tile, d.rc_codes + u * tb, nh * tb, bar);  // nh consecutive heads
       const unsigned char* rsrc = KIND == 0 ? reinterpret_cast<const unsigned char*>(d.r_x)
                                             : reinterpret_cast<const unsigned char*>(d.r_u);
       constexpr size_t rrow = static_cast<size_t>(P) * esz;
-      for (int hu = 0; hu < nh; ++hu) {
-        unsigned char* rdst = st + LY.st_rec + static_cast<size_t>(hu) * al16(C * P * 2);
-        const size_t uh = u + hu;
-        if (seg1) bulk_g2s(rdst, rsrc + (uh * C + head) * rrow, seg1 * rrow, bar);
-        if (seg2) bulk_g2s(rdst + seg1 * rrow, rsrc + uh * C * rrow, seg2 * rrow, bar);
+      if (SPL == 1) {
+        for (int hu = 0; hu < nh; ++hu) {
+          unsigned char* rdst = st + LY.st_rec + static_cast<size_t>(hu) * al16(C * P * 2);
+          const size_t uh = u + hu;
+          if (seg1) bulk_g2s(rdst, rsrc + (uh * C + head) * rrow, seg1 * rrow, bar);
+          if (seg2) bulk_g2s(rdst + seg1 * rrow, rsrc + uh * C * rrow, seg2 * rrow, bar);
+        }
+      } else {
+        // this part's rows of each buffered record: one copy per record
+        for (int j = 0; j < n; ++j)
+          bulk_g2s(st + LY.st_rec + static_cast<size_t>(j) * RPU * esz,
+                   rsrc + (u * C + ring_slot(head, j, C)) * rrow + static_cast<size_t>(w.sp) * RPU * esz, RPU * esz,
+                   bar);
       }
       // the group: keys and query, current tokens, decay rows, scalars, scales
       if (first) {
@@ -302,9 +386,9 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   // =============================== prologue warp ===============================
   if (warp == kPrologueWarp) {
     Walk w;
-    w.start(u0, H, hpg);
+    w.start(u0, H, hpg, SPL);
     int gi = -1, consumed = 0;
-    for (int i = 0; w.u < u1; ++i, w.next(H, hpg, step_of(w.b))) {
+    for (int i = 0; w.ui < u1; ++i, w.next(H, hpg, step_of(w.b), SPL)) {
       if (smisc[0]) break;
       const int s = i % stages;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(full + s, static_cast<uint32_t>((i / stages) & 1)))) {
@@ -315,7 +399,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
         break;
       }
       consumed = i + 1;
-      const bool first = i == 0 || w.hh == 0;
+      const bool first = i == 0 || (w.hh == 0 && w.sp == 0);
       if (first) ++gi;
       const int k = w.b - b0;
       const int head = sseq[3 * k], n = sseq[3 * k + 1];
@@ -331,10 +415,12 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
         const float4 kc4 = bf4(reinterpret_cast<const uint2*>(kb + n * N)[lane]);
         reinterpret_cast<float4*>(gb + LY.gb_qf)[lane] = q4;
         if (KIND == 1) reinterpret_cast<float4*>(gb + LY.gb_kf)[lane] = kc4;
-        const int hh_hi = min(hpg, w.hh + (u1 - w.u));  // heads of this group in this CTA
+        // heads of this group in this CTA; a head whose first part another CTA holds is
+        // appended by that CTA
+        const int hh_hi = min(hpg, w.hh + (u1 - w.ui + w.sp + SPL - 1) / SPL);
         if (!flush) {
           // append the current tokens of the group's heads in this CTA to the ring
-          for (int e = w.hh; e < hh_hi; ++e) {
+          for (int e = w.hh + (w.sp > 0 ? 1 : 0); e < hh_hi; ++e) {
             const size_t ue = ug + e;
             if (KIND == 0) {
               const uint16_t* xc = reinterpret_cast<const uint16_t*>(gb + LY.gb_cur) + e * P;
@@ -353,17 +439,45 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
             }
           }
         }
-        if (!flush && w.hh == 0) {
+        if (!flush && w.hh == 0 && w.sp == 0) {
           // the group's key row: appended by the CTA that holds the group's first head
           const size_t bg = static_cast<size_t>(w.b) * G + w.g;
           reinterpret_cast<uint2*>((KIND == 0 ? d.r_B : d.r_k) + (bg * C + slot) * N)[lane] =
               reinterpret_cast<const uint2*>(kb + n * N)[lane];
         }
+        if (PRO) {
+          // the group's key dot products, eight keys per transpose-reduce, then the
+          // coefficient tables of its heads in this CTA
+          float* gdq = reinterpret_cast<float*>(gb + LY.gb_dq);
+          float* gdk = gdq + al16(C * 4) / 4;
+          for (int jb = 0; jb <= n; jb += 8) {
+            float pq[8], pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float4 kj = jb + e <= n ? bf4(reinterpret_cast<const uint2*>(kb + (jb + e) * N)[lane])
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+              pq[e] = dot4(kj, q4);
+              pk[e] = dot4(kj, kc4);
+            }
+            const float tq = reduce8(pq, lane), tk = reduce8(pk, lane);
+            const int j = jb + (lane >> 2);
+            if ((lane & 3) == 0 && j <= n) {
+              gdq[j] = tq;
+              gdk[j] = tk;
+            }
+          }
+          __syncwarp();
+          const float dq = lane <= n ? gdq[lane] : 0.f;
+          const float dk = lane <= n ? gdk[lane] : 0.f;
+          const int slot_lane = lane < n ? ring_slot(head, lane, C) : 0;
+          for (int e = w.hh; e < hh_hi; ++e) head_table(gb, ug, e, n, dq, dk, slot_lane);
+        }
       }
       if (lane == 0) {
         unsigned char* st = smem + static_cast<size_t>(LY.st_size) * s;
         *reinterpret_cast<int4*>(st + LY.st_meta) = make_int4(
-            w.u, n | (flush ? 0x100 : 0) | (ok ? 0x200 : 0) | (first ? 0x400 : 0), slot, w.hh | ((gi & 1) << 16));
+            w.u, n | (flush ? 0x100 : 0) | (ok ? 0x200 : 0) | (first ? 0x400 : 0), slot,
+            w.hh | ((gi & 3) << 16) | (w.sp << 24));
         reinterpret_cast<int*>(st + LY.st_meta)[4] = 0;  // NVFP4 matrix amax
       }
       __syncwarp();
@@ -382,16 +496,18 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   }
 
   // =============================== computing warps ===============================
+  const int team = warp / TW, tw = warp - team * TW;  // team, warp in the team
   uint32_t amax_phase = 0;
-  int groups = 0;  // groups whose tables these warps have built
+  int groups = 0;  // groups whose tables this team has built
   Walk wc;
-  wc.start(u0, H, hpg);
-  for (int i = 0; wc.u < u1; ++i, wc.next(H, hpg, step_of(wc.b))) {
+  wc.start(u0, H, hpg, SPL);
+  for (int i = 0; wc.ui < u1; ++i, wc.next(H, hpg, step_of(wc.b), SPL)) {
     if (smisc[0]) break;
+    if (TEAMS > 1 && i % TEAMS != team) continue;
     const int s = i % stages;
     if (!__all_sync(0xffffffffu, mbar_wait_bounded(ready + s, static_cast<uint32_t>((i / stages) & 1)))) {
       if (lane == 0) {
-        report_error(d.err, DEVERR_TIMEOUT, (u0 + i) / H);
+        report_error(d.err, DEVERR_TIMEOUT, wc.b);
         smisc[0] = 1;
       }
       break;
@@ -399,20 +515,21 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     unsigned char* st = smem + static_cast<size_t>(LY.st_size) * s;
     const int4 meta = *reinterpret_cast<const int4*>(st + LY.st_meta);
     // ---- first unit of a group in this CTA: the group's key dot products and the
-    // coefficient tables of its heads, shared out over the eight warps (two bounded
-    // mbarriers order the phases) ----
-    if ((meta.y & 0x600) == 0x600) {
+    // coefficient tables of its heads, shared out over the team's warps (two bounded
+    // mbarriers order the phases); a later unit of the group computed by another
+    // team waits for the tables on the group buffer's barrier ----
+    if (!PRO && (meta.y & 0x600) == 0x600) {
       const int n = meta.y & 0xFF;
       const int hh_lo = meta.w & 0xFFFF;
       const size_t ug = static_cast<size_t>(meta.x) - hh_lo;  // first unit of the group
-      unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * (meta.w >> 16);
+      unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * ((meta.w >> 16) & 1);
       const uint16_t* kb = reinterpret_cast<const uint16_t*>(gb + LY.gb_key);
       float* gdq = reinterpret_cast<float*>(gb + LY.gb_dq);
       float* gdk = gdq + al16(C * 4) / 4;
       const float4 q4 = reinterpret_cast<const float4*>(gb + LY.gb_qf)[lane];
       const float4 kc4 =
           KIND == 1 ? reinterpret_cast<const float4*>(gb + LY.gb_kf)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int j = warp; j <= n; j += kThreads / 32) {
+      for (int j = tw; j <= n; j += TW) {
         const float4 kj = bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane]);
         float pq = dot4(kj, q4), pk = KIND == 1 ? dot4(kj, kc4) : 0.f;
 #pragma unroll
@@ -426,65 +543,40 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(dots_bar);
-      bool okg = __all_sync(0xffffffffu, mbar_wait_bounded(dots_bar, static_cast<uint32_t>(groups & 1)));
+      if (lane == 0) mbar_arrive(dots_bar + team);
+      bool okg = __all_sync(0xffffffffu, mbar_wait_bounded(dots_bar + team, static_cast<uint32_t>(groups & 1)));
       if (okg) {
         const float dq = lane <= n ? gdq[lane] : 0.f;  // lane j: k_j . q
         const float dk = (KIND == 1 && lane <= n) ? gdk[lane] : 0.f;  // lane j: k_j . k_cur
         const int head = meta.z - n < 0 ? meta.z - n + C : meta.z - n;
         const int slot_lane = lane < n ? ring_slot(head, lane, C) : 0;
-        const int hh_hi = min(hpg, hh_lo + (u1 - meta.x));  // heads of this group in this CTA
-        for (int e = hh_lo + warp; e < hh_hi; e += kThreads / 32) {
-          float* co = reinterpret_cast<float*>(gb + LY.gb_coef) + e * CS;
-          const float* la_row = reinterpret_cast<const float*>(gb + LY.gb_la) + e * Cp;
-          if (KIND == 0) {
-            const uint16_t* dt_row = reinterpret_cast<const uint16_t*>(gb + LY.gb_dt) + e * Cp;
-            const uint16_t dt_bits = reinterpret_cast<const uint16_t*>(gb + LY.gb_s1)[(ug & 7) + e];
-            const float dt_cur = bf(dt_bits);
-            const float la_cur = dt_cur * sA[static_cast<int>(ug % H) + e];
-            // records 0..n (current at n): w_j = exp(sum_{i=j+1..n} la_i), gamma = exp(sum_{i<=n} la_i)
-            const float sv = suffix_sum(lane < n ? la_row[slot_lane] : (lane == n ? la_cur : 0.f), lane, n);
-            const float excl = __shfl_down_sync(0xffffffffu, sv, 1);
-            const float Wl = lane <= n ? expf(lane < n ? excl : 0.f) : 0.f;
-            const float dtl = lane < n ? bf(dt_row[slot_lane]) : (lane == n ? dt_cur : 0.f);
-            if (lane <= n) {
-              co[lane] = Wl * dtl * dq;     // output coefficient on x_j[r]
-              co[2 * C + lane] = Wl * dtl;  // fold coefficient on x_j[r]
-            }
-            if (lane == 0) {
-              co[3 * C + CO_GAMMA] = expf(sv);
-              if (READ == READ_NVFP4)
-                co[3 * C + CO_MATSCALE] = reinterpret_cast<const float*>(gb + LY.gb_ms)[(ug & 3) + e];
-            }
-          } else {
-            // buffered records 0..n-1: w_j = exp(sum_{i=j+1..n-1} g_i), gamma = exp(sum_{i<n} g_i)
-            const float sv = suffix_sum(lane < n ? la_row[slot_lane] : 0.f, lane, n - 1);
-            const float excl = __shfl_down_sync(0xffffffffu, sv, 1);
-            const float Wl = lane < n ? expf(lane + 1 < n ? excl : 0.f) : 0.f;
-            const float g_cur = reinterpret_cast<const float*>(gb + LY.gb_s1)[(ug & 3) + e];
-            const float a = expf(g_cur);
-            if (lane < n) {
-              co[lane] = Wl * dk;         // coefficient of u_j[r] in S k
-              co[C + lane] = Wl * dq;     // coefficient of u_j[r] in S q
-              co[2 * C + lane] = a * Wl;  // fold coefficient of u_j[r]
-            }
-            const float kq_dot = __shfl_sync(0xffffffffu, dq, n);
-            if (lane == 0) {
-              co[3 * C + CO_GAMMA] = n > 0 ? expf(sv) : 1.f;
-              co[3 * C + CO_A] = a;
-              co[3 * C + CO_BETA] = reinterpret_cast<const float*>(gb + LY.gb_s2)[(ug & 3) + e];
-              co[3 * C + CO_KQ] = kq_dot;
-            }
-          }
+        const int hh_hi = min(hpg, hh_lo + (u1 - wc.ui + wc.sp + SPL - 1) / SPL);  // heads of this group in this CTA
+        for (int e = hh_lo + tw; e < hh_hi; e += TW) {
+          head_table(gb, ug, e, n, dq, dk, slot_lane);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(tab_bar);
-        okg = __all_sync(0xffffffffu, mbar_wait_bounded(tab_bar, static_cast<uint32_t>(groups & 1)));
+        if (lane == 0) mbar_arrive(tab_bar + team);
+        okg = __all_sync(0xffffffffu, mbar_wait_bounded(tab_bar + team, static_cast<uint32_t>(groups & 1)));
       }
       ++groups;
       if (!okg) {
         if (lane == 0) {
-          report_error(d.err, DEVERR_TIMEOUT, (u0 + i) / H);
+          report_error(d.err, DEVERR_TIMEOUT, wc.b);
+          smisc[0] = 1;
+        }
+        break;
+      }
+    }
+    if (TEAMS > 1 && !PRO) {
+      // the group buffer's barrier completes once per group that uses it (its first
+      // unit's team arrives, with or without tables); phase (group index / 2) & 1
+      if (meta.y & 0x400) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(grp_bar + ((meta.w >> 16) & 1));
+      } else if (!__all_sync(0xffffffffu, mbar_wait_bounded(grp_bar + ((meta.w >> 16) & 1),
+                                                             static_cast<uint32_t>((meta.w >> 17) & 1)))) {
+        if (lane == 0) {
+          report_error(d.err, DEVERR_TIMEOUT, wc.b);
           smisc[0] = 1;
         }
         break;
@@ -497,7 +589,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       const int n = meta.y & 0xFF;
       const int hh0 = meta.w & 0xFFFF;
       const size_t uh0 = static_cast<size_t>(meta.x);
-      const unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * (meta.w >> 16);
+      const unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * ((meta.w >> 16) & 1);
       const float* cob = reinterpret_cast<const float*>(gb + LY.gb_coef);
       const uint16_t* curb = reinterpret_cast<const uint16_t*>(gb + LY.gb_cur);
       const float4 q4 = reinterpret_cast<const float4*>(gb + LY.gb_qf)[lane];
@@ -506,7 +598,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       const uint16_t* xb = reinterpret_cast<const uint16_t*>(st + LY.st_rec);
 #pragma unroll
       for (int r0 = 0; r0 < RW; r0 += 8) {
-        const int Rq = warp + 8 * (r0 + kq);
+        const int Rq = tw + TW * (r0 + kq);
         float ry[HR], gsc[HR], part[HR][8];
 #pragma unroll
         for (int hu = 0; hu < HR; ++hu) {
@@ -528,7 +620,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
           const unsigned char* cb = st + LY.st_tile + hu * TBH;
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const int R = warp + 8 * (r0 + e);
+            const int R = tw + TW * (r0 + e);
             if (READ == READ_FP8) {
               const uint32_t wd = reinterpret_cast<const uint32_t*>(cb + R * N)[lane];
               const float2 lo = e4m3x2_to_f32x2(static_cast<uint16_t>(wd & 0xFFFFu));
@@ -559,20 +651,21 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       const bool flush = (meta.y & 0x100) != 0;
       const int slot = meta.z;
       const int hh = (meta.w & 0xFFFF) + hu;
-      const unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * (meta.w >> 16);
+      const int sp = meta.w >> 24;  // part of a split head: rows sp RPU .. sp RPU + RPU - 1
+      const unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * ((meta.w >> 16) & 1);
       const float* co = reinterpret_cast<const float*>(gb + LY.gb_coef) + hh * CS;
       const uint16_t* kb = reinterpret_cast<const uint16_t*>(gb + LY.gb_key);
-      const uint16_t* cur = reinterpret_cast<const uint16_t*>(gb + LY.gb_cur) + hh * P;  // x or v of this head
-      float* yrow = y + u * P;
+      const uint16_t* cur = reinterpret_cast<const uint16_t*>(gb + LY.gb_cur) + hh * P + sp * RPU;  // x or v
+      float* yrow = y + u * P + sp * RPU;
       float4* sT4 = reinterpret_cast<float4*>(st + LY.st_tile);
-      float4* gS4 = reinterpret_cast<float4*>(d.ckpt + u * tile);
+      float4* gS4 = reinterpret_cast<float4*>(d.ckpt + u * tile + sp * RPU * N);
       const float4 q4 = reinterpret_cast<const float4*>(gb + LY.gb_qf)[lane];
       const float gamma = co[3 * C + CO_GAMMA];
       if (KIND == 0) {
         const uint16_t* xb = reinterpret_cast<const uint16_t*>(st + LY.st_rec + static_cast<size_t>(hu) * al16(C * P * 2));
 #pragma unroll
         for (int r0 = 0; r0 < RW; r0 += 8) {
-          const int Rq = warp + 8 * (r0 + kq);
+          const int Rq = tw + TW * (r0 + kq);
           // buffered term of row Rq: lanes 4kq..4kq+3 split the records 0..n-1, lane jl = 0 adds record n
           float ry = jl == 0 ? co[n] * bf(cur[Rq]) : 0.f;
           for (int j = jl; j < n; j += 4) ry = fmaf(co[j], bf(xb[j * P + Rq]), ry);
@@ -586,7 +679,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
             const unsigned char* cb = st + LY.st_tile + hu * (READ == READ_FP8 ? tile : tile / 2);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              const int R = warp + 8 * (r0 + e);
+              const int R = tw + TW * (r0 + e);
               if (READ == READ_FP8) {
                 const uint32_t wd = reinterpret_cast<const uint32_t*>(cb + R * N)[lane];
                 const float2 lo = e4m3x2_to_f32x2(static_cast<uint16_t>(wd & 0xFFFFu));
@@ -605,7 +698,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
           } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              s4[e] = sT4[(warp + 8 * (r0 + e)) * SEG + lane];
+              s4[e] = sT4[(tw + TW * (r0 + e)) * SEG + lane];
               part[e] = dot4(s4[e], q4);
             }
           }
@@ -641,8 +734,8 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
             __syncwarp();
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              __stcs(gS4 + (warp + 8 * (r0 + e)) * SEG + lane, acc[e]);
-              if (READ != READ_NONE) sT4[(warp + 8 * (r0 + e)) * SEG + lane] = acc[e];
+              __stcs(gS4 + (tw + TW * (r0 + e)) * SEG + lane, acc[e]);
+              if (READ != READ_NONE) sT4[(tw + TW * (r0 + e)) * SEG + lane] = acc[e];
             }
           }
         }
@@ -652,7 +745,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
             uint32_t* codes = reinterpret_cast<uint32_t*>(d.rc_codes + u * tile);
 #pragma unroll
             for (int m = 0; m < RW; ++m) {
-              const int R = warp + 8 * m;
+              const int R = tw + TW * m;
               const float4 v4 = sT4[R * SEG + lane];
               float mx = fmaxf(fmaxf(fabsf(v4.x), fabsf(v4.y)), fmaxf(fabsf(v4.z), fabsf(v4.w)));
               mx = seg_max<32>(mx);
@@ -670,15 +763,16 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
             float mloc = 0.f;
 #pragma unroll
             for (int m = 0; m < RW; ++m) {
-              const float4 v4 = sT4[(warp + 8 * m) * SEG + lane];
+              const float4 v4 = sT4[(tw + TW * m) * SEG + lane];
               mloc = fmaxf(mloc, fmaxf(fmaxf(fabsf(v4.x), fabsf(v4.y)), fmaxf(fabsf(v4.z), fabsf(v4.w))));
             }
             mloc = seg_max<32>(mloc);
             int* slot_amax = reinterpret_cast<int*>(st + LY.st_meta) + 4;
             if (lane == 0) atomicMax(slot_amax, __float_as_int(mloc));  // non-negative floats order as ints
             __syncwarp();
-            if (lane == 0) mbar_arrive(amaxbar + s);
-            const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(amaxbar + s, (amax_phase >> s) & 1u));
+            if (lane == 0) mbar_arrive(amaxbar + 8 * team + s);
+            const bool got =
+                __all_sync(0xffffffffu, mbar_wait_bounded(amaxbar + 8 * team + s, (amax_phase >> s) & 1u));
             amax_phase ^= 1u << s;
             if (!got) {
               if (lane == 0) {
@@ -693,7 +787,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
               uint8_t* blk = d.rc_blkscale + u * (tile / 16);
 #pragma unroll
               for (int m = 0; m < RW; ++m) {
-                const int R = warp + 8 * m;
+                const int R = tw + TW * m;
                 const float4 v4 = sT4[R * SEG + lane];
                 float mb = fmaxf(fmaxf(fabsf(v4.x), fabsf(v4.y)), fmaxf(fabsf(v4.z), fabsf(v4.w)));
                 mb = seg_max<4>(mb);  // 4 lanes = one 16-element block
@@ -707,7 +801,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
                 codes[R * SEG + lane] = static_cast<uint16_t>(qv);
                 if ((lane & 3) == 0) blk[R * (N / 16) + (lane >> 2)] = static_cast<uint8_t>(bcode);
               }
-              if (warp == 0 && lane == 0) d.rc_matscale[u] = smat;
+              if (tw == 0 && lane == 0) d.rc_matscale[u] = smat;
             }
           }
         }
@@ -716,13 +810,13 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
         const float4 kc4 = reinterpret_cast<const float4*>(gb + LY.gb_kf)[lane];
         const float a = co[3 * C + CO_A], beta = co[3 * C + CO_BETA];
         const float kq_dot = co[3 * C + CO_KQ];
-        float* urow = d.r_u + (u * C + slot) * P;
+        float* urow = d.r_u + (u * C + slot) * P + sp * RPU;
 #pragma unroll
         for (int r0 = 0; r0 < RW; r0 += 8) {
-          const int Rq = warp + 8 * (r0 + kq);
+          const int Rq = tw + TW * (r0 + kq);
           float rk = 0.f, rq = 0.f;
           for (int j = jl; j < n; j += 4) {
-            const float uj = ub[j * P + Rq];
+            const float uj = ub[j * RPU + Rq];
             rk = fmaf(co[j], uj, rk);
             rq = fmaf(co[C + j], uj, rq);
           }
@@ -734,7 +828,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
           float pk[8], pq[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            s4[e] = sT4[(warp + 8 * (r0 + e)) * SEG + lane];
+            s4[e] = sT4[(tw + TW * (r0 + e)) * SEG + lane];
             pk[e] = dot4(s4[e], kc4);
             pq[e] = dot4(s4[e], q4);
           }
@@ -752,7 +846,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
             // the end of the last quad), then four records per broadcast read
             for (int jc = 0; 4 * jc < n; ++jc) {
               const int j = 4 * jc + jl;
-              mt[kq * kMtabRow + j] = j < n ? co[2 * C + j] * ub[j * P + Rq] : 0.f;
+              mt[kq * kMtabRow + j] = j < n ? co[2 * C + j] * ub[j * RPU + Rq] : 0.f;
             }
             __syncwarp();
             float4 acc[8];
@@ -776,7 +870,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
             }
             __syncwarp();
 #pragma unroll
-            for (int e = 0; e < 8; ++e) __stcs(gS4 + (warp + 8 * (r0 + e)) * SEG + lane, acc[e]);
+            for (int e = 0; e < 8; ++e) __stcs(gS4 + (tw + TW * (r0 + e)) * SEG + lane, acc[e]);
           }
         }
       }
@@ -786,7 +880,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   }
 }
 
-template <int KIND, int READ, int P>
+template <int KIND, int READ, int P, int TEAMS>
 cudaError_t launch128(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s) {
   const int hpg = d.H / d.G;
   const Lay128 LY = lay128(KIND, READ, P, d.C, d.Cp, d.H, hpg);
@@ -796,36 +890,44 @@ cudaError_t launch128(const LayerDev& d, const TokenIn& in, float* y, cudaStream
   // a group buffer is rewritten two groups later: every unit of that earlier
   // group must have left the pipeline, which holds when stages <= (units per
   // group) + 1; a non-flush read-copy unit holds read_heads(READ) heads
-  const int upg = hpg / read_heads(READ);
+  constexpr int SPL = (KIND == 1 && P == 128) ? 2 : 1;
+  const int upg = hpg * SPL / read_heads(READ);
   if (stages > upg + 1) stages = upg + 1;
   if (stages < 1) return cudaErrorInvalidConfiguration;
   const size_t smem = static_cast<size_t>(LY.st_size) * stages + 2u * LY.gb_size + LY.pe_size;
   // each CTA takes a contiguous range of heads, a multiple of read_heads(READ)
   const int hr = read_heads(READ);
-  const int total = d.B * d.H;
+  const int total = d.B * d.H * SPL;
   int grid = d.num_sms > 0 ? d.num_sms : 1;
   if (grid > total / hr) grid = total / hr;
   int per = ((total + grid - 1) / grid + hr - 1) / hr * hr;
-  while (per / d.H + 2 > kMaxSeq128) {
+  while (per / (d.H * SPL) + 2 > kMaxSeq128) {
     grid *= 2;
     per = ((total + grid - 1) / grid + hr - 1) / hr * hr;
   }
   grid = (total + per - 1) / per;
-  auto kernel = decode128_kernel<KIND, READ, P>;
+  auto kernel = decode128_kernel<KIND, READ, P, TEAMS>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
   kernel<<<grid, kThreads128, smem, s>>>(d, in, y, per, static_cast<int>(stages));
   return cudaGetLastError();
 }
 
-template <int P>
+template <int P, int TEAMS>
 cudaError_t launch128_p(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s) {
   if (d.kind == 0) {
-    if (d.read_mode == READ_FP8) return launch128<0, READ_FP8, P>(d, in, y, s);
-    if (d.read_mode == READ_NVFP4) return launch128<0, READ_NVFP4, P>(d, in, y, s);
-    return launch128<0, READ_NONE, P>(d, in, y, s);
+    if (d.read_mode == READ_FP8) return launch128<0, READ_FP8, P, TEAMS>(d, in, y, s);
+    if (d.read_mode == READ_NVFP4) return launch128<0, READ_NVFP4, P, TEAMS>(d, in, y, s);
+    return launch128<0, READ_NONE, P, TEAMS>(d, in, y, s);
   }
-  return launch128<1, READ_NONE, P>(d, in, y, s);
+  return launch128<1, READ_NONE, P, TEAMS>(d, in, y, s);
+}
+
+int decode128_teams(const LayerDev& d) {
+  const char* e = getenv("RS_DECODE_TEAMS");
+  if (e && e[0] == '1') return 1;
+  if (e && e[0] == '2') return 2;
+  return d.kind == 1 ? 2 : 1;
 }
 
 }  // namespace
@@ -840,7 +942,8 @@ bool decode128_supports(const LayerDev& d) {
 
 cudaError_t launch_decode128(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s) {
   if (!decode128_supports(d)) return cudaErrorInvalidValue;
-  return d.P == 64 ? launch128_p<64>(d, in, y, s) : launch128_p<128>(d, in, y, s);
+  if (decode128_teams(d) == 1) return d.P == 64 ? launch128_p<64, 1>(d, in, y, s) : launch128_p<128, 1>(d, in, y, s);
+  return d.P == 64 ? launch128_p<64, 2>(d, in, y, s) : launch128_p<128, 2>(d, in, y, s);
 }
 
 }  // namespace rs
