@@ -6,25 +6,27 @@
 // the work is fed and split, so that the computing warps do little besides the
 // pass over the state matrix:
 //
-//  * a work unit is one (sequence, head) state matrix [P][128] -- on a layer
-//    with a low-precision read copy, the non-flush units hold four heads of a
-//    group, whose codes fit where one FP32 matrix goes -- and CTA c owns a
-//    contiguous range of units, so it meets each group (and sequence) once;
-//  * a producer warp stages each unit with two bulk copies (cp.async.bulk):
-//    the state matrix (or its read copy) and the buffered records of that
-//    head.  What the heads of a group share, or what is small -- the group's
-//    keys and query, the current tokens of all its heads, the ring's per-head
-//    decay rows, the current per-head scalars, the read-copy scales -- is
-//    staged once per group into one of two group buffers;
-//  * a prologue warp, once per group, converts the query (and current key) to
-//    FP32 and appends the group's current tokens to the ring; per unit it
-//    publishes a 16-byte descriptor and signals `ready`;
-//  * at the first unit of a group the eight computing warps build the group's
-//    key dot products (records shared out over the warps) and then the
-//    per-head coefficient tables (one decay suffix scan per head, heads shared
-//    out over the warps) in the group buffer, the two phases ordered by
-//    bounded mbarriers;
-//  * eight computing warps each own rows w, w+8, .. of every unit: lane = 4
+//  * a work unit is one (sequence, head) state matrix [P][128] -- a Gated
+//    DeltaNet head of d_head 128 is two units of 64 rows; on a layer with a
+//    low-precision read copy, the non-flush units hold four heads of a group,
+//    whose codes fit where one FP32 matrix goes -- and CTA c owns a contiguous
+//    range of units, so it meets each group (and sequence) once;
+//  * a producer warp stages each unit with bulk copies (cp.async.bulk): the
+//    state matrix (or its read copy) and the buffered records of that head.
+//    What the heads of a group share, or what is small -- the group's keys and
+//    query, the current tokens of all its heads, the ring's per-head decay rows,
+//    the current per-head scalars, the read-copy scales -- is staged once per
+//    group, one group ahead, into one of three group buffers;
+//  * builder warps (two for Mamba-2, one for Gated DeltaNet), one group ahead of
+//    the computing warps: the query (and current key) in FP32, the group's key
+//    dot products (eight keys per transpose-reduce), the per-head coefficient
+//    tables (one decay suffix scan per head, two heads at once in 16-lane
+//    halves when the records fit), and the ring appends of the group's current
+//    tokens;
+//  * a prologue warp publishes per unit a 16-byte descriptor and signals
+//    `ready` (at a group's first unit, once its tables are in place);
+//  * the eight computing warps form one or two teams that take units in turn;
+//    a team's warps own rows w, w+T, .. of each of its units: lane = 4
 //    columns, 4 lanes per row split the buffered records, an 8-row
 //    transpose-reduce forms the row sums.  A flush unit folds in registers:
 //    each warp writes the fold coefficients of its 8 rows into a small table
@@ -40,9 +42,11 @@ namespace {
 constexpr int N = 128;               // d_state of this kernel
 constexpr int SEG = N / 4;           // lanes per state row (one float4 each)
 constexpr int kMaxSeq128 = 64;       // sequences one CTA may cover
-constexpr int kThreads128 = kThreads + 64;  // 8 computing warps, prologue warp, producer warp
+constexpr int kThreads128 = kThreads + 128;  // 8 computing warps, prologue, producer, 2 builders
 constexpr int kPrologueWarp = kThreads / 32;
 constexpr int kProducerWarp = kThreads / 32 + 1;
+constexpr int kBuilderWarp = kThreads / 32 + 2;  // first builder warp
+constexpr int kGroupBufs = 3;                    // group buffers (staged one group ahead)
 // row stride (floats) of a warp's fold-coefficient table: kMaxRec padded so the
 // 32 lanes' stores (8 rows x 4 records) fall in 32 different banks
 constexpr int kMtabRow = kMaxRec + 4;
@@ -55,11 +59,11 @@ __host__ __device__ __forceinline__ int coef_stride(int C) { return (3 * C + 8 +
 // per-head scalars after the 3C record coefficients
 enum : int { CO_GAMMA = 0, CO_A = 1, CO_BETA = 2, CO_KQ = 3, CO_MATSCALE = 4 };
 
-// Shared-memory layout (bytes): [stages][2 group buffers][persistent].
+// Shared-memory layout (bytes): [stages][3 group buffers][persistent].
 struct Lay128 {
   int st_tile, st_rec, st_meta, st_size;
-  int gb_key, gb_q, gb_cur, gb_la, gb_dt, gb_s1, gb_s2, gb_rs, gb_ms, gb_qf, gb_kf, gb_dq, gb_coef, gb_size;
-  int pe_A, pe_bars, pe_seq, pe_misc, pe_mtab, pe_size;
+  int gb_key, gb_q, gb_cur, gb_la, gb_dt, gb_s1, gb_s2, gb_rs, gb_ms, gb_qf, gb_kf, gb_coef, gb_size;
+  int pe_A, pe_bars, pe_seq, pe_misc, pe_mtab, pe_dq, pe_size;
 };
 
 // heads in a non-flush unit of a read-copy layer: 4 heads' codes fit where one
@@ -69,6 +73,7 @@ __host__ __device__ __forceinline__ int read_heads(int read) { return read == RE
 // units per head: a Gated DeltaNet head of d_head 128 is two units of 64 rows,
 // so that a stage holds 32 KB of state and five stages fit
 __host__ __device__ __forceinline__ int splits(int kind, int P) { return (kind == 1 && P == 128) ? 2 : 1; }
+
 
 __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int C, int Cp, int H, int hpg) {
   Lay128 l;
@@ -91,15 +96,15 @@ __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int
   l.gb_ms = o;    o += read == READ_NVFP4 ? span : 0;
   l.gb_qf = o;    o += N * 4;
   l.gb_kf = o;    o += kind == 0 ? 0 : N * 4;
-  l.gb_dq = o;    o += al16(C * 4) * 2;  // k_j . q, then (GDN) k_j . k_cur
   l.gb_coef = o;  o += hpg * coef_stride(C) * 4;
   l.gb_size = al128(o);
   o = 0;
   l.pe_A = o;     o += al16(H * 4);
-  l.pe_bars = o;  o += 48 * 8;  // full, empty, ready x 8 stages; amax x 2 teams x 8 stages; dots, tables x 2 teams; group tables x 2 buffers
+  l.pe_bars = o;  o += 48 * 8;  // full, empty, ready x 8 stages; amax x 2 teams x 8 stages; group full, tables x 3
   l.pe_seq = o;   o += 3 * kMaxSeq128 * 4;
   l.pe_misc = o;  o += 16;
   l.pe_mtab = o;  o += (kThreads / 32) * 8 * kMtabRow * 4;  // per computing warp: fold coefficients [8 rows][records]
+  l.pe_dq = o;    o += 2 * 2 * kMaxRec * 4;                 // per builder: k_j . q, k_j . k_cur
   l.pe_size = al128(o);
   return l;
 }
@@ -150,6 +155,34 @@ struct Walk {
   }
 };
 
+// Position of a group: sequence b, group g, and its first head-in-group hh0, part
+// sp0 and unit index ui0 in this CTA (a CTA's first group may start mid-group).
+struct GWalk {
+  int b, g, hh0, sp0, ui0;
+  __device__ __forceinline__ void start(int u0, int H, int hpg, int spl) {
+    b = u0 / (H * spl);
+    const int r = u0 - b * H * spl;
+    const int h = r / spl;
+    sp0 = r - h * spl;
+    g = h / hpg;
+    hh0 = h - g * hpg;
+    ui0 = u0;
+  }
+  __device__ __forceinline__ void next(int H, int G, int hpg, int spl) {
+    if (++g == G) {
+      g = 0;
+      ++b;
+    }
+    hh0 = 0;
+    sp0 = 0;
+    ui0 = (b * H + g * hpg) * spl;
+  }
+  // one past the last head-in-group of this group that has a unit in [ui0, u1)
+  __device__ __forceinline__ int hh_end(int u1, int hpg, int spl) const {
+    return min(hpg, hh0 + (u1 - ui0 + sp0 + spl - 1) / spl);
+  }
+};
+
 // TEAMS: the eight computing warps form TEAMS teams of 8 / TEAMS warps; team t
 // takes units t, t + TEAMS, ..., so that TEAMS units are computed at once
 template <int KIND, int READ, int P, int TEAMS>
@@ -160,10 +193,8 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   constexpr int SPL = (KIND == 1 && P == 128) ? 2 : 1;  // units per head
   constexpr int RPU = P / SPL;                          // state rows per unit
   constexpr int TW = 8 / TEAMS;                         // warps of a team
-  // Gated DeltaNet: the prologue warp builds each group's key dots and coefficient
-  // tables (two heads a group, little else to do there); Mamba-2: the computing warps
-  constexpr bool PRO = KIND == 1;
   constexpr int RW = RPU / TW;                          // rows per computing warp and unit
+  constexpr int NB = KIND == 0 ? 2 : 1;                 // builder warps (Mamba-2 groups hold more heads)
   constexpr int tile = P * N;                           // floats of one head's state
   constexpr int HR = READ == READ_NONE ? 1 : 4;         // heads of a non-flush read-copy unit
   const int H = d.H, G = d.G, C = d.C, L = d.L, Cp = d.Cp;
@@ -172,17 +203,17 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const Lay128 LY = lay128(KIND, READ, P, C, Cp, H, hpg);
   unsigned char* gbase = smem + static_cast<size_t>(LY.st_size) * stages;
-  unsigned char* pbase = gbase + 2 * LY.gb_size;
+  unsigned char* pbase = gbase + kGroupBufs * LY.gb_size;
   const float* sA = reinterpret_cast<const float*>(pbase + LY.pe_A);
   uint64_t* full = reinterpret_cast<uint64_t*>(pbase + LY.pe_bars);
   uint64_t* empty = full + 8;
   uint64_t* ready = full + 16;
-  uint64_t* amaxbar = full + 24;   // [team][stage]: NVFP4 matrix amax of a flushed unit
-  uint64_t* dots_bar = full + 40;  // [team]: the group's key dot products are in place
-  uint64_t* tab_bar = full + 42;   // [team]: the group's coefficient tables are in place
-  uint64_t* grp_bar = full + 44;   // [group buffer]: its tables are in place (for the other teams)
+  uint64_t* amaxbar = full + 24;  // [team][stage]: NVFP4 matrix amax of a flushed unit
+  uint64_t* gfull = full + 40;    // [group buffer]: the group's copies have landed
+  uint64_t* tready = full + 43;   // [group buffer]: the group's tables are in place
   int* sseq = reinterpret_cast<int*>(pbase + LY.pe_seq);
-  volatile int* smisc = reinterpret_cast<volatile int*>(pbase + LY.pe_misc);  // abort, issued, producer done
+  // abort, unit copies issued, producer done, group copies issued
+  volatile int* smisc = reinterpret_cast<volatile int*>(pbase + LY.pe_misc);
   // this warp's fold-coefficient table (computing warps)
   float* mt = reinterpret_cast<float*>(pbase + LY.pe_mtab) + (warp < kThreads / 32 ? warp : 0) * 8 * kMtabRow;
 
@@ -227,14 +258,14 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       mbar_init(ready + s, 1);
       for (int k = 0; k < TEAMS; ++k) mbar_init(amaxbar + 8 * k + s, TW);
     }
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(dots_bar + k, TW);
-      mbar_init(tab_bar + k, TW);
-      mbar_init(grp_bar + k, TW);
+    for (int k = 0; k < kGroupBufs; ++k) {
+      mbar_init(gfull + k, 1);
+      mbar_init(tready + k, NB);
     }
     smisc[0] = 0;
     smisc[1] = 0;
     smisc[2] = 0;
+    smisc[3] = 0;
   }
   __syncthreads();
 
@@ -243,52 +274,6 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     const int k = b - b0;
     return (HR > 1 && !(sseq[3 * k + 2] != 0 && sseq[3 * k + 1] + 1 == L)) ? HR : 1;
   };
-  // coefficient table of head-in-group e of the group in buffer gb (one warp): record
-  // coefficients and per-head scalars; lane j holds dq = k_j . q, dk = k_j . k_cur and
-  // the ring slot of record j
-  auto head_table = [&](unsigned char* gb, size_t ug, int e, int n, float dq, float dk, int slot_lane) {
-    float* co = reinterpret_cast<float*>(gb + LY.gb_coef) + e * CS;
-    const float* la_row = reinterpret_cast<const float*>(gb + LY.gb_la) + e * Cp;
-    if (KIND == 0) {
-      const uint16_t* dt_row = reinterpret_cast<const uint16_t*>(gb + LY.gb_dt) + e * Cp;
-      const uint16_t dt_bits = reinterpret_cast<const uint16_t*>(gb + LY.gb_s1)[(ug & 7) + e];
-      const float dt_cur = bf(dt_bits);
-      const float la_cur = dt_cur * sA[static_cast<int>(ug % H) + e];
-      // records 0..n (current at n): w_j = exp(sum_{i=j+1..n} la_i), gamma = exp(sum_{i<=n} la_i)
-      const float sv = suffix_sum(lane < n ? la_row[slot_lane] : (lane == n ? la_cur : 0.f), lane, n);
-      const float excl = __shfl_down_sync(0xffffffffu, sv, 1);
-      const float Wl = lane <= n ? expf(lane < n ? excl : 0.f) : 0.f;
-      const float dtl = lane < n ? bf(dt_row[slot_lane]) : (lane == n ? dt_cur : 0.f);
-      if (lane <= n) {
-        co[lane] = Wl * dtl * dq;     // output coefficient on x_j[r]
-        co[2 * C + lane] = Wl * dtl;  // fold coefficient on x_j[r]
-      }
-      if (lane == 0) {
-        co[3 * C + CO_GAMMA] = expf(sv);
-        if (READ == READ_NVFP4)
-          co[3 * C + CO_MATSCALE] = reinterpret_cast<const float*>(gb + LY.gb_ms)[(ug & 3) + e];
-      }
-    } else {
-      // buffered records 0..n-1: w_j = exp(sum_{i=j+1..n-1} g_i), gamma = exp(sum_{i<n} g_i)
-      const float sv = suffix_sum(lane < n ? la_row[slot_lane] : 0.f, lane, n - 1);
-      const float excl = __shfl_down_sync(0xffffffffu, sv, 1);
-      const float Wl = lane < n ? expf(lane + 1 < n ? excl : 0.f) : 0.f;
-      const float g_cur = reinterpret_cast<const float*>(gb + LY.gb_s1)[(ug & 3) + e];
-      const float a = expf(g_cur);
-      if (lane < n) {
-        co[lane] = Wl * dk;         // coefficient of u_j[r] in S k
-        co[C + lane] = Wl * dq;     // coefficient of u_j[r] in S q
-        co[2 * C + lane] = a * Wl;  // fold coefficient of u_j[r]
-      }
-      const float kq_dot = __shfl_sync(0xffffffffu, dq, n);
-      if (lane == 0) {
-        co[3 * C + CO_GAMMA] = n > 0 ? expf(sv) : 1.f;
-        co[3 * C + CO_A] = a;
-        co[3 * C + CO_BETA] = reinterpret_cast<const float*>(gb + LY.gb_s2)[(ug & 3) + e];
-        co[3 * C + CO_KQ] = kq_dot;
-      }
-    }
-  };
   // first element of the 16-byte block holding element e, for 2-byte / 4-byte arrays
   auto blk2 = [](size_t e) { return e & ~static_cast<size_t>(7); };
   auto blk4 = [](size_t e) { return e & ~static_cast<size_t>(3); };
@@ -296,41 +281,78 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   // =============================== producer warp ===============================
   if (warp == kProducerWarp) {
     if (lane != 0) return;
+    // the copies of group gw (its buffer x, barrier gfull[x]): keys and query,
+    // current tokens, decay rows, scalars, scales (and A with the first group)
+    auto stage_group = [&](const GWalk& gw, int x, bool with_A) {
+      const int k = gw.b - b0;
+      const int head = sseq[3 * k], n = sseq[3 * k + 1];
+      const int seg1 = min(n, C - head), seg2 = n - seg1;
+      const size_t ug = static_cast<size_t>(gw.b) * H + static_cast<size_t>(gw.g) * hpg;  // first head
+      const size_t bg = static_cast<size_t>(gw.b) * G + gw.g;
+      const uint32_t s1b = KIND == 0 ? static_cast<uint32_t>((blk2(ug + hpg + 7) - blk2(ug)) * 2)
+                                     : static_cast<uint32_t>((blk4(ug + hpg + 3) - blk4(ug)) * 4);
+      const uint32_t s4b = static_cast<uint32_t>((blk4(ug + hpg + 3) - blk4(ug)) * 4);
+      uint32_t bytes = static_cast<uint32_t>(n + 1) * N * 2 + N * 2 + hpg * P * 2 + hpg * Cp * 4 + s1b;
+      if (KIND == 0) bytes += hpg * Cp * 2;
+      else bytes += s4b;
+      if (READ == READ_FP8) bytes += hpg * P * 4;
+      if (READ == READ_NVFP4) bytes += hpg * P * (N / 16) + s4b;
+      if (with_A) bytes += al16(H * 4);
+      unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * x;
+      uint64_t* bar = gfull + x;
+      mbar_expect_tx(bar, bytes);
+      const uint16_t* rk = (KIND == 0 ? d.r_B : d.r_k) + bg * C * N;
+      if (seg1) bulk_g2s(gb + LY.gb_key, rk + static_cast<size_t>(head) * N, seg1 * N * 2, bar);
+      if (seg2) bulk_g2s(gb + LY.gb_key + seg1 * N * 2, rk, seg2 * N * 2, bar);
+      bulk_g2s(gb + LY.gb_key + n * N * 2, (KIND == 0 ? in.Bm : in.k) + bg * N, N * 2, bar);
+      bulk_g2s(gb + LY.gb_q, (KIND == 0 ? in.Cm : in.q) + bg * N, N * 2, bar);
+      bulk_g2s(gb + LY.gb_cur, (KIND == 0 ? in.x : in.v) + ug * P, hpg * P * 2, bar);
+      if (KIND == 0) {
+        bulk_g2s(gb + LY.gb_la, d.r_la + ug * Cp, hpg * Cp * 4, bar);
+        bulk_g2s(gb + LY.gb_dt, d.r_dt + ug * Cp, hpg * Cp * 2, bar);
+        bulk_g2s(gb + LY.gb_s1, in.dt + blk2(ug), s1b, bar);
+      } else {
+        bulk_g2s(gb + LY.gb_la, d.r_g + ug * Cp, hpg * Cp * 4, bar);
+        bulk_g2s(gb + LY.gb_s1, in.g + blk4(ug), s1b, bar);
+        bulk_g2s(gb + LY.gb_s2, in.beta + blk4(ug), s4b, bar);
+      }
+      if (READ == READ_FP8) bulk_g2s(gb + LY.gb_rs, d.rc_rowscale + ug * P, hpg * P * 4, bar);
+      if (READ == READ_NVFP4) {
+        bulk_g2s(gb + LY.gb_rs, d.rc_blkscale + ug * (P * (N / 16)), hpg * P * (N / 16), bar);
+        bulk_g2s(gb + LY.gb_ms, d.rc_matscale + blk4(ug), s4b, bar);
+      }
+      if (with_A) bulk_g2s(pbase + LY.pe_A, in.A, al16(H * 4), bar);
+    };
     Walk w;
     w.start(u0, H, hpg, SPL);
-    int gi = -1;
+    GWalk gn;  // the next group to stage
+    gn.start(u0, H, hpg, SPL);
+    int gi = -1, staged = 0;
     for (int i = 0; w.ui < u1; ++i, w.next(H, hpg, step_of(w.b), SPL)) {
       const int s = i % stages;
       if (i >= stages && !mbar_wait_bounded(empty + s, static_cast<uint32_t>(((i / stages) - 1) & 1))) break;
       if (smisc[0]) break;
       const bool first = i == 0 || (w.hh == 0 && w.sp == 0);
       if (first) ++gi;
+      // group buffers: the CTA's first group with its first unit, then group gi + 1
+      // at the first unit of group gi (its buffer's earlier group, gi - 2, has left
+      // the pipeline: stages <= units per group + 1)
+      if (i == 0) {
+        stage_group(gn, 0, KIND == 0);
+        gn.next(H, G, hpg, SPL);
+        smisc[3] = staged = 1;
+      }
       const int k = w.b - b0;
       const int head = sseq[3 * k], n = sseq[3 * k + 1];
       const bool flush = sseq[3 * k + 2] != 0 && n + 1 == L;
       unsigned char* st = smem + static_cast<size_t>(LY.st_size) * s;
-      unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * (gi & 1);
       uint64_t* bar = full + s;
       const size_t u = static_cast<size_t>(w.u);
       const int seg1 = min(n, C - head), seg2 = n - seg1;
       constexpr int esz = KIND == 0 ? 2 : 4;
       const int nh = step_of(w.b);  // heads in this unit
       const uint32_t tb = (READ == READ_NONE || flush) ? RPU * N * 4 : (READ == READ_FP8 ? tile : tile / 2);
-      uint32_t bytes = nh * (tb + static_cast<uint32_t>(n) * RPU * esz);
-      const size_t ug = static_cast<size_t>(w.b) * H + static_cast<size_t>(w.g) * hpg;  // first unit of the group
-      const size_t bg = static_cast<size_t>(w.b) * G + w.g;
-      const uint32_t s1b = KIND == 0 ? static_cast<uint32_t>((blk2(ug + hpg + 7) - blk2(ug)) * 2)
-                                     : static_cast<uint32_t>((blk4(ug + hpg + 3) - blk4(ug)) * 4);
-      const uint32_t s4b = static_cast<uint32_t>((blk4(ug + hpg + 3) - blk4(ug)) * 4);
-      if (first) {
-        bytes += static_cast<uint32_t>(n + 1) * N * 2 + N * 2 + hpg * P * 2 + hpg * Cp * 4 + s1b;
-        if (KIND == 0) bytes += hpg * Cp * 2;
-        else bytes += s4b;
-        if (READ == READ_FP8) bytes += hpg * P * 4;
-        if (READ == READ_NVFP4) bytes += hpg * P * (N / 16) + s4b;
-      }
-      if (KIND == 0 && i == 0) bytes += al16(H * 4);  // A (Mamba-2 only)
-      mbar_expect_tx(bar, bytes);
+      mbar_expect_tx(bar, nh * (tb + static_cast<uint32_t>(n) * RPU * esz));
       // the unit: state matrix (or read copy) and this head's buffered records
       if (READ == READ_NONE || flush) bulk_g2s(st + LY.st_tile, d.ckpt + u * tile + w.sp * RPU * N, tb, bar);
       else bulk_g2s(st + LY.st_tile, d.rc_codes + u * tb, nh * tb, bar);  // nh consecutive heads
@@ -351,33 +373,179 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
                    rsrc + (u * C + ring_slot(head, j, C)) * rrow + static_cast<size_t>(w.sp) * RPU * esz, RPU * esz,
                    bar);
       }
-      // the group: keys and query, current tokens, decay rows, scalars, scales
-      if (first) {
-        const uint16_t* rk = (KIND == 0 ? d.r_B : d.r_k) + bg * C * N;
-        if (seg1) bulk_g2s(gb + LY.gb_key, rk + static_cast<size_t>(head) * N, seg1 * N * 2, bar);
-        if (seg2) bulk_g2s(gb + LY.gb_key + seg1 * N * 2, rk, seg2 * N * 2, bar);
-        bulk_g2s(gb + LY.gb_key + n * N * 2, (KIND == 0 ? in.Bm : in.k) + bg * N, N * 2, bar);
-        bulk_g2s(gb + LY.gb_q, (KIND == 0 ? in.Cm : in.q) + bg * N, N * 2, bar);
-        bulk_g2s(gb + LY.gb_cur, (KIND == 0 ? in.x : in.v) + ug * P, hpg * P * 2, bar);
-        if (KIND == 0) {
-          bulk_g2s(gb + LY.gb_la, d.r_la + ug * Cp, hpg * Cp * 4, bar);
-          bulk_g2s(gb + LY.gb_dt, d.r_dt + ug * Cp, hpg * Cp * 2, bar);
-          bulk_g2s(gb + LY.gb_s1, in.dt + blk2(ug), s1b, bar);
-        } else {
-          bulk_g2s(gb + LY.gb_la, d.r_g + ug * Cp, hpg * Cp * 4, bar);
-          bulk_g2s(gb + LY.gb_s1, in.g + blk4(ug), s1b, bar);
-          bulk_g2s(gb + LY.gb_s2, in.beta + blk4(ug), s4b, bar);
-        }
-        if (READ == READ_FP8) bulk_g2s(gb + LY.gb_rs, d.rc_rowscale + ug * P, hpg * P * 4, bar);
-        if (READ == READ_NVFP4) {
-          bulk_g2s(gb + LY.gb_rs, d.rc_blkscale + ug * (P * (N / 16)), hpg * P * (N / 16), bar);
-          bulk_g2s(gb + LY.gb_ms, d.rc_matscale + blk4(ug), s4b, bar);
-        }
-      }
-      if (KIND == 0 && i == 0) bulk_g2s(pbase + LY.pe_A, in.A, al16(H * 4), bar);
       smisc[1] = i + 1;
+      if (first && gn.ui0 < u1) {
+        stage_group(gn, (gi + 1) % kGroupBufs, false);
+        gn.next(H, G, hpg, SPL);
+        smisc[3] = ++staged;
+      }
     }
     smisc[2] = 1;
+    return;
+  }
+
+  // =============================== builder warps ===============================
+  if (warp >= kBuilderWarp) {
+    const int bi = warp - kBuilderWarp;
+    if (bi >= NB) return;
+    float* pdq = reinterpret_cast<float*>(pbase + LY.pe_dq) + bi * 2 * kMaxRec;  // k_j . q
+    float* pdk = pdq + kMaxRec;                                                   // k_j . k_cur
+    GWalk gw;
+    gw.start(u0, H, hpg, SPL);
+    int built = 0;
+    for (int gi = 0; gw.ui0 < u1; ++gi, gw.next(H, G, hpg, SPL)) {
+      if (smisc[0]) break;
+      const int x = gi % kGroupBufs;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(gfull + x, static_cast<uint32_t>((gi / kGroupBufs) & 1)))) {
+        if (lane == 0) {
+          report_error(d.err, DEVERR_TIMEOUT, gw.b);
+          smisc[0] = 1;
+        }
+        break;
+      }
+      built = gi + 1;
+      const int k = gw.b - b0;
+      const int head = sseq[3 * k], n = sseq[3 * k + 1];
+      const bool ok = sseq[3 * k + 2] != 0;
+      const bool flush = ok && n + 1 == L;
+      const int slot = ring_slot(head, n, C);
+      unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * x;
+      const size_t ug = static_cast<size_t>(gw.b) * H + static_cast<size_t>(gw.g) * hpg;  // first head of the group
+      const int hh_hi = gw.hh_end(u1, hpg, SPL);
+      const uint16_t* kb = reinterpret_cast<const uint16_t*>(gb + LY.gb_key);
+      if (ok) {
+        // the query (and current key) in FP32
+        const float4 q4 = bf4(reinterpret_cast<const uint2*>(gb + LY.gb_q)[lane]);
+        const float4 kc4 = bf4(reinterpret_cast<const uint2*>(kb + n * N)[lane]);
+        if (bi == 0) {
+          reinterpret_cast<float4*>(gb + LY.gb_qf)[lane] = q4;
+          if (KIND == 1) reinterpret_cast<float4*>(gb + LY.gb_kf)[lane] = kc4;
+        }
+        // key dot products of records 0..n, eight keys per transpose-reduce
+        for (int jb = 0; jb <= n; jb += 8) {
+          float pq[8], pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 kj = jb + e <= n ? bf4(reinterpret_cast<const uint2*>(kb + (jb + e) * N)[lane])
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            pq[e] = dot4(kj, q4);
+            pk[e] = KIND == 1 ? dot4(kj, kc4) : 0.f;
+          }
+          const float tq = reduce8(pq, lane);
+          const float tk = KIND == 1 ? reduce8(pk, lane) : 0.f;
+          const int j = jb + (lane >> 2);
+          if ((lane & 3) == 0 && j <= n) {
+            pdq[j] = tq;
+            if (KIND == 1) pdk[j] = tk;
+          }
+        }
+        __syncwarp();
+        // coefficient tables: two heads at once in the 16-lane halves when records
+        // 0..n fit in 16 lanes; passes shared out over the builders
+        const int sw = n < 16 ? 16 : 32;
+        const int jl = lane & (sw - 1);
+        const float dq = jl <= n ? pdq[jl] : 0.f;
+        const float dk = (KIND == 1 && jl <= n) ? pdk[jl] : 0.f;
+        const int slot_j = jl < n ? ring_slot(head, jl, C) : 0;
+        for (int e0 = gw.hh0 + bi * (32 / sw); e0 < hh_hi; e0 += NB * (32 / sw)) {
+          const int e = e0 + lane / sw;
+          const bool act = e < hh_hi;
+          const float* la_row = reinterpret_cast<const float*>(gb + LY.gb_la) + e * Cp;
+          float* co = reinterpret_cast<float*>(gb + LY.gb_coef) + e * CS;
+          if (KIND == 0) {
+            // records 0..n (current at n): w_j = exp(sum_{i=j+1..n} la_i), gamma = exp(sum_{i<=n} la_i)
+            float dt_cur = 0.f, la_cur = 0.f;
+            if (act) {
+              dt_cur = bf(reinterpret_cast<const uint16_t*>(gb + LY.gb_s1)[(ug & 7) + e]);
+              la_cur = dt_cur * sA[gw.g * hpg + e];
+            }
+            float v = act ? (jl < n ? la_row[slot_j] : (jl == n ? la_cur : 0.f)) : 0.f;
+            for (int o = 1; o < sw; o <<= 1) {  // suffix sums within the segment
+              const float wv = __shfl_down_sync(0xffffffffu, v, o);
+              if (jl + o <= n) v += wv;
+            }
+            const float excl = __shfl_down_sync(0xffffffffu, v, 1);
+            if (act) {
+              const float Wl = jl <= n ? expf(jl < n ? excl : 0.f) : 0.f;
+              const uint16_t* dt_row = reinterpret_cast<const uint16_t*>(gb + LY.gb_dt) + e * Cp;
+              const float dtl = jl < n ? bf(dt_row[slot_j]) : (jl == n ? dt_cur : 0.f);
+              if (jl <= n) {
+                co[jl] = Wl * dtl * dq;     // output coefficient on x_j[r]
+                co[2 * C + jl] = Wl * dtl;  // fold coefficient on x_j[r]
+              }
+              if (jl == 0) {
+                co[3 * C + CO_GAMMA] = expf(v);
+                if (READ == READ_NVFP4)
+                  co[3 * C + CO_MATSCALE] = reinterpret_cast<const float*>(gb + LY.gb_ms)[(ug & 3) + e];
+              }
+            }
+          } else {
+            // buffered records 0..n-1: w_j = exp(sum_{i=j+1..n-1} g_i), gamma = exp(sum_{i<n} g_i)
+            float v = act && jl < n ? la_row[slot_j] : 0.f;
+            for (int o = 1; o < sw; o <<= 1) {  // suffix sums within the segment
+              const float wv = __shfl_down_sync(0xffffffffu, v, o);
+              if (jl + o <= n - 1) v += wv;
+            }
+            const float excl = __shfl_down_sync(0xffffffffu, v, 1);
+            const float kq_dot = __shfl_sync(0xffffffffu, dq, (lane & ~(sw - 1)) + n);  // k_cur . q
+            if (act) {
+              const float Wl = jl < n ? expf(jl + 1 < n ? excl : 0.f) : 0.f;
+              const float a = expf(reinterpret_cast<const float*>(gb + LY.gb_s1)[(ug & 3) + e]);
+              if (jl < n) {
+                co[jl] = Wl * dk;         // coefficient of u_j[r] in S k
+                co[C + jl] = Wl * dq;     // coefficient of u_j[r] in S q
+                co[2 * C + jl] = a * Wl;  // fold coefficient of u_j[r]
+              }
+              if (jl == 0) {
+                co[3 * C + CO_GAMMA] = n > 0 ? expf(v) : 1.f;
+                co[3 * C + CO_A] = a;
+                co[3 * C + CO_BETA] = reinterpret_cast<const float*>(gb + LY.gb_s2)[(ug & 3) + e];
+                co[3 * C + CO_KQ] = kq_dot;
+              }
+            }
+          }
+        }
+        if (!flush) {
+          // ring appends: the current tokens of the group's heads in this CTA (a head
+          // whose first part another CTA holds is appended by that CTA), and the group's
+          // key row from the CTA that holds the group's first head
+          for (int e = gw.hh0 + (gw.sp0 > 0 ? 1 : 0) + bi; e < hh_hi; e += NB) {
+            const size_t ue = ug + e;
+            if (KIND == 0) {
+              const uint16_t* xc = reinterpret_cast<const uint16_t*>(gb + LY.gb_cur) + e * P;
+              uint16_t* dst = d.r_x + (ue * C + slot) * P;
+              if (P == 64)
+                reinterpret_cast<uint32_t*>(dst)[lane] = reinterpret_cast<const uint32_t*>(xc)[lane];
+              else
+                reinterpret_cast<uint2*>(dst)[lane] = reinterpret_cast<const uint2*>(xc)[lane];
+              if (lane == 0) {
+                const uint16_t dt_bits = reinterpret_cast<const uint16_t*>(gb + LY.gb_s1)[(ug & 7) + e];
+                d.r_dt[ue * Cp + slot] = dt_bits;
+                d.r_la[ue * Cp + slot] = bf(dt_bits) * sA[gw.g * hpg + e];
+              }
+            } else if (lane == 0) {
+              d.r_g[ue * Cp + slot] = reinterpret_cast<const float*>(gb + LY.gb_s1)[(ug & 3) + e];
+            }
+          }
+          if (bi == 0 && gw.hh0 == 0 && gw.sp0 == 0) {
+            const size_t bg = static_cast<size_t>(gw.b) * G + gw.g;
+            reinterpret_cast<uint2*>((KIND == 0 ? d.r_B : d.r_k) + (bg * C + slot) * N)[lane] =
+                reinterpret_cast<const uint2*>(kb + n * N)[lane];
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tready + x);
+    }
+    // after an abort: let the group copies already issued land before the CTA exits
+    if (smisc[0] && bi == 0 && lane == 0) {
+      const uint64_t t0 = global_ns();
+      while (!smisc[2] && global_ns() - t0 < 2000000000ull) {
+      }
+      const int issued = smisc[3];
+      for (int j = built; j < issued; ++j)
+        mbar_wait_bounded(gfull + (j % kGroupBufs), static_cast<uint32_t>((j / kGroupBufs) & 1));
+    }
     return;
   }
 
@@ -387,7 +555,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   if (warp == kPrologueWarp) {
     Walk w;
     w.start(u0, H, hpg, SPL);
-    int gi = -1, consumed = 0;
+    int gi = -1, gx = 0, consumed = 0;
     for (int i = 0; w.ui < u1; ++i, w.next(H, hpg, step_of(w.b), SPL)) {
       if (smisc[0]) break;
       const int s = i % stages;
@@ -400,88 +568,30 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       }
       consumed = i + 1;
       const bool first = i == 0 || (w.hh == 0 && w.sp == 0);
-      if (first) ++gi;
-      const int k = w.b - b0;
-      const int head = sseq[3 * k], n = sseq[3 * k + 1];
-      const bool ok = sseq[3 * k + 2] != 0;
-      const bool flush = ok && n + 1 == L;
-      const int slot = ring_slot(head, n, C);
-      unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * (gi & 1);
-      if (first && ok) {
-        // ---- once per group: the query (and current key) in FP32, ring appends ----
-        const size_t ug = static_cast<size_t>(w.b) * H + static_cast<size_t>(w.g) * hpg;
-        const uint16_t* kb = reinterpret_cast<const uint16_t*>(gb + LY.gb_key);
-        const float4 q4 = bf4(reinterpret_cast<const uint2*>(gb + LY.gb_q)[lane]);
-        const float4 kc4 = bf4(reinterpret_cast<const uint2*>(kb + n * N)[lane]);
-        reinterpret_cast<float4*>(gb + LY.gb_qf)[lane] = q4;
-        if (KIND == 1) reinterpret_cast<float4*>(gb + LY.gb_kf)[lane] = kc4;
-        // heads of this group in this CTA; a head whose first part another CTA holds is
-        // appended by that CTA
-        const int hh_hi = min(hpg, w.hh + (u1 - w.ui + w.sp + SPL - 1) / SPL);
-        if (!flush) {
-          // append the current tokens of the group's heads in this CTA to the ring
-          for (int e = w.hh + (w.sp > 0 ? 1 : 0); e < hh_hi; ++e) {
-            const size_t ue = ug + e;
-            if (KIND == 0) {
-              const uint16_t* xc = reinterpret_cast<const uint16_t*>(gb + LY.gb_cur) + e * P;
-              uint16_t* dst = d.r_x + (ue * C + slot) * P;
-              if (P == 64)
-                reinterpret_cast<uint32_t*>(dst)[lane] = reinterpret_cast<const uint32_t*>(xc)[lane];
-              else
-                reinterpret_cast<uint2*>(dst)[lane] = reinterpret_cast<const uint2*>(xc)[lane];
-              if (lane == 0) {
-                const uint16_t dt_bits = reinterpret_cast<const uint16_t*>(gb + LY.gb_s1)[(ug & 7) + e];
-                d.r_dt[ue * Cp + slot] = dt_bits;
-                d.r_la[ue * Cp + slot] = bf(dt_bits) * sA[w.g * hpg + e];
-              }
-            } else if (lane == 0) {
-              d.r_g[ue * Cp + slot] = reinterpret_cast<const float*>(gb + LY.gb_s1)[(ug & 3) + e];
-            }
+      if (first) {
+        ++gi;
+        gx = gi % kGroupBufs;
+        // the group's tables are in place
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(tready + gx, static_cast<uint32_t>((gi / kGroupBufs) & 1)))) {
+          if (lane == 0) {
+            report_error(d.err, DEVERR_TIMEOUT, w.b);
+            smisc[0] = 1;
           }
-        }
-        if (!flush && w.hh == 0 && w.sp == 0) {
-          // the group's key row: appended by the CTA that holds the group's first head
-          const size_t bg = static_cast<size_t>(w.b) * G + w.g;
-          reinterpret_cast<uint2*>((KIND == 0 ? d.r_B : d.r_k) + (bg * C + slot) * N)[lane] =
-              reinterpret_cast<const uint2*>(kb + n * N)[lane];
-        }
-        if (PRO) {
-          // the group's key dot products, eight keys per transpose-reduce, then the
-          // coefficient tables of its heads in this CTA
-          float* gdq = reinterpret_cast<float*>(gb + LY.gb_dq);
-          float* gdk = gdq + al16(C * 4) / 4;
-          for (int jb = 0; jb <= n; jb += 8) {
-            float pq[8], pk[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float4 kj = jb + e <= n ? bf4(reinterpret_cast<const uint2*>(kb + (jb + e) * N)[lane])
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
-              pq[e] = dot4(kj, q4);
-              pk[e] = dot4(kj, kc4);
-            }
-            const float tq = reduce8(pq, lane), tk = reduce8(pk, lane);
-            const int j = jb + (lane >> 2);
-            if ((lane & 3) == 0 && j <= n) {
-              gdq[j] = tq;
-              gdk[j] = tk;
-            }
-          }
-          __syncwarp();
-          const float dq = lane <= n ? gdq[lane] : 0.f;
-          const float dk = lane <= n ? gdk[lane] : 0.f;
-          const int slot_lane = lane < n ? ring_slot(head, lane, C) : 0;
-          for (int e = w.hh; e < hh_hi; ++e) head_table(gb, ug, e, n, dq, dk, slot_lane);
+          break;
         }
       }
       if (lane == 0) {
+        const int k = w.b - b0;
+        const int head = sseq[3 * k], n = sseq[3 * k + 1];
+        const bool ok = sseq[3 * k + 2] != 0;
+        const bool flush = ok && n + 1 == L;
         unsigned char* st = smem + static_cast<size_t>(LY.st_size) * s;
-        *reinterpret_cast<int4*>(st + LY.st_meta) = make_int4(
-            w.u, n | (flush ? 0x100 : 0) | (ok ? 0x200 : 0) | (first ? 0x400 : 0), slot,
-            w.hh | ((gi & 3) << 16) | (w.sp << 24));
+        *reinterpret_cast<int4*>(st + LY.st_meta) =
+            make_int4(w.u, n | (flush ? 0x100 : 0) | (ok ? 0x200 : 0) | (first ? 0x400 : 0),
+                      ring_slot(head, n, C), w.hh | (gx << 16) | (w.sp << 24));
         reinterpret_cast<int*>(st + LY.st_meta)[4] = 0;  // NVFP4 matrix amax
+        mbar_arrive(ready + s);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ready + s);
     }
     // after an abort: let the copies already issued land before the CTA exits
     if (smisc[0] && lane == 0) {
@@ -498,7 +608,6 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   // =============================== computing warps ===============================
   const int team = warp / TW, tw = warp - team * TW;  // team, warp in the team
   uint32_t amax_phase = 0;
-  int groups = 0;  // groups whose tables this team has built
   Walk wc;
   wc.start(u0, H, hpg, SPL);
   for (int i = 0; wc.ui < u1; ++i, wc.next(H, hpg, step_of(wc.b), SPL)) {
@@ -514,74 +623,6 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     }
     unsigned char* st = smem + static_cast<size_t>(LY.st_size) * s;
     const int4 meta = *reinterpret_cast<const int4*>(st + LY.st_meta);
-    // ---- first unit of a group in this CTA: the group's key dot products and the
-    // coefficient tables of its heads, shared out over the team's warps (two bounded
-    // mbarriers order the phases); a later unit of the group computed by another
-    // team waits for the tables on the group buffer's barrier ----
-    if (!PRO && (meta.y & 0x600) == 0x600) {
-      const int n = meta.y & 0xFF;
-      const int hh_lo = meta.w & 0xFFFF;
-      const size_t ug = static_cast<size_t>(meta.x) - hh_lo;  // first unit of the group
-      unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * ((meta.w >> 16) & 1);
-      const uint16_t* kb = reinterpret_cast<const uint16_t*>(gb + LY.gb_key);
-      float* gdq = reinterpret_cast<float*>(gb + LY.gb_dq);
-      float* gdk = gdq + al16(C * 4) / 4;
-      const float4 q4 = reinterpret_cast<const float4*>(gb + LY.gb_qf)[lane];
-      const float4 kc4 =
-          KIND == 1 ? reinterpret_cast<const float4*>(gb + LY.gb_kf)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int j = tw; j <= n; j += TW) {
-        const float4 kj = bf4(reinterpret_cast<const uint2*>(kb + j * N)[lane]);
-        float pq = dot4(kj, q4), pk = KIND == 1 ? dot4(kj, kc4) : 0.f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          pq += __shfl_xor_sync(0xffffffffu, pq, o);
-          if (KIND == 1) pk += __shfl_xor_sync(0xffffffffu, pk, o);
-        }
-        if (lane == 0) {
-          gdq[j] = pq;
-          if (KIND == 1) gdk[j] = pk;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dots_bar + team);
-      bool okg = __all_sync(0xffffffffu, mbar_wait_bounded(dots_bar + team, static_cast<uint32_t>(groups & 1)));
-      if (okg) {
-        const float dq = lane <= n ? gdq[lane] : 0.f;  // lane j: k_j . q
-        const float dk = (KIND == 1 && lane <= n) ? gdk[lane] : 0.f;  // lane j: k_j . k_cur
-        const int head = meta.z - n < 0 ? meta.z - n + C : meta.z - n;
-        const int slot_lane = lane < n ? ring_slot(head, lane, C) : 0;
-        const int hh_hi = min(hpg, hh_lo + (u1 - wc.ui + wc.sp + SPL - 1) / SPL);  // heads of this group in this CTA
-        for (int e = hh_lo + tw; e < hh_hi; e += TW) {
-          head_table(gb, ug, e, n, dq, dk, slot_lane);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tab_bar + team);
-        okg = __all_sync(0xffffffffu, mbar_wait_bounded(tab_bar + team, static_cast<uint32_t>(groups & 1)));
-      }
-      ++groups;
-      if (!okg) {
-        if (lane == 0) {
-          report_error(d.err, DEVERR_TIMEOUT, wc.b);
-          smisc[0] = 1;
-        }
-        break;
-      }
-    }
-    if (TEAMS > 1 && !PRO) {
-      // the group buffer's barrier completes once per group that uses it (its first
-      // unit's team arrives, with or without tables); phase (group index / 2) & 1
-      if (meta.y & 0x400) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(grp_bar + ((meta.w >> 16) & 1));
-      } else if (!__all_sync(0xffffffffu, mbar_wait_bounded(grp_bar + ((meta.w >> 16) & 1),
-                                                             static_cast<uint32_t>((meta.w >> 17) & 1)))) {
-        if (lane == 0) {
-          report_error(d.err, DEVERR_TIMEOUT, wc.b);
-          smisc[0] = 1;
-        }
-        break;
-      }
-    }
     const int nh_unit = (READ != READ_NONE && !(meta.y & 0x100)) ? HR : 1;  // heads of this unit
     if (KIND == 0 && READ != READ_NONE && nh_unit == HR && (meta.y & 0x200)) {
       // non-flush unit of a read-copy layer: HR heads, their chains interleaved
@@ -589,7 +630,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       const int n = meta.y & 0xFF;
       const int hh0 = meta.w & 0xFFFF;
       const size_t uh0 = static_cast<size_t>(meta.x);
-      const unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * ((meta.w >> 16) & 1);
+      const unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * ((meta.w >> 16) & 3);
       const float* cob = reinterpret_cast<const float*>(gb + LY.gb_coef);
       const uint16_t* curb = reinterpret_cast<const uint16_t*>(gb + LY.gb_cur);
       const float4 q4 = reinterpret_cast<const float4*>(gb + LY.gb_qf)[lane];
@@ -652,7 +693,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       const int slot = meta.z;
       const int hh = (meta.w & 0xFFFF) + hu;
       const int sp = meta.w >> 24;  // part of a split head: rows sp RPU .. sp RPU + RPU - 1
-      const unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * ((meta.w >> 16) & 1);
+      const unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * ((meta.w >> 16) & 3);
       const float* co = reinterpret_cast<const float*>(gb + LY.gb_coef) + hh * CS;
       const uint16_t* kb = reinterpret_cast<const uint16_t*>(gb + LY.gb_key);
       const uint16_t* cur = reinterpret_cast<const uint16_t*>(gb + LY.gb_cur) + hh * P + sp * RPU;  // x or v
@@ -884,17 +925,18 @@ template <int KIND, int READ, int P, int TEAMS>
 cudaError_t launch128(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s) {
   const int hpg = d.H / d.G;
   const Lay128 LY = lay128(KIND, READ, P, d.C, d.Cp, d.H, hpg);
-  const long budget = 227L * 1024 - 2L * LY.gb_size - LY.pe_size;
+  const long budget = 227L * 1024 - static_cast<long>(kGroupBufs) * LY.gb_size - LY.pe_size;
   long stages = budget / LY.st_size;
   if (stages > 8) stages = 8;
-  // a group buffer is rewritten two groups later: every unit of that earlier
-  // group must have left the pipeline, which holds when stages <= (units per
-  // group) + 1; a non-flush read-copy unit holds read_heads(READ) heads
+  // a group buffer is restaged for the group three later, at the first unit of
+  // the group two later: every unit of the buffer's earlier group must have left
+  // the pipeline, which holds when stages <= (units per group) + 1; a non-flush
+  // read-copy unit holds read_heads(READ) heads
   constexpr int SPL = (KIND == 1 && P == 128) ? 2 : 1;
   const int upg = hpg * SPL / read_heads(READ);
   if (stages > upg + 1) stages = upg + 1;
   if (stages < 1) return cudaErrorInvalidConfiguration;
-  const size_t smem = static_cast<size_t>(LY.st_size) * stages + 2u * LY.gb_size + LY.pe_size;
+  const size_t smem = static_cast<size_t>(LY.st_size) * stages + static_cast<size_t>(kGroupBufs) * LY.gb_size + LY.pe_size;
   // each CTA takes a contiguous range of heads, a multiple of read_heads(READ)
   const int hr = read_heads(READ);
   const int total = d.B * d.H * SPL;
@@ -913,21 +955,16 @@ cudaError_t launch128(const LayerDev& d, const TokenIn& in, float* y, cudaStream
   return cudaGetLastError();
 }
 
-template <int P, int TEAMS>
+// two computing teams where a unit is one FP32 matrix; one team on a read-copy
+// layer, whose non-flush units already interleave four heads' chains
+template <int P>
 cudaError_t launch128_p(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s) {
   if (d.kind == 0) {
-    if (d.read_mode == READ_FP8) return launch128<0, READ_FP8, P, TEAMS>(d, in, y, s);
-    if (d.read_mode == READ_NVFP4) return launch128<0, READ_NVFP4, P, TEAMS>(d, in, y, s);
-    return launch128<0, READ_NONE, P, TEAMS>(d, in, y, s);
+    if (d.read_mode == READ_FP8) return launch128<0, READ_FP8, P, 1>(d, in, y, s);
+    if (d.read_mode == READ_NVFP4) return launch128<0, READ_NVFP4, P, 1>(d, in, y, s);
+    return launch128<0, READ_NONE, P, 2>(d, in, y, s);
   }
-  return launch128<1, READ_NONE, P, TEAMS>(d, in, y, s);
-}
-
-int decode128_teams(const LayerDev& d) {
-  const char* e = getenv("RS_DECODE_TEAMS");
-  if (e && e[0] == '1') return 1;
-  if (e && e[0] == '2') return 2;
-  return d.kind == 1 ? 2 : 1;
+  return launch128<1, READ_NONE, P, 2>(d, in, y, s);
 }
 
 }  // namespace
@@ -937,13 +974,12 @@ bool decode128_supports(const LayerDev& d) {
   // a read-copy layer's non-flush units span read_heads heads of one group
   if (d.H % read_heads(d.read_mode) != 0 || (d.H / d.G) % read_heads(d.read_mode) != 0) return false;
   const Lay128 LY = lay128(d.kind, d.read_mode, d.P, d.C, d.Cp, d.H, d.H / d.G);
-  return static_cast<long>(LY.st_size) + 2L * LY.gb_size + LY.pe_size <= 227L * 1024;
+  return static_cast<long>(LY.st_size) + static_cast<long>(kGroupBufs) * LY.gb_size + LY.pe_size <= 227L * 1024;
 }
 
 cudaError_t launch_decode128(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s) {
   if (!decode128_supports(d)) return cudaErrorInvalidValue;
-  if (decode128_teams(d) == 1) return d.P == 64 ? launch128_p<64, 1>(d, in, y, s) : launch128_p<128, 1>(d, in, y, s);
-  return d.P == 64 ? launch128_p<64, 2>(d, in, y, s) : launch128_p<128, 2>(d, in, y, s);
+  return d.P == 64 ? launch128_p<64>(d, in, y, s) : launch128_p<128>(d, in, y, s);
 }
 
 }  // namespace rs

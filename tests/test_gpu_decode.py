@@ -84,6 +84,15 @@ def test_gdn_multi_tile_ragged():
     assert _run_decode(pair, 20) == 3
 
 
+def test_gdn_d128_long_window_split_heads():
+    """d_head 128 heads computed as two 64-row parts; three heads a group (one half-warp of
+    the two-head table build idle); window 20, so groups of up to 20 records take the
+    full-warp table build; 5 x 6 x 2 parts spread over CTAs that start mid-head."""
+    shape = LayerShape(GDN, batch=5, n_heads=6, n_groups=2, d_head=128, d_state=128, ring_len=20)
+    pair = Pair(configs.GdnWorkload(shape, seed=16, s0_std=0.05))
+    assert _run_decode(pair, 45) == 2
+
+
 @pytest.mark.parametrize("N,P", [(32, 32), (128, 128), (16, 128), (128, 16)])
 def test_shapes_sweep(N, P):
     for kind in (MAMBA2, GDN):
