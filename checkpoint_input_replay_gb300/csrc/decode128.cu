@@ -192,6 +192,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int SPL = (KIND == 1 && P == 128) ? 2 : 1;  // units per head
   constexpr int RPU = P / SPL;                          // state rows per unit
+  static_assert(TEAMS == 1 || TEAMS == 2 || TEAMS == 4, "teams: a power of two dividing the 8 computing warps");
   constexpr int TW = 8 / TEAMS;                         // warps of a team
   constexpr int RW = RPU / TW;                          // rows per computing warp and unit
   constexpr int NB = KIND == 0 ? 2 : 1;                 // builder warps (Mamba-2 groups hold more heads)
@@ -328,10 +329,18 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     GWalk gn;  // the next group to stage
     gn.start(u0, H, hpg, SPL);
     int gi = -1, staged = 0;
+    int si = 0;        // stage of unit i
+    uint32_t ph = 0;   // parity of the stage's uses before unit i
     for (int i = 0; w.ui < u1; ++i, w.next(H, hpg, step_of(w.b), SPL)) {
-      const int s = i % stages;
-      if (i >= stages && !mbar_wait_bounded(empty + s, static_cast<uint32_t>(((i / stages) - 1) & 1))) break;
-      if (smisc[0]) break;
+      const int s = si;
+      const uint32_t par = ph ^ 1u;  // release of the stage's previous unit
+      if (++si == stages) {
+        si = 0;
+        ph ^= 1u;
+      }
+      if (i >= stages && !mbar_try_wait(empty + s, par)) {
+        if (smisc[0] || !mbar_wait_bounded(empty + s, par)) break;
+      }
       const bool first = i == 0 || (w.hh == 0 && w.sp == 0);
       if (first) ++gi;
       // group buffers: the CTA's first group with its first unit, then group gi + 1
@@ -556,15 +565,24 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     Walk w;
     w.start(u0, H, hpg, SPL);
     int gi = -1, gx = 0, consumed = 0;
+    int si = 0;
+    uint32_t ph = 0;
     for (int i = 0; w.ui < u1; ++i, w.next(H, hpg, step_of(w.b), SPL)) {
-      if (smisc[0]) break;
-      const int s = i % stages;
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(full + s, static_cast<uint32_t>((i / stages) & 1)))) {
-        if (lane == 0) {
-          report_error(d.err, DEVERR_TIMEOUT, w.b);
-          smisc[0] = 1;
+      const int s = si;
+      const uint32_t par = ph;
+      if (++si == stages) {
+        si = 0;
+        ph ^= 1u;
+      }
+      if (!__all_sync(0xffffffffu, mbar_try_wait(full + s, par))) {
+        if (smisc[0]) break;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(full + s, par))) {
+          if (lane == 0) {
+            report_error(d.err, DEVERR_TIMEOUT, w.b);
+            smisc[0] = 1;
+          }
+          break;
         }
-        break;
       }
       consumed = i + 1;
       const bool first = i == 0 || (w.hh == 0 && w.sp == 0);
@@ -610,16 +628,26 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   uint32_t amax_phase = 0;
   Walk wc;
   wc.start(u0, H, hpg, SPL);
+  int si = 0;
+  uint32_t ph = 0;
   for (int i = 0; wc.ui < u1; ++i, wc.next(H, hpg, step_of(wc.b), SPL)) {
-    if (smisc[0]) break;
-    if (TEAMS > 1 && i % TEAMS != team) continue;
-    const int s = i % stages;
-    if (!__all_sync(0xffffffffu, mbar_wait_bounded(ready + s, static_cast<uint32_t>((i / stages) & 1)))) {
-      if (lane == 0) {
-        report_error(d.err, DEVERR_TIMEOUT, wc.b);
-        smisc[0] = 1;
+    const int s = si;
+    const uint32_t par = ph;
+    if (++si == stages) {
+      si = 0;
+      ph ^= 1u;
+    }
+    if (TEAMS > 1 && (i & (TEAMS - 1)) != team) continue;
+    // the abort flag is read only when the unit is not ready at the first poll
+    if (!__all_sync(0xffffffffu, mbar_try_wait(ready + s, par))) {
+      if (smisc[0]) break;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(ready + s, par))) {
+        if (lane == 0) {
+          report_error(d.err, DEVERR_TIMEOUT, wc.b);
+          smisc[0] = 1;
+        }
+        break;
       }
-      break;
     }
     unsigned char* st = smem + static_cast<size_t>(LY.st_size) * s;
     const int4 meta = *reinterpret_cast<const int4*>(st + LY.st_meta);
