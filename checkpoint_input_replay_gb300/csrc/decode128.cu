@@ -880,8 +880,54 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
         const float a = co[3 * C + CO_A], beta = co[3 * C + CO_BETA];
         const float kq_dot = co[3 * C + CO_KQ];
         float* urow = d.r_u + (u * C + slot) * P + sp * RPU;
+        if (!flush) {
+          // the warp's 8-row blocks side by side, so that their chains (record terms,
+          // row dots, transpose-reduces) interleave
+          constexpr int NBK = RW / 8;
+          float rk[NBK], rq[NBK], tk[NBK], tq[NBK];
 #pragma unroll
-        for (int r0 = 0; r0 < RW; r0 += 8) {
+          for (int bk = 0; bk < NBK; ++bk) {
+            rk[bk] = 0.f;
+            rq[bk] = 0.f;
+          }
+          for (int j = jl; j < n; j += 4) {
+            const float ck = co[j], cq = co[C + j];
+#pragma unroll
+            for (int bk = 0; bk < NBK; ++bk) {
+              const float uj = ub[j * RPU + tw + TW * (8 * bk + kq)];
+              rk[bk] = fmaf(ck, uj, rk[bk]);
+              rq[bk] = fmaf(cq, uj, rq[bk]);
+            }
+          }
+#pragma unroll
+          for (int bk = 0; bk < NBK; ++bk) {
+            float pk[8], pq[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float4 s4 = sT4[(tw + TW * (8 * bk + e)) * SEG + lane];
+              pk[e] = dot4(s4, kc4);
+              pq[e] = dot4(s4, q4);
+            }
+            tk[bk] = reduce8(pk, lane);
+            tq[bk] = reduce8(pq, lane);
+          }
+#pragma unroll
+          for (int bk = 0; bk < NBK; ++bk) {
+            float r1 = rk[bk], r2 = rq[bk];
+            r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
+            r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
+            r2 += __shfl_xor_sync(0xffffffffu, r2, 1);
+            r2 += __shfl_xor_sync(0xffffffffu, r2, 2);
+            const int Rq = tw + TW * (8 * bk + kq);
+            const float uu = beta * (bf(cur[Rq]) - a * fmaf(gamma, tk[bk], r1));
+            if (jl == 0) {
+              yrow[Rq] = fmaf(a, fmaf(gamma, tq[bk], r2), uu * kq_dot);
+              urow[Rq] = uu;
+            }
+          }
+        }
+#pragma unroll
+        for (int r0 = 0; r0 < RW && flush; r0 += 8) {
           const int Rq = tw + TW * (r0 + kq);
           float rk = 0.f, rq = 0.f;
           for (int j = jl; j < n; j += 4) {
