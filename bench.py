@@ -240,8 +240,9 @@ def decode_leg(wl, dev, K, W, L, bytes_fn, barrier, distinct=16):
 
 
 def e2e_leg(wl, dev, K, W):
-    """Same metric through ReplayCache.decode_step_from_host: pinned host inputs copied in,
-    the step, y copied back, every step, on one stream."""
+    """Same metric through the C ABI's host-buffer call (rs_pipe_decode_step, via
+    ReplayCache.decode_step_from_host): every step its pinned host inputs are copied in and y
+    copied back to pinned host memory, the copies overlapping the neighbouring steps' kernels."""
     import torch
     cache = make_cache(wl, dev)
     host = []
@@ -258,11 +259,13 @@ def e2e_leg(wl, dev, K, W):
     stream = torch.cuda.current_stream(dev)
     for t in range(W):
         cache.decode_step_from_host(host[t % 16], y_host, stream=stream)
+    cache.host_sync(stream)
     torch.cuda.synchronize(dev)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record(stream)
     for t in range(K):
         cache.decode_step_from_host(host[(W + t) % 16], y_host, stream=stream)
+    cache.host_sync(stream)  # the last step's y is in host memory when `e` completes
     e.record(stream)
     torch.cuda.synchronize(dev)
     ms = s.elapsed_time(e)

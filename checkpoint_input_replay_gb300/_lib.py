@@ -35,7 +35,8 @@ RS_DEVERR_TIMEOUT = 3
 
 EXPORTED = ("rs_query_sizes", "rs_create_cache", "rs_destroy_cache", "rs_decode_step", "rs_verify",
             "rs_commit", "rs_flush", "rs_get_device_error", "rs_status_string", "rs_decode_step_noalloc",
-            "rs_selftest_wait_timeout")
+            "rs_selftest_wait_timeout", "rs_pipe_create", "rs_pipe_decode_step", "rs_pipe_sync",
+            "rs_pipe_destroy")
 
 
 class rs_config(ctypes.Structure):
@@ -81,10 +82,15 @@ def load() -> ctypes.CDLL:
         lib.rs_selftest_wait_timeout.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), vp]
         lib.rs_decode_step_noalloc.argtypes = [ctypes.POINTER(rs_config), ctypes.POINTER(rs_buffers),
                                                ctypes.POINTER(rs_inputs), vp, vp]
+        lib.rs_pipe_create.argtypes = [vp, ctypes.POINTER(vp)]
+        lib.rs_pipe_decode_step.argtypes = [vp, ctypes.POINTER(rs_inputs), vp, vp]
+        lib.rs_pipe_sync.argtypes = [vp, vp]
+        lib.rs_pipe_destroy.argtypes = [vp]
+        lib.rs_pipe_destroy.restype = None
         lib.rs_status_string.argtypes = [ctypes.c_int]
         lib.rs_status_string.restype = ctypes.c_char_p
         for name in EXPORTED:
-            if name not in ("rs_destroy_cache", "rs_status_string"):
+            if name not in ("rs_destroy_cache", "rs_status_string", "rs_pipe_destroy"):
                 getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -157,3 +163,23 @@ def rs_selftest_wait_timeout(limit_us: int, stream: int):
     code = ctypes.c_int32(-1)
     st = load().rs_selftest_wait_timeout(ctypes.c_int32(limit_us), ctypes.byref(code), ctypes.c_void_p(stream))
     return st, code.value
+
+
+def rs_pipe_create(handle):
+    """Returns (status, pipe handle) for host-buffer decode steps on this cache."""
+    p = ctypes.c_void_p()
+    st = load().rs_pipe_create(handle, ctypes.byref(p))
+    return st, p
+
+
+def rs_pipe_decode_step(pipe, host_inputs: rs_inputs, host_y_ptr: int, stream: int) -> int:
+    return load().rs_pipe_decode_step(pipe, ctypes.byref(host_inputs), ctypes.c_void_p(host_y_ptr),
+                                      ctypes.c_void_p(stream))
+
+
+def rs_pipe_sync(pipe, stream: int) -> int:
+    return load().rs_pipe_sync(pipe, ctypes.c_void_p(stream))
+
+
+def rs_pipe_destroy(pipe) -> None:
+    load().rs_pipe_destroy(pipe)

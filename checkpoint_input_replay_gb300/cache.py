@@ -61,6 +61,9 @@ class ReplayCache:
                    shape.ring_len, shape.max_draft, read_mode, device)
 
     def close(self) -> None:
+        if getattr(self, "_pipe", None):
+            _lib.rs_pipe_destroy(self._pipe)
+            self._pipe = None
         if getattr(self, "handle", None):
             _lib.rs_destroy_cache(self.handle)
             self.handle = None
@@ -126,7 +129,8 @@ class ReplayCache:
             stream = torch.cuda.current_stream(self.device)
         return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
-    def _inputs(self, inputs: dict, lead: tuple) -> _lib.rs_inputs:
+    def _inputs(self, inputs: dict, lead: tuple, device=None) -> _lib.rs_inputs:
+        device = self.device if device is None else device
         B, H, G, P, N = self.B, self.H, self.G, self.P, self.N
         if self.kind == _lib.RS_MAMBA2:
             spec = {"x": (torch.bfloat16, lead + (H, P)), "dt": (torch.bfloat16, lead + (H,)),
@@ -139,8 +143,8 @@ class ReplayCache:
         ptrs = {}
         for name, (dtype, shape) in spec.items():
             t = inputs[name]
-            if t.dtype != dtype or tuple(t.shape) != shape or not t.is_contiguous() or t.device != self.device:
-                raise ValueError(f"input {name}: want contiguous {dtype} {shape} on {self.device}, "
+            if t.dtype != dtype or tuple(t.shape) != shape or not t.is_contiguous() or t.device != device:
+                raise ValueError(f"input {name}: want contiguous {dtype} {shape} on {device}, "
                                  f"got {t.dtype} {tuple(t.shape)} on {t.device}")
             ptrs[name] = t.data_ptr()
         if self.kind == _lib.RS_MAMBA2:
@@ -189,18 +193,22 @@ class ReplayCache:
 
     # --- end to end from host memory --------------------------------------------------
     def decode_step_from_host(self, host_inputs: dict, host_y: torch.Tensor, stream=None) -> torch.Tensor:
-        """Decode step whose inputs live in (pinned) host memory and whose output
-        is read back to host memory: host->device copies, the step, and the
-        device->host copy of y, all ordered on one stream."""
-        dev = getattr(self, "_staging", None)
-        if dev is None:
-            dev = {k: torch.empty_like(v, device=self.device) for k, v in host_inputs.items()}
-            dev["_y"] = torch.empty(host_y.shape, dtype=torch.float32, device=self.device)
-            self._staging = dev
-        s = torch.cuda.current_stream(self.device) if stream is None else stream
-        with torch.cuda.stream(s):
-            for k, v in host_inputs.items():
-                dev[k].copy_(v, non_blocking=True)
-            self.decode_step({k: dev[k] for k in host_inputs}, dev["_y"], stream=s)
-            host_y.copy_(dev["_y"], non_blocking=True)
+        """Decode step whose inputs live in (pinned) host memory and whose output is
+        read back to host memory, through rs_pipe_decode_step: the input copies overlap
+        the previous step's kernel and the y copy the next step's.  host_y (f32
+        [B][H][P], pinned) is complete after host_sync() and a synchronise of the stream;
+        the host inputs must stay unchanged until then."""
+        if host_y.dtype != torch.float32 or tuple(host_y.shape) != (self.B, self.H, self.P) or \
+                host_y.device.type != "cpu" or not host_y.is_contiguous():
+            raise ValueError("host_y must be a contiguous f32 [B][H][P] host tensor")
+        if getattr(self, "_pipe", None) is None:
+            st, self._pipe = _lib.rs_pipe_create(self.handle)
+            check(st, "rs_pipe_create")
+        check(_lib.rs_pipe_decode_step(self._pipe, self._inputs(host_inputs, (self.B,), torch.device("cpu")),
+                                       host_y.data_ptr(), self._stream(stream)), "rs_pipe_decode_step")
         return host_y
+
+    def host_sync(self, stream=None) -> None:
+        """Make the stream wait for every host copy issued by decode_step_from_host."""
+        if getattr(self, "_pipe", None) is not None:
+            check(_lib.rs_pipe_sync(self._pipe, self._stream(stream)), "rs_pipe_sync")

@@ -336,6 +336,146 @@ rs_status rs_decode_step(rs_cache* h, const rs_inputs* in, float* y, rs_stream s
   return from_cuda(rs::launch_decode(h->dev, token_in(in), y, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// ---- host-buffer decode steps ----------------------------------------------
+
+struct rs_pipe {
+  rs_cache* cache;
+  cudaStream_t h2d, d2h;                              // input copies, output copies
+  cudaEvent_t in_ready[2], step_done[2], y_out[2];  // per slot
+  unsigned char* dev_in[2];                          // one step's inputs, five 256-byte-aligned sections
+  float* dev_y[2];
+  size_t off[5], bytes[5], in_bytes, y_bytes;
+  int64_t steps;
+};
+
+namespace {
+
+// the five input arrays of one decode step, in rs_inputs order for the kind
+void pipe_sections(const rs_config& c, size_t bytes[5]) {
+  const size_t B = c.batch, H = c.n_heads, G = c.n_groups, P = c.d_head, N = c.d_state;
+  if (c.kind == RS_MAMBA2) {
+    bytes[0] = B * H * P * 2;  // x
+    bytes[1] = B * H * 2;      // dt
+    bytes[2] = H * 4;          // A
+    bytes[3] = B * G * N * 2;  // Bm
+    bytes[4] = B * G * N * 2;  // Cm
+  } else {
+    bytes[0] = B * G * N * 2;  // q
+    bytes[1] = B * G * N * 2;  // k
+    bytes[2] = B * H * P * 2;  // v
+    bytes[3] = B * H * 4;      // g
+    bytes[4] = B * H * 4;      // beta
+  }
+}
+
+const void* pipe_src(const rs_config& c, const rs_inputs* in, int i) {
+  if (c.kind == RS_MAMBA2) {
+    const void* p[5] = {in->x, in->dt, in->A, in->Bm, in->Cm};
+    return p[i];
+  }
+  const void* p[5] = {in->q, in->k, in->v, in->g, in->beta};
+  return p[i];
+}
+
+void pipe_free(rs_pipe* p) {
+  for (int k = 0; k < 2; ++k) {
+    if (p->in_ready[k]) cudaEventDestroy(p->in_ready[k]);
+    if (p->step_done[k]) cudaEventDestroy(p->step_done[k]);
+    if (p->y_out[k]) cudaEventDestroy(p->y_out[k]);
+    if (p->dev_in[k]) cudaFree(p->dev_in[k]);
+    if (p->dev_y[k]) cudaFree(p->dev_y[k]);
+  }
+  if (p->h2d) cudaStreamDestroy(p->h2d);
+  if (p->d2h) cudaStreamDestroy(p->d2h);
+  delete p;
+}
+
+}  // namespace
+
+rs_status rs_pipe_create(rs_cache* cache, rs_pipe** out) {
+  if (!cache || !out) return RS_ERR_NULL;
+  *out = nullptr;
+  rs_pipe* p = new (std::nothrow) rs_pipe{};
+  if (!p) return RS_ERR_CUDA;
+  p->cache = cache;
+  pipe_sections(cache->cfg, p->bytes);
+  size_t o = 0;
+  for (int i = 0; i < 5; ++i) {
+    p->off[i] = o;
+    o = align256(o + p->bytes[i]);
+  }
+  p->in_bytes = o;
+  p->y_bytes = static_cast<size_t>(cache->cfg.batch) * cache->cfg.n_heads * cache->cfg.d_head * 4;
+  bool ok = cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking) == cudaSuccess;
+  for (int k = 0; k < 2 && ok; ++k) {
+    ok = cudaEventCreateWithFlags(&p->in_ready[k], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&p->step_done[k], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&p->y_out[k], cudaEventDisableTiming) == cudaSuccess &&
+         cudaMalloc(reinterpret_cast<void**>(&p->dev_in[k]), p->in_bytes) == cudaSuccess &&
+         cudaMalloc(reinterpret_cast<void**>(&p->dev_y[k]), p->y_bytes) == cudaSuccess;
+  }
+  if (!ok) {
+    pipe_free(p);
+    return RS_ERR_CUDA;
+  }
+  *out = p;
+  return RS_OK;
+}
+
+rs_status rs_pipe_decode_step(rs_pipe* p, const rs_inputs* host_in, float* host_y, rs_stream stream) {
+  if (!p || !host_in || !host_y) return RS_ERR_NULL;
+  const rs_config& c = p->cache->cfg;
+  for (int i = 0; i < 5; ++i)
+    if (!pipe_src(c, host_in, i)) return RS_ERR_NULL;
+  if (p->cache->pending) return RS_ERR_STATE;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int k = static_cast<int>(p->steps & 1);
+  cudaError_t e = cudaSuccess;
+  // inputs: into slot k once the kernel of two steps ago has read it
+  if (p->steps >= 2) e = cudaStreamWaitEvent(p->h2d, p->step_done[k], 0);
+  for (int i = 0; i < 5 && e == cudaSuccess; ++i)
+    e = cudaMemcpyAsync(p->dev_in[k] + p->off[i], pipe_src(c, host_in, i), p->bytes[i], cudaMemcpyHostToDevice,
+                        p->h2d);
+  if (e == cudaSuccess) e = cudaEventRecord(p->in_ready[k], p->h2d);
+  // the step on the caller's stream, once its inputs are in and y's slot has been read back
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, p->in_ready[k], 0);
+  if (e == cudaSuccess && p->steps >= 2) e = cudaStreamWaitEvent(s, p->y_out[k], 0);
+  if (e != cudaSuccess) return RS_ERR_CUDA;
+  rs_inputs din{};
+  const void* dp[5];
+  for (int i = 0; i < 5; ++i) dp[i] = p->dev_in[k] + p->off[i];
+  if (c.kind == RS_MAMBA2) {
+    din.x = dp[0]; din.dt = dp[1]; din.A = static_cast<const float*>(dp[2]); din.Bm = dp[3]; din.Cm = dp[4];
+  } else {
+    din.q = dp[0]; din.k = dp[1]; din.v = dp[2]; din.g = static_cast<const float*>(dp[3]);
+    din.beta = static_cast<const float*>(dp[4]);
+  }
+  const rs_status st = rs_decode_step(p->cache, &din, p->dev_y[k], stream);
+  if (st != RS_OK) return st;
+  // y back to the host on the output stream
+  e = cudaEventRecord(p->step_done[k], s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(p->d2h, p->step_done[k], 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(host_y, p->dev_y[k], p->y_bytes, cudaMemcpyDeviceToHost, p->d2h);
+  if (e == cudaSuccess) e = cudaEventRecord(p->y_out[k], p->d2h);
+  if (e != cudaSuccess) return RS_ERR_CUDA;
+  ++p->steps;
+  return RS_OK;
+}
+
+rs_status rs_pipe_sync(rs_pipe* p, rs_stream stream) {
+  if (!p) return RS_ERR_NULL;
+  if (p->steps == 0) return RS_OK;
+  return from_cuda(cudaStreamWaitEvent(reinterpret_cast<cudaStream_t>(stream), p->y_out[(p->steps - 1) & 1], 0));
+}
+
+void rs_pipe_destroy(rs_pipe* p) {
+  if (!p) return;
+  cudaStreamSynchronize(p->h2d);
+  cudaStreamSynchronize(p->d2h);
+  pipe_free(p);
+}
+
 rs_status rs_verify(rs_cache* h, int32_t T, const rs_inputs* in, float* y, rs_stream stream) {
   if (!h || !y) return RS_ERR_NULL;
   if (T < 1 || T > h->cfg.max_draft) return RS_ERR_RANGE;

@@ -231,6 +231,31 @@ rs_status rs_get_device_error(rs_cache *cache, rs_stream stream, int32_t *code);
 rs_status rs_decode_step_noalloc(const rs_config *cfg, const rs_buffers *bufs, const rs_inputs *in, float *y,
                                  rs_stream stream);
 
+/*
+ * Host-buffer decode steps.  A pipe serves one cache; it owns two device
+ * copies of one step's inputs and of y (allocated by rs_pipe_create, freed
+ * by rs_pipe_destroy -- the one exception to caller-owned device memory) and
+ * two non-blocking streams for the copies.  rs_pipe_decode_step copies the
+ * step's inputs from host memory (rs_inputs with host pointers, layouts as
+ * for rs_decode_step; pinned memory for overlap) into one slot, runs
+ * rs_decode_step on `stream`, and copies y f32 [B][H][P] back to host_y.
+ * Slots alternate, so step t's input copy overlaps step t-1's kernel and step
+ * t's y copy overlaps step t+1's kernel; events order every reuse of a slot.
+ * The paper has no counterpart of this call.
+ *   - Host inputs must stay unchanged, and host_y must not be read, until the
+ *     caller has called rs_pipe_sync(pipe, s) and synchronised s.
+ *   - Same errors as rs_decode_step (RS_ERR_NULL for a missing host array);
+ *     RS_ERR_CUDA for a failed copy or event call.
+ *   - Calls on one pipe must come from one host thread in order.
+ */
+typedef struct rs_pipe rs_pipe;
+rs_status rs_pipe_create(rs_cache *cache, rs_pipe **out);
+rs_status rs_pipe_decode_step(rs_pipe *pipe, const rs_inputs *host_in, float *host_y, rs_stream stream);
+/* Make `stream` wait for every copy the pipe has issued (then synchronise it). */
+rs_status rs_pipe_sync(rs_pipe *pipe, rs_stream stream);
+/* Waits for the pipe's copies, then frees its device memory, streams and events. */
+void rs_pipe_destroy(rs_pipe *pipe);
+
 /* Self-test of the bounded wait every kernel uses on its mbarriers: one GPU
  * thread waits on an mbarrier that nothing completes, giving up after
  * limit_us microseconds (1..1000000), with the same primitive and the same
