@@ -44,6 +44,21 @@ __host__ __device__ __forceinline__ uint32_t idesc_tf32(int M, int Nmma) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor of kind::f16 with bf16 A and B, f32 accumulator,
+// both operands K-major (same field layout as idesc_tf32, format code 1 = bf16).
+__host__ __device__ __forceinline__ uint32_t idesc_bf16(int M, int Nmma) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(Nmma >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Offset (elements) of 16-bit element (r, k) of a K-major operand in the
+// canonical layout without swizzle: core matrices of 8 rows x 8 elements (16
+// bytes a row), consecutive along K (LBO = 128 bytes), 8-row groups K/8 core
+// matrices apart (SBO = K * 16 bytes).
+__host__ __device__ __forceinline__ int canon_offset16(int r, int k, int K) {
+  return ((r >> 3) * (K >> 3) + (k >> 3)) * 64 + (r & 7) * 8 + (k & 7);
+}
+
 // One warp: allocate `ncols` (a power of two >= 32) tensor-memory columns; the
 // address is written to *slot (shared memory).
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
@@ -79,6 +94,18 @@ __device__ __forceinline__ void mma_tf32_ta(uint32_t tmem_d, uint32_t tmem_a, ui
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+      : "memory");
+}
+
+// D (tensor memory) (+)= A (tensor memory, two bf16 per 32-bit column along K)
+// x B (shared memory descriptor), kind::f16 with bf16 operands, M = 128, K = 16.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                            bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
       "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
       : "memory");
 }
@@ -126,6 +153,23 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t v[32]) 
       "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
       "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
+}
+
+// Store 16 consecutive 32-bit columns of a 32-lane quarter of tensor memory.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t v[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+// Two floats to bf16 (round to nearest even), packed with `lo` in bits 0-15.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }

@@ -18,15 +18,18 @@
 //    consecutive state rows of one group: two heads of d_head 64, or one head
 //    of d_head 128, so one tcgen05 MMA with M = 128 covers it.  The dense part
 //    S_ckpt [128][128] x [K_draft | Q] [128][16] runs on the tensor cores in
-//    kind::tf32 with FP32 accumulation in tensor memory.  The FP32 state is
-//    split exactly: kind::tf32 reads an FP32 operand with its low 13 mantissa
-//    bits ignored, so one pass takes the raw state and a second pass takes
-//    lo = S - trunc(S).  Both A operands are read from tensor memory (an MMA
-//    with A in shared memory costs about 1.7x one with A in tensor memory at
-//    these shapes): the split warps copy each 32-column block of the state
-//    rows, raw and lo, into a ring of tensor-memory chunks that the MMA thread
-//    consumes block by block.  The drafts' queries and keys are bf16, which
-//    TF32 holds exactly.  Roles (15 warps, one persistent CTA per SM):
+//    kind::f16 with bf16 operands and FP32 accumulation in tensor memory.  The
+//    FP32 state is split exactly into three bf16 parts, hi = bf16(S),
+//    mid = bf16(S - hi), lo = bf16(S - hi - mid) (each difference is exact,
+//    and 24 significand bits fit in three round-to-nearest pieces of 8), and
+//    the three parts accumulate into one result: 24 MMAs of K = 16 per unit,
+//    where the earlier kind::tf32 form (raw state + lo = S - trunc(S), K = 8)
+//    took 32.  The A operands are read from tensor memory (an MMA with A in
+//    shared memory costs about 1.7x one with A in tensor memory at these
+//    shapes): the split warps write each 32-column block of the state rows,
+//    as hi | mid | lo, into a ring of tensor-memory chunks that the MMA thread
+//    consumes block by block.  The drafts' queries and keys are bf16 already.
+//    Roles (15 warps, one persistent CTA per SM):
 //     * producer (1 thread): per unit, the state tile by four 2D TMA loads
 //       into one of two tile stages, and the unit's committed records and
 //       coefficient tables by bulk copies into one of up to three record
@@ -35,11 +38,11 @@
 //     * prologue warp: once per group, the MMA B operand; per unit a
 //       descriptor;
 //     * eight split warps (two per tensor-memory lane quarter, one for the
-//       even and one for the odd 32-column blocks): per block, the raw rows
-//       and lo = S - trunc(S) into a tensor-memory chunk (row r to lane r);
-//       the shared-memory tile is released once it has been read;
-//     * MMA thread: per chunk, four MMAs on the raw part and four on lo, into
-//       one of two accumulators;
+//       even and one for the odd 32-column blocks): per block, the three bf16
+//       parts of the rows into a tensor-memory chunk (row r to lane r); the
+//       shared-memory tile is released once it has been read;
+//     * MMA thread: per chunk, two MMAs on each of the three parts, into one
+//       of two accumulators;
 //     * four epilogue warps: accumulator rows back from tensor memory, the
 //       buffered-record terms, the triangular solve (Gated DeltaNet), outputs
 //       and the drafts' x (Mamba-2) or u (Gated DeltaNet) records.
@@ -68,8 +71,8 @@ constexpr int kWarpPro = 12, kWarpProd = 13, kWarpMma = 14;
 constexpr int kThreadsV = 15 * 32;
 constexpr int kPrepThreads = 128;
 // tensor memory: a ring of six A-operand chunks, each the 32 K-columns of one
-// 128-byte block of the state rows as [raw (32 columns) | lo (32 columns)],
-// then two accumulators
+// 128-byte block of the state rows as three bf16 parts [hi | mid | lo], 16
+// columns each (two bf16 a column), then two accumulators
 constexpr int kSlots = 6;
 constexpr uint32_t kSlotCols = 64;
 constexpr uint32_t kTmemCols = 512;
@@ -335,7 +338,7 @@ __host__ __device__ __forceinline__ VL vlayout(int kind, int C, int hpg, int P, 
   l.rec_size = al128(l.rec_meta + 32);                       // 32 bytes of descriptor
   o += NR * l.rec_size;
   int g = 0;
-  l.g_B = g;      g += kNmma * N * 4;
+  l.g_B = g;      g += kNmma * N * 2;
   l.g_key = g;    g += kT * N * 2;  // draft keys
   l.g_q = g;      g += kT * N * 2;  // draft queries
   l.g_dx = g;     g += al16(kT * hpg * P * 2);
@@ -558,13 +561,14 @@ __global__ void __launch_bounds__(kThreadsV, 1)
       const bool ok = sseq[3 * k + 2] != 0;
       unsigned char* gb = gb_at(gi & 1);
       if (first && ok) {
-        // the MMA B operand, canonical K-major: rows = [K_draft | Q] (GDN) or [Q] (Mamba-2)
+        // the MMA B operand in bf16, canonical K-major: rows = [K_draft | Q] (GDN) or [Q]
+        // (Mamba-2), zero-padded to kNmma rows; one 16-byte core-matrix row per store
         const uint16_t* kb = reinterpret_cast<const uint16_t*>(gb + LY.g_key);
         const uint16_t* qb = reinterpret_cast<const uint16_t*>(gb + LY.g_q);
-        float* Bs = reinterpret_cast<float*>(gb + LY.g_B);
-        for (int it = 0; it < kNmma * N / 4 / 32; ++it) {
-          const int rho = (it >> 3) * 8 + (lane & 7);
-          const int c = (it & 7) * 4 + (lane >> 3);
+        uint16_t* Bs = reinterpret_cast<uint16_t*>(gb + LY.g_B);
+        for (int it = 0; it < kNmma * N / 8 / 32; ++it) {
+          const int rho = 2 * it + (lane >> 4);  // B row
+          const int c = lane & 15;               // 8-element block along K
           const uint16_t* src = nullptr;
           if (KIND == 0) {
             if (rho < T) src = qb + rho * N;
@@ -572,8 +576,8 @@ __global__ void __launch_bounds__(kThreadsV, 1)
             if (rho < T) src = kb + rho * N;
             else if (rho < 2 * T) src = qb + (rho - T) * N;
           }
-          const float4 v = src ? bf4(reinterpret_cast<const uint2*>(src)[c]) : make_float4(0.f, 0.f, 0.f, 0.f);
-          *reinterpret_cast<float4*>(Bs + canon_offset(rho, 4 * c, N)) = v;
+          const uint4 v = src ? reinterpret_cast<const uint4*>(src)[c] : make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(Bs + canon_offset16(rho, 8 * c, N)) = v;
         }
       }
       if (lane == 0) {
@@ -588,7 +592,7 @@ __global__ void __launch_bounds__(kThreadsV, 1)
   } else if (warp == kWarpMma) {
     // ================================ MMA thread ================================
     if (lane == 0) {
-      const uint32_t idesc = idesc_tf32(kRows, kNmma);
+      const uint32_t idesc = idesc_bf16(kRows, kNmma);
       int issued = 0;
       for (int i = 0; i < nunits; ++i) {
         if (smisc[0]) break;
@@ -611,11 +615,11 @@ __global__ void __launch_bounds__(kThreadsV, 1)
           }
           tc_fence_after();
           const uint32_t a0 = tmem + slot * kSlotCols;
-          for (int kk = 0; kk < 4; ++kk)  // raw part
-            mma_tf32_ta(dacc, a0 + kk * 8, umma_desc(bsm + (4 * kb + kk) * 256, 128, (N / 4) * 128), idesc,
-                        kb > 0 || kk > 0);
-          for (int kk = 0; kk < 4; ++kk)  // lo part
-            mma_tf32_ta(dacc, a0 + 32 + kk * 8, umma_desc(bsm + (4 * kb + kk) * 256, 128, (N / 4) * 128), idesc, true);
+          // the three bf16 parts (hi, mid, lo) of the chunk's 32 K-columns, K = 16 per MMA
+          for (int part = 0; part < 3; ++part)
+            for (int kk = 0; kk < 2; ++kk)
+              mma_bf16_ta(dacc, a0 + part * 16 + kk * 8, umma_desc(bsm + (2 * kb + kk) * 256, 128, (N / 8) * 128),
+                          idesc, kb > 0 || part > 0 || kk > 0);
           mma_commit(chunk_free + slot);
           issued = i + 1;
         }
@@ -650,20 +654,28 @@ __global__ void __launch_bounds__(kThreadsV, 1)
           okc = false;
           break;
         }
-        uint32_t hi[32], lo[32];
+        // exact split x = hi + mid + lo into three bf16 (24 significand bits in three
+        // round-to-nearest pieces of 8; both differences are exact), two K-columns a word
+        uint32_t hm[32], lo[16];
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
           const float4 x = *reinterpret_cast<const float4*>(tl + kb * (kTileBytes / 4) + ((cc ^ (r & 7)) << 4));
           const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            hi[4 * cc + e] = __float_as_uint(xs[e]);
-            lo[4 * cc + e] = __float_as_uint(xs[e] - __uint_as_float(__float_as_uint(xs[e]) & 0xFFFFE000u));
+          for (int e = 0; e < 4; e += 2) {
+            const float a = xs[e], b = xs[e + 1];
+            const uint32_t h = pack_bf16x2(a, b);
+            const float ra = a - __uint_as_float(h << 16), rb = b - __uint_as_float(h & 0xFFFF0000u);
+            const uint32_t m = pack_bf16x2(ra, rb);
+            const float sa = ra - __uint_as_float(m << 16), sb = rb - __uint_as_float(m & 0xFFFF0000u);
+            hm[2 * cc + e / 2] = h;
+            hm[16 + 2 * cc + e / 2] = m;
+            lo[2 * cc + e / 2] = pack_bf16x2(sa, sb);
           }
         }
         const uint32_t ta = tmem + slot * kSlotCols + (static_cast<uint32_t>(quarter * 32) << 16);
-        tmem_st32(ta, hi);
-        tmem_st32(ta + 32, lo);
+        tmem_st32(ta, hm);
+        tmem_st16(ta + 32, lo);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
