@@ -103,7 +103,7 @@ constexpr int kPrepWarps = kPrepThreads / 32;
 constexpr int kHB = 4;  // heads per warp per batch
 
 template <int KIND>
-__global__ void __launch_bounds__(kPrepThreads, 6) verify_prep_kernel(const LayerDev d, const TokenIn in, const int T) {
+__global__ void __launch_bounds__(kPrepThreads, 8) verify_prep_kernel(const LayerDev d, const TokenIn in, const int T) {
   const int H = d.H, G = d.G, C = d.C, L = d.L, Cp = d.Cp;
   const int hpg = H / G, HS = head_stride(KIND, C);
   const int bg = blockIdx.x, b = bg / G, g = bg - b * G;
