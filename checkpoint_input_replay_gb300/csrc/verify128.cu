@@ -108,6 +108,9 @@ __global__ void __launch_bounds__(kPrepThreads, 8) verify_prep_kernel(const Laye
   const int hpg = H / G, HS = head_stride(KIND, C);
   const int bg = blockIdx.x, b = bg / G, g = bg - b * G;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  // the main kernel may be scheduled as SMs free up: it waits for this grid only
+  // before it reads the coefficient tables (programmatic dependent launch)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ uint2 skey[kMaxRec][N / 4];  // keys of records 0..n+T-1 (committed, then drafts)
   __shared__ uint2 sq[kT][N / 4];         // draft queries
   __shared__ float sdq[kMaxRec][kT];      // k_j . q_tau
@@ -520,6 +523,11 @@ __global__ void __launch_bounds__(kThreadsV, 1)
           if (seg1) bulk_g2s(dst, src + (base + head) * P * esz, seg1 * P * esz, bar);
           if (seg2) bulk_g2s(dst + static_cast<size_t>(seg1) * P * esz, src + base * P * esz, seg2 * P * esz, bar);
         }
+        // the tables come from the prep kernel, which may still be running
+        if (i == 0) {
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // then read by the bulk copies
+        }
         bulk_g2s(rec + LY.rec_tab, d.vtab + bh0 * HS, HPU * HS * 4, bar);
         if (first) {
           for (int tau = 0; tau < T; ++tau) {
@@ -835,8 +843,19 @@ cudaError_t launch_v128(const LayerDev& d, const CUtensorMap& tmap, const TokenI
   auto kernel = verify128_kernel<KIND, P>;
   e = set_smem_limit(reinterpret_cast<const void*>(kernel), LY.total);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kThreadsV, LY.total, s>>>(tmap, d, in, T, y, per, NR);
-  return cudaGetLastError();
+  // launched as a programmatic dependent of the prep kernel: its setup and first
+  // tile loads overlap the prep kernel's last wave (see griddepcontrol.wait)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreadsV);
+  cfg.dynamicSmemBytes = LY.total;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tmap, d, in, T, y, per, NR);
 }
 
 }  // namespace
