@@ -165,6 +165,51 @@ def upload(inp: dict, dev) -> dict:
     return out
 
 
+class Shard:
+    """Sequences [b0, b1) of a workload whose batch is the whole job's: rank r of N
+    takes the r-th slice (the generator is a pure function of the sequence index,
+    so a slice equals the same rows of the whole job's inputs)."""
+
+    def __init__(self, wl, b0: int, b1: int):
+        self.wl, self.b0, self.b1 = wl, b0, b1
+        self.shape = wl.shape.with_batch(b1 - b0)
+        self.s0_std = wl.s0_std
+
+    def _range(self, lo, hi):
+        hi = self.shape.batch if hi is None else hi
+        return self.b0 + lo, self.b0 + hi
+
+    def step(self, t, lo=0, hi=None):
+        return self.wl.step(t, *self._range(lo, hi))
+
+    def S0(self, lo=0, hi=None):
+        return self.wl.S0(*self._range(lo, hi))
+
+    def draft(self, s, T, lo=0, hi=None):
+        return self.wl.draft(s, T, *self._range(lo, hi))
+
+    def accepted(self, s, T, lo=0, hi=None):
+        return self.wl.accepted(s, T, *self._range(lo, hi))
+
+    def __getattr__(self, name):  # A(), c() and the like: per layer, not per sequence
+        if name in ("wl", "b0", "b1"):
+            raise AttributeError(name)
+        return getattr(self.wl, name)
+
+
+def shard_of(wl, rank: int, world: int) -> Shard:
+    """This rank's equal slice of the whole job's batch."""
+    per = wl.shape.batch // world
+    if per * world != wl.shape.batch:
+        raise ValueError("the job's batch must be a multiple of the number of ranks")
+    return Shard(wl, rank * per, (rank + 1) * per)
+
+
+def job_value(world: int, batch_per_rank: int, steps: int, elapsed_ms_max: float) -> float:
+    """Whole-job sequence-steps per second: every rank's units over the slowest rank's time."""
+    return world * batch_per_rank * steps / (elapsed_ms_max / 1e3)
+
+
 def make_cache(wl, dev, read_mode=None, seed=0):
     """Cache with a seeded synthetic initial state N(0, s0_std) drawn on the device."""
     import torch
@@ -206,11 +251,11 @@ def run_decode_loop(cache, steps_inputs, K, W, dev, barrier):
     return start.elapsed_time(end), [a.elapsed_time(b) for a, b in ev]
 
 
-def decode_leg(wl, dev, K, W, L, bytes_fn, barrier, distinct=16):
+def decode_leg(wl, dev, K, W, L, bytes_fn, barrier, distinct=16, seed=0):
     """Decode steps of one layer; warm-up W rounded up so timing starts at a window boundary."""
     import torch
     W = int(math.ceil(W / L) * L)
-    cache = make_cache(wl, dev)
+    cache = make_cache(wl, dev, seed=seed)
     A = torch.from_numpy(wl.A()).to(dev) if hasattr(wl, "A") else None
     steps = []
     for t in range(distinct):
@@ -473,11 +518,12 @@ def main(argv=None):
         barrier = lambda: None
 
     K, W = args.steps, args.warmup
-    wl1 = configs.config1(batch=args.batch)
+    # each rank decodes its own slice of a world x B job (weak scaling, no exchange)
+    wl1 = shard_of(configs.config1(batch=world * args.batch), rank, world)
     with ClockSampler(local) as clk:
-        m2 = decode_leg(wl1, dev, K, W, 16, m2_bytes, barrier)
+        m2 = decode_leg(wl1, dev, K, W, 16, m2_bytes, barrier, seed=rank)
     elapsed = max_over_ranks(m2["elapsed_ms"], world, dev)
-    value = world * wl1.shape.batch * K / (elapsed / 1e3)
+    value = job_value(world, wl1.shape.batch, K, elapsed)
 
     hbm, peak_kind = peaks()
     achieved = m2["bytes_total"] / (m2["launch_ms_total"] * 1e6)
@@ -496,7 +542,7 @@ def main(argv=None):
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": "mamba2 decode, 1 layer: B=256 nheads=128 headdim=64 dstate=128 ngroups=8, "
                                    "FP32 checkpoint, bf16 x/dt/B/C, L=16 (15 non-flush + 1 flush per window)",
-                       "batch_per_gpu": wl1.shape.batch, "ring_len": 16,
+                       "batch_per_gpu": wl1.shape.batch, "global_batch": world * wl1.shape.batch, "ring_len": 16,
                        "l2": "no flush: the %d MiB state per step exceeds the 129 MB L2" % (wl1.shape.batch * 4),
                        "inputs": "16 distinct seeded input steps resident in HBM, cycled; initial state N(0,0.1)"},
             "roofline": roofline, "gpu_launches": m2["launches"], "clocks": clk.summary(),
