@@ -93,6 +93,24 @@ def test_gdn_d128_long_window_split_heads():
     assert _run_decode(pair, 45) == 2
 
 
+@pytest.mark.parametrize("kind,P", [(MAMBA2, 64), (MAMBA2, 128), (GDN, 64), (GDN, 128)])
+def test_d128_one_head_per_group(kind, P):
+    """d_state 128 with as many groups as heads: one unit per group (two for a GDN
+    head of d_head 128), so the decode kernel runs with its fewest stages (units per
+    group + 1) and a group buffer restaged every one or two units."""
+    shape = LayerShape(kind, batch=3, n_heads=5, n_groups=5, d_head=P, d_state=128, ring_len=4)
+    wl = configs.workload(shape, seed=17, s0_std=0.1 if kind == MAMBA2 else 0.05)
+    assert _run_decode(Pair(wl), 13) == 3
+
+
+@pytest.mark.parametrize("kind,P", [(MAMBA2, 64), (GDN, 128)])
+def test_d128_single_sequence_single_head(kind, P):
+    """The smallest grid: one sequence, one head (one or two units in all)."""
+    shape = LayerShape(kind, batch=1, n_heads=1, n_groups=1, d_head=P, d_state=128, ring_len=2)
+    wl = configs.workload(shape, seed=18, s0_std=0.1 if kind == MAMBA2 else 0.05)
+    assert _run_decode(Pair(wl), 7) == 3
+
+
 @pytest.mark.parametrize("N,P", [(32, 32), (128, 128), (16, 128), (128, 16)])
 def test_shapes_sweep(N, P):
     for kind in (MAMBA2, GDN):
