@@ -87,6 +87,13 @@ __device__ __forceinline__ float4 axpy4x2(float a, const float4 x, const float4 
   return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
+// a . b with two packed FMAs (pairs (x, y) and (z, w)) and one add
+__device__ __forceinline__ float dot4p(const float4 a, const float4 b) {
+  float2 t = fma2(make_float2(a.x, a.y), make_float2(b.x, b.y), make_float2(0.f, 0.f));
+  t = fma2(make_float2(a.z, a.w), make_float2(b.z, b.w), t);
+  return t.x + t.y;
+}
+
 __device__ __forceinline__ float4 scale4(float a, const float4 x) {
   return make_float4(a * x.x, a * x.y, a * x.z, a * x.w);
 }

@@ -694,13 +694,13 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
               const uint32_t wd = reinterpret_cast<const uint32_t*>(cb + R * N)[lane];
               const float2 lo = e4m3x2_to_f32x2(static_cast<uint16_t>(wd & 0xFFFFu));
               const float2 hi = e4m3x2_to_f32x2(static_cast<uint16_t>(wd >> 16));
-              part[hu][e] = dot4(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
+              part[hu][e] = dot4p(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
             } else {
               const uint32_t wd = reinterpret_cast<const uint16_t*>(cb + R * (N / 2))[lane];
               const float2 lo = e2m1x2_to_f32x2(wd & 0xFFu);
               const float2 hi = e2m1x2_to_f32x2(wd >> 8);
               const float bs = e4m3_to_f32(gb[LY.gb_rs + ((hh0 + hu) * P + R) * (N / 16) + (lane >> 2)]);
-              part[hu][e] = bs * dot4(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
+              part[hu][e] = bs * dot4p(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
             }
           }
         }
@@ -753,13 +753,13 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
                 const uint32_t wd = reinterpret_cast<const uint32_t*>(cb + R * N)[lane];
                 const float2 lo = e4m3x2_to_f32x2(static_cast<uint16_t>(wd & 0xFFFFu));
                 const float2 hi = e4m3x2_to_f32x2(static_cast<uint16_t>(wd >> 16));
-                part[e] = dot4(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
+                part[e] = dot4p(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
               } else {
                 const uint32_t wd = reinterpret_cast<const uint16_t*>(cb + R * (N / 2))[lane];
                 const float2 lo = e2m1x2_to_f32x2(wd & 0xFFu);
                 const float2 hi = e2m1x2_to_f32x2(wd >> 8);
                 const float bs = e4m3_to_f32(gb[LY.gb_rs + (hh * P + R) * (N / 16) + (lane >> 2)]);
-                part[e] = bs * dot4(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
+                part[e] = bs * dot4p(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
               }
             }
             row_scale = READ == READ_FP8 ? reinterpret_cast<const float*>(gb + LY.gb_rs)[hh * P + Rq]
@@ -905,8 +905,8 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const float4 s4 = sT4[(tw + TW * (8 * bk + e)) * SEG + lane];
-              pk[e] = dot4(s4, kc4);
-              pq[e] = dot4(s4, q4);
+              pk[e] = dot4p(s4, kc4);
+              pq[e] = dot4p(s4, q4);
             }
             tk[bk] = reduce8(pk, lane);
             tq[bk] = reduce8(pq, lane);
@@ -944,8 +944,8 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             s4[e] = sT4[(tw + TW * (r0 + e)) * SEG + lane];
-            pk[e] = dot4(s4[e], kc4);
-            pq[e] = dot4(s4[e], q4);
+            pk[e] = dot4p(s4[e], kc4);
+            pq[e] = dot4p(s4[e], q4);
           }
           const float tk = reduce8(pk, lane);
           const float tq = reduce8(pq, lane);
