@@ -111,6 +111,19 @@ def test_d128_single_sequence_single_head(kind, P):
     assert _run_decode(Pair(wl), 7) == 3
 
 
+@pytest.mark.slow
+def test_d128_grid_doubling_many_sequences():
+    """10000 single-head sequences: a CTA's share would cover more sequences than its
+    per-CTA cursor table holds, so the launcher doubles the grid.  Sampled sequences
+    at the edges of the CTA ranges are checked against the oracle; every cursor is
+    checked against the plain ring rule."""
+    shape = LayerShape(MAMBA2, batch=10000, n_heads=1, n_groups=1, d_head=64, d_state=128, ring_len=3)
+    pair = Pair(configs.Mamba2Workload(shape, seed=19, s0_std=0.1), seqs=[0, 1, 32, 33, 5000, 9998, 9999])
+    assert _run_decode(pair, 7) == 2
+    cur = pair.cache.cursor.cpu().numpy()[:10000]
+    assert (cur[:, 0] == 0).all() and (cur[:, 1] == 1).all()  # 7 steps at L = 3: flushed twice (head 6 mod 3)
+
+
 @pytest.mark.parametrize("N,P", [(32, 32), (128, 128), (16, 128), (128, 16)])
 def test_shapes_sweep(N, P):
     for kind in (MAMBA2, GDN):

@@ -122,3 +122,23 @@ def test_tensor_core_verify_many_units_per_cta(kind):
         wl = configs.GdnWorkload(shape, seed=42, s0_std=0.05)
         seqs = [0, 19, 39]
     _spec_session(Pair(wl, seqs=seqs), 20, 4)
+
+
+@pytest.mark.slow
+def test_tensor_core_verify_grid_doubling_many_sequences():
+    """10000 single-head sequences of d_head 128 through the tensor-core verify and the
+    balanced commit: more sequences per CTA than the per-CTA cursor table holds, so the
+    launchers enlarge the grid.  Sampled sequences against the oracle."""
+    shape = LayerShape(MAMBA2, batch=10000, n_heads=1, n_groups=1, d_head=128, d_state=128, ring_len=4,
+                       max_draft=2)
+    pair = Pair(configs.Mamba2Workload(shape, seed=29, s0_std=0.1), seqs=[0, 1, 31, 32, 5000, 9999])
+    for t in range(2):
+        y, ref = pair.decode(t)
+        assert_close(y, ref, f"decode {t}")
+    for s in range(3):
+        y, ref = pair.verify(s, 2)
+        assert_close(y, ref, f"verify {s}")
+        pair.commit(s, 2)
+        pair.check_cursor(f"commit {s}")
+    pair.check_ckpt("checkpoint")
+    assert pair.cache.device_error() == 0
