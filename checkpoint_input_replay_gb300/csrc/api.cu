@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/replayssm.h: argument
 // validation, the buffer layout, call-order rules and kernel launches.
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -283,6 +284,10 @@ rs_status rs_create_cache(const rs_config* cfg, const rs_buffers* bufs, rs_cache
       return RS_ERR_CUDA;
     d.num_sms = sms;
   }
+  // debug: RS_DEBUG_CTA_PERMUTE=<m> (m >= 2) permutes which CTA of the persistent
+  // decode and commit launches takes which unit range, to check that no result
+  // depends on the order in which CTAs run or arrive
+  if (const char* e = getenv("RS_DEBUG_CTA_PERMUTE")) d.cta_mult = atoi(e) >= 2 ? atoi(e) : 0;
   d.ckpt = static_cast<float*>(bufs->ckpt);
   char* ring = static_cast<char*>(bufs->ring);
   if (cfg->kind == RS_MAMBA2) {

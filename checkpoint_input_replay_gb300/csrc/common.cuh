@@ -87,6 +87,13 @@ __device__ __forceinline__ float4 axpy4x2(float a, const float4 x, const float4 
   return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
+// Unit range of this CTA in a persistent launch: blockIdx.x, or the debug
+// permutation (c * mult + 7) mod grid when mult > 0 (mult coprime with the grid).
+__device__ __forceinline__ int cta_index(int mult) {
+  if (mult <= 0) return static_cast<int>(blockIdx.x);
+  return static_cast<int>((static_cast<long long>(blockIdx.x) * mult + 7) % gridDim.x);
+}
+
 // a . b with two packed FMAs (pairs (x, y) and (z, w)) and one add
 __device__ __forceinline__ float dot4p(const float4 a, const float4 b) {
   float2 t = fma2(make_float2(a.x, a.y), make_float2(b.x, b.y), make_float2(0.f, 0.f));

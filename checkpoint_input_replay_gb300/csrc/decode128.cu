@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
 
   const int upseq = H * SPL;  // units of a sequence
   const int total_units = d.B * upseq;
-  const int u0 = blockIdx.x * units_per_cta;
+  const int u0 = cta_index(d.cta_mult) * units_per_cta;
   const int u1 = min(u0 + units_per_cta, total_units);
   if (u0 >= u1) return;
   const int b0 = u0 / upseq, b1 = (u1 - 1) / upseq;
@@ -1025,7 +1025,9 @@ cudaError_t launch128(const LayerDev& d, const TokenIn& in, float* y, cudaStream
   auto kernel = decode128_kernel<KIND, READ, P, TEAMS>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kThreads128, smem, s>>>(d, in, y, per, static_cast<int>(stages));
+  LayerDev dd = d;
+  dd.cta_mult = coprime_mult(d.cta_mult, grid);
+  kernel<<<grid, kThreads128, smem, s>>>(dd, in, y, per, static_cast<int>(stages));
   return cudaGetLastError();
 }
 

@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
   for (int w = 0; w < kThreadsF / 32; ++w) K += s_cnt[w];
   const int total_units = K * H;
   const int per = (total_units + gridDim.x - 1) / gridDim.x;
-  const int u0 = min(static_cast<int>(blockIdx.x) * per, total_units);
+  const int u0 = min(cta_index(d.cta_mult) * per, total_units);
   const int u1 = min(u0 + per, total_units);
   const int nunits = u1 - u0;
   const int k0 = u0 / H;  // first staged sequence of this CTA (in the numbering)
@@ -494,7 +494,9 @@ cudaError_t launch_f128(const LayerDev& d, int mode, const int* accepted, const 
   auto kernel = fold128_kernel<KIND, READ, P>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kThreadsF, smem, s>>>(d, mode, accepted, mask, T_pending, static_cast<int>(stages));
+  LayerDev dd = d;
+  dd.cta_mult = coprime_mult(d.cta_mult, grid);
+  kernel<<<grid, kThreadsF, smem, s>>>(dd, mode, accepted, mask, T_pending, static_cast<int>(stages));
   return cudaGetLastError();
 }
 

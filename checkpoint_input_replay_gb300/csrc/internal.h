@@ -23,6 +23,10 @@ struct LayerDev {
   int kind, B, H, G, P, N, L, C, T_max, read_mode;
   int Cp;                      // ring row stride of the per-head scalars: C rounded up to 8
   int num_sms;                 // SMs of the device (persistent grid size)
+  // debug (ordering check): a persistent launch's CTA c takes unit range
+  // (c * cta_mult + 7) mod grid instead of c; 0 = off.  Launchers make it coprime
+  // with the grid, so the map is a permutation.
+  int cta_mult;
   float* ckpt;                 // [B][H][P][N]
   // Mamba-2 ring
   uint16_t* r_x;               // bf16 [B][H][C][P]
@@ -84,5 +88,20 @@ int verify_table_stride(int kind, int C);
 cudaError_t make_ckpt_tmap(const LayerDev& d, CUtensorMap* out);
 cudaError_t launch_verify128(const LayerDev& d, const CUtensorMap& tmap, const TokenIn& in, int T, float* y,
                              cudaStream_t s);
+
+// smallest m' >= m coprime with g (a CTA permutation multiplier); 0 stays 0
+inline int coprime_mult(int m, int g) {
+  if (m <= 0) return 0;
+  auto gcd = [](int a, int b) {
+    while (b) {
+      const int t = a % b;
+      a = b;
+      b = t;
+    }
+    return a;
+  };
+  while (gcd(m, g) != 1) ++m;
+  return m;
+}
 
 }  // namespace rs

@@ -181,3 +181,51 @@ def test_flush_with_mask_and_export():
     pair.oracle.flush()
     pair.check_ckpt("after full flush")
     assert pair.cache.device_error() == 0
+
+
+def _run_layer(shape, seed, steps, rounds):
+    """Decode steps, verify + commit rounds, decode steps again, through the C ABI;
+    returns every output and the caches' final contents."""
+    from checkpoint_input_replay_gb300 import ReplayCache
+    from tests.harness import to_dev
+    wl = configs.workload(shape, seed=seed, s0_std=0.1 if shape.kind == MAMBA2 else 0.05)
+    cache = ReplayCache.for_shape(shape)
+    cache.ckpt.copy_(torch.from_numpy(wl.S0()))
+    A = torch.from_numpy(wl.A()).cuda() if shape.kind == MAMBA2 else None
+
+    def dev(inp):
+        d = to_dev(inp)
+        if A is not None:
+            d["A"] = A
+        return d
+
+    ys = [cache.decode_step(dev(wl.step(t))).clone() for t in range(steps)]
+    for s in range(rounds):
+        ys.append(cache.verify(2, dev(wl.draft(s, 2))).clone())
+        cache.commit(torch.from_numpy(wl.accepted(s, 2)).cuda())
+    ys += [cache.decode_step(dev(wl.step(steps + t))).clone() for t in range(steps)]
+    torch.cuda.synchronize()
+    out = [cache.ckpt.cpu().numpy(), cache.cursor.cpu().numpy(),
+           {k: (v.view(torch.int16) if v.dtype == torch.bfloat16 else v).cpu().numpy()
+            for k, v in cache.ring_views().items()}]
+    assert cache.device_error() == 0
+    cache.close()
+    return [y.cpu().numpy() for y in ys], out
+
+
+@pytest.mark.parametrize("kind,P", [(MAMBA2, 64), (GDN, 128)])
+def test_cta_order_permuted_gives_identical_results(kind, P, monkeypatch):
+    """The debug permutation of unit ranges over the CTAs of the persistent decode and
+    commit launches (RS_DEBUG_CTA_PERMUTE) changes which CTA runs, arrives and writes
+    cursors when: outputs, checkpoints, cursors and ring must stay bit for bit."""
+    shape = LayerShape(kind, batch=37, n_heads=8, n_groups=2, d_head=P, d_state=128, ring_len=3, max_draft=2)
+    monkeypatch.delenv("RS_DEBUG_CTA_PERMUTE", raising=False)
+    ys0, st0 = _run_layer(shape, 41, 7, 3)
+    monkeypatch.setenv("RS_DEBUG_CTA_PERMUTE", "5")
+    ys1, st1 = _run_layer(shape, 41, 7, 3)
+    for a, b in zip(ys0, ys1):
+        np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(st0[0], st1[0])
+    np.testing.assert_array_equal(st0[1], st1[1])
+    for k in st0[2]:
+        np.testing.assert_array_equal(st0[2][k], st1[2][k])
