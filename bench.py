@@ -205,6 +205,29 @@ def shard_of(wl, rank: int, world: int) -> Shard:
     return Shard(wl, rank * per, (rank + 1) * per)
 
 
+class nvtx_range:
+    """An NVTX range around a bench leg (for nsys / ncu range filters); a no-op when
+    the torch build has no NVTX."""
+
+    def __init__(self, name: str):
+        self.name = name
+
+    def __enter__(self):
+        try:
+            import torch
+            torch.cuda.nvtx.range_push(self.name)
+            self.on = True
+        except Exception:
+            self.on = False
+        return self
+
+    def __exit__(self, *exc):
+        if self.on:
+            import torch
+            torch.cuda.nvtx.range_pop()
+        return False
+
+
 def job_value(world: int, batch_per_rank: int, steps: int, elapsed_ms_max: float) -> float:
     """Whole-job sequence-steps per second: every rank's units over the slowest rank's time."""
     return world * batch_per_rank * steps / (elapsed_ms_max / 1e3)
@@ -521,7 +544,8 @@ def main(argv=None):
     # each rank decodes its own slice of a world x B job (weak scaling, no exchange)
     wl1 = shard_of(configs.config1(batch=world * args.batch), rank, world)
     with ClockSampler(local) as clk:
-        m2 = decode_leg(wl1, dev, K, W, 16, m2_bytes, barrier, seed=rank)
+        with nvtx_range("decode mamba2 (headline)"):
+            m2 = decode_leg(wl1, dev, K, W, 16, m2_bytes, barrier, seed=rank)
     elapsed = max_over_ranks(m2["elapsed_ms"], world, dev)
     value = job_value(world, wl1.shape.batch, K, elapsed)
 
@@ -550,25 +574,29 @@ def main(argv=None):
     if rank == 0 and args.decode_only:
         print(json.dumps(line), flush=True)
     elif rank == 0:
-        line["e2e"] = e2e_leg(wl1, dev, min(K, 320), W)
+        with nvtx_range("decode mamba2 from host buffers"):
+            line["e2e"] = e2e_leg(wl1, dev, min(K, 320), W)
         rate, secs = oracle_sample(wl1, 8, [0, 1])
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": "8 decode steps of sequences 0-1 of the B=256 workload "
                                           f"(float64 numpy, one thread, {secs:.1f} s)"}
         if not args.no_extra:
-            gdn = decode_leg(configs.config2(), dev, min(K, 1600), W, 16, gdn_bytes, lambda: None)
+            with nvtx_range("decode gdn"):
+                gdn = decode_leg(configs.config2(), dev, min(K, 1600), W, 16, gdn_bytes, lambda: None)
             line["gdn"] = {"workload": "gdn decode, 1 layer: B=256 Hv=32 Hk=16 dk=dv=128, L=16",
                            "value": configs.config2().shape.batch * min(K, 1600) / (gdn["elapsed_ms"] / 1e3),
                            "unit": UNIT, "achieved_gbs": gdn["bytes_total"] / (gdn["launch_ms_total"] * 1e6),
                            "nonflush_gbs": gdn["nonflush_gbs"], "flush_gbs": gdn["flush_gbs"],
                            "nonflush_us": gdn["nonflush_us"], "flush_us": gdn["flush_us"],
                            "frac": gdn["bytes_total"] / (gdn["launch_ms_total"] * 1e6) / hbm}
-            line["verify"] = [verify_leg(configs.config3_mamba2(), dev, 64, 4, lambda: None),
-                              verify_leg(configs.config3_gdn(), dev, 64, 4, lambda: None)]
+            with nvtx_range("verify + commit"):
+                line["verify"] = [verify_leg(configs.config3_mamba2(), dev, 64, 4, lambda: None),
+                                  verify_leg(configs.config3_gdn(), dev, 64, 4, lambda: None)]
             rc = []
             for mode in ("fp8", "nvfp4"):
                 try:
-                    rc.append(read_copy_leg(configs.config4(), dev, mode, min(K, 1600), W))
+                    with nvtx_range(f"decode read copy {mode}"):
+                        rc.append(read_copy_leg(configs.config4(), dev, mode, min(K, 1600), W))
                 except Exception as e:  # read copy reported as missing, not silently dropped
                     rc.append({"mode": mode, "error": str(e).splitlines()[0]})
             line["read_copy"] = rc
