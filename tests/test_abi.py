@@ -84,6 +84,14 @@ def test_null_and_alignment_errors_need_no_device():
     st, code = rs.rs_get_device_error(None, 0)
     assert st == rs.RS_ERR_NULL
     rs.rs_destroy_cache(None)
+    # host-buffer pipe: null handles are rejected before any CUDA call
+    st, pipe = rs.rs_pipe_create(None)
+    assert st == rs.RS_ERR_NULL
+    assert rs.rs_pipe_decode_step(None, rs.rs_inputs(), 0, 0) == rs.RS_ERR_NULL
+    assert rs.rs_pipe_sync(None, 0) == rs.RS_ERR_NULL
+    rs.rs_pipe_destroy(None)
+    assert rs.rs_decode_step_noalloc(cfg, rs.rs_buffers(None, None, None, None, None), rs.rs_inputs(), 0, 0) \
+        == rs.RS_ERR_NULL
 
 
 def test_status_strings():
