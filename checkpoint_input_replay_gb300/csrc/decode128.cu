@@ -50,6 +50,11 @@ constexpr int kGroupBufs = 3;                    // group buffers (staged one gr
 // row stride (floats) of a warp's fold-coefficient table: kMaxRec padded so the
 // 32 lanes' stores (8 rows x 4 records) fall in 32 different banks
 constexpr int kMtabRow = kMaxRec + 4;
+// rows of a warp's fold-coefficient table: 16 where a flush unit folds both of a
+// warp's 8-row blocks in one pass (Mamba-2, d_head 64, FP32 reads), else 8
+__host__ __device__ __forceinline__ constexpr int mtab_rows(int kind, int read, int P) {
+  return (kind == 0 && read == 0 && P == 64) ? 16 : 8;
+}
 
 __host__ __device__ __forceinline__ int al16(int x) { return (x + 15) & ~15; }
 __host__ __device__ __forceinline__ int al128(int x) { return (x + 127) & ~127; }
@@ -103,7 +108,7 @@ __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int
   l.pe_bars = o;  o += 48 * 8;  // full, empty, ready x 8 stages; amax x 2 teams x 8 stages; group full, tables x 3
   l.pe_seq = o;   o += 3 * kMaxSeq128 * 4;
   l.pe_misc = o;  o += 16;
-  l.pe_mtab = o;  o += (kThreads / 32) * 8 * kMtabRow * 4;  // per computing warp: fold coefficients [8 rows][records]
+  l.pe_mtab = o;  o += (kThreads / 32) * mtab_rows(kind, read, P) * kMtabRow * 4;  // per computing warp: fold coefficients [rows][records]
   l.pe_dq = o;    o += 2 * 2 * kMaxRec * 4;                 // per builder: k_j . q, k_j . k_cur
   l.pe_size = al128(o);
   return l;
@@ -216,7 +221,8 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   // abort, unit copies issued, producer done, group copies issued
   volatile int* smisc = reinterpret_cast<volatile int*>(pbase + LY.pe_misc);
   // this warp's fold-coefficient table (computing warps)
-  float* mt = reinterpret_cast<float*>(pbase + LY.pe_mtab) + (warp < kThreads / 32 ? warp : 0) * 8 * kMtabRow;
+  constexpr int MR = mtab_rows(KIND, READ, P);
+  float* mt = reinterpret_cast<float*>(pbase + LY.pe_mtab) + (warp < kThreads / 32 ? warp : 0) * MR * kMtabRow;
 
   const int upseq = H * SPL;  // units of a sequence
   const int total_units = d.B * upseq;
@@ -732,8 +738,55 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       const float gamma = co[3 * C + CO_GAMMA];
       if (KIND == 0) {
         const uint16_t* xb = reinterpret_cast<const uint16_t*>(st + LY.st_rec + static_cast<size_t>(hu) * al16(C * P * 2));
+        if (MR == 16 && RW == 16 && flush) {
+          // flush unit, both of this warp's 8-row blocks in one pass over the records:
+          // the keys are loaded once for the two, and the two blocks' accumulations
+          // interleave (table rows 8 bk + kq hold block bk's fold coefficients)
+          float4 acc[2][8];
 #pragma unroll
-        for (int r0 = 0; r0 < RW; r0 += 8) {
+          for (int bk = 0; bk < 2; ++bk) {
+            const int Rq = tw + TW * (8 * bk + kq);
+            float ry = jl == 0 ? co[n] * bf(cur[Rq]) : 0.f;
+            for (int j = jl; j < n; j += 4) ry = fmaf(co[j], bf(xb[j * P + Rq]), ry);
+            ry += __shfl_xor_sync(0xffffffffu, ry, 1);
+            ry += __shfl_xor_sync(0xffffffffu, ry, 2);
+            float part[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float4 s4 = sT4[(tw + TW * (8 * bk + e)) * SEG + lane];
+              part[e] = dot4(s4, q4);
+              acc[bk][e] = scale4(gamma, s4);
+            }
+            const float tot = reduce8(part, lane);
+            if (jl == 0) yrow[Rq] = fmaf(gamma, tot, ry);
+            for (int jc = 0; 4 * jc <= n; ++jc) {
+              const int j = 4 * jc + jl;
+              mt[(8 * bk + kq) * kMtabRow + j] = j <= n ? co[2 * C + j] * bf(j < n ? xb[j * P + Rq] : cur[Rq]) : 0.f;
+            }
+          }
+          __syncwarp();
+          for (int jq = 0; 4 * jq <= n; ++jq) {
+            float4 k4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              k4[i] = 4 * jq + i <= n ? bf4(reinterpret_cast<const uint2*>(kb + (4 * jq + i) * N)[lane])
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float4 m4 = *reinterpret_cast<const float4*>(mt + e * kMtabRow + 4 * jq);
+              float4& a = acc[e >> 3][e & 7];
+              a = axpy4x2(m4.x, k4[0], a);
+              a = axpy4x2(m4.y, k4[1], a);
+              a = axpy4x2(m4.z, k4[2], a);
+              a = axpy4x2(m4.w, k4[3], a);
+            }
+          }
+          __syncwarp();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) __stcs(gS4 + (tw + TW * e) * SEG + lane, acc[e >> 3][e & 7]);
+        }
+#pragma unroll
+        for (int r0 = 0; r0 < RW && !(MR == 16 && RW == 16 && flush); r0 += 8) {
           const int Rq = tw + TW * (r0 + kq);
           // buffered term of row Rq: lanes 4kq..4kq+3 split the records 0..n-1, lane jl = 0 adds record n
           float ry = jl == 0 ? co[n] * bf(cur[Rq]) : 0.f;
