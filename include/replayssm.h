@@ -247,6 +247,7 @@ rs_status rs_decode_step_noalloc(const rs_config *cfg, const rs_buffers *bufs, c
  *   - Same errors as rs_decode_step (RS_ERR_NULL for a missing host array);
  *     RS_ERR_CUDA for a failed copy or event call.
  *   - Calls on one pipe must come from one host thread in order.
+ *   - The pipe keeps a pointer to its cache: destroy the pipe before the cache.
  */
 typedef struct rs_pipe rs_pipe;
 rs_status rs_pipe_create(rs_cache *cache, rs_pipe **out);
