@@ -30,6 +30,10 @@
  * - Calls are asynchronous and stream-ordered on the caller's stream.  Calls
  *   on one cache must not overlap in time (use one stream, or order them).
  * - bf16 = IEEE bfloat16 bit patterns (uint16); f32 = float.
+ * - Environment (debug only): RS_DEBUG_CTA_PERMUTE=<m>, m >= 2, read by
+ *   rs_create_cache, permutes which CTA of the persistent decode and commit
+ *   launches takes which range of work (an ordering check); results do not
+ *   change.  Unset in normal use.
  * - Kernels never trap.  A problem found on the device (corrupt cursor,
  *   accepted count out of range, a staged copy that did not arrive in time)
  *   sets a sticky device error word and leaves that sequence untouched;
