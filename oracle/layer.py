@@ -28,7 +28,7 @@ from workloads import rng
 from workloads.configs import GDN, MAMBA2, LayerShape
 
 from . import codecs
-from .recurrence import gdn_step, mamba2_step
+from .recurrence import gdn_delta, gdn_step, mamba2_step
 from .ring import RingModel
 
 
@@ -71,6 +71,8 @@ class OracleLayer:
         for i in range(len(self.seqs)):
             self._refresh_read_copy(i)
         self.last_read_out = None
+        # GDN: delta records u of the tokens of the last decode ([b][H][P]) or verify ([b][T][H][P])
+        self.last_deltas = None
 
     # --- one token ---------------------------------------------------------
     def _token(self, S, tok: dict):
@@ -80,6 +82,12 @@ class OracleLayer:
             return S_new, y, tok["dt"] * self.A[None, :]
         S_new, o = gdn_step(S, tok["q"], tok["k"], tok["v"], tok["g"], tok["beta"])
         return S_new, o, tok["g"]
+
+    def _delta(self, S, tok: dict):
+        """GDN: the token's delta record u from the state before it (None for Mamba-2)."""
+        if self.shape.kind == MAMBA2:
+            return None
+        return gdn_delta(S, tok["k"], tok["v"], tok["g"], tok["beta"])
 
     # --- calls ---------------------------------------------------------------
     def decode(self, inp: dict) -> np.ndarray:
@@ -96,6 +104,7 @@ class OracleLayer:
         """
         tok = _wide(inp)
         S_prev_ckpt = self.ckpt.copy() if self.read_mode else None
+        self.last_deltas = self._delta(self.S, tok)
         self.S, y, ld = self._token(self.S, tok)
         self.logdecay += ld
         if self.read_mode:
@@ -116,10 +125,14 @@ class OracleLayer:
         """Outputs of all T draft positions [b][T][H][P]; the committed state is unchanged."""
         tok = {k: v[:, :T] for k, v in _wide(drafts).items()}
         Sd = self.S.copy()
-        outs = []
+        outs, deltas = [], []
         for t in range(T):
-            Sd, y, _ = self._token(Sd, {k: v[:, t] for k, v in tok.items()})
+            tk = {k: v[:, t] for k, v in tok.items()}
+            deltas.append(self._delta(Sd, tk))
+            Sd, y, _ = self._token(Sd, tk)
             outs.append(y)
+        # GDN: delta record of every draft, from the draft chain's own states [b][T][H][P]
+        self.last_deltas = None if deltas[0] is None else np.stack(deltas, axis=1)
         for r in self.rings:
             r.verify(T)
         self._drafts = (tok, T)

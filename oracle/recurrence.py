@@ -62,3 +62,23 @@ def gdn_step(S, q, k, v, g, beta):
     S_new = a * (S - b * Sk[:, :, :, None] * kk[:, :, None, :]) + b * v[:, :, :, None] * kk[:, :, None, :]
     o = np.einsum("bhvk,bhk->bhv", S_new, qq)
     return S_new, o
+
+
+def gdn_delta(S, k, v, g, beta):
+    """The delta record of one Gated DeltaNet token: u_t = b_t (v_t - a_t S_{t-1} k_t).
+
+    Expanding the gated delta rule gives S_t = a_t S_{t-1} + u_t k_t^T, so u_t is
+    the value-side vector a ring record must hold for the unrolled form to
+    reproduce S_t ([warp-studio] 推測デコーディングにおける革新と実装詳細: the
+    buffered records "(d, k, g)", read as d = u).  Computed here from the
+    step-by-step state S_{t-1}, not from the unrolled form.
+
+    S  [b][Hv][dv][dk] float64 (the state before the token)
+    k [b][Hk][dk]   v [b][Hv][dv]   g, beta [b][Hv]
+    Returns u [b][Hv][dv].
+    """
+    Hv = S.shape[1]
+    kh = group_of_head(Hv, k.shape[1])
+    kk = k[:, kh, :]
+    Sk = np.einsum("bhvk,bhk->bhv", S, kk)
+    return beta[:, :, None] * (v - np.exp(g)[:, :, None] * Sk)

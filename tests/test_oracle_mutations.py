@@ -111,3 +111,103 @@ def test_gdn_mistake_is_caught(monkeypatch, variant):
     monkeypatch.setattr(pins, "gdn_step", bad)
     monkeypatch.setattr(layer_mod, "gdn_step", bad)
     assert _some_pin_fails(GDN_PINS)
+
+
+# --- read-copy branch of OracleLayer ------------------------------------------
+
+import tests.test_oracle_readcopy_pins as rc_pins  # noqa: E402
+from oracle.layer import OracleLayer, _wide  # noqa: E402
+
+
+class _DecayOffByOne(OracleLayer):
+    """Mistake: the copy error is decayed by the records before this token only
+    (the current token's decay left out of the sum)."""
+
+    def decode(self, inp):
+        tok = _wide(inp)
+        S_prev_ckpt = self.ckpt.copy()
+        before = self.logdecay.copy()
+        self.S, y, ld = self._token(self.S, tok)
+        self.logdecay += ld
+        grp = (np.arange(self.shape.n_heads) * self.shape.n_groups) // self.shape.n_heads
+        err = np.einsum("bhpn,bhn->bhp", self.read_copy - S_prev_ckpt, tok["C"][:, grp, :])
+        self.last_read_out = y + np.exp(before)[:, :, None] * err
+        for i, r in enumerate(self.rings):
+            if r.decode():
+                self.ckpt[i] = self.S[i]
+                self.logdecay[i] = 0.0
+                self.last_read_out[i] = y[i]
+                self._refresh_read_copy(i)
+        return y
+
+
+class _StaleCopy(OracleLayer):
+    """Mistake: a fold re-quantises the copy from the checkpoint as it was before the fold."""
+
+    def _refresh_read_copy(self, i):
+        if self.read_mode is None:
+            return
+        old = getattr(self, "_ckpt_before", None)
+        if old is None:
+            return super()._refresh_read_copy(i)
+        keep = self.ckpt[i].copy()
+        self.ckpt[i] = old[i]
+        super()._refresh_read_copy(i)
+        self.ckpt[i] = keep
+
+    def decode(self, inp):
+        self._ckpt_before = self.ckpt.copy()
+        return super().decode(inp)
+
+    def commit(self, accepted):
+        self._ckpt_before = self.ckpt.copy()
+        return super().commit(accepted)
+
+
+RC_PINS = ["test_fp8_read_copy_dyadic_hand_values"]
+
+
+def _rc_pin_fails() -> bool:
+    cases = [lambda: rc_pins.test_fp8_read_copy_dyadic_hand_values()]
+    for mode in ("fp8", "nvfp4"):
+        cases.append(lambda m=mode: rc_pins.test_read_copy_output_equals_recurrence_restarted_from_the_copy(m))
+        cases.append(lambda m=mode: rc_pins.test_read_copy_output_after_commits_equals_restarted_recurrence(m))
+    failed = 0
+    for c in cases:
+        try:
+            c()
+        except AssertionError:
+            failed += 1
+    return failed > 0
+
+
+@pytest.mark.parametrize("bad", [_DecayOffByOne, _StaleCopy])
+def test_read_copy_mistake_is_caught(monkeypatch, bad):
+    monkeypatch.setattr(rc_pins, "OracleLayer", bad)
+    assert _rc_pin_fails()
+
+
+def test_read_copy_pins_pass_unmutated():
+    assert not _rc_pin_fails()
+
+
+def _bad_delta(S, k, v, g, beta):
+    """Mistake: the delta record without the decay on the erased value."""
+    kh = group_of_head(S.shape[1], k.shape[1])
+    Sk = np.einsum("bhvk,bhk->bhv", S, k[:, kh, :])
+    return beta[:, :, None] * (v - Sk)
+
+
+def test_gdn_delta_mistake_is_caught(monkeypatch):
+    import oracle.recurrence as rec
+    monkeypatch.setattr(rec, "gdn_delta", _bad_delta)
+    monkeypatch.setattr(layer_mod, "gdn_delta", _bad_delta)
+    names = ["test_gdn_delta_reproduces_the_state_and_vanishes_without_write",
+             "test_oracle_layer_records_draft_deltas_along_the_draft_chain"]
+    failed = 0
+    for n in names:
+        try:
+            getattr(pins, n)()
+        except AssertionError:
+            failed += 1
+    assert failed > 0

@@ -350,3 +350,55 @@ def test_commit_advances_by_accepted_prefix():
     close(spec.S[1], S_after2[1])
     close(spec.S[2], plain.S[2])
     assert spec.cursor()[:, 1].tolist() == [0, 2, 4]
+
+
+# --- Gated DeltaNet delta record ---------------------------------------------
+
+def test_gdn_delta_dyadic_hand_values():
+    """u = b (v - a S_{t-1} k), hand-derived on the dyadic GDN case."""
+    from oracle.recurrence import gdn_delta
+    case = json.load(open(os.path.join(GOLDEN, "dyadic_cases.json")))["gdn"]
+    S = np.array(case["S0"], dtype=np.float64)[None, None]
+    for st in case["steps"]:
+        args = (np.array([[st["k"]]], float), np.array([[st["v"]]], float), np.array([[st["g"]]]),
+                np.array([[st["beta"]]]))
+        u = gdn_delta(S, *args)
+        assert np.array_equal(u[0, 0], np.array(st["u"], float))
+        S, _ = gdn_step(S, np.array([[st["q"]]], float), *args)
+
+
+def test_gdn_delta_reproduces_the_state_and_vanishes_without_write():
+    """S_t = a S_{t-1} + u k^T for the step-by-step state; b = 0 gives u = 0."""
+    from oracle.recurrence import gdn_delta
+    Hv, Hk, d = 4, 2, 6
+    S = R.standard_normal((2, Hv, d, d))
+    q = R.standard_normal((2, Hk, d))
+    k = R.standard_normal((2, Hk, d))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = R.standard_normal((2, Hv, d))
+    g = -R.uniform(0.1, 2.0, (2, Hv))
+    beta = R.uniform(0.1, 0.9, (2, Hv))
+    u = gdn_delta(S, k, v, g, beta)
+    S1, _ = gdn_step(S, q, k, v, g, beta)
+    kk = k[:, group_of_head(Hv, Hk), :]
+    close(S1, np.exp(g)[:, :, None, None] * S + u[:, :, :, None] * kk[:, :, None, :])
+    assert np.array_equal(gdn_delta(S, k, v, g, np.zeros_like(beta)), np.zeros_like(v))
+
+
+def test_oracle_layer_records_draft_deltas_along_the_draft_chain():
+    """Verify's per-draft deltas come from the draft chain's own states: draft t's u
+    equals gdn_delta of the state after drafts 0..t-1."""
+    from oracle.recurrence import gdn_delta
+    shape = LayerShape(GDN, batch=2, n_heads=2, n_groups=1, d_head=3, d_state=4, ring_len=4, max_draft=3)
+    S0 = R.standard_normal((2, 2, 3, 4))
+    lay = OracleLayer(shape, [0, 1], S0)
+    k = R.standard_normal((2, 3, 1, 4))
+    drafts = {"q": R.standard_normal((2, 3, 1, 4)), "k": k / np.linalg.norm(k, axis=-1, keepdims=True),
+              "v": R.standard_normal((2, 3, 2, 3)), "g": -R.uniform(0.1, 1.0, (2, 3, 2)),
+              "beta": R.uniform(0.1, 0.9, (2, 3, 2))}
+    lay.verify(drafts, 3)
+    S = S0.copy()
+    for t in range(3):
+        tk = {n: v[:, t] for n, v in drafts.items()}
+        close(lay.last_deltas[:, t], gdn_delta(S, tk["k"], tk["v"], tk["g"], tk["beta"]))
+        S, _ = gdn_step(S, tk["q"], tk["k"], tk["v"], tk["g"], tk["beta"])
