@@ -25,10 +25,10 @@ from __future__ import annotations
 import numpy as np
 
 from workloads import rng
-from workloads.configs import GDN, MAMBA2, LayerShape
+from workloads.configs import GDN, KDA, MAMBA2, LayerShape
 
 from . import codecs
-from .recurrence import gdn_delta, gdn_step, mamba2_step
+from .recurrence import gdn_delta, gdn_step, kda_delta, kda_step, mamba2_step
 from .ring import RingModel
 
 
@@ -64,8 +64,9 @@ class OracleLayer:
         C = shape.ring_len + shape.max_draft
         self.rings = [RingModel(shape.ring_len, C) for _ in self.seqs]
         self._drafts = None
+        self._tree = None  # parents of the pending tree verify (None: chain-shaped drafts)
         # sum of log decays applied to the state since the last flush, per head
-        self.logdecay = np.zeros((len(self.seqs), shape.n_heads))
+        self.logdecay = np.zeros((len(self.seqs), shape.n_heads) + ((shape.d_state,) if shape.kind == KDA else ()))
         # dequantised read copy (float64) of each followed sequence's checkpoint
         self.read_copy = np.zeros_like(self.S) if read_mode else None
         for i in range(len(self.seqs)):
@@ -80,13 +81,19 @@ class OracleLayer:
         if self.shape.kind == MAMBA2:
             S_new, y = mamba2_step(S, tok["x"], tok["dt"], self.A, tok["B"], tok["C"])
             return S_new, y, tok["dt"] * self.A[None, :]
+        if self.shape.kind == KDA:
+            S_new, o = kda_step(S, tok["q"], tok["k"], tok["v"], tok["g"], tok["beta"])
+            return S_new, o, tok["g"]
         S_new, o = gdn_step(S, tok["q"], tok["k"], tok["v"], tok["g"], tok["beta"])
         return S_new, o, tok["g"]
 
     def _delta(self, S, tok: dict):
-        """GDN: the token's delta record u from the state before it (None for Mamba-2)."""
+        """GDN / per-channel gate: the token's delta record u from the state before it
+        (None for Mamba-2)."""
         if self.shape.kind == MAMBA2:
             return None
+        if self.shape.kind == KDA:
+            return kda_delta(S, tok["k"], tok["v"], tok["g"], tok["beta"])
         return gdn_delta(S, tok["k"], tok["v"], tok["g"], tok["beta"])
 
     # --- calls ---------------------------------------------------------------
@@ -136,10 +143,65 @@ class OracleLayer:
         for r in self.rings:
             r.verify(T)
         self._drafts = (tok, T)
+        self._tree = None
         return np.stack(outs, axis=1)
+
+    def verify_tree(self, drafts: dict, T: int, parents) -> np.ndarray:
+        """Tree-shaped drafts: draft tau continues draft parents[tau] (-1: the last
+        committed record; otherwise an earlier draft, so parents[tau] < tau).  Each
+        draft's output is the conventional recurrence run along its root-to-draft path
+        from the committed state; the committed state is unchanged.  Draft records
+        still take the slots after the committed ones, in draft order, so accepted
+        records need not be contiguous in the buffer ([warp-studio]
+        推測デコーディングにおける革新と実装詳細, the sentence on tree-based
+        speculative decoding).  Returns [b][T][H][P]."""
+        par = [int(p) for p in parents]
+        if len(par) != T or any(not -1 <= p < t for t, p in enumerate(par)):
+            raise ValueError("parents[tau] must lie in -1..tau-1")
+        tok = {k: v[:, :T] for k, v in _wide(drafts).items()}
+        node_states, outs, deltas = [], [], []
+        for t in range(T):
+            base = self.S if par[t] < 0 else node_states[par[t]]
+            tk = {k: v[:, t] for k, v in tok.items()}
+            deltas.append(self._delta(base, tk))
+            St, y, _ = self._token(base, tk)
+            node_states.append(St)
+            outs.append(y)
+        for r in self.rings:
+            r.verify(T)
+        self.last_deltas = None if deltas[0] is None else np.stack(deltas, axis=1)
+        self._drafts = (tok, T)
+        self._tree = par
+        return np.stack(outs, axis=1)
+
+    def commit_path(self, paths) -> None:
+        """Commit, per sequence, the drafts listed in paths[i]: a root-to-draft path of the
+        last tree verify, in order (empty: none).  The committed state advances token by
+        token along the path; the cursor advances by its length."""
+        tok, T = self._drafts
+        par = self._tree if self._tree is not None else list(range(-1, T - 1))
+        for i, path in enumerate(paths):
+            prev = -1
+            for node in path:
+                if not 0 <= node < T or par[node] != prev:
+                    raise ValueError("not a root-to-draft path of the last verify")
+                prev = node
+                S_new, _, ld = self._token(self.S[i:i + 1], {k: v[i:i + 1, node] for k, v in tok.items()})
+                self.S[i] = S_new[0]
+                self.logdecay[i] += ld[0]
+        for i, r in enumerate(self.rings):
+            if r.commit(len(paths[i])):
+                self.ckpt[i] = self.S[i]
+                self.logdecay[i] = 0.0
+                self._refresh_read_copy(i)
+        self._drafts = None
+        self._tree = None
 
     def commit(self, accepted) -> None:
         """Commit the first accepted[i] drafts of each sequence."""
+        if self._tree is not None and self._tree != list(range(-1, len(self._tree) - 1)):
+            raise RuntimeError("a prefix commit needs chain-shaped drafts; use commit_path")
+        self._tree = None
         tok, T = self._drafts
         n = np.asarray(accepted)
         for t in range(T):

@@ -82,3 +82,40 @@ def gdn_delta(S, k, v, g, beta):
     kk = k[:, kh, :]
     Sk = np.einsum("bhvk,bhk->bhv", S, kk)
     return beta[:, :, None] * (v - np.exp(g)[:, :, None] * Sk)
+
+
+def kda_step(S, q, k, v, g, beta):
+    """One token of the delta rule with a per-channel gate (the gate form of Kimi
+    Delta Attention), conventional form.
+
+    S_t = S_{t-1} Diag(a_t) (I - b_t k_t k_t^T) + b_t v_t k_t^T and o_t = S_t q_t,
+    per value head, with a_t = exp(g_t) a vector over the key channels (Gated
+    DeltaNet is the case of equal channels).  The pages note that the method
+    generalises to this rule ([richland] Why it matters) without writing it; the
+    channel-wise form here is the plainest one: the scalar decay of the gated delta
+    rule becomes a diagonal matrix on the key side.
+    S_{t-1} Diag(a)(I - b k k^T) is expanded as S' - b (S' k) k^T with S' = S_{t-1} Diag(a).
+
+    S  [b][Hv][dv][dk] float64   q, k [b][Hk][dk]   v [b][Hv][dv]
+    g  [b][Hv][dk] (log decay per key channel)   beta [b][Hv]
+    Returns (S_t, o_t) with o_t [b][Hv][dv].
+    """
+    Hv = S.shape[1]
+    kh = group_of_head(Hv, k.shape[1])
+    kk = k[:, kh, :]
+    qq = q[:, kh, :]
+    b = beta[:, :, None, None]
+    Sd = S * np.exp(g)[:, :, None, :]                   # S_{t-1} Diag(a)
+    Sk = np.einsum("bhvk,bhk->bhv", Sd, kk)
+    S_new = Sd - b * Sk[:, :, :, None] * kk[:, :, None, :] + b * v[:, :, :, None] * kk[:, :, None, :]
+    o = np.einsum("bhvk,bhk->bhv", S_new, qq)
+    return S_new, o
+
+
+def kda_delta(S, k, v, g, beta):
+    """The delta record of one per-channel-gated token: u_t = b_t (v_t - S_{t-1} (a_t * k_t)),
+    so that S_t = S_{t-1} Diag(a_t) + u_t k_t^T (shapes as kda_step)."""
+    Hv = S.shape[1]
+    kk = k[:, group_of_head(Hv, k.shape[1]), :]
+    Sk = np.einsum("bhvk,bhk->bhv", S, np.exp(g) * kk)
+    return beta[:, :, None] * (v - Sk)

@@ -211,3 +211,95 @@ def test_gdn_delta_mistake_is_caught(monkeypatch):
         except AssertionError:
             failed += 1
     assert failed > 0
+
+
+# --- tree verify and path commit ------------------------------------------------
+
+import tests.test_oracle_tree_pins as tree_pins  # noqa: E402
+
+
+class _TreeAsChain(OracleLayer):
+    """Mistake: the parents are ignored and the drafts verified as a chain."""
+
+    def verify_tree(self, drafts, T, parents):
+        Y = self.verify(drafts, T)
+        self._tree = [int(p) for p in parents]
+        return Y
+
+
+class _PathAsPrefix(OracleLayer):
+    """Mistake: a path commit advances the state by the first len(path) drafts."""
+
+    def commit_path(self, paths):
+        tok, T = self._drafts
+        for i, path in enumerate(paths):
+            for node in range(len(path)):
+                S_new, _, ld = self._token(self.S[i:i + 1], {k: v[i:i + 1, node] for k, v in tok.items()})
+                self.S[i] = S_new[0]
+                self.logdecay[i] += ld[0]
+        for i, r in enumerate(self.rings):
+            if r.commit(len(paths[i])):
+                self.ckpt[i] = self.S[i]
+                self.logdecay[i] = 0.0
+        self._drafts = None
+        self._tree = None
+
+
+def _tree_pin_fails() -> bool:
+    cases = []
+    for par in tree_pins.TREES:
+        cases.append(lambda p=par: tree_pins.test_mamba2_tree_verify_is_the_ancestor_masked_chunkwise_form(p))
+        cases.append(lambda p=par: tree_pins.test_gdn_tree_verify_is_the_ancestor_masked_triangular_solve(p))
+    for par, path in [([-1, -1, 0, 1], [1, 3]), ([-1, 0, 0, 2], [0, 2, 3])]:
+        cases.append(lambda p=par, q=path: tree_pins.test_commit_path_equals_plain_decode_along_the_path(p, q))
+    failed = 0
+    for c in cases:
+        try:
+            c()
+        except AssertionError:
+            failed += 1
+    return failed > 0
+
+
+@pytest.mark.parametrize("bad", [_TreeAsChain, _PathAsPrefix])
+def test_tree_mistake_is_caught(monkeypatch, bad):
+    monkeypatch.setattr(tree_pins, "OracleLayer", bad)
+    assert _tree_pin_fails()
+
+
+def test_tree_pins_pass_unmutated():
+    assert not _tree_pin_fails()
+
+
+def _kda(variant):
+    def step(S, q, k, v, g, beta):
+        kh = group_of_head(S.shape[1], k.shape[1])
+        kk, qq = k[:, kh, :], q[:, kh, :]
+        b = beta[:, :, None, None]
+        a = np.exp(g)
+        if variant == "erase_before_decay":      # S (I - b k k^T) Diag(a): the order swapped
+            Sk = np.einsum("bhvk,bhk->bhv", S, kk)
+            S_new = (S - b * Sk[..., None] * kk[:, :, None, :]) * a[:, :, None, :] + b * v[..., None] * kk[:, :, None, :]
+        else:                                    # decay on the value side: Diag(a) applied to rows
+            Sd = S * a[:, :, :, None] if a.shape[-1] == S.shape[2] else S * a[:, :, None, :]
+            Sd = np.swapaxes(np.swapaxes(S, 2, 3) * a[:, :, None, :], 2, 3)
+            Sk = np.einsum("bhvk,bhk->bhv", Sd, kk)
+            S_new = Sd - b * Sk[..., None] * kk[:, :, None, :] + b * v[..., None] * kk[:, :, None, :]
+        return S_new, np.einsum("bhvk,bhk->bhv", S_new, qq)
+    return step
+
+
+@pytest.mark.parametrize("variant", ["erase_before_decay", "decay_on_value_side"])
+def test_kda_mistake_is_caught(monkeypatch, variant):
+    import oracle.recurrence as rec
+    bad = _kda(variant)
+    monkeypatch.setattr(rec, "kda_step", bad)
+    names = ["test_kda_dyadic_hand_values", "test_kda_with_equal_channels_is_gated_deltanet",
+             "test_kda_without_write_is_per_channel_decay", "test_kda_unrolled_identity"]
+    failed = 0
+    for n in names:
+        try:
+            getattr(pins, n)()
+        except AssertionError:
+            failed += 1
+    assert failed > 0

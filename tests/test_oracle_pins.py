@@ -402,3 +402,72 @@ def test_oracle_layer_records_draft_deltas_along_the_draft_chain():
         tk = {n: v[:, t] for n, v in drafts.items()}
         close(lay.last_deltas[:, t], gdn_delta(S, tk["k"], tk["v"], tk["g"], tk["beta"]))
         S, _ = gdn_step(S, tk["q"], tk["k"], tk["v"], tk["g"], tk["beta"])
+
+
+# --- delta rule with a per-channel gate ------------------------------------------
+
+def test_kda_dyadic_hand_values():
+    from oracle.recurrence import kda_delta, kda_step
+    case = json.load(open(os.path.join(GOLDEN, "dyadic_cases.json")))["kda"]
+    S = np.array(case["S0"], dtype=np.float64)[None, None]
+    for st in case["steps"]:
+        g = np.log(np.array([[st["a"]]], float))
+        args = (np.array([[st["k"]]], float), np.array([[st["v"]]], float), g, np.array([[st["beta"]]]))
+        close(kda_delta(S, *args)[0, 0], st["u"], tol=1e-15)
+        S, o = kda_step(S, np.array([[st["q"]]], float), *args)
+        close(S[0, 0], st["S"], tol=1e-15)
+        close(o[0, 0], st["o"], tol=1e-15)
+
+
+def test_kda_with_equal_channels_is_gated_deltanet():
+    from oracle.recurrence import kda_step
+    Hv, Hk, d = 4, 2, 6
+    S = R.standard_normal((2, Hv, d, d))
+    q = _unit(R.standard_normal((2, Hk, d)))
+    k = _unit(R.standard_normal((2, Hk, d)))
+    v = R.standard_normal((2, Hv, d))
+    g = -R.uniform(0.05, 2.0, (2, Hv))
+    beta = R.uniform(0.1, 0.9, (2, Hv))
+    S1, o1 = kda_step(S, q, k, v, np.repeat(g[:, :, None], d, axis=2), beta)
+    S2, o2 = gdn_step(S, q, k, v, g, beta)
+    close(S1, S2)
+    close(o1, o2)
+
+
+def test_kda_without_write_is_per_channel_decay():
+    """b = 0: every column c of the state decays by its own a_c, token after token."""
+    from oracle.recurrence import kda_step
+    Hv, Hk, d, T = 2, 1, 5, 6
+    S0 = R.standard_normal((1, Hv, d, d))
+    S = S0.copy()
+    total = np.zeros((1, Hv, d))
+    for _ in range(T):
+        g = -R.uniform(0.0, 1.0, (1, Hv, d))
+        total += g
+        S, _ = kda_step(S, _unit(R.standard_normal((1, Hk, d))), _unit(R.standard_normal((1, Hk, d))),
+                        R.standard_normal((1, Hv, d)), g, np.zeros((1, Hv)))
+    close(S, S0 * np.exp(total)[:, :, None, :])
+
+
+def test_kda_unrolled_identity():
+    """h tokens after a checkpoint: S_h = S_c Diag(G_h) + sum_j u_j (k_j * W_j(h))^T with
+    G_h the channel-wise product of all decays and W_j(h) the product of the decays after
+    record j -- the checkpoint-plus-buffer form the decode kernel uses for this gate."""
+    from oracle.recurrence import kda_delta, kda_step
+    Hv, Hk, d, h = 3, 1, 6, 7
+    Sc = R.standard_normal((1, Hv, d, d))
+    S = Sc.copy()
+    us, ks, gs = [], [], []
+    for _ in range(h):
+        q, k = _unit(R.standard_normal((1, Hk, d))), _unit(R.standard_normal((1, Hk, d)))
+        v, g, b = R.standard_normal((1, Hv, d)), -R.uniform(0.0, 0.8, (1, Hv, d)), R.uniform(0.1, 0.9, (1, Hv))
+        us.append(kda_delta(S, k, v, g, b)[0])
+        ks.append(k[0, 0])
+        gs.append(g[0])
+        S, _ = kda_step(S, q, k, v, g, b)
+    for hd in range(Hv):
+        unrolled = Sc[0, hd] * np.exp(sum(gg[hd] for gg in gs))[None, :]
+        for j in range(h):
+            W = np.exp(sum(gs[i][hd] for i in range(j + 1, h))) if j + 1 < h else np.ones(d)
+            unrolled = unrolled + np.outer(us[j][hd], ks[j] * W)
+        close(S[0, hd], unrolled)

@@ -34,6 +34,7 @@ from . import rng
 
 MAMBA2 = 0
 GDN = 1
+KDA = 2   # Gated-DeltaNet-style layer with a per-key-channel decay gate
 
 
 @dataclasses.dataclass(frozen=True)
@@ -199,6 +200,58 @@ class GdnWorkload:
         return np.minimum(np.floor(u * (T + 1)), T).astype(np.int32)
 
 
+class KdaWorkload:
+    """Inputs of one delta-rule layer with a per-channel gate: per-step (q, k, v, g,
+    beta) with g a log decay per key channel, the initial state, and nothing for
+    verification (this layer kind is decoded only).
+
+    Distributions: q, k, v, beta as the Gated DeltaNet layer; the log decay of key
+    channel c of value head h is g = -softplus(N(0,1)) * r_{h,c} / 8 with the per
+    (head, channel) rate r = exp(U(0, ln 16)), so decays spread over channels."""
+
+    def __init__(self, shape: LayerShape, seed: int, s0_std: float):
+        assert shape.kind == KDA
+        self.shape = shape
+        self.seed = seed
+        self.s0_std = s0_std
+
+    def channel_rate(self) -> np.ndarray:
+        s = self.shape
+        u = rng.uniform(self.seed, "kda/rate", 0, s.n_heads * s.d_state).reshape(s.n_heads, s.d_state)
+        return np.exp(u * math.log(16.0)) / 8.0
+
+    def S0(self, b0: int = 0, b1: int | None = None) -> np.ndarray:
+        s = self.shape
+        b1 = s.batch if b1 is None else b1
+        full = (s.batch, s.n_heads, s.d_head, s.d_state)
+        if self.s0_std == 0.0:
+            return np.zeros((b1 - b0,) + full[1:], dtype=np.float32)
+        return (self.s0_std * _normal_rows(self.seed, "kda/S0", full, b0, b1)).astype(np.float32)
+
+    def _tokens(self, tag: str, lead: tuple, b0: int, b1: int) -> dict:
+        s = self.shape
+        q = _normal_rows(self.seed, f"kda/{tag}/q", lead + (s.n_groups, s.d_state), b0, b1)
+        k = _normal_rows(self.seed, f"kda/{tag}/k", lead + (s.n_groups, s.d_state), b0, b1)
+        v = _normal_rows(self.seed, f"kda/{tag}/v", lead + (s.n_heads, s.d_head), b0, b1)
+        zb = _normal_rows(self.seed, f"kda/{tag}/beta", lead + (s.n_heads,), b0, b1)
+        zg = _normal_rows(self.seed, f"kda/{tag}/g", lead + (s.n_heads, s.d_state), b0, b1)
+        q = q / np.linalg.norm(q, axis=-1, keepdims=True)
+        k = k / np.linalg.norm(k, axis=-1, keepdims=True)
+        return {
+            "q": _bf16(q),
+            "k": _bf16(k),
+            "v": _bf16(v),
+            "beta": (1.0 / (1.0 + np.exp(-zb))).astype(np.float32),
+            "g": (-_softplus(zg) * self.channel_rate()).astype(np.float32),
+        }
+
+    def step(self, t: int, b0: int = 0, b1: int | None = None) -> dict:
+        """Decode-step t inputs, rows b0:b1: q, k [b][Hk][dk], v [b][Hv][dv] (bf16 bits),
+        g [b][Hv][dk], beta [b][Hv] f32."""
+        b1 = self.shape.batch if b1 is None else b1
+        return self._tokens(f"step{t}", (self.shape.batch,), b0, b1)
+
+
 # The five workloads of the hot path ------------------------------------------
 
 CONFIG0 = LayerShape(MAMBA2, batch=2, n_heads=4, n_groups=1, d_head=16, d_state=16, ring_len=4)
@@ -214,6 +267,8 @@ STEPS = {0: 64, 1: 160, 2: 160, 3: 64, 4: 4096}
 def workload(shape: LayerShape, seed: int, s0_std: float):
     if shape.kind == MAMBA2:
         return Mamba2Workload(shape, seed, s0_std)
+    if shape.kind == KDA:
+        return KdaWorkload(shape, seed, s0_std)
     return GdnWorkload(shape, seed, s0_std)
 
 
@@ -240,3 +295,11 @@ def config3_gdn(batch: int = 512):
 
 def config4(batch: int = 256):
     return Mamba2Workload(CONFIG4.with_batch(batch), seed=4, s0_std=0.1)
+
+
+# The per-channel-gate layer at the config-2 shape (the window-length row's gate variant)
+CONFIG_KDA = LayerShape(KDA, batch=256, n_heads=32, n_groups=16, d_head=128, d_state=128, ring_len=16)
+
+
+def config_kda(batch: int = 256):
+    return KdaWorkload(CONFIG_KDA.with_batch(batch), seed=5, s0_std=0.05)
