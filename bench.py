@@ -1,14 +1,18 @@
 """Benchmark of the ReplaySSM decode hot path on one GB300 (or N, one process per GPU).
 
 A step is one standard decode step of one Mamba-2 layer at B = 256
-(nheads 128, headdim 64, dstate 128, ngroups 8, FP32 checkpoint, L = 16):
-non-flush steps and the flush step every 16th token, at their natural
-ratio, through the C ABI.  The timed region holds whole windows of steps with
-inputs already resident in HBM; the 1 GiB state is larger than L2, so no L2
-flush is needed between steps.  Per-launch CUDA events on the launching
-stream give the roofline of the decode kernel.  Extra objects time the
-Gated DeltaNet layer (B = 256), speculative verify + commit (B = 512, T = 4)
-and the FP8 / NVFP4 read copies.
+(nheads 128, headdim 64, dstate 128, ngroups 8, FP32 checkpoint, L = 16)
+through the C ABI, with inputs already resident in HBM; the 1 GiB state is
+larger than L2, so no L2 flush is needed between steps.  Timing starts at a
+window boundary and covers exactly --steps launches, so the timed region
+holds floor-or-ceil(K / 16) flush steps; `natural_window` restates the rate
+at the natural 15 : 1 mix from the per-launch means.  Per-launch CUDA events
+on the launching stream give the roofline of the decode kernel.  Extra
+objects time the Gated DeltaNet layer (B = 256), speculative verify + commit
+(B = 512, T = 4), the FP8 / NVFP4 read copies (with their per-window error
+against the exact output), the conventional read-modify-write and
+snapshot-per-draft kernels on the same GPU (and the ratios), a batch sweep
+and a window-length sweep.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -38,6 +42,7 @@ sys.path.insert(0, ROOT)
 METRIC = "SSM decode seq·steps/s per layer at B=256 (Mamba-2/GDN); HBM GB/s vs 8 TB/s"
 UNIT = "seq·steps/s"
 FALLBACK_HBM_GBS = 6800.0
+E2E_STEPS = 320  # host-buffer leg: 20 whole windows, whatever --steps is
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -57,21 +62,16 @@ def kernel_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(name: str):
-    """(DRAM bytes, algorithmic bytes) of one non-flush launch, from profiles/<name>.md, for the
-    current kernel source; None when the summary is missing or was taken on other source."""
-    p = os.path.join(ROOT, "profiles", name + ".md")
+def ncu_record(name: str):
+    """The ncu DRAM figures in profiles/<name>.json (written beside the summary of the
+    same name) when they were taken on the current decode kernel source, else None."""
+    p = os.path.join(ROOT, "profiles", name + ".json")
     if not os.path.exists(p):
         return None
-    fields = {}
-    keys = ("traffic_bytes_per_launch", "algorithmic_bytes_per_launch", "kernel_sha")
-    for line in open(p):
-        if ":" in line and line.strip().startswith(keys):
-            k, v = line.split(":", 1)
-            fields[k.strip()] = v.strip().strip("`")
-    if fields.get("kernel_sha") != kernel_sha() or "traffic_bytes_per_launch" not in fields:
+    rec = json.load(open(p))
+    if rec.get("kernel_sha") != kernel_sha():
         return None
-    return float(fields["traffic_bytes_per_launch"]), float(fields.get("algorithmic_bytes_per_launch", "nan"))
+    return rec
 
 
 class ClockSampler:
@@ -300,11 +300,27 @@ def decode_leg(wl, dev, K, W, L, bytes_fn, barrier, distinct=16, seed=0):
         "flush_gbs": sum(flush_b) / (sum(flush_ms) * 1e6) if flush_ms else None,
         "nonflush_us": 1e3 * statistics.mean(nonflush_ms) if nonflush_ms else None,
         "flush_us": 1e3 * statistics.mean(flush_ms) if flush_ms else None,
-        "device_error": err, "launches": K,
+        "device_error": err, "launches": K, "flush_launches": len(flush_ms),
+        "gap_us": 1e3 * (elapsed - sum(per)) / K,
     }
+    res["natural_window"] = natural_window(res, wl.shape, L, bytes_fn)
     del cache, steps
     torch.cuda.empty_cache()
     return res
+
+
+def natural_window(res, shape, L, bytes_fn):
+    """The decode rate at the natural mix of one window (L - 1 non-flush steps, one
+    flush), from the per-launch means and the mean gap between launches; and the
+    window's algorithmic bytes over the summed launch times."""
+    if res["nonflush_us"] is None or res["flush_us"] is None:
+        return None
+    us = (L - 1) * res["nonflush_us"] + res["flush_us"] + L * res["gap_us"]
+    nbytes = sum(bytes_fn(shape, h, h == L - 1) for h in range(L)) * shape.batch
+    kern_us = (L - 1) * res["nonflush_us"] + res["flush_us"]
+    return {"value": shape.batch * L / (us * 1e-6), "unit": UNIT, "us_per_step": us / L,
+            "achieved_gbs": nbytes / (kern_us * 1e3), "window_bytes": nbytes,
+            "note": f"{L - 1} non-flush + 1 flush launch at their mean times plus the mean launch gap"}
 
 
 def e2e_leg(wl, dev, K, W):
@@ -405,15 +421,183 @@ def read_copy_leg(wl, dev, mode, K, W):
     L = s.ring_len
     W = int(math.ceil(W / L) * L)
     elapsed, per = run_decode_loop(cache, steps, K, W, dev, lambda: None)
-    nonflush = [p for t, p in enumerate(per) if (W + t) % L != L - 1]
+    nf = [(t, p) for t, p in enumerate(per) if (W + t) % L != L - 1]
+    nonflush = [p for _, p in nf]
     H, P, N = s.n_heads, s.d_head, s.d_state
+    state = H * P * N * 4
     rc = H * P * N + H * P * 4 if mode == "fp8" else H * P * N // 2 + H * P * N // 16 + H * 4
+    # all algorithmic bytes of a non-flush launch: the copy in place of the FP32 state,
+    # plus the buffered records, this token's inputs, the output and the appended record
+    nf_bytes = sum((m2_bytes(s, (W + t) % L, False) - state + rc) * s.batch for t, _ in nf)
     assert cache.device_error() == 0
     del cache
     torch.cuda.empty_cache()
     return {"mode": mode, "nonflush_us": 1e3 * statistics.mean(nonflush),
-            "read_copy_gbs": s.batch * rc / (statistics.mean(nonflush) * 1e6),
-            "seq_steps_per_s": s.batch * K / (elapsed / 1e3)}
+            "nonflush_gbs": nf_bytes / (sum(nonflush) * 1e6),
+            "copy_bytes_per_seq": rc, "seq_steps_per_s": s.batch * K / (elapsed / 1e3)}
+
+
+def _timed_launches(fn, K, W, dev):
+    """W untimed calls, then K calls each bracketed by CUDA events on the current stream;
+    returns (elapsed ms over the K calls, per-call ms)."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    for t in range(W):
+        fn(t)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for t in range(K):
+        ev[t][0].record(stream)
+        fn(W + t)
+        ev[t][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    return start.elapsed_time(end), [a.elapsed_time(b) for a, b in ev]
+
+
+def _random_state(t, std, seed):
+    import torch
+    g = torch.Generator(device=t.device)
+    g.manual_seed(seed)
+    for b0 in range(0, t.shape[0], 32):
+        t[b0:b0 + 32].normal_(0.0, std, generator=g)
+
+
+def _uploaded_steps(wl, dev, n):
+    import torch
+    A = torch.from_numpy(wl.A()).to(dev) if wl.shape.kind == 0 else None
+    out = []
+    for t in range(n):
+        inp = upload(wl.step(t), dev)
+        if A is not None:
+            inp["A"] = A
+        out.append(inp)
+    return out
+
+
+def conventional_decode_leg(wl, dev, K, W):
+    """The conventional read-modify-write decode step on the same GPU: the whole state is
+    read and written back every token (rs_conventional_decode_step)."""
+    import torch
+    from checkpoint_input_replay_gb300 import ConventionalLayer
+    s = wl.shape
+    layer = ConventionalLayer.for_shape(s, device=dev)
+    _random_state(layer.state, wl.s0_std, 2000)
+    steps = _uploaded_steps(wl, dev, 16)
+    y = torch.empty(s.batch, s.n_heads, s.d_head, dtype=torch.float32, device=dev)
+    elapsed, per = _timed_launches(lambda t: layer.decode_step(steps[t % 16], y), K, W, dev)
+    H, G, P, N = s.n_heads, s.n_groups, s.d_head, s.d_state
+    inputs = (H * P * 2 + H * 2 + 2 * G * N * 2) if s.kind == 0 else (2 * G * N * 2 + H * P * 2 + 2 * H * 4)
+    nbytes = s.batch * (2 * H * P * N * 4 + inputs + H * P * 4)
+    us = 1e3 * statistics.mean(per)
+    del layer, steps
+    torch.cuda.empty_cache()
+    return {"us_per_step": us, "achieved_gbs": nbytes / (us * 1e3), "bytes_per_step": nbytes,
+            "value": s.batch * K / (elapsed / 1e3), "unit": UNIT, "launches": K}
+
+
+def snapshot_leg(wl, dev, rounds, W):
+    """Snapshot-per-draft speculative verify (one state read, T = 4 snapshot writes) and
+    rollback by slot select, on the same GPU (rs_snapshot_verify / rs_snapshot_commit)."""
+    import torch
+    from checkpoint_input_replay_gb300 import SnapshotLayer
+    T = 4
+    s = wl.shape
+    layer = SnapshotLayer.for_shape(s, device=dev)
+    _random_state(layer.pool[:, 0], wl.s0_std, 3000)
+    A = torch.from_numpy(wl.A()).to(dev) if s.kind == 0 else None
+    drafts, accs = [], []
+    for r in range(4):
+        inp = upload(wl.draft(r, T), dev)
+        if A is not None:
+            inp["A"] = A
+        drafts.append(inp)
+        accs.append(torch.from_numpy(wl.accepted(r, T)).to(dev))
+    y = torch.empty(s.batch, T, s.n_heads, s.d_head, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one(r):
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        layer.verify(T, drafts[r % 4], y, stream=stream)
+        e1.record(stream)
+        layer.commit(accs[r % 4], stream=stream)
+        e2.record(stream)
+        return e0, e1, e2
+    for r in range(W):
+        one(r)
+    torch.cuda.synchronize(dev)
+    evs = [one(W + r) for r in range(rounds)]
+    torch.cuda.synchronize(dev)
+    ver = [a.elapsed_time(b) for a, b, _ in evs]
+    com = [b.elapsed_time(c) for _, b, c in evs]
+    total = evs[0][0].elapsed_time(evs[-1][2])
+    H, P, N = s.n_heads, s.d_head, s.d_state
+    vbytes = s.batch * ((1 + T) * H * P * N * 4 + T * H * P * 4)
+    assert layer.device_error() == 0
+    del layer
+    torch.cuda.empty_cache()
+    return {"verify_us": 1e3 * statistics.mean(ver), "commit_us": 1e3 * statistics.mean(com),
+            "verify_gbs": vbytes / (statistics.mean(ver) * 1e6), "round_us": 1e3 * total / rounds,
+            "tokens_per_s": s.batch * T * rounds / (total / 1e3), "rounds": rounds}
+
+
+def read_copy_error_leg(wl, dev, mode, steps):
+    """Per-window rel-L2 of the read-copy outputs against the FP32-checkpoint outputs of
+    the same kernels on the same inputs (two caches side by side; the FP32 path itself
+    matches the float64 recurrence within 2e-4 in the tests), and the non-flush launch's
+    algorithmic bytes over its time."""
+    import torch
+    s = wl.shape
+    L = s.ring_len
+    from checkpoint_input_replay_gb300 import ReplayCache
+    exact = make_cache(wl, dev, seed=7)
+    quant = ReplayCache.for_shape(s, read_mode=mode, device=dev)
+    quant.ckpt.copy_(exact.ckpt)
+    quant.flush()
+    steps_in = _uploaded_steps(wl, dev, 16)
+    y0 = torch.empty(s.batch, s.n_heads, s.d_head, dtype=torch.float32, device=dev)
+    y1 = torch.empty_like(y0)
+    nw = steps // L
+    num = torch.zeros(nw, dtype=torch.float64, device=dev)
+    den = torch.zeros(nw, dtype=torch.float64, device=dev)
+    for t in range(steps):
+        exact.decode_step(steps_in[t % 16], y0)
+        quant.decode_step(steps_in[t % 16], y1)
+        w = t // L
+        num[w] += ((y1 - y0).double() ** 2).sum()
+        den[w] += (y0.double() ** 2).sum()
+    per_window = torch.sqrt(num / den).cpu().numpy()
+    assert exact.device_error() == 0 and quant.device_error() == 0
+    del exact, quant
+    torch.cuda.empty_cache()
+    return {"per_window_rel_l2": [round(float(x), 6) for x in per_window],
+            "windows": nw, "max_window_ge1": float(per_window[1:].max()),
+            "aggregate_rel_l2": float(np.sqrt(num.sum().item() / den.sum().item())),
+            "first8_mean": float(per_window[1:9].mean()), "last8_mean": float(per_window[-8:].mean()),
+            "inputs": "16 distinct seeded input steps cycled; initial state N(0,0.1)"}
+
+
+def sweep_leg(dev, kind, batch, L, K, W, with_conventional=True):
+    """One point of the batch / window-length sweeps: the ReplaySSM decode at its natural
+    window mix and, at the same shape, the conventional decode step."""
+    import dataclasses as dc
+    from workloads import configs
+    base = configs.CONFIG1 if kind == 0 else configs.CONFIG2
+    shape = dc.replace(base, batch=batch, ring_len=L)
+    wl = configs.Mamba2Workload(shape, seed=1, s0_std=0.1) if kind == 0 else \
+        configs.GdnWorkload(shape, seed=2, s0_std=0.05)
+    r = decode_leg(wl, dev, K, W, L, m2_bytes if kind == 0 else gdn_bytes, lambda: None)
+    nat = r["natural_window"]
+    out = {"batch": batch, "L": L, "value": nat["value"], "us_per_step": nat["us_per_step"],
+           "nonflush_us": r["nonflush_us"], "flush_us": r["flush_us"], "achieved_gbs": nat["achieved_gbs"]}
+    if with_conventional:
+        c = conventional_decode_leg(wl, dev, max(K // 2, 4), 3)
+        out["conventional_us_per_step"] = c["us_per_step"]
+        out["speedup_vs_conventional"] = c["us_per_step"] / nat["us_per_step"]
+    return out
 
 
 # ----------------------------------------------------------------------------- oracle arm
@@ -429,6 +613,117 @@ def oracle_sample(wl, steps: int, seqs: list[int]):
         lay.decode(inputs[t])
     dt = time.perf_counter() - t0
     return len(seqs) * steps / dt, dt
+
+
+def _oracle_worker(args):
+    """One host process of the CPU baseline: the oracle on one sequence of the
+    config-1 workload (runs in a spawned process, one BLAS thread)."""
+    seq, steps = args
+    from workloads import configs
+    return oracle_sample(configs.config1(), steps, [seq])
+
+
+def cpu_baseline_leg(steps_single=512, steps_each=256):
+    """The float64 oracle timed on the host: one core on one sequence (>= 1 s of work),
+    then one spawned process per host core, each on its own sequence, run together."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    env_keep = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in env_keep:
+        os.environ[k] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(1) as pool:
+            rate1, secs1 = pool.map(_oracle_worker, [(0, steps_single)])[0]
+        with ctx.Pool(cores) as pool:
+            res = pool.map(_oracle_worker, [(i, steps_each) for i in range(cores)])
+    finally:
+        for k, v in env_keep.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    wall = max(r[1] for r in res)
+    return {"value": cores * steps_each / wall, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{steps_each} decode steps of each of sequences 0-{cores - 1} of the B=256 config-1 "
+                      f"workload, one float64 numpy process per host core, run together "
+                      f"(slowest process {wall:.1f} s)",
+            "single_core": {"value": rate1, "unit": UNIT, "cores": 1,
+                            "sample": f"{steps_single} decode steps of sequence 0 ({secs1:.1f} s)"}}
+
+
+def window_state_ratio(win, shape):
+    """Measured state bytes of one L = 16 window over (L + 1) |S|: the ncu DRAM bytes of the
+    window's 16 decode launches (one capture, B = win["batch"]) minus their non-state
+    algorithmic bytes (records, tokens, outputs), divided by L + 1 state reads/writes."""
+    L = shape.ring_len
+    state = shape.n_heads * shape.d_head * shape.d_state * 4
+    launches = sorted(win["launches"], key=lambda r: r["pos"])
+    dram = sum(r["dram_bytes"] for r in launches)
+    alg = sum(m2_bytes(shape, r["pos"], r["pos"] == L - 1) for r in launches) * shape.batch
+    state_alg = (L + 1) * state * shape.batch
+    return {"window_state_ratio": (dram - (alg - state_alg)) / state_alg,
+            "window_traffic_over_algorithmic": dram / alg,
+            "window_capture": f"ncu DRAM bytes of the {len(launches)} decode launches of one window at "
+                              f"B={shape.batch} ({win['summary']})"}
+
+
+def extras(line, args, dev, hbm, m2):
+    """The other legs: GDN decode, verify + commit, read copies, the conventional kernels
+    and the ratios, the batch and window-length sweeps."""
+    from workloads import configs
+    W = args.warmup
+    Kx = 64  # four windows per leg
+    with nvtx_range("decode gdn"):
+        gdn = decode_leg(configs.config2(), dev, Kx, W, 16, gdn_bytes, lambda: None)
+    line["gdn"] = {"workload": "gdn decode, 1 layer: B=256 Hv=32 Hk=16 dk=dv=128, L=16",
+                   "value": configs.config2().shape.batch * Kx / (gdn["elapsed_ms"] / 1e3),
+                   "unit": UNIT, "achieved_gbs": gdn["bytes_total"] / (gdn["launch_ms_total"] * 1e6),
+                   "nonflush_gbs": gdn["nonflush_gbs"], "flush_gbs": gdn["flush_gbs"],
+                   "nonflush_us": gdn["nonflush_us"], "flush_us": gdn["flush_us"],
+                   "frac": gdn["bytes_total"] / (gdn["launch_ms_total"] * 1e6) / hbm,
+                   "natural_window": gdn["natural_window"]}
+    with nvtx_range("verify + commit"):
+        ver = [verify_leg(configs.config3_mamba2(), dev, 64, 4, lambda: None),
+               verify_leg(configs.config3_gdn(), dev, 64, 4, lambda: None)]
+    for v in ver:
+        v["verify_frac"] = v["verify_state_gbs"] / hbm
+    line["verify"] = ver
+    rc = []
+    for mode in ("fp8", "nvfp4"):
+        with nvtx_range(f"decode read copy {mode}"):
+            r = read_copy_leg(configs.config4(), dev, mode, Kx, W)
+        r["nonflush_frac"] = r["nonflush_gbs"] / hbm
+        r["speedup_vs_fp32_nonflush"] = m2["nonflush_us"] / r["nonflush_us"]
+        with nvtx_range(f"read copy error {mode}"):
+            r["error_vs_fp32_outputs"] = read_copy_error_leg(configs.config4(), dev, mode, 4096)
+        rc.append(r)
+    line["read_copy"] = rc
+    with nvtx_range("conventional kernels"):
+        cm2 = conventional_decode_leg(configs.config1(), dev, 32, W)
+        cgdn = conventional_decode_leg(configs.config2(), dev, 32, W)
+        sm2 = snapshot_leg(configs.config3_mamba2(), dev, 32, 4)
+        sgdn = snapshot_leg(configs.config3_gdn(), dev, 32, 4)
+    for c in (cm2, cgdn):
+        c["frac"] = c["achieved_gbs"] / hbm
+    for c in (sm2, sgdn):
+        c["verify_frac"] = c["verify_gbs"] / hbm
+    line["conventional"] = {
+        "decode_mamba2": cm2, "decode_gdn": cgdn, "snapshot_spec_mamba2": sm2, "snapshot_spec_gdn": sgdn,
+        "decode_speedup_mamba2": cm2["us_per_step"] / m2["natural_window"]["us_per_step"],
+        "decode_speedup_gdn": cgdn["us_per_step"] / gdn["natural_window"]["us_per_step"],
+        "spec_speedup_mamba2": ver[0]["tokens_per_s"] / sm2["tokens_per_s"],
+        "spec_speedup_gdn": ver[1]["tokens_per_s"] / sgdn["tokens_per_s"],
+        "note": "same GPU, same shapes: decode at the natural 15:1 window mix vs the read-modify-write "
+                "step; speculative T=4 verify + commit rounds at B=512 vs snapshot-per-draft verify + "
+                "slot-select commit"}
+    with nvtx_range("batch sweep"):
+        line["batch_sweep"] = [sweep_leg(dev, 0, b, 16, 32, 16) for b in (1, 16, 64, 256, 1024)]
+    with nvtx_range("window sweep"):
+        line["window_sweep"] = [sweep_leg(dev, kind, 256, L, 2 * L, L, with_conventional=False)
+                                for kind in (0, 1) for L in (4, 8, 16, 32)]
+        for r, kind in zip(line["window_sweep"], [0] * 4 + [1] * 4):
+            r["kind"] = "mamba2" if kind == 0 else "gdn"
 
 
 # ----------------------------------------------------------------------------- main
@@ -503,6 +798,9 @@ def main(argv=None):
                     help="time only the GDN decode leg, at --batch sequences (a profiling case)")
     ap.add_argument("--read-copy-only", choices=["fp8", "nvfp4"],
                     help="time only the non-flush decode with a read copy, at --batch sequences (a profiling case)")
+    ap.add_argument("--conventional-only", choices=["mamba2", "gdn"],
+                    help="time only the conventional read-modify-write decode step, at --batch sequences "
+                         "(a profiling case)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -529,6 +827,12 @@ def main(argv=None):
             print(json.dumps({"gdn": {"batch": args.batch, "nonflush_us": r["nonflush_us"], "flush_us": r["flush_us"],
                                       "nonflush_gbs": r["nonflush_gbs"], "launches": r["launches"]}}))
         return 0
+    if args.conventional_only:
+        wl = (configs.config1 if args.conventional_only == "mamba2" else configs.config2)(batch=args.batch)
+        res = conventional_decode_leg(wl, dev, args.steps, args.warmup)
+        if rank == 0:
+            print(json.dumps({"conventional": res}))
+        return 0
     if args.read_copy_only:
         res = read_copy_leg(configs.config1(batch=args.batch), dev, args.read_copy_only, args.steps, args.warmup)
         if rank == 0:
@@ -551,55 +855,40 @@ def main(argv=None):
 
     hbm, peak_kind = peaks()
     achieved = m2["bytes_total"] / (m2["launch_ms_total"] * 1e6)
-    tr = ncu_traffic("decode_mamba2_b256") if wl1.shape.batch == 256 else None
-    traffic = tr[0] if tr else None
+    tr = ncu_record("decode_mamba2_b256") if wl1.shape.batch == 256 else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": traffic, "peak_kind": peak_kind,
+                "traffic": tr["traffic_bytes_per_launch"] if tr else None, "peak_kind": peak_kind,
                 "nonflush_gbs": m2["nonflush_gbs"], "nonflush_frac": m2["nonflush_gbs"] / hbm,
                 "flush_gbs": m2["flush_gbs"], "nonflush_us": m2["nonflush_us"], "flush_us": m2["flush_us"]}
     if tr:
         # a non-flush launch: DRAM bytes (ncu) over the algorithmic bytes of the same launch
-        roofline["traffic_launch"] = "non-flush, window position 6-7, scaled from a B=64 capture"
-        roofline["traffic_over_algorithmic"] = tr[0] / tr[1]
+        roofline["traffic_launch"] = tr["launch"]
+        roofline["traffic_over_algorithmic"] = tr["traffic_bytes_per_launch"] / tr["algorithmic_bytes_per_launch"]
+    win = ncu_record("decode_mamba2_window_b64")
+    if win:
+        roofline.update(window_state_ratio(win, configs.CONFIG1.with_batch(win["batch"])))
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": elapsed / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": "mamba2 decode, 1 layer: B=256 nheads=128 headdim=64 dstate=128 ngroups=8, "
                                    "FP32 checkpoint, bf16 x/dt/B/C, L=16 (15 non-flush + 1 flush per window)",
                        "batch_per_gpu": wl1.shape.batch, "global_batch": world * wl1.shape.batch, "ring_len": 16,
+                       "timed_launches": K, "flush_launches_timed": m2["flush_launches"],
                        "l2": "no flush: the %d MiB state per step exceeds the 129 MB L2" % (wl1.shape.batch * 4),
                        "inputs": "16 distinct seeded input steps resident in HBM, cycled; initial state N(0,0.1)"},
+            "natural_window": m2["natural_window"],
             "roofline": roofline, "gpu_launches": m2["launches"], "clocks": clk.summary(),
             "device_error": m2["device_error"]}
     if rank == 0 and args.decode_only:
         print(json.dumps(line), flush=True)
     elif rank == 0:
         with nvtx_range("decode mamba2 from host buffers"):
-            line["e2e"] = e2e_leg(wl1, dev, min(K, 320), W)
-        rate, secs = oracle_sample(wl1, 8, [0, 1])
-        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                "sample": "8 decode steps of sequences 0-1 of the B=256 workload "
-                                          f"(float64 numpy, one thread, {secs:.1f} s)"}
+            line["e2e"] = e2e_leg(wl1, dev, E2E_STEPS, W)
+        line["e2e"]["steps"] = E2E_STEPS
+        if world == 1:
+            line["cpu_baseline"] = cpu_baseline_leg()
         if not args.no_extra:
-            with nvtx_range("decode gdn"):
-                gdn = decode_leg(configs.config2(), dev, min(K, 1600), W, 16, gdn_bytes, lambda: None)
-            line["gdn"] = {"workload": "gdn decode, 1 layer: B=256 Hv=32 Hk=16 dk=dv=128, L=16",
-                           "value": configs.config2().shape.batch * min(K, 1600) / (gdn["elapsed_ms"] / 1e3),
-                           "unit": UNIT, "achieved_gbs": gdn["bytes_total"] / (gdn["launch_ms_total"] * 1e6),
-                           "nonflush_gbs": gdn["nonflush_gbs"], "flush_gbs": gdn["flush_gbs"],
-                           "nonflush_us": gdn["nonflush_us"], "flush_us": gdn["flush_us"],
-                           "frac": gdn["bytes_total"] / (gdn["launch_ms_total"] * 1e6) / hbm}
-            with nvtx_range("verify + commit"):
-                line["verify"] = [verify_leg(configs.config3_mamba2(), dev, 64, 4, lambda: None),
-                                  verify_leg(configs.config3_gdn(), dev, 64, 4, lambda: None)]
-            rc = []
-            for mode in ("fp8", "nvfp4"):
-                try:
-                    with nvtx_range(f"decode read copy {mode}"):
-                        rc.append(read_copy_leg(configs.config4(), dev, mode, min(K, 1600), W))
-                except Exception as e:  # read copy reported as missing, not silently dropped
-                    rc.append({"mode": mode, "error": str(e).splitlines()[0]})
-            line["read_copy"] = rc
+            extras(line, args, dev, hbm, m2)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -36,7 +36,8 @@ RS_DEVERR_TIMEOUT = 3
 EXPORTED = ("rs_query_sizes", "rs_create_cache", "rs_destroy_cache", "rs_decode_step", "rs_verify",
             "rs_commit", "rs_flush", "rs_get_device_error", "rs_status_string", "rs_decode_step_noalloc",
             "rs_selftest_wait_timeout", "rs_pipe_create", "rs_pipe_decode_step", "rs_pipe_sync",
-            "rs_pipe_destroy")
+            "rs_pipe_destroy", "rs_conventional_decode_step", "rs_snapshot_query_sizes", "rs_snapshot_verify",
+            "rs_snapshot_commit", "rs_verify_tree", "rs_commit_path")
 
 
 class rs_config(ctypes.Structure):
@@ -77,6 +78,9 @@ def load() -> ctypes.CDLL:
         lib.rs_decode_step.argtypes = [vp, ctypes.POINTER(rs_inputs), vp, vp]
         lib.rs_verify.argtypes = [vp, ctypes.c_int32, ctypes.POINTER(rs_inputs), vp, vp]
         lib.rs_commit.argtypes = [vp, vp, vp]
+        lib.rs_verify_tree.argtypes = [vp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(rs_inputs),
+                                       vp, vp]
+        lib.rs_commit_path.argtypes = [vp, vp, vp, vp]
         lib.rs_flush.argtypes = [vp, vp, vp]
         lib.rs_get_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
         lib.rs_selftest_wait_timeout.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), vp]
@@ -87,6 +91,12 @@ def load() -> ctypes.CDLL:
         lib.rs_pipe_sync.argtypes = [vp, vp]
         lib.rs_pipe_destroy.argtypes = [vp]
         lib.rs_pipe_destroy.restype = None
+        lib.rs_conventional_decode_step.argtypes = [ctypes.POINTER(rs_config), vp, ctypes.POINTER(rs_inputs), vp,
+                                                    vp]
+        lib.rs_snapshot_query_sizes.argtypes = [ctypes.POINTER(rs_config), sz]
+        lib.rs_snapshot_verify.argtypes = [ctypes.POINTER(rs_config), vp, vp, ctypes.c_int32,
+                                           ctypes.POINTER(rs_inputs), vp, vp]
+        lib.rs_snapshot_commit.argtypes = [ctypes.POINTER(rs_config), vp, vp, ctypes.c_int32, vp]
         lib.rs_status_string.argtypes = [ctypes.c_int]
         lib.rs_status_string.restype = ctypes.c_char_p
         for name in EXPORTED:
@@ -137,6 +147,18 @@ def rs_commit(handle, accepted_ptr: int, stream: int) -> int:
     return load().rs_commit(handle, ctypes.c_void_p(accepted_ptr), ctypes.c_void_p(stream))
 
 
+def rs_verify_tree(handle, T: int, parents, inputs: rs_inputs, y_ptr: int, stream: int) -> int:
+    """parents: T ints (host), parents[tau] in -1..tau-1."""
+    arr = (ctypes.c_int32 * max(len(parents), 1))(*[int(p) for p in parents])
+    return load().rs_verify_tree(handle, int(T), arr, ctypes.byref(inputs), ctypes.c_void_p(y_ptr),
+                                 ctypes.c_void_p(stream))
+
+
+def rs_commit_path(handle, path_len_ptr: int, path_ptr: int, stream: int) -> int:
+    return load().rs_commit_path(handle, ctypes.c_void_p(path_len_ptr), ctypes.c_void_p(path_ptr),
+                                 ctypes.c_void_p(stream))
+
+
 def rs_flush(handle, mask_ptr: int | None, stream: int) -> int:
     return load().rs_flush(handle, ctypes.c_void_p(mask_ptr or 0), ctypes.c_void_p(stream))
 
@@ -183,3 +205,28 @@ def rs_pipe_sync(pipe, stream: int) -> int:
 
 def rs_pipe_destroy(pipe) -> None:
     load().rs_pipe_destroy(pipe)
+
+
+# --- the conventional path (comparison) ------------------------------------------
+
+def rs_conventional_decode_step(cfg: rs_config, state_ptr: int, inputs: rs_inputs, y_ptr: int, stream: int) -> int:
+    return load().rs_conventional_decode_step(ctypes.byref(cfg), ctypes.c_void_p(state_ptr), ctypes.byref(inputs),
+                                              ctypes.c_void_p(y_ptr), ctypes.c_void_p(stream))
+
+
+def rs_snapshot_query_sizes(cfg: rs_config):
+    """Returns (status, [pool, slots] bytes)."""
+    out = (ctypes.c_size_t * 2)()
+    st = load().rs_snapshot_query_sizes(ctypes.byref(cfg), out)
+    return st, list(out)
+
+
+def rs_snapshot_verify(cfg: rs_config, pool_ptr: int, slots_ptr: int, T: int, inputs: rs_inputs, y_ptr: int,
+                       stream: int) -> int:
+    return load().rs_snapshot_verify(ctypes.byref(cfg), ctypes.c_void_p(pool_ptr), ctypes.c_void_p(slots_ptr),
+                                     int(T), ctypes.byref(inputs), ctypes.c_void_p(y_ptr), ctypes.c_void_p(stream))
+
+
+def rs_snapshot_commit(cfg: rs_config, slots_ptr: int, accepted_ptr: int, T: int, stream: int) -> int:
+    return load().rs_snapshot_commit(ctypes.byref(cfg), ctypes.c_void_p(slots_ptr), ctypes.c_void_p(accepted_ptr),
+                                     int(T), ctypes.c_void_p(stream))

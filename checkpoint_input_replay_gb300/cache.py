@@ -26,6 +26,28 @@ def _a256(x: int) -> int:
     return (x + 255) & ~255
 
 
+def marshal_inputs(kind: int, H: int, G: int, P: int, N: int, inputs: dict, lead: tuple, device) -> _lib.rs_inputs:
+    """rs_inputs for one call's token tensors (checked: dtype, shape, contiguity, device)."""
+    if kind == _lib.RS_MAMBA2:
+        spec = {"x": (torch.bfloat16, lead + (H, P)), "dt": (torch.bfloat16, lead + (H,)),
+                "A": (torch.float32, (H,)), "B": (torch.bfloat16, lead + (G, N)),
+                "C": (torch.bfloat16, lead + (G, N))}
+    else:
+        spec = {"q": (torch.bfloat16, lead + (G, N)), "k": (torch.bfloat16, lead + (G, N)),
+                "v": (torch.bfloat16, lead + (H, P)), "g": (torch.float32, lead + (H,)),
+                "beta": (torch.float32, lead + (H,))}
+    ptrs = {}
+    for name, (dtype, shape) in spec.items():
+        t = inputs[name]
+        if t.dtype != dtype or tuple(t.shape) != shape or not t.is_contiguous() or t.device != device:
+            raise ValueError(f"input {name}: want contiguous {dtype} {shape} on {device}, "
+                             f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+        ptrs[name] = t.data_ptr()
+    if kind == _lib.RS_MAMBA2:
+        return _lib.rs_inputs(ptrs["x"], ptrs["dt"], ptrs["A"], ptrs["B"], ptrs["C"], None, None, None, None, None)
+    return _lib.rs_inputs(None, None, None, None, None, ptrs["q"], ptrs["k"], ptrs["v"], ptrs["g"], ptrs["beta"])
+
+
 class ReplayCache:
     """A ReplaySSM cache for one layer.
 
@@ -131,27 +153,7 @@ class ReplayCache:
 
     def _inputs(self, inputs: dict, lead: tuple, device=None) -> _lib.rs_inputs:
         device = self.device if device is None else device
-        B, H, G, P, N = self.B, self.H, self.G, self.P, self.N
-        if self.kind == _lib.RS_MAMBA2:
-            spec = {"x": (torch.bfloat16, lead + (H, P)), "dt": (torch.bfloat16, lead + (H,)),
-                    "A": (torch.float32, (H,)), "B": (torch.bfloat16, lead + (G, N)),
-                    "C": (torch.bfloat16, lead + (G, N))}
-        else:
-            spec = {"q": (torch.bfloat16, lead + (G, N)), "k": (torch.bfloat16, lead + (G, N)),
-                    "v": (torch.bfloat16, lead + (H, P)), "g": (torch.float32, lead + (H,)),
-                    "beta": (torch.float32, lead + (H,))}
-        ptrs = {}
-        for name, (dtype, shape) in spec.items():
-            t = inputs[name]
-            if t.dtype != dtype or tuple(t.shape) != shape or not t.is_contiguous() or t.device != device:
-                raise ValueError(f"input {name}: want contiguous {dtype} {shape} on {device}, "
-                                 f"got {t.dtype} {tuple(t.shape)} on {t.device}")
-            ptrs[name] = t.data_ptr()
-        if self.kind == _lib.RS_MAMBA2:
-            return _lib.rs_inputs(ptrs["x"], ptrs["dt"], ptrs["A"], ptrs["B"], ptrs["C"], None, None, None, None,
-                                  None)
-        return _lib.rs_inputs(None, None, None, None, None, ptrs["q"], ptrs["k"], ptrs["v"], ptrs["g"],
-                              ptrs["beta"])
+        return marshal_inputs(self.kind, self.H, self.G, self.P, self.N, inputs, lead, device)
 
     def decode_step(self, inputs: dict, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
         """One decode token per sequence; returns y f32 [B][H][P]."""
@@ -168,6 +170,27 @@ class ReplayCache:
         check(_lib.rs_verify(self.handle, T, self._inputs(inputs, (self.B, T)), y.data_ptr(), self._stream(stream)),
               "rs_verify")
         return y
+
+    def verify_tree(self, T: int, parents, inputs: dict, y: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+        """Tree-shaped drafts (draft tau continues draft parents[tau], -1 = the committed
+        records); y f32 [B][T][H][P]; commit_path (or, for a chain, commit) must follow."""
+        if y is None:
+            y = torch.empty(self.B, T, self.H, self.P, dtype=torch.float32, device=self.device)
+        check(_lib.rs_verify_tree(self.handle, T, list(parents), self._inputs(inputs, (self.B, T)), y.data_ptr(),
+                                  self._stream(stream)), "rs_verify_tree")
+        return y
+
+    def commit_path(self, path_len: torch.Tensor, path: torch.Tensor, stream=None) -> None:
+        """path_len int32 [B], path int32 [B][T_max] on the device: each sequence's accepted
+        root-to-draft path of the pending verify."""
+        if path_len.dtype != torch.int32 or tuple(path_len.shape) != (self.B,) or path_len.device != self.device:
+            raise ValueError("path_len must be int32 [B] on the cache's device")
+        if path.dtype != torch.int32 or tuple(path.shape) != (self.B, self.T_max) or path.device != self.device \
+                or not path.is_contiguous():
+            raise ValueError("path must be contiguous int32 [B][T_max] on the cache's device")
+        check(_lib.rs_commit_path(self.handle, path_len.data_ptr(), path.data_ptr(), self._stream(stream)),
+              "rs_commit_path")
 
     def commit(self, accepted: torch.Tensor, stream=None) -> None:
         """accepted: int32 [B] on the device."""

@@ -15,6 +15,8 @@ struct rs_cache {
   rs_config cfg;
   rs::LayerDev dev;
   int pending;    // drafts appended by the last rs_verify and not yet committed
+  uint32_t pending_parents;  // their tree: parent + 1 of draft tau in byte tau
+  bool pending_chain;        // the pending drafts form a chain (a prefix commit applies)
   bool map_ok;
 };
 
@@ -325,6 +327,8 @@ rs_status rs_create_cache(const rs_config* cfg, const rs_buffers* bufs, rs_cache
   h->cfg = *cfg;
   h->dev = d;
   h->pending = 0;
+  h->pending_parents = 0;
+  h->pending_chain = true;
   h->map_ok = rs::verify128_supports(d) && rs::make_ckpt_tmap(d, &h->ckpt_map) == cudaSuccess;
   *out = h;
   return RS_OK;
@@ -481,25 +485,82 @@ void rs_pipe_destroy(rs_pipe* p) {
   pipe_free(p);
 }
 
-rs_status rs_verify(rs_cache* h, int32_t T, const rs_inputs* in, float* y, rs_stream stream) {
+namespace {
+
+// Ancestor mask and packed parents of a draft tree (parents[tau] in -1..tau-1);
+// false for an invalid tree.
+bool tree_of(int T, const int32_t* parents, uint32_t* anc, uint32_t* packed, bool* chain) {
+  *anc = 0;
+  *packed = 0;
+  *chain = true;
+  for (int tau = 0; tau < T; ++tau) {
+    const int p = parents[tau];
+    if (p < -1 || p >= tau) return false;
+    *chain = *chain && p == tau - 1;
+    *packed |= static_cast<uint32_t>(p + 1) << (8 * tau);
+    uint32_t row = 1u << tau;  // tau itself
+    if (p >= 0) row |= (*anc >> (4 * p)) & 0xFu;
+    *anc |= row << (4 * tau);
+  }
+  return true;
+}
+
+rs_status verify_with_tree(rs_cache* h, int32_t T, const int32_t* parents, const rs_inputs* in, float* y,
+                           rs_stream stream) {
   if (!h || !y) return RS_ERR_NULL;
   if (T < 1 || T > h->cfg.max_draft) return RS_ERR_RANGE;
+  uint32_t anc = 0, packed = 0;
+  bool chain = true;
+  if (!tree_of(T, parents, &anc, &packed, &chain)) return RS_ERR_RANGE;
   const rs_status st = check_inputs(h, in);
   if (st != RS_OK) return st;
   if (!aligned16(y)) return RS_ERR_ALIGN;
   if (h->pending) return RS_ERR_STATE;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const cudaError_t e = h->map_ok ? rs::launch_verify128(h->dev, h->ckpt_map, token_in(in), T, y, s)
-                                  : rs::launch_verify(h->dev, token_in(in), T, y, s);
+  rs::LayerDev d = h->dev;
+  d.tree_anc = anc;
+  const cudaError_t e = h->map_ok ? rs::launch_verify128(d, h->ckpt_map, token_in(in), T, y, s)
+                                  : rs::launch_verify(d, token_in(in), T, y, s);
   if (e != cudaSuccess) return RS_ERR_CUDA;
   h->pending = T;
+  h->pending_parents = packed;
+  h->pending_chain = chain;
+  return RS_OK;
+}
+
+}  // namespace
+
+rs_status rs_verify(rs_cache* h, int32_t T, const rs_inputs* in, float* y, rs_stream stream) {
+  const int32_t chain[4] = {-1, 0, 1, 2};
+  return verify_with_tree(h, T, chain, in, y, stream);
+}
+
+rs_status rs_verify_tree(rs_cache* h, int32_t T, const int32_t* parents, const rs_inputs* in, float* y,
+                         rs_stream stream) {
+  if (!parents) return RS_ERR_NULL;
+  return verify_with_tree(h, T, parents, in, y, stream);
+}
+
+rs_status rs_commit_path(rs_cache* h, const int32_t* path_len, const int32_t* path, rs_stream stream) {
+  if (!h || !path_len || !path) return RS_ERR_NULL;
+  if (!aligned16(path_len) || !aligned16(path)) return RS_ERR_ALIGN;
+  if (!h->pending) return RS_ERR_STATE;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the accepted counts the commit launch applies live in the verify-table scratch,
+  // which only rs_verify uses
+  int* acc = reinterpret_cast<int*>(h->dev.vtab);
+  cudaError_t e = rs::launch_tree_compact(h->dev, path_len, path, h->cfg.max_draft, h->pending,
+                                          h->pending_parents, acc, s);
+  if (e == cudaSuccess) e = rs::launch_fold(h->dev, rs::FOLD_COMMIT, acc, nullptr, h->pending, s);
+  if (e != cudaSuccess) return RS_ERR_CUDA;
+  h->pending = 0;
   return RS_OK;
 }
 
 rs_status rs_commit(rs_cache* h, const int32_t* accepted, rs_stream stream) {
   if (!h || !accepted) return RS_ERR_NULL;
   if (!aligned16(accepted)) return RS_ERR_ALIGN;
-  if (!h->pending) return RS_ERR_STATE;
+  if (!h->pending || !h->pending_chain) return RS_ERR_STATE;
   const cudaError_t e = rs::launch_fold(h->dev, rs::FOLD_COMMIT, accepted, nullptr, h->pending,
                                         reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return RS_ERR_CUDA;

@@ -105,6 +105,12 @@ __device__ __forceinline__ float4 scale4(float a, const float4 x) {
   return make_float4(a * x.x, a * x.y, a * x.z, a * x.w);
 }
 
+// Draft sigma lies on the path from the committed records to draft tau (tau
+// itself included) in the ancestor mask of a verify (bit 4 tau + sigma).
+__device__ __forceinline__ bool on_tree_path(uint32_t anc, int tau, int sigma) {
+  return sigma >= 0 && sigma < 4 && tau >= 0 && tau < 4 && ((anc >> (4 * tau + sigma)) & 1u) != 0;
+}
+
 // ---- error word and cursor bookkeeping -------------------------------------
 
 __device__ __forceinline__ void report_error(int* err, int code, int seq) {

@@ -48,6 +48,10 @@ struct LayerDev {
   float* rc_matscale;          // NVFP4: [B][H]
   // verify coefficient tables (scratch): f32 [B][H][verify_table_stride]
   float* vtab;
+  // verify: the drafts' tree as an ancestor mask, bit 4 tau + sigma set when draft
+  // sigma lies on the path from the committed records to draft tau (sigma = tau
+  // included); chain-shaped drafts have every bit with sigma <= tau.  Set per call.
+  uint32_t tree_anc;
 };
 
 struct TokenIn {
@@ -88,6 +92,14 @@ int verify_table_stride(int kind, int C);
 cudaError_t make_ckpt_tmap(const LayerDev& d, CUtensorMap* out);
 cudaError_t launch_verify128(const LayerDev& d, const CUtensorMap& tmap, const TokenIn& in, int T, float* y,
                              cudaStream_t s);
+
+// Tree speculative commit: move the records of each sequence's accepted path
+// (drafts path[b][0..len) of the pending verify, whose parents are packed one
+// byte each, parent + 1, in `parents`) to the slots right after the committed
+// records, and write the accepted count the commit launch then applies (the
+// path length, or -1 for a path that is not one, which that launch reports).
+cudaError_t launch_tree_compact(const LayerDev& d, const int* path_len, const int* path, int path_stride,
+                                int T_pending, uint32_t parents, int* accepted_out, cudaStream_t s);
 
 // smallest m' >= m coprime with g (a CTA permutation multiplier); 0 stays 0
 inline int coprime_mult(int m, int g) {

@@ -13,6 +13,8 @@
 // instead (kNoAllocMaxBatch int32 = 64 KiB, held by every GPU that loads the
 // library until the process exits) and allocates nothing: no cudaMalloc, no
 // cudaFree, no allocating library routine.
+#include <stdlib.h>
+
 #include <mutex>
 
 #include "internal.h"
@@ -28,24 +30,47 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) int g_noalloc_arrive[kNoAllocMaxBatch];
 
 struct DeviceScratch {
-  int* addr = nullptr;  // device address of g_noalloc_arrive on this device
+  int* addr = nullptr;        // device address of g_noalloc_arrive on this device
+  CUcontext ctx = nullptr;    // the context that address belongs to
   bool ready = false;
 };
 
 DeviceScratch g_devices[kMaxDevices];
 std::mutex g_mutex;
 
-// Once per device, with that device current: resolve the array's device address.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// The driver's cuCtxGetCurrent, found once through the runtime (no link to libcuda).
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult qr{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &qr) != cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(f);
+  }();
+  return fn;
+}
+
+// Once per device (and again if the device's context was replaced, e.g. after a
+// cudaDeviceReset), with that device current: resolve the array's device address.
 rs_status scratch_for_current_device(int** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RS_ERR_CUDA;
+  CUcontext ctx = nullptr;
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceScratch& s = g_devices[dev];
+  const CtxGetCurrentFn get = ctx_get_current();
+  if (s.ready && get && (get(&ctx) != CUDA_SUCCESS || ctx != s.ctx)) s.ready = false;
   if (!s.ready) {
     int* ptr = nullptr;
     if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_arrive) != cudaSuccess || !ptr)
       return RS_ERR_CUDA;
+    ctx = nullptr;
+    if (get && get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
     s.addr = ptr;
+    s.ctx = ctx;
     s.ready = true;
   }
   *out = s.addr;
@@ -61,6 +86,8 @@ extern "C" rs_status rs_decode_step_noalloc(const rs_config* cfg, const rs_buffe
   rs::LayerDev d{};
   rs_status st = rs::bind_layer(cfg, bufs, false, &d);
   if (st != RS_OK) return st;
+  // the same debug ordering check as rs_create_cache (see the header)
+  if (const char* e = getenv("RS_DEBUG_CTA_PERMUTE")) d.cta_mult = atoi(e) >= 2 ? atoi(e) : 0;
   rs::TokenIn tok{};
   st = rs::bind_inputs(cfg->kind, in, &tok);
   if (st != RS_OK) return st;

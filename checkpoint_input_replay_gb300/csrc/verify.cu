@@ -394,13 +394,15 @@ __global__ void __launch_bounds__(kVerifyThreads, 1) verify_kernel(const LayerDe
         const size_t idx_l = (static_cast<size_t>(v.b) * T + (dl >= 0 && dl < T ? dl : 0)) * H + v.h;
         la_d = chunk[(dl >= 0 && dl < T ? dl : 0) * 4 + (idx_l & 3)];
       }
-      const float lj = lane < n ? la_slot[lane < n ? ring_slot(v.head, lane, C) : 0] : (lane <= last ? la_d : 0.f);
+      // records on draft tau's path: the committed ones, then tau's ancestors and tau
+      const bool onp = lane < n || on_tree_path(d.tree_anc, tau, dl);
+      const float lj = lane < n ? la_slot[lane < n ? ring_slot(v.head, lane, C) : 0] : (onp ? la_d : 0.f);
       const float vq = suffix_sum(lj, lane, last);
       const float exq = __shfl_down_sync(0xffffffffu, vq, 1);
       if (lane <= last) tW[lane * kTMax + tau] = expf(lane < last ? exq : 0.f);
       if (lane == 0) tS[tau] = expf(vq);  // D (Mamba-2) / G2 (GDN)
       if (KIND == 1) {
-        const float vk = suffix_sum(lane < last ? lj : 0.f, lane, last - 1);
+        const float vk = suffix_sum((onp && dl != tau) ? lj : 0.f, lane, last - 1);
         const float exk = __shfl_down_sync(0xffffffffu, vk, 1);
         if (lane < last) tWk[lane * kTMax + tau] = expf(lane + 1 < last ? exk : 0.f);
         if (lane == 0) {
@@ -423,7 +425,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 1) verify_kernel(const LayerDe
           const size_t idx = (static_cast<size_t>(v.b) * T + (j - n)) * H + v.h;
           dtj = bf(reinterpret_cast<const uint16_t*>(st + SL.chunk)[(j - n) * 8 + (idx & 7)]);
         }
-        tC1[e] = j <= n + tau ? tW[e] * tD[e] * dtj : 0.f;
+        tC1[e] = (j < n || on_tree_path(d.tree_anc, tau, j - n)) ? tW[e] * tD[e] * dtj : 0.f;
       } else if (j < n) {
         tC1[e] = tWk[e] * tDk[e];  // coefficient of u_j[r] in S k_tau
         tC2[e] = tW[e] * tD[e];    // coefficient of u_j[r] in S q_tau
@@ -432,10 +434,10 @@ __global__ void __launch_bounds__(kVerifyThreads, 1) verify_kernel(const LayerDe
     if (KIND == 1 && t < kTMax * kTMax) {
       const int tau = t / kTMax, sg = t - tau * kTMax;
       const int j = n + sg;
-      tM[t] = (tau < T && sg < tau) ? tS[3 * kTMax + tau] * tS[2 * kTMax + tau] * tWk[j * kTMax + tau] *
+      tM[t] = (tau < T && sg != tau && on_tree_path(d.tree_anc, tau, sg)) ? tS[3 * kTMax + tau] * tS[2 * kTMax + tau] * tWk[j * kTMax + tau] *
                                           tDk[j * kTMax + tau]
                                     : 0.f;
-      tQd[t] = (tau < T && sg <= tau) ? tW[j * kTMax + tau] * tD[j * kTMax + tau] : 0.f;
+      tQd[t] = (tau < T && on_tree_path(d.tree_anc, tau, sg)) ? tW[j * kTMax + tau] * tD[j * kTMax + tau] : 0.f;
     }
     compute_sync();
     // per-row buffered terms

@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kPrepThreads, 8) verify_prep_kernel(const Laye
         const float dtj = px[hb];
         float v[kT];
 #pragma unroll
-        for (int tau = 0; tau < kT; ++tau) v[tau] = lane <= n + tau ? lj : 0.f;
+        for (int tau = 0; tau < kT; ++tau) v[tau] = (lane < n || on_tree_path(d.tree_anc, tau, sigma)) ? lj : 0.f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
 #pragma unroll
@@ -241,7 +241,8 @@ __global__ void __launch_bounds__(kPrepThreads, 8) verify_prep_kernel(const Laye
         for (int tau = 0; tau < kT; ++tau) {
           // w_j = prod_{i=j+1..n+tau} a_i, D = prod_{i<=n+tau} a_i
           const float ex = __shfl_down_sync(0xffffffffu, v[tau], 1);
-          const float W = lane <= n + tau ? expf(lane < n + tau ? ex : 0.f) : 0.f;
+          const bool onp = lane < n || on_tree_path(d.tree_anc, tau, sigma);  // record on draft tau's path
+          const float W = onp ? expf(lane < n + tau ? ex : 0.f) : 0.f;
           c1[tau] = tau < T ? W * dq[tau] * dtj : 0.f;
           Dv[tau] = tau < T ? expf(__shfl_sync(0xffffffffu, v[tau], 0)) : 0.f;
         }
@@ -259,8 +260,10 @@ __global__ void __launch_bounds__(kPrepThreads, 8) verify_prep_kernel(const Laye
         float vq[kT], vk[kT];
 #pragma unroll
         for (int tau = 0; tau < kT; ++tau) {
-          vq[tau] = lane <= n + tau ? lj : 0.f;
-          vk[tau] = lane < n + tau ? lj : 0.f;
+          // records on draft tau's path (vq: tau included; vk: before tau)
+          const bool onp = lane < n || on_tree_path(d.tree_anc, tau, sigma);
+          vq[tau] = onp ? lj : 0.f;
+          vk[tau] = (onp && sigma != tau) ? lj : 0.f;
         }
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -292,8 +295,9 @@ __global__ void __launch_bounds__(kPrepThreads, 8) verify_prep_kernel(const Laye
           c1[tau] = (live && lane < n) ? tWk * dk[tau] : 0.f;  // coefficient of u_j[r] in S k_tau
           c2[tau] = (live && lane < n) ? tW * dq[tau] : 0.f;   // coefficient of u_j[r] in S q_tau
           // lane n + s: M[tau][s] (s < tau), Qd[tau][s] (s <= tau)
-          Mv[tau] = (live && is_draft && sigma < tau) ? b_t[tau] * a_t[tau] * tWk * dk[tau] : 0.f;
-          Qv[tau] = (live && is_draft && sigma <= tau) ? tW * dq[tau] : 0.f;
+          const bool anc = is_draft && on_tree_path(d.tree_anc, tau, sigma);
+          Mv[tau] = (live && anc && sigma != tau) ? b_t[tau] * a_t[tau] * tWk * dk[tau] : 0.f;
+          Qv[tau] = (live && anc) ? tW * dq[tau] : 0.f;
         }
         if (lane < n) {
           reinterpret_cast<float4*>(co)[lane] = make_float4(c1[0], c1[1], c1[2], c1[3]);

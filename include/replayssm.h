@@ -31,9 +31,9 @@
  *   on one cache must not overlap in time (use one stream, or order them).
  * - bf16 = IEEE bfloat16 bit patterns (uint16); f32 = float.
  * - Environment (debug only): RS_DEBUG_CTA_PERMUTE=<m>, m >= 2, read by
- *   rs_create_cache, permutes which CTA of the persistent decode and commit
- *   launches takes which range of work (an ordering check); results do not
- *   change.  Unset in normal use.
+ *   rs_create_cache and by every rs_decode_step_noalloc call, permutes which
+ *   CTA of the persistent decode and commit launches takes which range of
+ *   work (an ordering check); results do not change.  Unset in normal use.
  * - Kernels never trap.  A problem found on the device (corrupt cursor,
  *   accepted count out of range, a staged copy that did not arrive in time)
  *   sets a sticky device error word and leaves that sequence untouched;
@@ -154,13 +154,23 @@ typedef struct {
 
 typedef struct rs_cache rs_cache;
 
-/* Byte sizes of ckpt, ring, cursor, read_copy, scratch for this config.
+/* Byte sizes of ckpt, ring, cursor, read_copy, scratch for this config: the
+ * high-precision checkpoint plus the per-layer ring of the last L input
+ * records that the method keeps instead of a per-token state ("ReplaySSM
+ * caches SSM inputs..." (richland.au), "What shipped", the paragraph on
+ * unrolling the recurrence: a checkpoint and a 16-record buffer per layer;
+ * ai-jitan-hub.com, "ReplaySSMは何をする手法か", first bullet), with room for
+ * T_max draft records after the committed ones ("What shipped", the paragraph
+ * on speculative decoding: drafts are appended to the input buffer).
  * Pure host call.  RS_ERR_SHAPE / RS_ERR_RANGE for invalid configs,
  * RS_ERR_UNSUPPORTED for valid configs outside the built kernels. */
 rs_status rs_query_sizes(const rs_config *cfg, size_t bytes[5]);
 
 /* Bind a config to caller-owned buffers and zero the cursor, the error word
- * and the arrival counters (synchronously, on the legacy default stream).
+ * and the arrival counters (synchronously, on the legacy default stream):
+ * an empty ring whose pointer starts at slot 0 ("ReplaySSM caches SSM
+ * inputs..." (richland.au), "What shipped": the buffer holds the inputs since
+ * the checkpoint and is addressed through a pointer, like a KV cache).
  * The checkpoint is not touched.  With a read copy, call rs_flush once after
  * the initial checkpoint is written so that the copy is quantised from it. */
 rs_status rs_create_cache(const rs_config *cfg, const rs_buffers *bufs, rs_cache **out);
@@ -189,8 +199,8 @@ rs_status rs_decode_step(rs_cache *cache, const rs_inputs *in, float *y, rs_stre
  * position and W the causally masked decay matrix; K^T Q is formed once per
  * group.  The cursor does not move ("ReplaySSM caches SSM inputs..."
  * (richland.au), "What shipped", the paragraphs on speculative decoding).
- * Exactly one rs_commit must follow before the next decode, verify or flush
- * (RS_ERR_STATE otherwise). */
+ * Exactly one rs_commit (or rs_commit_path) must follow before the next
+ * decode, verify or flush (RS_ERR_STATE otherwise). */
 rs_status rs_verify(rs_cache *cache, int32_t T, const rs_inputs *in, float *y, rs_stream stream);
 
 /* Commit accepted[b] (device int32 [B], 0 <= accepted[b] <= T of the pending
@@ -199,15 +209,52 @@ rs_status rs_verify(rs_cache *cache, int32_t T, const rs_inputs *in, float *y, r
  * reaches L or more is folded in the same launch (all its records), written
  * once, and its cursor moves to head += count, count = 0.  An out-of-range
  * accepted[b] sets RS_DEVERR_ACCEPTED and leaves that sequence unchanged.
- * RS_ERR_STATE if no verify is pending. */
+ * The accepted prefix is committed by moving the ring pointer, with no state
+ * snapshot; records past it are ignored and later overwritten ("ReplaySSM
+ * caches SSM inputs..." (richland.au), "What shipped", the paragraph on the
+ * second benefit for speculative decoding; ai.warp-studio.com,
+ * "推測デコーディングにおける革新と実装詳細").
+ * RS_ERR_STATE if no verify is pending, or if the pending drafts are a tree
+ * that is not a chain (use rs_commit_path). */
 rs_status rs_commit(rs_cache *cache, const int32_t *accepted, rs_stream stream);
+
+/* Tree-shaped speculative verification: as rs_verify, but draft tau continues
+ * draft parents[tau] (host int32 [T], parents[tau] in -1..tau-1, -1 = the last
+ * committed record; one tree for the whole batch).  Each draft's output is the
+ * recurrence along its own path from the committed state: in the chunkwise
+ * form, W and the Gated DeltaNet T x T system keep only the records on that
+ * path.  Draft tau's record goes to slot head + count + tau as for a chain, so
+ * an accepted path need not be contiguous in the buffer ("ReplaySSM：ハイブリッド
+ * モデルの高速デコーディングを実現する状態ストレージ再考" (ai.warp-studio.com),
+ * "推測デコーディングにおける革新と実装詳細", the sentence on tree-based
+ * speculative decoding).  parents = {-1, 0, 1, ..} is rs_verify.
+ * RS_ERR_RANGE for an invalid tree; then exactly one rs_commit_path (or, for a
+ * chain, rs_commit) must follow. */
+rs_status rs_verify_tree(rs_cache *cache, int32_t T, const int32_t *parents, const rs_inputs *in, float *y,
+                         rs_stream stream);
+
+/* Commit by index list: per sequence b, path_len[b] (device int32 [B]) drafts
+ * path[b][0..path_len[b]) (device int32 [B][T_max]) of the pending verify, a
+ * path from the root (path[b][0]'s parent is -1, each next draft's parent the
+ * previous one).  Their records are moved to the slots right after the
+ * committed records, in path order, then the pointer advances by path_len[b]
+ * and the sequence folds if its count reaches L, as in rs_commit.  A list that
+ * is not such a path sets RS_DEVERR_ACCEPTED and leaves that sequence
+ * unchanged.  Uses the verify-table section of the scratch buffer.
+ * RS_ERR_STATE if no verify is pending. */
+rs_status rs_commit_path(rs_cache *cache, const int32_t *path_len, const int32_t *path, rs_stream stream);
 
 /* Fold all buffered records of the sequences with seq_mask[b] != 0 (device
  * u8 [B]; NULL = all sequences) into the checkpoint and refresh their read
  * copy; count = 0, last_flush = 1 for them, last_flush = 0 for the others.
  * Use after writing an initial checkpoint (read-copy quantisation), to export
  * the state (after rs_flush the checkpoint is the full state), or at the end
- * of a sequence.  RS_ERR_STATE if drafts are pending. */
+ * of a sequence.  This is the flush of the method -- fold the buffered
+ * records into the checkpoint, write it to HBM once, clear the buffer
+ * ("ReplaySSM caches SSM inputs..." (richland.au), "What shipped", the
+ * paragraph on unrolling the recurrence; ai-jitan-hub.com,
+ * "ReplaySSMは何をする手法か", third bullet) -- on demand rather than on fill.
+ * RS_ERR_STATE if drafts are pending. */
 rs_status rs_flush(rs_cache *cache, const uint8_t *seq_mask, rs_stream stream);
 
 /* Synchronise the stream and read the device error word (RS_DEVERR_*) into
@@ -226,6 +273,9 @@ rs_status rs_get_device_error(rs_cache *cache, rs_stream stream, int32_t *code);
  *   - batch must be <= 16384, else RS_ERR_UNSUPPORTED.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     The address is kept per device and context: after a cudaDeviceReset
+ *     (or any other replacement of the device's context) the next call looks
+ *     it up again, so make that call, too, before any stream capture.
  *   - Every call clears the counters it uses on `stream`, then launches.  All
  *     calls on a device share the array: calls that overlap on the GPU (other
  *     streams, other caches, other threads) race and must be ordered by the
@@ -260,6 +310,51 @@ rs_status rs_pipe_decode_step(rs_pipe *pipe, const rs_inputs *host_in, float *ho
 rs_status rs_pipe_sync(rs_pipe *pipe, rs_stream stream);
 /* Waits for the pipe's copies, then frees its device memory, streams and events. */
 void rs_pipe_destroy(rs_pipe *pipe);
+
+/*
+ * The conventional path, on the same GPU, for comparison: the decoders the
+ * method replaces.  Stateless calls (no rs_cache; the caller owns the state);
+ * cfg->ring_len is ignored, read_mode must be RS_READ_NONE.
+ *
+ * rs_conventional_decode_step: one token per sequence, the plain per-token
+ * recurrence -- read the whole state, apply the rank-1 update, write the state
+ * back, y_t = S_t q_t ("ReplaySSM caches SSM inputs..." (richland.au), "What
+ * shipped", the paragraph on why the conventional decode kernel is
+ * bandwidth-bound; ai-jitan-hub.com, "何がどれだけ速くなったのか", item 1).
+ *   state  f32 [B][H][P][N], updated in place;  y  f32 [B][H][P];
+ *   in     as for rs_decode_step.
+ * One read and one write of the state per token (2 |S| bytes).
+ */
+rs_status rs_conventional_decode_step(const rs_config *cfg, float *state, const rs_inputs *in, float *y,
+                                      rs_stream stream);
+
+/*
+ * Snapshot-per-draft speculative decoding: the state of every sequence lives
+ * in one of T_max + 1 slots; rs_snapshot_verify reads the current slot once,
+ * runs the T drafts token by token and writes the state after each draft to
+ * its own slot (one read and T writes of the state), and rs_snapshot_commit
+ * rolls back by selecting the slot of the accepted prefix ("ReplaySSM caches
+ * SSM inputs..." (richland.au), "What shipped", the paragraph on the snapshot
+ * stored after every draft token; ai-jitan-hub.com, "何がどれだけ速くなったのか",
+ * item 2).  cfg->max_draft = T_max in 1..4.
+ *   pool   f32 [B][T_max+1][H][P][N]: slot s of sequence b at index (b, s).
+ *   slots  int32 [B] (the current slot of each sequence, 0 initially: zero the
+ *          array and write the initial state into slot 0), followed by a
+ *          device error word int32 [4] = {code, sequence, 0, 0}.
+ * rs_snapshot_query_sizes gives bytes[0] = pool, bytes[1] = slots + error word.
+ * rs_snapshot_verify: drafts as for rs_verify ([B][T] lead dims), y f32
+ * [B][T][H][P]; the state after draft tau goes to slot (cur + 1 + tau) mod
+ * (T_max + 1); a slot index out of range sets RS_DEVERR_CURSOR and skips the
+ * sequence.  rs_snapshot_commit: accepted int32 [B] in 0..T (the T of the
+ * verify it follows) sets cur = (cur + accepted) mod (T_max + 1); out of range
+ * sets RS_DEVERR_ACCEPTED and leaves the sequence unchanged.  Read the error
+ * word with a device-to-host copy after synchronising.
+ */
+rs_status rs_snapshot_query_sizes(const rs_config *cfg, size_t bytes[2]);
+rs_status rs_snapshot_verify(const rs_config *cfg, float *pool, const int32_t *slots, int32_t T,
+                             const rs_inputs *drafts, float *y, rs_stream stream);
+rs_status rs_snapshot_commit(const rs_config *cfg, int32_t *slots, const int32_t *accepted, int32_t T,
+                             rs_stream stream);
 
 /* Self-test of the bounded wait every kernel uses on its mbarriers: one GPU
  * thread waits on an mbarrier that nothing completes, giving up after

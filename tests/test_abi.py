@@ -98,3 +98,23 @@ def test_status_strings():
     for s in range(9):
         assert rs.rs_status_string(s) and rs.rs_status_string(s) != "unknown status"
     assert rs.rs_status_string(42) == "unknown status"
+
+
+def test_conventional_path_host_checks_need_no_device():
+    """The comparison path's calls size the snapshot pool and reject bad arguments on the host."""
+    cfg = rs.rs_config(0, 512, 128, 8, 64, 128, 16, 4, 0)
+    st, sz = rs.rs_snapshot_query_sizes(cfg)
+    assert st == rs.RS_OK
+    assert sz[0] == 512 * 5 * 128 * 64 * 128 * 4 and sz[1] == 512 * 4 + 16
+    assert rs.rs_snapshot_query_sizes(rs.rs_config(0, 4, 4, 1, 16, 16, 4, 0, 0))[0] == rs.RS_ERR_RANGE
+    assert rs.rs_snapshot_query_sizes(rs.rs_config(0, 4, 4, 1, 16, 16, 4, 5, 0))[0] == rs.RS_ERR_RANGE
+    assert rs.rs_snapshot_query_sizes(rs.rs_config(0, 4, 4, 1, 16, 16, 4, 2, 1))[0] == rs.RS_ERR_UNSUPPORTED
+    small = rs.rs_config(0, 2, 4, 1, 16, 16, 4, 2, 0)
+    assert rs.rs_conventional_decode_step(small, 0, rs.rs_inputs(), 4096, 0) == rs.RS_ERR_NULL
+    assert rs.rs_conventional_decode_step(small, 4096 + 4, rs.rs_inputs(), 4096, 0) == rs.RS_ERR_ALIGN
+    assert rs.rs_conventional_decode_step(small, 4096, rs.rs_inputs(), 4096, 0) == rs.RS_ERR_NULL  # inputs
+    assert rs.rs_snapshot_verify(small, 4096, 4096, 3, rs.rs_inputs(), 4096, 0) == rs.RS_ERR_RANGE  # T > T_max
+    assert rs.rs_snapshot_verify(small, 4096, 4096, 0, rs.rs_inputs(), 4096, 0) == rs.RS_ERR_RANGE
+    assert rs.rs_snapshot_verify(small, 4096, 4096 + 8, 1, rs.rs_inputs(), 4096, 0) == rs.RS_ERR_ALIGN
+    assert rs.rs_snapshot_commit(small, 0, 4096, 1, 0) == rs.RS_ERR_NULL
+    assert rs.rs_snapshot_commit(small, 4096, 4096, 3, 0) == rs.RS_ERR_RANGE

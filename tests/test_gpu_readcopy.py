@@ -1,12 +1,18 @@
 """GPU parity of the low-precision read copy (FP8 per-row, NVFP4).
 
-* The copy quantised from an initial checkpoint is compared code by code with
-  the oracle's codecs (both sides take the rounding decisions in float32).
-* Decode outputs with the copy are compared with the oracle's quantised-read
-  output (the copy replaces S_ckpt only in the decayed S_ckpt q term) and,
-  per window, with the exact FP32-recurrence output: rel-L2 must stay below
-  1% (FP8) / 6% (NVFP4) from the second window on and must not grow with the
-  window index, because the copy never feeds the recurrence.
+* The copy quantised from an initial checkpoint, and the copy re-quantised at
+  every fold (decode flush steps, commits that fold), are compared code by
+  code and scale by scale with the oracle's codecs applied to the device's
+  own FP32 checkpoint (both sides take the rounding decisions in float32).
+* Decode outputs with the copy are compared element by element, within
+  2e-4 * max(|ref|, 1e-3), with the oracle's read-copy output (the copy
+  replaces S_ckpt only in the decayed S_ckpt q term).  Where the oracle's copy
+  (quantised from its float64 checkpoint rounded to FP32) rounds an element
+  differently from the device's copy, the expected output is shifted by the
+  decayed product of the two copies' difference with q (tests/harness.py).
+* Per window, the output error against the exact FP32-recurrence output must
+  stay below 1% (FP8) / 6% (NVFP4) rel-L2 from the second window on and must
+  not grow with the window index, because the copy never feeds the recurrence.
 """
 
 import numpy as np
@@ -54,13 +60,9 @@ def test_small_read_copy_decode_matches_oracle(mode):
     pair = Pair(configs.Mamba2Workload(shape, seed=42, s0_std=0.1), read_mode=mode)
     for t in range(20):
         y, ref = pair.decode(t)
-        yq = pair.oracle.last_read_out
-        if t < 3:
-            # first window: the copy was quantised from the exact initial state on both sides
-            assert_close(y, yq, f"{mode} step {t}")
-        else:
-            assert _rel_l2(y, yq) < 2e-3, (t, _rel_l2(y, yq))
+        assert_close(y, pair.last_read_expected, f"{mode} step {t}")
         pair.check_cursor(f"step {t}")
+        pair.check_ring(f"step {t}")
         if pair.cursor_gpu()[:, 2].any():
             assert_close(y, ref, f"{mode} flush step {t} reads the FP32 checkpoint")
             pair.check_ckpt(f"step {t}")
@@ -74,27 +76,31 @@ def _config4_windows(mode, steps, seqs):
     L = wl.shape.ring_len
     num = np.zeros(steps // L)
     den = np.zeros(steps // L)
-    num_q = np.zeros(steps // L)
+    differing = 0
     for t in range(steps):
         y, ref = pair.decode(t)
+        assert_close(y, pair.last_read_expected, f"{mode} step {t}")
+        differing = max(differing, pair.copy_rows_differing)
         w = t // L
         num[w] += np.sum((y - ref) ** 2)
         den[w] += np.sum(ref ** 2)
-        num_q[w] += np.sum((y - pair.oracle.last_read_out) ** 2)
     assert pair.cache.device_error() == 0
-    return np.sqrt(num / den), np.sqrt(num_q / den), float(np.sqrt(num.sum() / den.sum()))
+    return np.sqrt(num / den), differing, float(np.sqrt(num.sum() / den.sum()))
 
 
 @pytest.mark.parametrize("mode,bound", [("fp8", 0.01), ("nvfp4", 0.06)])
 def test_config4_error_per_window(mode, bound):
     """Config-4 shape (B=256, H=128, P=64, N=128, G=8, L=16), 512 steps = 32 windows,
     oracle on two sampled sequences."""
-    per_window, vs_quantised_oracle, aggregate = _config4_windows(mode, 512, [0, 255])
+    per_window, differing, aggregate = _config4_windows(mode, 512, [0, 255])
     assert np.all(per_window[1:] <= bound), per_window
     assert aggregate <= bound
     # the copy never feeds the recurrence: no growth with the window index
     assert per_window[-8:].mean() <= 1.1 * per_window[1:9].mean(), per_window
-    assert np.all(vs_quantised_oracle <= 2e-3), vs_quantised_oracle
+    # rows whose two copies differ at all (most by one FP32 ulp of the row scale, when the
+    # two FP32 checkpoints' row maxima differ in the last bit) are still compared element
+    # by element above, against the oracle's output shifted by the copies' difference
+    assert 0 <= differing <= 2 * 128 * 64
 
 
 @pytest.mark.slow
@@ -103,7 +109,7 @@ def test_config4_full_4096_steps(mode, bound):
     """All 4096 steps; the per-window rel-L2 is taken over four sequences spread
     across the batch (one sequence alone gives a noisy estimate of the batch's
     error: its FP8 windows scatter around 0.8% with single windows near 1%)."""
-    per_window, _, aggregate = _config4_windows(mode, 4096, [0, 85, 170, 255])
+    per_window, differing, aggregate = _config4_windows(mode, 4096, [0, 85, 170, 255])
     assert np.all(per_window[1:] <= bound)
     assert aggregate <= bound
     assert per_window[-32:].mean() <= 1.1 * per_window[1:33].mean()
@@ -121,24 +127,23 @@ def test_read_copy_d128_mixed_window_positions(mode):
     _check_initial_copy(pair, mode, list(range(5)))
     for t in range(2):  # first window: the copy and the oracle's copy come from the same state
         y, ref = pair.decode(t)
-        assert_close(y, pair.oracle.last_read_out, f"{mode} step {t}")
+        assert_close(y, pair.last_read_expected, f"{mode} step {t}")
     for s, acc in enumerate([[0, 1, 2, 1, 0], [2, 0, 1, 2, 1], [1, 2, 0, 0, 2]]):
         y, ref = pair.verify(s, 2)
         assert_close(y, ref, f"{mode} verify {s}")
+        pair.check_ring(f"{mode} verify {s}")
         pair.commit(s, 2, accepted=acc)
         pair.check_cursor(f"{mode} commit {s}")
     mixed = 0
     for t in range(2, 26):
         y, ref = pair.decode(t)
-        yq = pair.oracle.last_read_out
         flushed = pair.cursor_gpu()[:, 2].astype(bool)
         mixed += int(0 < flushed.sum() < len(flushed))
-        for b in range(5):
-            if flushed[b]:
-                assert_close(y[b], ref[b], f"{mode} step {t} seq {b} (flush reads the FP32 checkpoint)")
-            else:
-                assert _rel_l2(y[b], yq[b]) < 2e-3, (t, b, _rel_l2(y[b], yq[b]))
+        # flushing sequences read the FP32 checkpoint (expected = the exact output)
+        assert_close(y, pair.last_read_expected, f"{mode} step {t}")
+        assert_close(y[flushed], ref[flushed], f"{mode} step {t} flush rows")
         pair.check_cursor(f"{mode} step {t}")
+        pair.check_ring(f"{mode} step {t}")
         if flushed.any():
             pair.check_ckpt(f"{mode} step {t}")
     assert mixed > 0  # some launches had flush and non-flush sequences together

@@ -24,18 +24,38 @@ from workloads.configs import GDN, MAMBA2, LayerShape
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("kind", [MAMBA2, GDN])
-def test_noalloc_matches_rs_decode_step_on_two_calls(kind):
-    if kind == MAMBA2:
-        shape = LayerShape(MAMBA2, batch=5, n_heads=8, n_groups=2, d_head=64, d_state=128, ring_len=2)
+_SHAPES = {
+    # d_state 128: the persistent grouped kernel
+    "mamba2_d128": LayerShape(MAMBA2, batch=5, n_heads=8, n_groups=2, d_head=64, d_state=128, ring_len=2),
+    "gdn_d128": LayerShape(GDN, batch=5, n_heads=4, n_groups=2, d_head=128, d_state=128, ring_len=2),
+    # a small d_state: the generic decode kernel
+    "mamba2_d16": LayerShape(MAMBA2, batch=2, n_heads=4, n_groups=1, d_head=16, d_state=16, ring_len=2),
+}
+
+
+@pytest.mark.parametrize("name,read_mode,permute", [
+    ("mamba2_d128", None, None), ("gdn_d128", None, None), ("mamba2_d16", None, None),
+    ("mamba2_d128", "fp8", None), ("mamba2_d128", None, "5"),
+])
+def test_noalloc_matches_rs_decode_step_on_two_calls(name, read_mode, permute, monkeypatch):
+    """Two calls in a row (a non-flush step, then a flush step at L = 2) give the same
+    outputs, cursors and checkpoint (and read copy) as rs_decode_step on an identical
+    cache; also with the debug CTA permutation, which this call reads too."""
+    shape = _SHAPES[name]
+    kind = shape.kind
+    if permute is None:
+        monkeypatch.delenv("RS_DEBUG_CTA_PERMUTE", raising=False)
     else:
-        shape = LayerShape(GDN, batch=5, n_heads=4, n_groups=2, d_head=128, d_state=128, ring_len=2)
+        monkeypatch.setenv("RS_DEBUG_CTA_PERMUTE", permute)
     wl = configs.workload(shape, seed=51, s0_std=0.1)
     S0 = torch.from_numpy(wl.S0())
-    regular = ReplayCache.for_shape(shape)
-    static = ReplayCache.for_shape(shape)
+    regular = ReplayCache.for_shape(shape, read_mode=read_mode)
+    static = ReplayCache.for_shape(shape, read_mode=read_mode)
     regular.ckpt.copy_(S0)
     static.ckpt.copy_(S0)
+    if read_mode is not None:
+        regular.flush()
+        static.flush()
     A = torch.from_numpy(wl.A()).cuda() if kind == MAMBA2 else None
     stream = torch.cuda.current_stream().cuda_stream
     no_scratch = _lib.rs_buffers(static.bufs.ckpt, static.bufs.ring, static.bufs.cursor, static.bufs.read_copy,
@@ -54,6 +74,8 @@ def test_noalloc_matches_rs_decode_step_on_two_calls(kind):
         np.testing.assert_array_equal(static.cursor.cpu().numpy(), regular.cursor.cpu().numpy())
     assert static.cursor.cpu().numpy()[:, 2].all()            # the second call folded
     assert_close(static.ckpt.cpu().numpy(), regular.ckpt.cpu().numpy(), "checkpoint after the flush")
+    for k, v in static.read_copy_views().items():            # the copy re-quantised by the flush step
+        np.testing.assert_array_equal(v.cpu().numpy(), regular.read_copy_views()[k].cpu().numpy())
     assert static.device_error() == 0 and regular.device_error() == 0
 
 
