@@ -154,6 +154,17 @@ def gdn_bytes(shape, h: int, flush: bool) -> int:
     return b + (state if flush else record)
 
 
+def kda_bytes(shape, h: int, flush: bool) -> int:
+    """Per-channel-gate layer: records carry a log decay per key channel."""
+    H, G, P, N = shape.n_heads, shape.n_groups, shape.d_head, shape.d_state
+    state = H * P * N * 4
+    record = H * P * 4 + H * N * 4 + G * N * 2               # u, g, k
+    inputs = 2 * G * N * 2 + H * P * 2 + H * N * 4 + H * 4     # q, k, v, g, beta
+    out = H * P * 4
+    b = state + h * record + inputs + out
+    return b + (state if flush else record)
+
+
 def upload(inp: dict, dev) -> dict:
     import torch
     out = {}
@@ -313,11 +324,12 @@ def natural_window(res, shape, L, bytes_fn):
     """The decode rate at the natural mix of one window (L - 1 non-flush steps, one
     flush), from the per-launch means and the mean gap between launches; and the
     window's algorithmic bytes over the summed launch times."""
-    if res["nonflush_us"] is None or res["flush_us"] is None:
+    if res["flush_us"] is None or (L > 1 and res["nonflush_us"] is None):
         return None
-    us = (L - 1) * res["nonflush_us"] + res["flush_us"] + L * res["gap_us"]
+    nf = res["nonflush_us"] if L > 1 else 0.0
+    us = (L - 1) * nf + res["flush_us"] + L * res["gap_us"]
     nbytes = sum(bytes_fn(shape, h, h == L - 1) for h in range(L)) * shape.batch
-    kern_us = (L - 1) * res["nonflush_us"] + res["flush_us"]
+    kern_us = (L - 1) * nf + res["flush_us"]
     return {"value": shape.batch * L / (us * 1e-6), "unit": UNIT, "us_per_step": us / L,
             "achieved_gbs": nbytes / (kern_us * 1e3), "window_bytes": nbytes,
             "note": f"{L - 1} non-flush + 1 flush launch at their mean times plus the mean launch gap"}
@@ -580,6 +592,68 @@ def read_copy_error_leg(wl, dev, mode, steps):
             "inputs": "16 distinct seeded input steps cycled; initial state N(0,0.1)"}
 
 
+def mixed_phase_leg(wl, dev, K, W):
+    """Decode with the sequences at staggered window positions (after step k of the first
+    window, the sequences b with b % L == k are folded by rs_flush), so that every launch
+    mixes flush and non-flush sequences, about one in L folding."""
+    import torch
+    s = wl.shape
+    L = s.ring_len
+    cache = make_cache(wl, dev, seed=11)
+    steps = _uploaded_steps(wl, dev, 16)
+    y = torch.empty(s.batch, s.n_heads, s.d_head, dtype=torch.float32, device=dev)
+    for k in range(L):
+        cache.decode_step(steps[k % 16], y)
+        mask = torch.tensor([1 if b % L == k else 0 for b in range(s.batch)], dtype=torch.uint8, device=dev)
+        cache.flush(mask)
+    elapsed, per = _timed_launches(lambda t: cache.decode_step(steps[t % 16], y), K, W, dev)
+    folding = int(cache.cursor[:, 2].sum().item())
+    assert cache.device_error() == 0
+    del cache, steps
+    torch.cuda.empty_cache()
+    us = 1e3 * elapsed / K
+    return {"us_per_step": us, "value": s.batch * K / (elapsed / 1e3), "unit": UNIT, "launches": K,
+            "folding_last_step": folding,
+            "note": f"sequences at {L} staggered window positions; every launch folds about 1/{L} of them"}
+
+
+def graph_window_leg(wl, dev, windows, warm):
+    """One window of decode steps (L launches) captured once as a CUDA graph and replayed."""
+    import torch
+    s = wl.shape
+    L = s.ring_len
+    cache = make_cache(wl, dev, seed=12)
+    steps = _uploaded_steps(wl, dev, L)
+    ys = [torch.empty(s.batch, s.n_heads, s.d_head, dtype=torch.float32, device=dev) for _ in range(L)]
+    for t in range(L):  # eager first window: every kernel configured before the capture
+        cache.decode_step(steps[t], ys[t])
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream(dev)
+    cs.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(g, stream=cs):
+            for t in range(L):
+                cache.decode_step(steps[t], ys[t], stream=cs)
+    torch.cuda.current_stream(dev).wait_stream(cs)
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(windows):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    assert cache.device_error() == 0
+    del g, cache, steps
+    torch.cuda.empty_cache()
+    return {"us_per_step": 1e3 * ms / (windows * L), "value": s.batch * windows * L / (ms / 1e3), "unit": UNIT,
+            "windows": windows, "note": f"one captured window of {L} decode launches, replayed"}
+
+
 def sweep_leg(dev, kind, batch, L, K, W, with_conventional=True):
     """One point of the batch / window-length sweeps: the ReplaySSM decode at its natural
     window mix and, at the same shape, the conventional decode step."""
@@ -683,6 +757,13 @@ def extras(line, args, dev, hbm, m2):
                    "nonflush_us": gdn["nonflush_us"], "flush_us": gdn["flush_us"],
                    "frac": gdn["bytes_total"] / (gdn["launch_ms_total"] * 1e6) / hbm,
                    "natural_window": gdn["natural_window"]}
+    with nvtx_range("decode per-channel gate"):
+        kda = decode_leg(configs.config_kda(), dev, Kx, W, 16, kda_bytes, lambda: None)
+    line["kda"] = {"workload": "decode, delta rule with a per-key-channel gate, 1 layer: B=256 Hv=32 Hk=16 "
+                               "dk=dv=128, L=16", "unit": UNIT, "natural_window": kda["natural_window"],
+                   "nonflush_us": kda["nonflush_us"], "flush_us": kda["flush_us"],
+                   "nonflush_gbs": kda["nonflush_gbs"], "flush_gbs": kda["flush_gbs"],
+                   "frac": kda["natural_window"]["achieved_gbs"] / hbm}
     with nvtx_range("verify + commit"):
         ver = [verify_leg(configs.config3_mamba2(), dev, 64, 4, lambda: None),
                verify_leg(configs.config3_gdn(), dev, 64, 4, lambda: None)]
@@ -704,19 +785,35 @@ def extras(line, args, dev, hbm, m2):
         cgdn = conventional_decode_leg(configs.config2(), dev, 32, W)
         sm2 = snapshot_leg(configs.config3_mamba2(), dev, 32, 4)
         sgdn = snapshot_leg(configs.config3_gdn(), dev, 32, 4)
-    for c in (cm2, cgdn):
-        c["frac"] = c["achieved_gbs"] / hbm
+        # the same read-modify-write per token, run by the ReplaySSM decode kernel at L = 1
+        # (every step folds its one record and writes the state)
+        l1m2 = sweep_leg(dev, 0, 256, 1, 16, 16, with_conventional=False)
+        l1gdn = sweep_leg(dev, 1, 256, 1, 16, 16, with_conventional=False)
     for c in (sm2, sgdn):
         c["verify_frac"] = c["verify_gbs"] / hbm
+    for c in (cm2, cgdn):
+        c["frac"] = c["achieved_gbs"] / hbm
+    best_m2 = min(cm2["us_per_step"], l1m2["us_per_step"])
+    best_gdn = min(cgdn["us_per_step"], l1gdn["us_per_step"])
     line["conventional"] = {
         "decode_mamba2": cm2, "decode_gdn": cgdn, "snapshot_spec_mamba2": sm2, "snapshot_spec_gdn": sgdn,
-        "decode_speedup_mamba2": cm2["us_per_step"] / m2["natural_window"]["us_per_step"],
-        "decode_speedup_gdn": cgdn["us_per_step"] / gdn["natural_window"]["us_per_step"],
+        "decode_mamba2_as_window_1": l1m2, "decode_gdn_as_window_1": l1gdn,
+        "decode_speedup_mamba2": best_m2 / m2["natural_window"]["us_per_step"],
+        "decode_speedup_gdn": best_gdn / gdn["natural_window"]["us_per_step"],
         "spec_speedup_mamba2": ver[0]["tokens_per_s"] / sm2["tokens_per_s"],
         "spec_speedup_gdn": ver[1]["tokens_per_s"] / sgdn["tokens_per_s"],
-        "note": "same GPU, same shapes: decode at the natural 15:1 window mix vs the read-modify-write "
-                "step; speculative T=4 verify + commit rounds at B=512 vs snapshot-per-draft verify + "
+        "note": "same GPU, same shapes: decode at the natural 15:1 window mix vs the faster of the two "
+                "read-modify-write steps (the conventional kernel, and the ReplaySSM kernel at L=1); "
+                "speculative T=4 verify + commit rounds at B=512 vs snapshot-per-draft verify + "
                 "slot-select commit"}
+    with nvtx_range("mixed window positions"):
+        mp = mixed_phase_leg(configs.config1(), dev, 64, 16)
+    mp["vs_synchronized_window"] = m2["natural_window"]["us_per_step"] / mp["us_per_step"]
+    line["mixed_phase"] = mp
+    with nvtx_range("cuda graph window"):
+        gw = graph_window_leg(configs.config1(), dev, 8, 2)
+    gw["vs_eager_window"] = m2["natural_window"]["us_per_step"] / gw["us_per_step"]
+    line["graph_window"] = gw
     with nvtx_range("batch sweep"):
         line["batch_sweep"] = [sweep_leg(dev, 0, b, 16, 32, 16) for b in (1, 16, 64, 256, 1024)]
     with nvtx_range("window sweep"):
@@ -798,6 +895,8 @@ def main(argv=None):
                     help="time only the GDN decode leg, at --batch sequences (a profiling case)")
     ap.add_argument("--read-copy-only", choices=["fp8", "nvfp4"],
                     help="time only the non-flush decode with a read copy, at --batch sequences (a profiling case)")
+    ap.add_argument("--kda-decode-only", action="store_true",
+                    help="time only the per-channel-gate decode leg, at --batch sequences (a profiling case)")
     ap.add_argument("--conventional-only", choices=["mamba2", "gdn"],
                     help="time only the conventional read-modify-write decode step, at --batch sequences "
                          "(a profiling case)")
@@ -826,6 +925,14 @@ def main(argv=None):
         if rank == 0:
             print(json.dumps({"gdn": {"batch": args.batch, "nonflush_us": r["nonflush_us"], "flush_us": r["flush_us"],
                                       "nonflush_gbs": r["nonflush_gbs"], "launches": r["launches"]}}))
+        return 0
+    if args.kda_decode_only:
+        wl = configs.config_kda(batch=args.batch)
+        r = decode_leg(wl, dev, args.steps, args.warmup, 16, kda_bytes, lambda: None)
+        if rank == 0:
+            print(json.dumps({"kda": {"batch": args.batch, "nonflush_us": r["nonflush_us"], "flush_us": r["flush_us"],
+                                      "nonflush_gbs": r["nonflush_gbs"], "natural_window": r["natural_window"],
+                                      "launches": r["launches"]}}))
         return 0
     if args.conventional_only:
         wl = (configs.config1 if args.conventional_only == "mamba2" else configs.config2)(batch=args.batch)

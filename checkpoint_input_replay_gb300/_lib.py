@@ -24,6 +24,7 @@ RS_ERR_DEVICE = 8
 
 RS_MAMBA2 = 0
 RS_GDN = 1
+RS_KDA = 2
 RS_READ_NONE = 0
 RS_READ_FP8_ROW = 1
 RS_READ_NVFP4 = 2

@@ -22,7 +22,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libreplayssm.so")
 
 SOURCES = ["api.cu", "decode.cu", "decode128.cu", "verify.cu", "verify128.cu", "fold.cu", "fold128.cu", "noalloc.cu", "selftest.cu",
-           "conventional.cu", "tree.cu"]
+           "conventional.cu", "tree.cu", "kda.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -14,7 +14,7 @@ import torch
 from . import _lib
 from ._lib import check
 
-_KIND = {"mamba2": _lib.RS_MAMBA2, "gdn": _lib.RS_GDN}
+_KIND = {"mamba2": _lib.RS_MAMBA2, "gdn": _lib.RS_GDN, "kda": _lib.RS_KDA}
 _READ = {None: _lib.RS_READ_NONE, "none": _lib.RS_READ_NONE, "fp8": _lib.RS_READ_FP8_ROW,
          "nvfp4": _lib.RS_READ_NVFP4}
 
@@ -33,8 +33,9 @@ def marshal_inputs(kind: int, H: int, G: int, P: int, N: int, inputs: dict, lead
                 "A": (torch.float32, (H,)), "B": (torch.bfloat16, lead + (G, N)),
                 "C": (torch.bfloat16, lead + (G, N))}
     else:
+        g_shape = lead + ((H, N) if kind == _lib.RS_KDA else (H,))
         spec = {"q": (torch.bfloat16, lead + (G, N)), "k": (torch.bfloat16, lead + (G, N)),
-                "v": (torch.bfloat16, lead + (H, P)), "g": (torch.float32, lead + (H,)),
+                "v": (torch.bfloat16, lead + (H, P)), "g": (torch.float32, g_shape),
                 "beta": (torch.float32, lead + (H,))}
     ptrs = {}
     for name, (dtype, shape) in spec.items():
@@ -123,10 +124,15 @@ class ReplayCache:
                 "B": m[o3:o3 + B * G * C * N * 2].view(torch.bfloat16).view(B, G, C, N),
             }
         o1 = _a256(B * H * C * P * 4)
-        o2 = o1 + _a256(B * H * Cp * 4)
+        if self.kind == _lib.RS_KDA:   # g: a log decay per key channel
+            o2 = o1 + _a256(B * H * C * N * 4)
+            g = m[o1:o1 + B * H * C * N * 4].view(torch.float32).view(B, H, C, N)
+        else:
+            o2 = o1 + _a256(B * H * Cp * 4)
+            g = m[o1:o1 + B * H * Cp * 4].view(torch.float32).view(B, H, Cp)
         return {
             "u": m[0:B * H * C * P * 4].view(torch.float32).view(B, H, C, P),
-            "g": m[o1:o1 + B * H * Cp * 4].view(torch.float32).view(B, H, Cp),
+            "g": g,
             "k": m[o2:o2 + B * G * C * N * 2].view(torch.bfloat16).view(B, G, C, N),
         }
 

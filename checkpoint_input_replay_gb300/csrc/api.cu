@@ -48,7 +48,7 @@ size_t decode_smem(const rs_config& c) {
 
 rs_status validate(const rs_config* c) {
   if (!c) return RS_ERR_NULL;
-  if (c->kind != RS_MAMBA2 && c->kind != RS_GDN) return RS_ERR_RANGE;
+  if (c->kind != RS_MAMBA2 && c->kind != RS_GDN && c->kind != RS_KDA) return RS_ERR_RANGE;
   if (c->read_mode < RS_READ_NONE || c->read_mode > RS_READ_NVFP4) return RS_ERR_RANGE;
   if (c->batch < 1 || c->n_heads < 1 || c->n_groups < 1 || c->d_head < 1 || c->d_state < 1 ||
       c->ring_len < 1 || c->max_draft < 0)
@@ -59,6 +59,8 @@ rs_status validate(const rs_config* c) {
   if (static_cast<long long>(c->d_head) * c->d_state * 4 > rs::kMaxTileBytes) return RS_ERR_UNSUPPORTED;
   if (c->ring_len + c->max_draft > rs::kMaxRec || c->max_draft > 4) return RS_ERR_UNSUPPORTED;
   if (c->read_mode != RS_READ_NONE && c->kind != RS_MAMBA2) return RS_ERR_UNSUPPORTED;
+  // the per-channel-gate layer is decoded and flushed; no speculative path
+  if (c->kind == RS_KDA && c->max_draft != 0) return RS_ERR_UNSUPPORTED;
   if (decode_smem(*c) > 227 * 1024) return RS_ERR_UNSUPPORTED;
   return RS_OK;
 }
@@ -75,10 +77,16 @@ Layout layout_of(const rs_config& c) {
     L.r2 = L.r1 + align256(B * H * Cp * 2);     // la f32  [B][H][Cp]
     L.r3 = L.r2 + align256(B * H * Cp * 4);     // B  bf16 [B][G][C][N]
     L.ring = L.r3 + align256(B * G * C * N * 2);
-  } else {
+  } else if (c.kind == RS_GDN) {
     L.r0 = 0;                                   // u f32  [B][H][C][P]
     L.r1 = L.r0 + align256(B * H * C * P * 4);  // g f32  [B][H][Cp]
     L.r2 = L.r1 + align256(B * H * Cp * 4);     // k bf16 [B][G][C][N]
+    L.r3 = L.r2;
+    L.ring = L.r2 + align256(B * G * C * N * 2);
+  } else {
+    L.r0 = 0;                                   // u f32  [B][H][C][P]
+    L.r1 = L.r0 + align256(B * H * C * P * 4);  // g f32  [B][H][C][N] (a log decay per key channel)
+    L.r2 = L.r1 + align256(B * H * C * N * 4);  // k bf16 [B][G][C][N]
     L.r3 = L.r2;
     L.ring = L.r2 + align256(B * G * C * N * 2);
   }
@@ -372,7 +380,7 @@ void pipe_sections(const rs_config& c, size_t bytes[5]) {
     bytes[0] = B * G * N * 2;  // q
     bytes[1] = B * G * N * 2;  // k
     bytes[2] = B * H * P * 2;  // v
-    bytes[3] = B * H * 4;      // g
+    bytes[3] = c.kind == RS_KDA ? B * H * N * 4 : B * H * 4;  // g (per key channel for KDA)
     bytes[4] = B * H * 4;      // beta
   }
 }

@@ -1187,6 +1187,7 @@ size_t decode_smem_bytes(const LayerDev& d) {
 }
 
 cudaError_t launch_decode(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s) {
+  if (d.kind == RS_KDA) return launch_kda_decode(d, in, y, s);
   // d_state 128, d_head 64 or 128: the grouped kernel (decode128.cu)
   if (decode128_supports(d)) return launch_decode128(d, in, y, s);
   if (d.kind == 0) {

@@ -42,6 +42,11 @@ namespace {
 constexpr int N = 128;               // d_state of this kernel
 constexpr int SEG = N / 4;           // lanes per state row (one float4 each)
 constexpr int kMaxSeq128 = 64;       // sequences one CTA may cover
+// the weighted work split (batches up to kBalanceMaxB sequences): relative cost of
+// a unit that folds this step and of one that does not (measured: flush step
+// ~2.2x a non-flush step at the workload shapes)
+constexpr int kBalanceMaxB = 4096;
+constexpr int kWPlain = 4, kWFlush = 9;
 constexpr int kThreads128 = kThreads + 128;  // 8 computing warps, prologue, producer, 2 builders
 constexpr int kPrologueWarp = kThreads / 32;
 constexpr int kProducerWarp = kThreads / 32 + 1;
@@ -112,6 +117,12 @@ __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int
   l.pe_dq = o;    o += 2 * 2 * kMaxRec * 4;                 // per builder: k_j . q, k_j . k_cur
   l.pe_size = al128(o);
   return l;
+}
+
+// the weighted work split needs the batch's per-sequence weights in shared memory
+// (in the computing warps' fold tables, before they are used)
+__host__ __device__ __forceinline__ bool balanced(const Lay128& l, int B) {
+  return B <= kBalanceMaxB && B * 4 <= l.pe_dq - l.pe_mtab;
 }
 
 __device__ __forceinline__ int ring_slot(int head, int j, int C) {
@@ -226,13 +237,68 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
 
   const int upseq = H * SPL;  // units of a sequence
   const int total_units = d.B * upseq;
-  const int u0 = cta_index(d.cta_mult) * units_per_cta;
-  const int u1 = min(u0 + units_per_cta, total_units);
-  if (u0 >= u1) return;
-  const int b0 = u0 / upseq, b1 = (u1 - 1) / upseq;
-  const int nseq = b1 - b0 + 1;
+  const int cta = cta_index(d.cta_mult);
+  int u0, u1;
+  if (balanced(LY, d.B)) {
+    // Work split by weight: a unit of a sequence that folds this step costs about
+    // kWFlush / kWPlain times a non-flush unit, so in a batch whose sequences are
+    // at different window positions the CTAs take equal shares of the weighted
+    // total rather than of the units (every CTA computes every boundary from the
+    // same cursors, which no CTA changes before all have read them, below).
+    int* wts = reinterpret_cast<int*>(pbase + LY.pe_mtab);  // the fold tables are not in use yet
+    for (int b = t; b < d.B; b += kThreads128) {
+      const int head = d.cursor[4 * b], cnt = d.cursor[4 * b + 1];
+      const bool fl = static_cast<unsigned>(head) < static_cast<unsigned>(C) &&
+                      static_cast<unsigned>(cnt) < static_cast<unsigned>(L) && cnt + 1 == L;
+      wts[b] = fl ? kWFlush : kWPlain;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int per_l = (d.B + 31) / 32;
+      const int lo = min(lane * per_l, d.B), hi = min(lo + per_l, d.B);
+      long long sw = 0;
+      for (int b = lo; b < hi; ++b) sw += wts[b];
+      long long incl = sw;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const long long W = __shfl_sync(0xffffffffu, incl, 31) * upseq;
+      const long long cum0 = (incl - sw) * upseq;  // weight before this lane's first sequence
+      int bound[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        // units whose weight interval starts before T = (cta + e) W / grid
+        const long long T = static_cast<long long>(cta + e) * W / gridDim.x;
+        long long cum = cum0;
+        int cntu = 0;
+        for (int b = lo; b < hi; ++b) {
+          const int w = wts[b];
+          if (T > cum) cntu += static_cast<int>(min(static_cast<long long>(upseq), (T - cum + w - 1) / w));
+          cum += static_cast<long long>(w) * upseq;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cntu += __shfl_xor_sync(0xffffffffu, cntu, o);
+        bound[e] = cntu - cntu % HR;  // a non-flush read-copy unit spans HR heads
+      }
+      if (lane == 0) {
+        smisc[0] = bound[0];
+        smisc[1] = cta + 1 == static_cast<int>(gridDim.x) ? total_units : bound[1];
+      }
+    }
+    __syncthreads();
+    u0 = smisc[0];
+    u1 = smisc[1];
+    __syncthreads();
+  } else {
+    u0 = cta * units_per_cta;
+    u1 = min(u0 + units_per_cta, total_units);
+  }
+  const int b0 = u0 / upseq, b1 = u1 > u0 ? (u1 - 1) / upseq : b0;
+  const int nseq = u1 > u0 ? b1 - b0 + 1 : 0;
 
-  // --- cursors of the covered sequences; arrival; new cursors by the last arriver ---
+  // --- cursors of the covered sequences ---
   if (t < nseq) {
     const int b = b0 + t;
     const int head = d.cursor[4 * b], cnt = d.cursor[4 * b + 1];
@@ -241,12 +307,20 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     sseq[3 * t] = ok ? head : 0;  // a rejected cursor stages nothing from the ring
     sseq[3 * t + 1] = ok ? cnt : 0;
     sseq[3 * t + 2] = ok ? 1 : 0;
-    const int lo = max(u0, b * upseq), hi = min(u1, (b + 1) * upseq);
+  }
+  // Every CTA counts itself in once it has read all the cursors it needs; the last
+  // one writes every new cursor, so no CTA can see a cursor of this step's batch
+  // already advanced (the count lives in arrive[0] and returns to zero).
+  __syncthreads();
+  if (t == 0) {
     __threadfence();
-    const int prev = atomicAdd(d.arrive + b, hi - lo);
-    if (prev + (hi - lo) == upseq) {  // every CTA of this sequence has read its cursor
-      atomicExch(d.arrive + b, 0);
-      if (!ok) {
+    smisc[0] = atomicAdd(d.arrive, 1) == static_cast<int>(gridDim.x) - 1;
+  }
+  __syncthreads();
+  if (smisc[0]) {
+    for (int b = t; b < d.B; b += kThreads128) {
+      const int head = d.cursor[4 * b], cnt = d.cursor[4 * b + 1];
+      if (static_cast<unsigned>(head) >= static_cast<unsigned>(C) || static_cast<unsigned>(cnt) >= static_cast<unsigned>(L)) {
         report_error(d.err, DEVERR_CURSOR, b);
       } else if (cnt + 1 == L) {
         d.cursor[4 * b] = ring_slot(head, cnt + 1, C);
@@ -257,7 +331,10 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
         d.cursor[4 * b + 2] = 0;
       }
     }
+    if (t == 0) atomicExch(d.arrive, 0);
   }
+  __syncthreads();
+  if (u0 >= u1) return;
   if (t == kThreads) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(full + s, 1);
@@ -667,7 +744,11 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       const unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * ((meta.w >> 16) & 3);
       const float* cob = reinterpret_cast<const float*>(gb + LY.gb_coef);
       const uint16_t* curb = reinterpret_cast<const uint16_t*>(gb + LY.gb_cur);
-      const float4 q4 = reinterpret_cast<const float4*>(gb + LY.gb_qf)[lane];
+      // the query times 2^64: the codes are decoded as their values times 2^-120
+      // (e4m3) or 2^-126 (e2m1), so each product is the true one times 2^-56 or
+      // 2^-62 (exact scalings); the output scale gsc undoes it
+      const float4 q4s = scale4(0x1p64f, reinterpret_cast<const float4*>(gb + LY.gb_qf)[lane]);
+      constexpr float kUnscale = READ == READ_FP8 ? 0x1p56f : 0x1p62f;
       constexpr int TBH = READ == READ_FP8 ? tile : tile / 2;  // code bytes per head
       const int recH = al16(C * P * 2) / 2;                   // record elements per head
       const uint16_t* xb = reinterpret_cast<const uint16_t*>(st + LY.st_rec);
@@ -681,7 +762,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
           ry[hu] = jl == 0 ? co[n] * bf(curb[(hh0 + hu) * P + Rq]) : 0.f;
           gsc[hu] = co[3 * C + CO_GAMMA] * (READ == READ_FP8
                                                 ? reinterpret_cast<const float*>(gb + LY.gb_rs)[(hh0 + hu) * P + Rq]
-                                                : co[3 * C + CO_MATSCALE]);
+                                                : co[3 * C + CO_MATSCALE]) * kUnscale;
         }
         // buffered terms: lanes 4kq..4kq+3 split the records 0..n-1 (lane jl = 0 took record n)
         for (int j = jl; j < n; j += 4) {
@@ -698,15 +779,11 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
             const int R = tw + TW * (r0 + e);
             if (READ == READ_FP8) {
               const uint32_t wd = reinterpret_cast<const uint32_t*>(cb + R * N)[lane];
-              const float2 lo = e4m3x2_to_f32x2(static_cast<uint16_t>(wd & 0xFFFFu));
-              const float2 hi = e4m3x2_to_f32x2(static_cast<uint16_t>(wd >> 16));
-              part[hu][e] = dot4p(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
+              part[hu][e] = dot4p(e4m3x4_scaled(wd), q4s);
             } else {
               const uint32_t wd = reinterpret_cast<const uint16_t*>(cb + R * (N / 2))[lane];
-              const float2 lo = e2m1x2_to_f32x2(wd & 0xFFu);
-              const float2 hi = e2m1x2_to_f32x2(wd >> 8);
-              const float bs = e4m3_to_f32(gb[LY.gb_rs + ((hh0 + hu) * P + R) * (N / 16) + (lane >> 2)]);
-              part[hu][e] = bs * dot4p(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
+              const float bs = e4m3_value(gb[LY.gb_rs + ((hh0 + hu) * P + R) * (N / 16) + (lane >> 2)]);
+              part[hu][e] = bs * dot4p(e2m1x4_scaled(wd), q4s);
             }
           }
         }
@@ -1070,7 +1147,9 @@ cudaError_t launch128(const LayerDev& d, const TokenIn& in, float* y, cudaStream
   int grid = d.num_sms > 0 ? d.num_sms : 1;
   if (grid > total / hr) grid = total / hr;
   int per = ((total + grid - 1) / grid + hr - 1) / hr * hr;
-  while (per / (d.H * SPL) + 2 > kMaxSeq128) {
+  // a weighted share may stretch to kWFlush / kWPlain times the even share
+  auto span_seqs = [&](int p) { return (balanced(LY, d.B) ? p * kWFlush / kWPlain : p) / (d.H * SPL) + 2; };
+  while (span_seqs(per) > kMaxSeq128) {
     grid *= 2;
     per = ((total + grid - 1) / grid + hr - 1) / hr * hr;
   }

@@ -200,6 +200,7 @@ cudaError_t launch_n(const LayerDev& d, int mode, const int* accepted, const uin
 
 cudaError_t launch_fold(const LayerDev& d, int mode, const int* accepted, const uint8_t* mask, int T_pending,
                         cudaStream_t s) {
+  if (d.kind == RS_KDA) return mode == FOLD_FLUSH ? launch_kda_fold(d, mask, s) : cudaErrorInvalidValue;
   // d_state 128, d_head 64 or 128: the persistent kernel that skips non-folding sequences (fold128.cu)
   if (fold128_supports(d)) return launch_fold128(d, mode, accepted, mask, T_pending, s);
   const size_t smem = static_cast<size_t>(d.P) * d.N * 4 + 16 +

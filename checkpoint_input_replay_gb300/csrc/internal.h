@@ -33,7 +33,7 @@ struct LayerDev {
   uint16_t* r_dt;              // bf16 [B][H][Cp]
   float* r_la;                 // f32  [B][H][Cp]  log decay dt*A
   uint16_t* r_B;               // bf16 [B][G][C][N]
-  // GDN ring
+  // GDN ring (and the per-channel-gate layer's: g f32 [B][H][C][N] there)
   float* r_u;                  // f32  [B][H][C][P] delta u
   float* r_g;                  // f32  [B][H][Cp]   log decay g
   uint16_t* r_k;               // bf16 [B][G][C][N]
@@ -92,6 +92,10 @@ int verify_table_stride(int kind, int C);
 cudaError_t make_ckpt_tmap(const LayerDev& d, CUtensorMap* out);
 cudaError_t launch_verify128(const LayerDev& d, const CUtensorMap& tmap, const TokenIn& in, int T, float* y,
                              cudaStream_t s);
+
+// Per-channel-gate layers (kind 2): decode step and fold (kda.cu).
+cudaError_t launch_kda_decode(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s);
+cudaError_t launch_kda_fold(const LayerDev& d, const uint8_t* mask, cudaStream_t s);
 
 // Tree speculative commit: move the records of each sequence's accepted path
 // (drafts path[b][0..len) of the pending verify, whose parents are packed one

@@ -70,7 +70,12 @@ typedef enum {
   RS_ERR_DEVICE = 8       /* the device error word is set                       */
 } rs_status;
 
-typedef enum { RS_MAMBA2 = 0, RS_GDN = 1 } rs_kind;
+/* RS_KDA: the Gated DeltaNet rule with a per-key-channel gate (the gate form of
+ * Kimi Delta Attention), S_t = S_{t-1} Diag(a_t) (I - b_t k_t k_t^T) + b_t v_t k_t^T,
+ * a_t = exp(g_t) over the d_state key channels, o_t = S_t q_t -- a recurrence the
+ * method generalises to ("ReplaySSM caches SSM inputs..." (richland.au), "Why it
+ * matters").  Decode and flush only (max_draft must be 0). */
+typedef enum { RS_MAMBA2 = 0, RS_GDN = 1, RS_KDA = 2 } rs_kind;
 
 /* Low-precision read copy of the checkpoint, used only for the checkpoint
  * read of non-flush decode steps and never fed back into the recurrence
@@ -111,6 +116,8 @@ typedef struct {
  *                       log a = dt*A f32 [B][H][Cp] | B bf16 [B][G][C][N]
  *              GDN:     u f32 [B][H][C][P] (delta u = b (v - a S_{t-1} k)) |
  *                       g f32 [B][H][Cp] | k bf16 [B][G][C][N]
+ *              KDA:     u f32 [B][H][C][P] (u = b (v - S_{t-1} (a * k))) |
+ *                       g f32 [B][H][C][N] | k bf16 [B][G][C][N]
  * cursor     int32 [B][4] = {head, count, last_flush, 0} followed by the
  *            device error word int32 [4] = {code, sequence, 0, 0}.
  *            last_flush is 1 if the last call folded that sequence.
@@ -139,6 +146,7 @@ typedef struct {
  *            A f32 [H], Bm bf16 [..][G][N], Cm bf16 [..][G][N]
  *   GDN:     q bf16 [..][G][N], k bf16 [..][G][N], v bf16 [..][H][P],
  *            g f32 [..][H] (log decay), beta f32 [..][H]
+ *   KDA:     as GDN, with g f32 [..][H][N] (log decay per key channel)
  * Pointers of the other kind are ignored and may be NULL.  The decode kernel
  * stages the per-head scalars (dt, A, g, beta) in 16-byte blocks, so each of
  * those arrays must stay readable up to the next 16-byte boundary after its

@@ -52,7 +52,8 @@ def test_query_sizes_scratch_with_drafts():
 
 
 @pytest.mark.parametrize("fields,status", [
-    ((2, 1, 4, 1, 16, 16, 4, 0, 0), rs.RS_ERR_RANGE),        # kind
+    ((3, 1, 4, 1, 16, 16, 4, 0, 0), rs.RS_ERR_RANGE),        # kind
+    ((2, 1, 4, 1, 16, 16, 4, 2, 0), rs.RS_ERR_UNSUPPORTED),  # per-channel gate: no drafts
     ((0, 1, 4, 1, 16, 16, 4, 0, 7), rs.RS_ERR_RANGE),        # read mode
     ((0, 0, 4, 1, 16, 16, 4, 0, 0), rs.RS_ERR_SHAPE),        # batch
     ((0, 1, 4, 3, 16, 16, 4, 0, 0), rs.RS_ERR_SHAPE),        # heads not a multiple of groups
@@ -118,3 +119,12 @@ def test_conventional_path_host_checks_need_no_device():
     assert rs.rs_snapshot_verify(small, 4096, 4096 + 8, 1, rs.rs_inputs(), 4096, 0) == rs.RS_ERR_ALIGN
     assert rs.rs_snapshot_commit(small, 0, 4096, 1, 0) == rs.RS_ERR_NULL
     assert rs.rs_snapshot_commit(small, 4096, 4096, 3, 0) == rs.RS_ERR_RANGE
+
+
+def test_query_sizes_per_channel_gate_ring():
+    """The per-channel-gate layer's ring keeps a log decay per key channel."""
+    B, H, G, P, N, L = 4, 8, 2, 32, 64, 6
+    st, sz = rs.rs_query_sizes(rs.rs_config(2, B, H, G, P, N, L, 0, 0))
+    a = lambda x: (x + 255) // 256 * 256
+    assert st == rs.RS_OK
+    assert sz[1] == a(B * H * L * P * 4) + a(B * H * L * N * 4) + a(B * G * L * N * 2)

@@ -14,6 +14,8 @@ the launcher's rule -- and the walk over units and over groups must agree.
 
 import random
 
+import numpy as np
+
 import pytest
 
 
@@ -134,3 +136,43 @@ def test_the_model_catches_one_stage_too_many():
         for _ in range(20):
             _simulate(256, 32, 16, 2, 1, 8, 2, 152, {b for b in range(256) if rnd.random() < 0.2}, rnd,
                       extra_stages=1)
+
+
+# --- weighted work split of the decode launch ------------------------------------
+
+def _split(weights, upseq, grid, hr=1):
+    """Unit range of every CTA: units whose weight interval starts in
+    [c W / grid, (c + 1) W / grid), rounded down to multiples of hr (the launch's rule)."""
+    W = sum(weights) * upseq
+    def units_before(T):
+        cum, n = 0, 0
+        for w in weights:
+            if T > cum:
+                n += min(upseq, -(-(T - cum) // w))
+            cum += w * upseq
+        return n - n % hr
+    bounds = [units_before(c * W // grid) for c in range(grid)] + [len(weights) * upseq]
+    return list(zip(bounds[:-1], bounds[1:]))
+
+
+@pytest.mark.parametrize("flush_every", [0, 1, 16, 5])
+def test_weighted_split_covers_every_unit_once_and_balances(flush_every):
+    rng = np.random.default_rng(flush_every)
+    B, upseq, grid = 256, 128, 152
+    flush = (rng.integers(0, flush_every, B) == 0) if flush_every else np.zeros(B, bool)
+    weights = [9 if f else 4 for f in flush]
+    ranges = _split(weights, upseq, grid)
+    assert ranges[0][0] == 0 and ranges[-1][1] == B * upseq
+    assert all(a[1] == b[0] for a, b in zip(ranges, ranges[1:]))
+    assert all(lo <= hi for lo, hi in ranges)
+    unit_w = np.repeat(weights, upseq)
+    cost = np.array([unit_w[lo:hi].sum() for lo, hi in ranges])
+    assert cost.max() <= cost.mean() + 9          # within one unit of an even share
+    seqs = [(hi - 1) // upseq - lo // upseq + 1 for lo, hi in ranges if hi > lo]
+    assert max(seqs) + 2 <= 64                    # the per-CTA cursor table
+
+
+def test_weighted_split_keeps_read_copy_units_whole():
+    weights = [9 if b % 7 == 0 else 4 for b in range(40)]
+    for lo, hi in _split(weights, 16, 152, hr=4):
+        assert lo % 4 == 0 and hi % 4 == 0

@@ -71,10 +71,12 @@ def test_config3_ring_sampled_sequences(kind):
     assert pair.cache.device_error() == 0
 
 
-@pytest.mark.parametrize("kind,P,L", [(MAMBA2, 64, 32), (GDN, 128, 32), (MAMBA2, 64, 8), (GDN, 128, 4)])
+@pytest.mark.parametrize("kind,P,L", [(MAMBA2, 64, 32), (GDN, 128, 32), (MAMBA2, 64, 8), (GDN, 128, 4),
+                                      (MAMBA2, 64, 1), (GDN, 128, 1)])
 def test_d128_window_lengths_of_the_sweep(kind, P, L):
-    """The window lengths the bench sweeps (4, 8, 32; 16 is the workloads' own): two
-    windows and a half, every output, cursor and ring slot, the checkpoint at each flush."""
+    """The window lengths the bench sweeps (1, 4, 8, 32; 16 is the workloads' own; at 1
+    every step folds): two windows and a half, every output, cursor and ring slot, the
+    checkpoint at each flush."""
     shape = LayerShape(kind, batch=3, n_heads=8, n_groups=2, d_head=P, d_state=128, ring_len=L)
     wl = configs.workload(shape, seed=77 + L, s0_std=0.1 if kind == MAMBA2 else 0.05)
     pair = Pair(wl)
