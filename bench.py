@@ -592,14 +592,19 @@ def read_copy_error_leg(wl, dev, mode, steps):
             "inputs": "16 distinct seeded input steps cycled; initial state N(0,0.1)"}
 
 
-def mixed_phase_leg(wl, dev, K, W):
+def mixed_phase_leg(wl, dev, K, W, uniform=False):
     """Decode with the sequences at staggered window positions (after step k of the first
     window, the sequences b with b % L == k are folded by rs_flush), so that every launch
     mixes flush and non-flush sequences, about one in L folding."""
     import torch
     s = wl.shape
     L = s.ring_len
-    cache = make_cache(wl, dev, seed=11)
+    if uniform:  # the even split of units over the CTAs, for comparison
+        os.environ["RS_DEBUG_UNIFORM_SPLIT"] = "1"
+    try:
+        cache = make_cache(wl, dev, seed=11)
+    finally:
+        os.environ.pop("RS_DEBUG_UNIFORM_SPLIT", None)
     steps = _uploaded_steps(wl, dev, 16)
     y = torch.empty(s.batch, s.n_heads, s.d_head, dtype=torch.float32, device=dev)
     for k in range(L):
@@ -808,7 +813,10 @@ def extras(line, args, dev, hbm, m2):
                 "slot-select commit"}
     with nvtx_range("mixed window positions"):
         mp = mixed_phase_leg(configs.config1(), dev, 64, 16)
+        mp_even = mixed_phase_leg(configs.config1(), dev, 64, 16, uniform=True)
     mp["vs_synchronized_window"] = m2["natural_window"]["us_per_step"] / mp["us_per_step"]
+    mp["even_split_us_per_step"] = mp_even["us_per_step"]
+    mp["weighted_split_speedup"] = mp_even["us_per_step"] / mp["us_per_step"]
     line["mixed_phase"] = mp
     with nvtx_range("cuda graph window"):
         gw = graph_window_leg(configs.config1(), dev, 8, 2)

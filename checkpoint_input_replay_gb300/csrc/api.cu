@@ -298,6 +298,9 @@ rs_status rs_create_cache(const rs_config* cfg, const rs_buffers* bufs, rs_cache
   // decode and commit launches takes which unit range, to check that no result
   // depends on the order in which CTAs run or arrive
   if (const char* e = getenv("RS_DEBUG_CTA_PERMUTE")) d.cta_mult = atoi(e) >= 2 ? atoi(e) : 0;
+  // debug: RS_DEBUG_UNIFORM_SPLIT=1 makes the d_state-128 decode split its units evenly
+  // rather than by weight (to measure what the weighted split buys)
+  if (const char* e = getenv("RS_DEBUG_UNIFORM_SPLIT")) d.uniform_split = atoi(e) != 0;
   d.ckpt = static_cast<float*>(bufs->ckpt);
   char* ring = static_cast<char*>(bufs->ring);
   if (cfg->kind == RS_MAMBA2) {

@@ -254,34 +254,15 @@ __device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
   return __half22float2(hv);
 }
 
-// ---- e4m3 / e2m1 decoding with integer operations (the read-copy hot loops) ----
-// The conversion instructions above issue at a fraction of the integer rate, so
-// the decode loops build each value's FP32 bit pattern instead: the code's sign
-// goes to bit 31 and its exponent and mantissa bits right below the lowest
-// exponent bits of FP32, which yields the code's value times a fixed power of
-// two (2^-120 for e4m3, 2^-126 for e2m1), exact for normal and subnormal codes
-// alike (the bit fields of both formats, OCP MX specification).  Callers fold
-// the power of two into the other factor of each product.
-
-// four e4m3 codes (code i in byte i) -> their values times 2^-120
-__device__ __forceinline__ float4 e4m3x4_scaled(uint32_t w) {
-  return make_float4(__uint_as_float(((w << 24) & 0x80000000u) | ((w << 20) & 0x07F00000u)),
-                     __uint_as_float(((w << 16) & 0x80000000u) | ((w << 12) & 0x07F00000u)),
-                     __uint_as_float(((w << 8) & 0x80000000u) | ((w << 4) & 0x07F00000u)),
-                     __uint_as_float((w & 0x80000000u) | ((w >> 4) & 0x07F00000u)));
-}
-
-// one e4m3 code (low byte) -> its value (exact: the scaled pattern times 2^120)
-__device__ __forceinline__ float e4m3_value(uint32_t b) {
-  return __uint_as_float(((b << 24) & 0x80000000u) | ((b << 20) & 0x07F00000u)) * 0x1p120f;
-}
-
-// four e2m1 codes (code i in nibble i of the low 16 bits) -> their values times 2^-126
-__device__ __forceinline__ float4 e2m1x4_scaled(uint32_t w) {
-  return make_float4(__uint_as_float(((w << 28) & 0x80000000u) | ((w << 22) & 0x01C00000u)),
-                     __uint_as_float(((w << 24) & 0x80000000u) | ((w << 18) & 0x01C00000u)),
-                     __uint_as_float(((w << 20) & 0x80000000u) | ((w << 14) & 0x01C00000u)),
-                     __uint_as_float(((w << 16) & 0x80000000u) | ((w << 10) & 0x01C00000u)));
+// x / d rounded to nearest for many x over one divisor d, given r = the
+// correctly rounded reciprocal of d (__frcp_rn): q = x r is within one ulp of
+// x / d, and one fused correction q + (x - q d) r rounds it correctly
+// (Markstein's theorem on FMA-based division), away from overflow and
+// underflow -- which the read-copy quotients stay clear of wherever a code's
+// rounding depends on them (|x / d| <= 448 and codes below 2^-10 are 0).
+__device__ __forceinline__ float div_by(float x, float d, float r) {
+  const float q = __fmul_rn(x, r);
+  return __fmaf_rn(__fmaf_rn(-q, d, x), r, q);
 }
 
 // Sum each of v[0..7] over the 32 lanes of the warp (transpose-reduce: 9

@@ -73,7 +73,7 @@ enum : int { CO_GAMMA = 0, CO_A = 1, CO_BETA = 2, CO_KQ = 3, CO_MATSCALE = 4 };
 struct Lay128 {
   int st_tile, st_rec, st_meta, st_size;
   int gb_key, gb_q, gb_cur, gb_la, gb_dt, gb_s1, gb_s2, gb_rs, gb_ms, gb_qf, gb_kf, gb_coef, gb_size;
-  int pe_A, pe_bars, pe_seq, pe_misc, pe_mtab, pe_dq, pe_size;
+  int pe_A, pe_bars, pe_seq, pe_misc, pe_cnt, pe_mtab, pe_dq, pe_size;
 };
 
 // heads in a non-flush unit of a read-copy layer: 4 heads' codes fit where one
@@ -113,6 +113,7 @@ __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int
   l.pe_bars = o;  o += 48 * 8;  // full, empty, ready x 8 stages; amax x 2 teams x 8 stages; group full, tables x 3
   l.pe_seq = o;   o += 3 * kMaxSeq128 * 4;
   l.pe_misc = o;  o += 16;
+  l.pe_cnt = o;   o += 16;  // computing warps that have finished this CTA's units
   l.pe_mtab = o;  o += (kThreads / 32) * mtab_rows(kind, read, P) * kMtabRow * 4;  // per computing warp: fold coefficients [rows][records]
   l.pe_dq = o;    o += 2 * 2 * kMaxRec * 4;                 // per builder: k_j . q, k_j . k_cur
   l.pe_size = al128(o);
@@ -122,13 +123,48 @@ __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int
 // the weighted work split needs the batch's per-sequence weights in shared memory
 // (in the computing warps' fold tables, before they are used)
 __host__ __device__ __forceinline__ bool balanced(const Lay128& l, int B) {
-  return B <= kBalanceMaxB && B * 4 <= l.pe_dq - l.pe_mtab;
+  return B <= kBalanceMaxB && ((B + 3) & ~3) * 4 + B * 8 + 8 <= l.pe_dq - l.pe_mtab;
 }
 
 __device__ __forceinline__ int ring_slot(int head, int j, int C) {
   int s = head + j;
   return s >= C ? s - C : s;
 }
+
+// One warp: count this CTA in on the launch-wide counter (arrive[0]); the last CTA
+// advances every sequence's cursor and returns the counter to zero.
+__device__ __forceinline__ void finish_launch(const LayerDev& d, int lane, int C, int L) {
+  int last = 0;
+  if (lane == 0) {
+    __threadfence();
+    last = atomicAdd(d.arrive, 1) == static_cast<int>(gridDim.x) - 1;
+  }
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  // eight cursors a lane per round: all loads of a round before its stores
+  for (int b0r = 0; b0r < d.B; b0r += 8 * 32) {
+    int4 cur[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int b = b0r + 32 * k + lane;
+      cur[k] = b < d.B ? reinterpret_cast<const int4*>(d.cursor)[b] : make_int4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int b = b0r + 32 * k + lane;
+      if (b >= d.B) continue;
+      const int head = cur[k].x, cnt = cur[k].y;
+      if (static_cast<unsigned>(head) >= static_cast<unsigned>(C) || static_cast<unsigned>(cnt) >= static_cast<unsigned>(L)) {
+        report_error(d.err, DEVERR_CURSOR, b);
+      } else if (cnt + 1 == L) {
+        reinterpret_cast<int4*>(d.cursor)[b] = make_int4(ring_slot(head, cnt + 1, C), 0, 1, cur[k].w);
+      } else {
+        reinterpret_cast<int4*>(d.cursor)[b] = make_int4(head, cnt + 1, 0, cur[k].w);
+      }
+    }
+  }
+  if (lane == 0) atomicExch(d.arrive, 0);
+}
+
 
 // Position of a unit: its index ui, sequence b, head (u = b H + h), group g,
 // head-in-group hh and part sp of a split head; advanced one unit at a time so
@@ -239,18 +275,24 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   const int total_units = d.B * upseq;
   const int cta = cta_index(d.cta_mult);
   int u0, u1;
-  if (balanced(LY, d.B)) {
+  const bool bal = balanced(LY, d.B) && !d.uniform_split;
+  // scratch before the computing warps' fold tables are used: per-sequence weights,
+  // the batch's cursors (head, count) and the two range bounds
+  int* wts = reinterpret_cast<int*>(pbase + LY.pe_mtab);
+  int2* snap = reinterpret_cast<int2*>(wts + ((d.B + 3) & ~3));
+  int* sbound = reinterpret_cast<int*>(snap + d.B);
+  if (bal) {
     // Work split by weight: a unit of a sequence that folds this step costs about
     // kWFlush / kWPlain times a non-flush unit, so in a batch whose sequences are
     // at different window positions the CTAs take equal shares of the weighted
-    // total rather than of the units (every CTA computes every boundary from the
-    // same cursors, which no CTA changes before all have read them, below).
-    int* wts = reinterpret_cast<int*>(pbase + LY.pe_mtab);  // the fold tables are not in use yet
+    // total rather than of the units.  Every CTA computes every boundary from the
+    // same cursors: no CTA changes a cursor before all have read them (below).
     for (int b = t; b < d.B; b += kThreads128) {
       const int head = d.cursor[4 * b], cnt = d.cursor[4 * b + 1];
       const bool fl = static_cast<unsigned>(head) < static_cast<unsigned>(C) &&
                       static_cast<unsigned>(cnt) < static_cast<unsigned>(L) && cnt + 1 == L;
       wts[b] = fl ? kWFlush : kWPlain;
+      snap[b] = make_int2(head, cnt);
     }
     __syncthreads();
     if (warp == 0) {
@@ -266,11 +308,11 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       }
       const long long W = __shfl_sync(0xffffffffu, incl, 31) * upseq;
       const long long cum0 = (incl - sw) * upseq;  // weight before this lane's first sequence
-      int bound[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        // units whose weight interval starts before T = (cta + e) W / grid
-        const long long T = static_cast<long long>(cta + e) * W / gridDim.x;
+        // units whose weight interval starts before T = (cta + e) ceil(W / grid): with
+        // equal weights these are the even split's boundaries
+        const long long T = min(W, static_cast<long long>(cta + e) * ((W + gridDim.x - 1) / gridDim.x));
         long long cum = cum0;
         int cntu = 0;
         for (int b = lo; b < hi; ++b) {
@@ -280,17 +322,13 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) cntu += __shfl_xor_sync(0xffffffffu, cntu, o);
-        bound[e] = cntu - cntu % HR;  // a non-flush read-copy unit spans HR heads
-      }
-      if (lane == 0) {
-        smisc[0] = bound[0];
-        smisc[1] = cta + 1 == static_cast<int>(gridDim.x) ? total_units : bound[1];
+        // a non-flush read-copy unit spans HR heads; the last CTA ends the batch
+        if (lane == 0) sbound[e] = (e == 1 && cta + 1 == static_cast<int>(gridDim.x)) ? total_units : cntu - cntu % HR;
       }
     }
     __syncthreads();
-    u0 = smisc[0];
-    u1 = smisc[1];
-    __syncthreads();
+    u0 = sbound[0];
+    u1 = sbound[1];
   } else {
     u0 = cta * units_per_cta;
     u1 = min(u0 + units_per_cta, total_units);
@@ -301,40 +339,14 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   // --- cursors of the covered sequences ---
   if (t < nseq) {
     const int b = b0 + t;
-    const int head = d.cursor[4 * b], cnt = d.cursor[4 * b + 1];
+    const int2 hc = bal ? snap[b] : make_int2(d.cursor[4 * b], d.cursor[4 * b + 1]);
+    const int head = hc.x, cnt = hc.y;
     const bool ok = static_cast<unsigned>(head) < static_cast<unsigned>(C) &&
                     static_cast<unsigned>(cnt) < static_cast<unsigned>(L);
     sseq[3 * t] = ok ? head : 0;  // a rejected cursor stages nothing from the ring
     sseq[3 * t + 1] = ok ? cnt : 0;
     sseq[3 * t + 2] = ok ? 1 : 0;
   }
-  // Every CTA counts itself in once it has read all the cursors it needs; the last
-  // one writes every new cursor, so no CTA can see a cursor of this step's batch
-  // already advanced (the count lives in arrive[0] and returns to zero).
-  __syncthreads();
-  if (t == 0) {
-    __threadfence();
-    smisc[0] = atomicAdd(d.arrive, 1) == static_cast<int>(gridDim.x) - 1;
-  }
-  __syncthreads();
-  if (smisc[0]) {
-    for (int b = t; b < d.B; b += kThreads128) {
-      const int head = d.cursor[4 * b], cnt = d.cursor[4 * b + 1];
-      if (static_cast<unsigned>(head) >= static_cast<unsigned>(C) || static_cast<unsigned>(cnt) >= static_cast<unsigned>(L)) {
-        report_error(d.err, DEVERR_CURSOR, b);
-      } else if (cnt + 1 == L) {
-        d.cursor[4 * b] = ring_slot(head, cnt + 1, C);
-        d.cursor[4 * b + 1] = 0;
-        d.cursor[4 * b + 2] = 1;
-      } else {
-        d.cursor[4 * b + 1] = cnt + 1;
-        d.cursor[4 * b + 2] = 0;
-      }
-    }
-    if (t == 0) atomicExch(d.arrive, 0);
-  }
-  __syncthreads();
-  if (u0 >= u1) return;
   if (t == kThreads) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(full + s, 1);
@@ -350,8 +362,14 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     smisc[1] = 0;
     smisc[2] = 0;
     smisc[3] = 0;
+    *reinterpret_cast<int*>(pbase + LY.pe_cnt) = 0;
   }
   __syncthreads();
+  // An empty CTA counts itself in at once (the others when their units are done, at the end)
+  if (u0 >= u1) {
+    if (warp == 0) finish_launch(d, lane, C, L);
+    return;
+  }
 
   // heads in the unit that starts at sequence b: HR unless b flushes this step
   auto step_of = [&](int b) {
@@ -744,11 +762,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       const unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * ((meta.w >> 16) & 3);
       const float* cob = reinterpret_cast<const float*>(gb + LY.gb_coef);
       const uint16_t* curb = reinterpret_cast<const uint16_t*>(gb + LY.gb_cur);
-      // the query times 2^64: the codes are decoded as their values times 2^-120
-      // (e4m3) or 2^-126 (e2m1), so each product is the true one times 2^-56 or
-      // 2^-62 (exact scalings); the output scale gsc undoes it
-      const float4 q4s = scale4(0x1p64f, reinterpret_cast<const float4*>(gb + LY.gb_qf)[lane]);
-      constexpr float kUnscale = READ == READ_FP8 ? 0x1p56f : 0x1p62f;
+      const float4 q4 = reinterpret_cast<const float4*>(gb + LY.gb_qf)[lane];
       constexpr int TBH = READ == READ_FP8 ? tile : tile / 2;  // code bytes per head
       const int recH = al16(C * P * 2) / 2;                   // record elements per head
       const uint16_t* xb = reinterpret_cast<const uint16_t*>(st + LY.st_rec);
@@ -762,7 +776,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
           ry[hu] = jl == 0 ? co[n] * bf(curb[(hh0 + hu) * P + Rq]) : 0.f;
           gsc[hu] = co[3 * C + CO_GAMMA] * (READ == READ_FP8
                                                 ? reinterpret_cast<const float*>(gb + LY.gb_rs)[(hh0 + hu) * P + Rq]
-                                                : co[3 * C + CO_MATSCALE]) * kUnscale;
+                                                : co[3 * C + CO_MATSCALE]);
         }
         // buffered terms: lanes 4kq..4kq+3 split the records 0..n-1 (lane jl = 0 took record n)
         for (int j = jl; j < n; j += 4) {
@@ -779,11 +793,15 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
             const int R = tw + TW * (r0 + e);
             if (READ == READ_FP8) {
               const uint32_t wd = reinterpret_cast<const uint32_t*>(cb + R * N)[lane];
-              part[hu][e] = dot4p(e4m3x4_scaled(wd), q4s);
+              const float2 lo = e4m3x2_to_f32x2(static_cast<uint16_t>(wd & 0xFFFFu));
+              const float2 hi = e4m3x2_to_f32x2(static_cast<uint16_t>(wd >> 16));
+              part[hu][e] = dot4p(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
             } else {
               const uint32_t wd = reinterpret_cast<const uint16_t*>(cb + R * (N / 2))[lane];
-              const float bs = e4m3_value(gb[LY.gb_rs + ((hh0 + hu) * P + R) * (N / 16) + (lane >> 2)]);
-              part[hu][e] = bs * dot4p(e2m1x4_scaled(wd), q4s);
+              const float2 lo = e2m1x2_to_f32x2(wd & 0xFFu);
+              const float2 hi = e2m1x2_to_f32x2(wd >> 8);
+              const float bs = e4m3_to_f32(gb[LY.gb_rs + ((hh0 + hu) * P + R) * (N / 16) + (lane >> 2)]);
+              part[hu][e] = bs * dot4p(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
             }
           }
         }
@@ -951,8 +969,9 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
               const float scale = __fdiv_rn(mx, 448.0f);
               uint32_t packed = 0;
               if (scale != 0.0f) {
-                const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(v4.x, scale), __fdiv_rn(v4.y, scale));
-                const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(v4.z, scale), __fdiv_rn(v4.w, scale));
+                const float rs = __frcp_rn(scale);
+                const uint32_t lo = f32x2_to_e4m3x2(div_by(v4.x, scale, rs), div_by(v4.y, scale, rs));
+                const uint32_t hi = f32x2_to_e4m3x2(div_by(v4.z, scale, rs), div_by(v4.w, scale, rs));
                 packed = lo | (hi << 16);
               }
               codes[R * SEG + lane] = packed;
@@ -994,9 +1013,11 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
                 if (six_s != 0.0f) bcode = f32x2_to_e4m3x2(__fdiv_rn(mb, six_s), 0.0f) & 0xFFu;
                 const float dd = __fmul_rn(e4m3_to_f32(bcode), smat);
                 uint32_t qv = 0;
-                if (dd != 0.0f)
-                  qv = f32x4_to_e2m1x4(__fdiv_rn(v4.x, dd), __fdiv_rn(v4.y, dd), __fdiv_rn(v4.z, dd),
-                                       __fdiv_rn(v4.w, dd));
+                if (dd != 0.0f) {
+                  const float rd = __frcp_rn(dd);
+                  qv = f32x4_to_e2m1x4(div_by(v4.x, dd, rd), div_by(v4.y, dd, rd), div_by(v4.z, dd, rd),
+                                       div_by(v4.w, dd, rd));
+                }
                 codes[R * SEG + lane] = static_cast<uint16_t>(qv);
                 if ((lane & 3) == 0) blk[R * (N / 16) + (lane >> 2)] = static_cast<uint8_t>(bcode);
               }
@@ -1123,6 +1144,13 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + s);
   }
+  // This CTA's units are done (or it aborted): the last of its computing warps counts
+  // the CTA in; the launch's last CTA writes every new cursor.  Every CTA read all the
+  // cursors it needed before its first unit, so none can see a cursor of this step
+  // already advanced.
+  int done = 0;
+  if (lane == 0) done = atomicAdd(reinterpret_cast<int*>(pbase + LY.pe_cnt), 1);
+  if (__shfl_sync(0xffffffffu, done, 0) == kThreads / 32 - 1) finish_launch(d, lane, C, L);
 }
 
 template <int KIND, int READ, int P, int TEAMS>

@@ -419,8 +419,9 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         const float scale = __fdiv_rn(mx, 448.0f);
         uint32_t packed = 0;
         if (scale != 0.0f) {
-          const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(v4.x, scale), __fdiv_rn(v4.y, scale));
-          const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(v4.z, scale), __fdiv_rn(v4.w, scale));
+          const float rs = __frcp_rn(scale);
+          const uint32_t lo = f32x2_to_e4m3x2(div_by(v4.x, scale, rs), div_by(v4.y, scale, rs));
+          const uint32_t hi = f32x2_to_e4m3x2(div_by(v4.z, scale, rs), div_by(v4.w, scale, rs));
           packed = lo | (hi << 16);
         }
         codes[R * SEG + lane] = packed;
@@ -461,8 +462,10 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           if (six_s != 0.0f) bcode = f32x2_to_e4m3x2(__fdiv_rn(mb, six_s), 0.0f) & 0xFFu;
           const float dd = __fmul_rn(e4m3_to_f32(bcode), smat);
           uint32_t qv = 0;
-          if (dd != 0.0f)
-            qv = f32x4_to_e2m1x4(__fdiv_rn(v4.x, dd), __fdiv_rn(v4.y, dd), __fdiv_rn(v4.z, dd), __fdiv_rn(v4.w, dd));
+          if (dd != 0.0f) {
+            const float rd = __frcp_rn(dd);
+            qv = f32x4_to_e2m1x4(div_by(v4.x, dd, rd), div_by(v4.y, dd, rd), div_by(v4.z, dd, rd), div_by(v4.w, dd, rd));
+          }
           codes[R * SEG + lane] = static_cast<uint16_t>(qv);
           if ((lane & 3) == 0) blk[R * (N / 16) + (lane >> 2)] = static_cast<uint8_t>(bcode);
         }

@@ -27,6 +27,9 @@ struct LayerDev {
   // (c * cta_mult + 7) mod grid instead of c; 0 = off.  Launchers make it coprime
   // with the grid, so the map is a permutation.
   int cta_mult;
+  // debug (comparison): the d_state-128 decode splits its units evenly instead of
+  // by weight; 0 = off
+  int uniform_split;
   float* ckpt;                 // [B][H][P][N]
   // Mamba-2 ring
   uint16_t* r_x;               // bf16 [B][H][C][P]

@@ -12,15 +12,18 @@
 // the scalar gate, the decayed keys k_j * W_j differ per value head, so the
 // record dot products are formed per head, not per key group.
 //
-// One CTA of 256 threads per (sequence, head).  It stages the buffered records
-// (log decays, keys, deltas) in shared memory, forms the decayed keys by a
-// channel-wise suffix scan, then makes one pass over the checkpoint rows:
+// One CTA of 256 threads per (sequence, head, block of up to 64 rows).  Every
+// thread issues its checkpoint rows' loads first, so that they are in flight
+// while the CTA stages the buffered records (log decays, keys, its rows'
+// deltas), forms the decayed keys by a channel-wise suffix scan and the record
+// dot products; then it finishes its rows:
 //   S k' = S_ckpt (G' * k) + sum_j u_j (k_j * W'_j . k),   S q' likewise,
 // with G', W' including this token's decay; u = b (v - S k'), o = S q' + u (k . q).
 // A non-flush step appends (g, u, k) to the ring and stores no state; the flush
 // step (the L-th record) writes S_ckpt Diag(G') + sum_j u_j (k_j * W'_j)^T + u k^T
 // once.  The fold without a token (rs_flush) writes S_ckpt Diag(G_n) +
-// sum_j u_j (k_j * W_j(n))^T.  The last CTA of a sequence advances its cursor.
+// sum_j u_j (k_j * W_j(n))^T.  The last CTA of a sequence to read its cursor
+// advances it.
 #include <math.h>
 #include <stdint.h>
 
@@ -31,22 +34,31 @@ namespace rs {
 namespace {
 
 constexpr int kKdaThreads = 256;
-constexpr int kPass = 8;  // row passes per warp batch
+constexpr int kWarps = kKdaThreads / 32;
+constexpr int kPass = 8;  // row passes per warp: one 16-byte load each in flight per thread
 
 __device__ __forceinline__ int kslot(int head, int j, int C) {
   const int s = head + j;
   return s >= C ? s - C : s;
 }
 
+// rows of one CTA: every warp takes kPass passes of 32 / (N/4) rows
+__host__ __device__ __forceinline__ int kda_rows(int N, int P) {
+  const int rows = kWarps * kPass * (32 / (N / 4));
+  return P < rows ? P : rows;
+}
+
 struct KdaSmem {
   int kt, u, kb, k, q, G, gq, gk, ck, cq, misc, size;  // float offsets
+  int ustride;                                          // floats per row of the deltas
 };
 
-__host__ __device__ __forceinline__ KdaSmem kda_smem(int P, int N, int C) {
+__host__ __device__ __forceinline__ KdaSmem kda_smem(int R, int N, int C) {
   KdaSmem m;
   int o = 0;
-  m.kt = o;   o += C * N;   // decayed keys k_j * W'_j  [records][N] (log decays first, in place)
-  m.u = o;    o += C * P;   // deltas u_j [records][P]
+  m.ustride = C | 1;        // odd: the lanes of a row read consecutive records without bank conflicts
+  m.kt = o;   o += C * N;   // decayed keys k_j * W'_j [records][N] (the log decays first, in place)
+  m.u = o;    o += (R * m.ustride + 3) & ~3;  // this CTA's rows' deltas [rows][records]
   m.kb = o;   o += C * N / 2;  // the records' keys, bf16 [records][N]
   m.k = o;    o += N;       // this token's key
   m.q = o;    o += N;       // this token's query
@@ -55,7 +67,7 @@ __host__ __device__ __forceinline__ KdaSmem kda_smem(int P, int N, int C) {
   m.gq = o;   o += N;       // G' * q
   m.ck = o;   o += C;       // (k_j * W'_j) . k
   m.cq = o;   o += C;       // (k_j * W'_j) . q
-  m.misc = o; o += 8;       // k . q, cursor head / count / status
+  m.misc = o; o += 4;       // k . q
   m.size = o;
   return m;
 }
@@ -63,18 +75,22 @@ __host__ __device__ __forceinline__ KdaSmem kda_smem(int P, int N, int C) {
 // FOLD = false: one decode token per sequence; true: fold the buffered records
 // of the masked sequences (no token).
 template <int N, bool FOLD>
-__global__ void __launch_bounds__(kKdaThreads) kda_kernel(const LayerDev d, const TokenIn in, float* __restrict__ y,
-                                                           const uint8_t* __restrict__ mask) {
+__global__ void __launch_bounds__(kKdaThreads, 3) kda_kernel(const LayerDev d, const TokenIn in,
+                                                              float* __restrict__ y,
+                                                              const uint8_t* __restrict__ mask) {
   constexpr int SEG = N / 4, RPP = 32 / SEG, ROWS = kPass * RPP;
   extern __shared__ __align__(16) float sm[];
   const int P = d.P, H = d.H, G = d.G, C = d.C, L = d.L;
+  const int R = kda_rows(N, P), parts = (P + R - 1) / R;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int c = lane % SEG, rsub = lane / SEG;
-  const int u = blockIdx.x;
+  const int blk = blockIdx.x;
+  const int u = blk / parts, part = blk - u * parts;
   const int b = u / H, h = u - b * H;
   const int g = h / (H / G);
+  const int r0 = part * R;  // first row of this CTA
   const size_t bh = static_cast<size_t>(u), bg = static_cast<size_t>(b) * G + g;
-  const KdaSmem M = kda_smem(P, N, C);
+  const KdaSmem M = kda_smem(R, N, C);
   float* skt = sm + M.kt;
   float* su = sm + M.u;
   uint16_t* skb = reinterpret_cast<uint16_t*>(sm + M.kb);
@@ -87,41 +103,72 @@ __global__ void __launch_bounds__(kKdaThreads) kda_kernel(const LayerDev d, cons
   float* scq = sm + M.cq;
   float* smisc = sm + M.misc;
 
+  // this thread's checkpoint rows and values first: in flight during the staging below
+  float4* S4 = reinterpret_cast<float4*>(d.ckpt + bh * static_cast<size_t>(P) * N);
+  const int wrow = r0 + warp * ROWS + rsub;  // row of pass 0 (pass k adds k RPP)
+  float4 s[kPass];
+  float vr[kPass];
+#pragma unroll
+  for (int k = 0; k < kPass; ++k) {
+    const int row = wrow + k * RPP;
+    const bool in_cta = row < r0 + R && row < P;
+    s[k] = in_cta ? __ldcs(S4 + static_cast<size_t>(row) * SEG + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    vr[k] = (!FOLD && in_cta) ? bf(in.v[bh * P + row]) : 0.f;
+  }
+
+  // this token's key, query and channel decay (thread t < N holds channel t), beta
+  const float gch = (!FOLD && t < N) ? in.g[bh * N + t] : 0.f;
+  const uint16_t kbits = (!FOLD && t < N) ? in.k[bg * N + t] : 0, qbits = (!FOLD && t < N) ? in.q[bg * N + t] : 0;
+  const float beta = FOLD ? 0.f : in.beta[bh];
+
   const int head = d.cursor[4 * b], cnt = d.cursor[4 * b + 1];
   const bool ok = static_cast<unsigned>(head) < static_cast<unsigned>(C) &&
                   static_cast<unsigned>(cnt) < static_cast<unsigned>(L);
   const bool work = ok && (!FOLD || mask == nullptr || mask[b] != 0);
   const int n = work ? cnt : 0;                  // buffered records
   const bool flush = work && (FOLD || cnt + 1 == L);
+  // The last CTA of the sequence to have read its cursor advances it (no CTA reads
+  // another sequence's cursor); thread 0's atomic overlaps the staging below.
+  if (t == 0 && arrive_last(d.arrive, b, H * parts)) {
+    if (!ok) {
+      report_error(d.err, DEVERR_CURSOR, b);
+    } else if (flush) {
+      d.cursor[4 * b] = kslot(head, FOLD ? cnt : cnt + 1, C);
+      d.cursor[4 * b + 1] = 0;
+      d.cursor[4 * b + 2] = 1;
+    } else if (FOLD) {
+      d.cursor[4 * b + 2] = 0;
+    } else {
+      d.cursor[4 * b + 1] = cnt + 1;
+      d.cursor[4 * b + 2] = 0;
+    }
+  }
 
   if (work) {
-    // stage: records' log decays (into skt, turned into decayed keys below), keys, deltas
+    // stage: the records' log decays (into skt, turned into decayed keys below) and
+    // keys, this CTA's rows' deltas, this token's key and query
     const float* rg = d.r_g + bh * C * N;
     const uint16_t* rk = d.r_k + bg * C * N;
     const float* ru = d.r_u + bh * C * P;
     for (int e = t; e < n * N; e += kKdaThreads) {
       const int j = e / N, ch = e - j * N;
-      skt[e] = rg[static_cast<size_t>(kslot(head, j, C)) * N + ch];
+      const size_t src = static_cast<size_t>(kslot(head, j, C)) * N + ch;
+      skt[e] = rg[src];
+      skb[e] = rk[src];
     }
-    for (int e = t; e < n * P; e += kKdaThreads) {
-      const int j = e / P, r = e - j * P;
-      su[e] = ru[static_cast<size_t>(kslot(head, j, C)) * P + r];
+    for (int e = t; e < n * R; e += kKdaThreads) {
+      const int j = e / R, r = e - j * R;
+      su[r * M.ustride + j] = r0 + r < P ? ru[static_cast<size_t>(kslot(head, j, C)) * P + r0 + r] : 0.f;
     }
-    for (int e = t; e < n * N; e += kKdaThreads) {
-      const int j = e / N, ch = e - j * N;
-      skb[e] = rk[static_cast<size_t>(kslot(head, j, C)) * N + ch];
-    }
-    if (!FOLD) {
-      for (int e = t; e < N; e += kKdaThreads) {
-        sk[e] = bf(in.k[bg * N + e]);
-        sq[e] = bf(in.q[bg * N + e]);
-      }
+    if (!FOLD && t < N) {
+      sk[t] = bf(kbits);
+      sq[t] = bf(qbits);
     }
     __syncthreads();
     // channel-wise suffix scan: W'_j = exp(sum of the log decays after record j,
     // this token's included), decayed key k_j * W'_j; G' = exp(all of them)
     for (int ch = t; ch < N; ch += kKdaThreads) {
-      float acc = FOLD ? 0.f : in.g[bh * N + ch];
+      float acc = gch;  // this token's log decay (0 for a fold)
       for (int j = n - 1; j >= 0; --j) {
         const float gj = skt[j * N + ch];
         skt[j * N + ch] = bf(skb[j * N + ch]) * expf(acc);
@@ -137,120 +184,91 @@ __global__ void __launch_bounds__(kKdaThreads) kda_kernel(const LayerDev d, cons
     __syncthreads();
     if (!FOLD) {
       // record dots (k_j * W'_j) . k and . q, and k . q: one warp per item
-      for (int it = warp; it < 2 * n + 1; it += kKdaThreads / 32) {
+      for (int it = warp; it < 2 * n + 1; it += kWarps) {
         const float* a = it < 2 * n ? skt + (it >> 1) * N : sk;
         const float* bvec = (it < 2 * n && (it & 1) == 0) ? sk : sq;
-        float s = 0.f;
-        for (int ch = lane; ch < N; ch += 32) s = fmaf(a[ch], bvec[ch], s);
-        s = seg_sum<32>(s);
+        float sacc = 0.f;
+        for (int ch = lane; ch < N; ch += 32) sacc = fmaf(a[ch], bvec[ch], sacc);
+        sacc = seg_sum<32>(sacc);
         if (lane == 0) {
-          if (it == 2 * n) smisc[0] = s;
-          else if ((it & 1) == 0) sck[it >> 1] = s;
-          else scq[it >> 1] = s;
+          if (it == 2 * n) smisc[0] = sacc;
+          else if ((it & 1) == 0) sck[it >> 1] = sacc;
+          else scq[it >> 1] = sacc;
         }
       }
       __syncthreads();
     }
-  }
 
-  if (work) {
     const float4 G4 = reinterpret_cast<const float4*>(sG)[c];
     const float4 gk4 = FOLD ? make_float4(0.f, 0.f, 0.f, 0.f) : reinterpret_cast<const float4*>(sgk)[c];
     const float4 gq4 = FOLD ? make_float4(0.f, 0.f, 0.f, 0.f) : reinterpret_cast<const float4*>(sgq)[c];
     const float4 k4 = FOLD ? make_float4(0.f, 0.f, 0.f, 0.f) : reinterpret_cast<const float4*>(sk)[c];
     const float kq = FOLD ? 0.f : smisc[0];
-    const float beta = FOLD ? 0.f : in.beta[bh];
-    float4* S4 = reinterpret_cast<float4*>(d.ckpt + bh * static_cast<size_t>(P) * N);
     const int slot = kslot(head, n, C);
-    for (int base = warp * ROWS; base < P; base += (kKdaThreads / 32) * ROWS) {
-      float4 s[kPass];
+    float ud[kPass];
+    if (!FOLD) {
+      // checkpoint terms (row totals over the row's lanes) and buffered-record terms
+      // (the row's lanes split the records)
+      float tk[kPass], tq[kPass];
 #pragma unroll
       for (int k = 0; k < kPass; ++k) {
-        const int row = base + k * RPP + rsub;
-        s[k] = row < P ? __ldcs(S4 + static_cast<size_t>(row) * SEG + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      float ud[kPass];
-      if (!FOLD) {
-        // checkpoint terms (row totals over the row's lanes) and buffered-record terms
-        // (the row's lanes split the records)
-        float tk[kPass], tq[kPass];
-#pragma unroll
-        for (int k = 0; k < kPass; ++k) {
-          const int row = base + k * RPP + rsub;
-          float pk = dot4(s[k], gk4), pq = dot4(s[k], gq4);
-          if (row < P) {
-            for (int j = c; j < n; j += SEG) {
-              const float uj = su[j * P + row];
-              pk = fmaf(uj, sck[j], pk);
-              pq = fmaf(uj, scq[j], pq);
-            }
+        const int row = wrow + k * RPP;
+        float pk = dot4(s[k], gk4), pq = dot4(s[k], gq4);
+        if (row < r0 + R && row < P) {
+          const float* urow = su + (row - r0) * M.ustride;
+          for (int j = c; j < n; j += SEG) {
+            const float uj = urow[j];
+            pk = fmaf(uj, sck[j], pk);
+            pq = fmaf(uj, scq[j], pq);
           }
-          tk[k] = seg_sum<SEG>(pk);
-          tq[k] = seg_sum<SEG>(pq);
         }
+        tk[k] = seg_sum<SEG>(pk);
+        tq[k] = seg_sum<SEG>(pq);
+      }
 #pragma unroll
-        for (int k = 0; k < kPass; ++k) {
-          const int row = base + k * RPP + rsub;
-          ud[k] = 0.f;
-          if (row < P) {
-            ud[k] = beta * (bf(in.v[bh * P + row]) - tk[k]);  // u = b (v - S k')
-            if (c == 0) {
-              y[bh * P + row] = fmaf(ud[k], kq, tq[k]);      // o = S q' + u (k . q)
-              if (!flush) d.r_u[(bh * C + slot) * P + row] = ud[k];
-            }
+      for (int k = 0; k < kPass; ++k) {
+        const int row = wrow + k * RPP;
+        ud[k] = 0.f;
+        if (row < r0 + R && row < P) {
+          ud[k] = beta * (vr[k] - tk[k]);  // u = b (v - S k')
+          if (c == 0) {
+            y[bh * P + row] = fmaf(ud[k], kq, tq[k]);  // o = S q' + u (k . q)
+            if (!flush) d.r_u[(bh * C + slot) * P + row] = ud[k];
           }
         }
       }
-      if (flush) {
-        // S_new = S_ckpt Diag(G') + sum_j u_j (k_j * W'_j)^T (+ u k^T for a token)
+    }
+    if (flush) {
+      // S_new = S_ckpt Diag(G') + sum_j u_j (k_j * W'_j)^T (+ u k^T for a token)
 #pragma unroll
-        for (int k = 0; k < kPass; ++k) {
-          const int row = base + k * RPP + rsub;
-          if (row >= P) continue;
-          float4 acc = make_float4(s[k].x * G4.x, s[k].y * G4.y, s[k].z * G4.z, s[k].w * G4.w);
-          for (int j = 0; j < n; ++j)
-            acc = axpy4(su[j * P + row], reinterpret_cast<const float4*>(skt + j * N)[c], acc);
-          if (!FOLD) acc = axpy4(ud[k], k4, acc);
-          __stcs(S4 + static_cast<size_t>(row) * SEG + c, acc);
-        }
+      for (int k = 0; k < kPass; ++k) {
+        const int row = wrow + k * RPP;
+        if (row >= r0 + R || row >= P) continue;
+        const float* urow = su + (row - r0) * M.ustride;
+        float4 acc = make_float4(s[k].x * G4.x, s[k].y * G4.y, s[k].z * G4.z, s[k].w * G4.w);
+        for (int j = 0; j < n; ++j) acc = axpy4(urow[j], reinterpret_cast<const float4*>(skt + j * N)[c], acc);
+        if (!FOLD) acc = axpy4(ud[k], k4, acc);
+        __stcs(S4 + static_cast<size_t>(row) * SEG + c, acc);
       }
     }
-  }
-
-  // a non-flush step appends this token's record: g over the key channels and u
-  // (above) per head, k once per key group
-  if (!FOLD && work && !flush) {
-    const int slot = kslot(head, n, C);
-    for (int ch = t; ch < N; ch += kKdaThreads) {
-      d.r_g[(bh * C + slot) * N + ch] = in.g[bh * N + ch];
-      if (h % (H / G) == 0) d.r_k[(bg * C + slot) * N + ch] = in.k[bg * N + ch];
-    }
-  }
-  // the last CTA of the sequence advances the cursor (every CTA has read it by now)
-  __syncthreads();
-  if (t == 0 && arrive_last(d.arrive, b, H)) {
-    if (!ok) {
-      report_error(d.err, DEVERR_CURSOR, b);
-    } else if (flush) {
-      d.cursor[4 * b] = kslot(head, FOLD ? cnt : cnt + 1, C);
-      d.cursor[4 * b + 1] = 0;
-      d.cursor[4 * b + 2] = 1;
-    } else if (FOLD) {
-      d.cursor[4 * b + 2] = 0;
-    } else {
-      d.cursor[4 * b + 1] = cnt + 1;
-      d.cursor[4 * b + 2] = 0;
+    // a non-flush step appends this token's record: g over the key channels and u
+    // (above) per head, k once per key group (by the CTAs of the group's first head)
+    if (!FOLD && !flush && part == 0 && t < N) {
+      d.r_g[(bh * C + slot) * N + t] = gch;
+      if (h % (H / G) == 0) d.r_k[(bg * C + slot) * N + t] = kbits;
     }
   }
 }
 
 template <int N, bool FOLD>
 cudaError_t launch_kda_n(const LayerDev& d, const TokenIn& in, float* y, const uint8_t* mask, cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(kda_smem(d.P, N, d.C).size) * 4;
+  const int R = kda_rows(N, d.P);
+  const int parts = (d.P + R - 1) / R;
+  const size_t smem = static_cast<size_t>(kda_smem(R, N, d.C).size) * 4;
   auto kernel = kda_kernel<N, FOLD>;
   const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
-  kernel<<<d.B * d.H, kKdaThreads, smem, s>>>(d, in, y, mask);
+  kernel<<<d.B * d.H * parts, kKdaThreads, smem, s>>>(d, in, y, mask);
   return cudaGetLastError();
 }
 

@@ -33,7 +33,11 @@
  * - Environment (debug only): RS_DEBUG_CTA_PERMUTE=<m>, m >= 2, read by
  *   rs_create_cache and by every rs_decode_step_noalloc call, permutes which
  *   CTA of the persistent decode and commit launches takes which range of
- *   work (an ordering check); results do not change.  Unset in normal use.
+ *   work (an ordering check); results do not change.  RS_DEBUG_UNIFORM_SPLIT=1,
+ *   read by rs_create_cache, makes the d_state-128 decode launch split its work
+ *   evenly over its CTAs instead of by weight (a flush unit counts more), to
+ *   measure what the weighted split buys in batches at mixed window positions;
+ *   results do not change.  Unset in normal use.
  * - Kernels never trap.  A problem found on the device (corrupt cursor,
  *   accepted count out of range, a staged copy that did not arrive in time)
  *   sets a sticky device error word and leaves that sequence untouched;

@@ -142,7 +142,8 @@ def test_the_model_catches_one_stage_too_many():
 
 def _split(weights, upseq, grid, hr=1):
     """Unit range of every CTA: units whose weight interval starts in
-    [c W / grid, (c + 1) W / grid), rounded down to multiples of hr (the launch's rule)."""
+    [c ceil(W / grid), (c + 1) ceil(W / grid)), rounded down to multiples of hr (the
+    launch's rule)."""
     W = sum(weights) * upseq
     def units_before(T):
         cum, n = 0, 0
@@ -151,7 +152,8 @@ def _split(weights, upseq, grid, hr=1):
                 n += min(upseq, -(-(T - cum) // w))
             cum += w * upseq
         return n - n % hr
-    bounds = [units_before(c * W // grid) for c in range(grid)] + [len(weights) * upseq]
+    per_w = -(-W // grid)
+    bounds = [units_before(min(W, c * per_w)) for c in range(grid)] + [len(weights) * upseq]
     return list(zip(bounds[:-1], bounds[1:]))
 
 
@@ -176,3 +178,10 @@ def test_weighted_split_keeps_read_copy_units_whole():
     weights = [9 if b % 7 == 0 else 4 for b in range(40)]
     for lo, hi in _split(weights, 16, 152, hr=4):
         assert lo % 4 == 0 and hi % 4 == 0
+
+
+def test_weighted_split_with_equal_weights_is_the_even_split():
+    B, upseq, grid = 256, 64, 152
+    per = -(-B * upseq // grid)
+    ranges = _split([4] * B, upseq, grid)
+    assert ranges == [(min(c * per, B * upseq), min((c + 1) * per, B * upseq)) for c in range(grid)]

@@ -35,12 +35,18 @@ def _stagger(pair, L):
         pair.check_cursor(f"stagger flush {k}")
 
 
-@pytest.mark.parametrize("kind,P,permute", [(MAMBA2, 64, None), (GDN, 128, None), (MAMBA2, 64, "7")])
-def test_mixed_window_positions_every_step(kind, P, permute, monkeypatch):
+@pytest.mark.parametrize("kind,P,permute,even", [(MAMBA2, 64, None, False), (GDN, 128, None, False),
+                                                 (MAMBA2, 64, "7", False), (GDN, 128, None, True)])
+def test_mixed_window_positions_every_step(kind, P, permute, even, monkeypatch):
+    """Also with the CTA order permuted, and with the even split (the debug comparison)."""
     if permute is None:
         monkeypatch.delenv("RS_DEBUG_CTA_PERMUTE", raising=False)
     else:
         monkeypatch.setenv("RS_DEBUG_CTA_PERMUTE", permute)
+    if even:
+        monkeypatch.setenv("RS_DEBUG_UNIFORM_SPLIT", "1")
+    else:
+        monkeypatch.delenv("RS_DEBUG_UNIFORM_SPLIT", raising=False)
     L = 6
     shape = LayerShape(kind, batch=37, n_heads=8, n_groups=2, d_head=P, d_state=128, ring_len=L)
     wl = configs.workload(shape, seed=141 + P, s0_std=0.1 if kind == MAMBA2 else 0.05)

@@ -148,3 +148,50 @@ def test_read_copy_d128_mixed_window_positions(mode):
             pair.check_ckpt(f"{mode} step {t}")
     assert mixed > 0  # some launches had flush and non-flush sequences together
     assert pair.cache.device_error() == 0
+
+
+def _adversarial_state(shape, seed):
+    """Rows whose elements sit at, or one FP32 ulp either side of, the midpoints between
+    neighbouring e4m3 / e2m1 values once divided by the row's (or block's) scale: the
+    cases where the quantiser's quotient decides the code."""
+    rng = np.random.default_rng(seed)
+    B, H, P, N = shape.batch, shape.n_heads, shape.d_head, shape.d_state
+    e4m3 = np.unique(np.abs(codecs.e4m3_decode(np.arange(0, 0x7F))))
+    mids = (e4m3[1:] + e4m3[:-1]) / 2
+    e2m1 = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    mids2 = (e2m1[1:] + e2m1[:-1]) / 2
+    S = np.empty((B, H, P, N), dtype=np.float32)
+    for idx in np.ndindex(B, H, P):
+        scale = np.float32(np.exp(rng.uniform(-6, 2)))
+        pick = mids if idx[2] % 2 == 0 else mids2
+        v = rng.choice(pick, N) * scale
+        v = np.nextafter(v.astype(np.float32), rng.choice([-np.inf, np.inf], N).astype(np.float32)) \
+            if idx[2] % 3 == 0 else v.astype(np.float32)
+        v = v * rng.choice([-1, 1], N)
+        v[0] = np.float32(448.0) * scale            # row maximum fixes the FP8 scale
+        S[idx] = v
+    return S
+
+
+@pytest.mark.parametrize("mode", ["fp8", "nvfp4"])
+def test_quantiser_at_rounding_midpoints_bit_exact(mode):
+    """The quantiser divides by a per-row / per-block scale with a reciprocal and one
+    fused correction; at midpoints and one ulp beside them its codes must still be
+    those of the oracle codec (IEEE division, round-to-nearest-even)."""
+    shape = LayerShape(MAMBA2, batch=2, n_heads=4, n_groups=2, d_head=64, d_state=128, ring_len=4)
+    from checkpoint_input_replay_gb300 import ReplayCache
+    cache = ReplayCache.for_shape(shape, read_mode=mode)
+    S = _adversarial_state(shape, 45)
+    cache.ckpt.copy_(torch.from_numpy(S))
+    cache.flush()
+    v = cache.read_copy_views()
+    if mode == "fp8":
+        codes, sc = codecs.fp8_rows_quantize(S)
+        np.testing.assert_array_equal(v["row_scale"].cpu().numpy(), sc)
+        np.testing.assert_array_equal(v["codes"].cpu().numpy(), codes)
+    else:
+        packed, bs, sm = codecs.nvfp4_quantize(S)
+        np.testing.assert_array_equal(v["matrix_scale"].cpu().numpy(), sm)
+        np.testing.assert_array_equal(v["block_scale"].cpu().numpy(), bs)
+        np.testing.assert_array_equal(v["codes"].cpu().numpy(), packed)
+    assert cache.device_error() == 0
