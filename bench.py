@@ -585,7 +585,8 @@ def read_copy_error_leg(wl, dev, mode, steps):
     assert exact.device_error() == 0 and quant.device_error() == 0
     del exact, quant
     torch.cuda.empty_cache()
-    return {"per_window_rel_l2": [round(float(x), 6) for x in per_window],
+    return {"per_window_rel_l2_first8": [round(float(x), 6) for x in per_window[:8]],
+            "per_window_rel_l2_last4": [round(float(x), 6) for x in per_window[-4:]],
             "windows": nw, "max_window_ge1": float(per_window[1:].max()),
             "aggregate_rel_l2": float(np.sqrt(num.sum().item() / den.sum().item())),
             "first8_mean": float(per_window[1:9].mean()), "last8_mean": float(per_window[-8:].mean()),

@@ -12,11 +12,12 @@
 // the scalar gate, the decayed keys k_j * W_j differ per value head, so the
 // record dot products are formed per head, not per key group.
 //
-// One CTA of 256 threads per (sequence, head, block of up to 64 rows).  Every
-// thread issues its checkpoint rows' loads first, so that they are in flight
-// while the CTA stages the buffered records (log decays, keys, its rows'
-// deltas), forms the decayed keys by a channel-wise suffix scan and the record
-// dot products; then it finishes its rows:
+// One CTA of 256 threads per (sequence, head, block of up to 64 rows).  The
+// block's checkpoint rows (contiguous) are requested first, by one bulk copy
+// into shared memory, so that they are in flight while the CTA stages the
+// buffered records (log decays, keys, its rows' deltas), forms the decayed keys
+// by a channel-wise suffix scan and the record dot products; then it finishes
+// its rows:
 //   S k' = S_ckpt (G' * k) + sum_j u_j (k_j * W'_j . k),   S q' likewise,
 // with G', W' including this token's decay; u = b (v - S k'), o = S q' + u (k . q).
 // A non-flush step appends (g, u, k) to the ring and stores no state; the flush
@@ -49,14 +50,16 @@ __host__ __device__ __forceinline__ int kda_rows(int N, int P) {
 }
 
 struct KdaSmem {
-  int kt, u, kb, k, q, G, gq, gk, ck, cq, misc, size;  // float offsets
-  int ustride;                                          // floats per row of the deltas
+  int tile, bar, kt, u, kb, k, q, G, gq, gk, ck, cq, misc, size;  // float offsets
+  int ustride;                                                     // floats per row of the deltas
 };
 
 __host__ __device__ __forceinline__ KdaSmem kda_smem(int R, int N, int C) {
   KdaSmem m;
   int o = 0;
   m.ustride = C | 1;        // odd: the lanes of a row read consecutive records without bank conflicts
+  m.tile = o; o += R * N;   // the CTA's checkpoint rows, by one bulk copy
+  m.bar = o;  o += 4;       // its mbarrier
   m.kt = o;   o += C * N;   // decayed keys k_j * W'_j [records][N] (the log decays first, in place)
   m.u = o;    o += (R * m.ustride + 3) & ~3;  // this CTA's rows' deltas [rows][records]
   m.kb = o;   o += C * N / 2;  // the records' keys, bf16 [records][N]
@@ -75,7 +78,7 @@ __host__ __device__ __forceinline__ KdaSmem kda_smem(int R, int N, int C) {
 // FOLD = false: one decode token per sequence; true: fold the buffered records
 // of the masked sequences (no token).
 template <int N, bool FOLD>
-__global__ void __launch_bounds__(kKdaThreads, 3) kda_kernel(const LayerDev d, const TokenIn in,
+__global__ void __launch_bounds__(kKdaThreads, 4) kda_kernel(const LayerDev d, const TokenIn in,
                                                               float* __restrict__ y,
                                                               const uint8_t* __restrict__ mask) {
   constexpr int SEG = N / 4, RPP = 32 / SEG, ROWS = kPass * RPP;
@@ -103,17 +106,23 @@ __global__ void __launch_bounds__(kKdaThreads, 3) kda_kernel(const LayerDev d, c
   float* scq = sm + M.cq;
   float* smisc = sm + M.misc;
 
-  // this thread's checkpoint rows and values first: in flight during the staging below
+  // The CTA's checkpoint rows (contiguous) by one bulk copy into shared memory, in
+  // flight during the staging below; this thread's rows' values v.
   float4* S4 = reinterpret_cast<float4*>(d.ckpt + bh * static_cast<size_t>(P) * N);
+  const int nrows = min(R, P - r0);
+  uint64_t* tbar = reinterpret_cast<uint64_t*>(sm + M.bar);
+  if (t == 0) {
+    mbar_init(tbar, 1);
+    mbar_expect_tx(tbar, static_cast<uint32_t>(nrows * N * 4));
+    bulk_g2s(sm + M.tile, d.ckpt + (bh * P + r0) * static_cast<size_t>(N), static_cast<uint32_t>(nrows * N * 4), tbar);
+  }
+  __syncthreads();  // the barrier's initialisation before anyone waits on it
   const int wrow = r0 + warp * ROWS + rsub;  // row of pass 0 (pass k adds k RPP)
-  float4 s[kPass];
   float vr[kPass];
 #pragma unroll
   for (int k = 0; k < kPass; ++k) {
     const int row = wrow + k * RPP;
-    const bool in_cta = row < r0 + R && row < P;
-    s[k] = in_cta ? __ldcs(S4 + static_cast<size_t>(row) * SEG + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-    vr[k] = (!FOLD && in_cta) ? bf(in.v[bh * P + row]) : 0.f;
+    vr[k] = (!FOLD && row < r0 + nrows) ? bf(in.v[bh * P + row]) : 0.f;
   }
 
   // this token's key, query and channel decay (thread t < N holds channel t), beta
@@ -199,6 +208,20 @@ __global__ void __launch_bounds__(kKdaThreads, 3) kda_kernel(const LayerDev d, c
       __syncthreads();
     }
 
+    // the rows have landed (bounded wait; on a timeout the CTA reports it, waits once
+    // more for its copy and skips the sequence)
+    if (!__syncthreads_and(mbar_wait_bounded(tbar, 0))) {
+      if (t == 0) report_error(d.err, DEVERR_TIMEOUT, b);
+      mbar_wait_bounded(tbar, 0);
+      return;
+    }
+    float4 s[kPass];
+#pragma unroll
+    for (int k = 0; k < kPass; ++k) {
+      const int row = wrow + k * RPP;
+      s[k] = row < r0 + nrows ? reinterpret_cast<const float4*>(sm + M.tile)[(row - r0) * SEG + c]
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     const float4 G4 = reinterpret_cast<const float4*>(sG)[c];
     const float4 gk4 = FOLD ? make_float4(0.f, 0.f, 0.f, 0.f) : reinterpret_cast<const float4*>(sgk)[c];
     const float4 gq4 = FOLD ? make_float4(0.f, 0.f, 0.f, 0.f) : reinterpret_cast<const float4*>(sgq)[c];
@@ -257,6 +280,10 @@ __global__ void __launch_bounds__(kKdaThreads, 3) kda_kernel(const LayerDev d, c
       d.r_g[(bh * C + slot) * N + t] = gch;
       if (h % (H / G) == 0) d.r_k[(bg * C + slot) * N + t] = kbits;
     }
+  } else {
+    // nothing to do for this sequence: the rows' copy must still land before the
+    // CTA's shared memory is released
+    mbar_wait_bounded(tbar, 0);
   }
 }
 
