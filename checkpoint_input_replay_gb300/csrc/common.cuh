@@ -265,6 +265,27 @@ __device__ __forceinline__ float div_by(float x, float d, float r) {
   return __fmaf_rn(__fmaf_rn(-q, d, x), r, q);
 }
 
+// Sum each of v[0..7] over the eight lanes that share lane >> 3 (transpose-reduce:
+// 7 shuffles).  Lane L returns the total of v[L & 7] over its eight lanes.
+__device__ __forceinline__ float reduce8_lanes3(const float v[8], int lane) {
+  const bool b2 = (lane & 4) != 0, b1 = (lane & 2) != 0, b0 = (lane & 1) != 0;
+  float w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = b2 ? v[i] : v[i + 4];
+    const float keep = b2 ? v[i + 4] : v[i];
+    w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  float x[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = b1 ? w[i] : w[i + 2];
+    const float keep = b1 ? w[i + 2] : w[i];
+    x[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  }
+  return (b0 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, b0 ? x[0] : x[1], 1);
+}
+
 // Sum each of v[0..7] over the 32 lanes of the warp (transpose-reduce: 9
 // shuffles).  Lane L returns the total of v[(L >> 2) & 7].
 __device__ __forceinline__ float reduce8(const float v[8], int lane) {

@@ -71,7 +71,7 @@ enum : int { CO_GAMMA = 0, CO_A = 1, CO_BETA = 2, CO_KQ = 3, CO_MATSCALE = 4 };
 
 // Shared-memory layout (bytes): [stages][3 group buffers][persistent].
 struct Lay128 {
-  int st_tile, st_rec, st_meta, st_size;
+  int st_tile, st_rec, st_meta, st_size, rec_stride;
   int gb_key, gb_q, gb_cur, gb_la, gb_dt, gb_s1, gb_s2, gb_rs, gb_ms, gb_qf, gb_kf, gb_coef, gb_size;
   int pe_A, pe_bars, pe_seq, pe_misc, pe_cnt, pe_mtab, pe_dq, pe_size;
 };
@@ -90,7 +90,9 @@ __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int
   int o = 0;
   const int rpu = P / splits(kind, P);  // state rows per unit
   l.st_tile = o;  o += rpu * N * 4;
-  l.st_rec = o;   o += kind == 0 ? read_heads(read) * al16(C * P * 2) : C * rpu * 4;
+  // a read-copy unit's heads' record blocks sit 16 bytes off the 128-byte bank period
+  l.rec_stride = al16(C * P * 2) + (read == READ_NONE ? 0 : 16);
+  l.st_rec = o;   o += kind == 0 ? read_heads(read) * l.rec_stride : C * rpu * 4;
   l.st_meta = o;  o += 32;              // int4 descriptor, NVFP4 amax word
   l.st_size = al128(o);
   o = 0;
@@ -121,9 +123,11 @@ __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int
 }
 
 // the weighted work split needs the batch's per-sequence weights in shared memory
-// (in the computing warps' fold tables, before they are used)
-__host__ __device__ __forceinline__ bool balanced(const Lay128& l, int B) {
-  return B <= kBalanceMaxB && ((B + 3) & ~3) * 4 + B * 8 + 8 <= l.pe_dq - l.pe_mtab;
+// (in the computing warps' fold tables, before they are used), and its weight sums
+// (units x kWFlush at most) in 32 bits
+__host__ __device__ __forceinline__ bool balanced(const Lay128& l, int B, int upseq) {
+  return B <= kBalanceMaxB && ((B + 3) & ~3) * 4 + B * 8 + 8 <= l.pe_dq - l.pe_mtab &&
+         static_cast<long long>(B) * upseq * kWFlush < (1LL << 30);
 }
 
 __device__ __forceinline__ int ring_slot(int head, int j, int C) {
@@ -275,7 +279,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   const int total_units = d.B * upseq;
   const int cta = cta_index(d.cta_mult);
   int u0, u1;
-  const bool bal = balanced(LY, d.B) && !d.uniform_split;
+  const bool bal = balanced(LY, d.B, upseq) && !d.uniform_split;
   // scratch before the computing warps' fold tables are used: per-sequence weights,
   // the batch's cursors (head, count) and the two range bounds
   int* wts = reinterpret_cast<int*>(pbase + LY.pe_mtab);
@@ -288,7 +292,8 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     // total rather than of the units.  Every CTA computes every boundary from the
     // same cursors: no CTA changes a cursor before all have read them (below).
     for (int b = t; b < d.B; b += kThreads128) {
-      const int head = d.cursor[4 * b], cnt = d.cursor[4 * b + 1];
+      const int2 hc = reinterpret_cast<const int2*>(d.cursor)[2 * b];
+      const int head = hc.x, cnt = hc.y;
       const bool fl = static_cast<unsigned>(head) < static_cast<unsigned>(C) &&
                       static_cast<unsigned>(cnt) < static_cast<unsigned>(L) && cnt + 1 == L;
       wts[b] = fl ? kWFlush : kWPlain;
@@ -296,29 +301,35 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     }
     __syncthreads();
     if (warp == 0) {
+      // 32-bit sums (the launcher keeps total_units * kWFlush below 2^31) and
+      // constant divisors: this scan delays every CTA's first copy
       const int per_l = (d.B + 31) / 32;
       const int lo = min(lane * per_l, d.B), hi = min(lo + per_l, d.B);
-      long long sw = 0;
+      int sw = 0;
       for (int b = lo; b < hi; ++b) sw += wts[b];
-      long long incl = sw;
+      int incl = sw;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
       }
-      const long long W = __shfl_sync(0xffffffffu, incl, 31) * upseq;
-      const long long cum0 = (incl - sw) * upseq;  // weight before this lane's first sequence
+      const int W = __shfl_sync(0xffffffffu, incl, 31) * upseq;
+      const int cum0 = (incl - sw) * upseq;  // weight before this lane's first sequence
+      const int share = (W + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         // units whose weight interval starts before T = (cta + e) ceil(W / grid): with
         // equal weights these are the even split's boundaries
-        const long long T = min(W, static_cast<long long>(cta + e) * ((W + gridDim.x - 1) / gridDim.x));
-        long long cum = cum0;
+        const int T = min(W, (cta + e) * share);
+        int cum = cum0;
         int cntu = 0;
         for (int b = lo; b < hi; ++b) {
           const int w = wts[b];
-          if (T > cum) cntu += static_cast<int>(min(static_cast<long long>(upseq), (T - cum + w - 1) / w));
-          cum += static_cast<long long>(w) * upseq;
+          if (T > cum) {
+            const int x = T - cum;
+            cntu += min(upseq, w == kWPlain ? (x + kWPlain - 1) / kWPlain : (x + kWFlush - 1) / kWFlush);
+          }
+          cum += w * upseq;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) cntu += __shfl_xor_sync(0xffffffffu, cntu, o);
@@ -471,7 +482,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       constexpr size_t rrow = static_cast<size_t>(P) * esz;
       if (SPL == 1) {
         for (int hu = 0; hu < nh; ++hu) {
-          unsigned char* rdst = st + LY.st_rec + static_cast<size_t>(hu) * al16(C * P * 2);
+          unsigned char* rdst = st + LY.st_rec + static_cast<size_t>(hu) * LY.rec_stride;
           const size_t uh = u + hu;
           if (seg1) bulk_g2s(rdst, rsrc + (uh * C + head) * rrow, seg1 * rrow, bar);
           if (seg2) bulk_g2s(rdst + seg1 * rrow, rsrc + uh * C * rrow, seg2 * rrow, bar);
@@ -753,66 +764,84 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
     unsigned char* st = smem + static_cast<size_t>(LY.st_size) * s;
     const int4 meta = *reinterpret_cast<const int4*>(st + LY.st_meta);
     const int nh_unit = (READ != READ_NONE && !(meta.y & 0x100)) ? HR : 1;  // heads of this unit
-    if (KIND == 0 && READ != READ_NONE && nh_unit == HR && (meta.y & 0x200)) {
-      // non-flush unit of a read-copy layer: HR heads, their chains interleaved
-      // (record terms, code decoding and row reductions of the heads are independent)
+    if constexpr (KIND == 0 && READ != READ_NONE) if (nh_unit == HR && (meta.y & 0x200)) {
+      // Non-flush unit of a read-copy layer: HR heads of one group; warp tw takes
+      // rows RW tw .. RW tw + RW - 1 of each.  Codes: in pass f, lane 8 rq + cb
+      // decodes channels 16 cb .. 16 cb + 15 of row RW tw + 4 f + rq (one 16- or
+      // 8-byte shared load, one NVFP4 block scale), and the eight lanes of a row
+      // add their block dot products by a transpose-reduce that leaves each
+      // (head, row) total in one lane.  That lane also sums the row's buffered
+      // records (lanes of a warp read 16 distinct banks: the heads' record
+      // blocks are 16 bytes off the 128-byte period) and writes y.
+      static_assert(HR == 4 && RW % 4 == 0 && (RW / 4 * HR) % 8 == 0, "read-copy unit shape");
+      constexpr int NPASS = RW / 4;
+      constexpr int NV = NPASS * HR;  // block dot products per lane, reduced 8 at a time
       const int n = meta.y & 0xFF;
       const int hh0 = meta.w & 0xFFFF;
       const size_t uh0 = static_cast<size_t>(meta.x);
       const unsigned char* gb = gbase + static_cast<size_t>(LY.gb_size) * ((meta.w >> 16) & 3);
       const float* cob = reinterpret_cast<const float*>(gb + LY.gb_coef);
       const uint16_t* curb = reinterpret_cast<const uint16_t*>(gb + LY.gb_cur);
-      const float4 q4 = reinterpret_cast<const float4*>(gb + LY.gb_qf)[lane];
       constexpr int TBH = READ == READ_FP8 ? tile : tile / 2;  // code bytes per head
-      const int recH = al16(C * P * 2) / 2;                   // record elements per head
-      const uint16_t* xb = reinterpret_cast<const uint16_t*>(st + LY.st_rec);
+      const int rq = lane >> 3, cbk = lane & 7;
+      float2 qv[8];
 #pragma unroll
-      for (int r0 = 0; r0 < RW; r0 += 8) {
-        const int Rq = tw + TW * (r0 + kq);
-        float ry[HR], gsc[HR], part[HR][8];
+      for (int i = 0; i < 4; ++i) {
+        const float4 q4 = reinterpret_cast<const float4*>(gb + LY.gb_qf)[4 * cbk + i];
+        qv[2 * i] = make_float2(q4.x, q4.y);
+        qv[2 * i + 1] = make_float2(q4.z, q4.w);
+      }
+      float v[NV];
 #pragma unroll
-        for (int hu = 0; hu < HR; ++hu) {
-          const float* co = cob + (hh0 + hu) * CS;
-          ry[hu] = jl == 0 ? co[n] * bf(curb[(hh0 + hu) * P + Rq]) : 0.f;
-          gsc[hu] = co[3 * C + CO_GAMMA] * (READ == READ_FP8
-                                                ? reinterpret_cast<const float*>(gb + LY.gb_rs)[(hh0 + hu) * P + Rq]
-                                                : co[3 * C + CO_MATSCALE]);
-        }
-        // buffered terms: lanes 4kq..4kq+3 split the records 0..n-1 (lane jl = 0 took record n)
-        for (int j = jl; j < n; j += 4) {
-#pragma unroll
-          for (int hu = 0; hu < HR; ++hu)
-            ry[hu] = fmaf(cob[(hh0 + hu) * CS + j], bf(xb[hu * recH + j * P + Rq]), ry[hu]);
-        }
-        // the checkpoint term from the low-precision copies
+      for (int f = 0; f < NPASS; ++f) {
+        const int R = RW * tw + 4 * f + rq;
 #pragma unroll
         for (int hu = 0; hu < HR; ++hu) {
-          const unsigned char* cb = st + LY.st_tile + hu * TBH;
+          const unsigned char* cbp = st + LY.st_tile + hu * TBH;
+          float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+          if (READ == READ_FP8) {
+            const uint4 wv = *reinterpret_cast<const uint4*>(cbp + R * N + 16 * cbk);
+            const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int R = tw + TW * (r0 + e);
-            if (READ == READ_FP8) {
-              const uint32_t wd = reinterpret_cast<const uint32_t*>(cb + R * N)[lane];
-              const float2 lo = e4m3x2_to_f32x2(static_cast<uint16_t>(wd & 0xFFFFu));
-              const float2 hi = e4m3x2_to_f32x2(static_cast<uint16_t>(wd >> 16));
-              part[hu][e] = dot4p(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
-            } else {
-              const uint32_t wd = reinterpret_cast<const uint16_t*>(cb + R * (N / 2))[lane];
-              const float2 lo = e2m1x2_to_f32x2(wd & 0xFFu);
-              const float2 hi = e2m1x2_to_f32x2(wd >> 8);
-              const float bs = e4m3_to_f32(gb[LY.gb_rs + ((hh0 + hu) * P + R) * (N / 16) + (lane >> 2)]);
-              part[hu][e] = bs * dot4p(make_float4(lo.x, lo.y, hi.x, hi.y), q4);
+            for (int i = 0; i < 4; ++i) {
+              a0 = fma2(e4m3x2_to_f32x2(static_cast<uint16_t>(wd[i] & 0xFFFFu)), qv[2 * i], a0);
+              a1 = fma2(e4m3x2_to_f32x2(static_cast<uint16_t>(wd[i] >> 16)), qv[2 * i + 1], a1);
             }
+            v[f * HR + hu] = (a0.x + a0.y) + (a1.x + a1.y);
+          } else {
+            const uint2 wv = *reinterpret_cast<const uint2*>(cbp + R * (N / 2) + 8 * cbk);
+            const uint32_t wd[2] = {wv.x, wv.y};
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              a0 = fma2(e2m1x2_to_f32x2(wd[i] & 0xFFu), qv[4 * i], a0);
+              a1 = fma2(e2m1x2_to_f32x2((wd[i] >> 8) & 0xFFu), qv[4 * i + 1], a1);
+              a0 = fma2(e2m1x2_to_f32x2((wd[i] >> 16) & 0xFFu), qv[4 * i + 2], a0);
+              a1 = fma2(e2m1x2_to_f32x2(wd[i] >> 24), qv[4 * i + 3], a1);
+            }
+            const float bs = e4m3_to_f32(gb[LY.gb_rs + ((hh0 + hu) * P + R) * (N / 16) + cbk]);
+            v[f * HR + hu] = bs * ((a0.x + a0.y) + (a1.x + a1.y));
           }
         }
+      }
 #pragma unroll
-        for (int hu = 0; hu < HR; ++hu) {
-          float r = ry[hu];
-          r += __shfl_xor_sync(0xffffffffu, r, 1);
-          r += __shfl_xor_sync(0xffffffffu, r, 2);
-          const float tot = reduce8(part[hu], lane);
-          if (jl == 0) y[(uh0 + hu) * P + Rq] = fmaf(gsc[hu], tot, r);
+      for (int g = 0; g < NV / 8; ++g) {
+        // this lane's total: value 8 g + cb, i.e. head cb mod 4, pass 2 g + cb / 4
+        const float tot = reduce8_lanes3(v + 8 * g, lane);
+        const int hu = cbk & 3;
+        const int R = RW * tw + 4 * (2 * g + (cbk >> 2)) + rq;
+        const float* co = cob + (hh0 + hu) * CS;
+        const uint16_t* xr = reinterpret_cast<const uint16_t*>(st + LY.st_rec + hu * LY.rec_stride) + R;
+        float r0 = co[n] * bf(curb[(hh0 + hu) * P + R]), r1 = 0.f;
+        int j = 0;
+        for (; j + 1 < n; j += 2) {
+          r0 = fmaf(co[j], bf(xr[j * P]), r0);
+          r1 = fmaf(co[j + 1], bf(xr[(j + 1) * P]), r1);
         }
+        if (j < n) r0 = fmaf(co[j], bf(xr[j * P]), r0);
+        const float gsc = co[3 * C + CO_GAMMA] * (READ == READ_FP8
+                                                      ? reinterpret_cast<const float*>(gb + LY.gb_rs)[(hh0 + hu) * P + R]
+                                                      : co[3 * C + CO_MATSCALE]);
+        y[(uh0 + hu) * P + R] = fmaf(gsc, tot, r0 + r1);
       }
     }
     for (int hu = 0; hu < 1 && nh_unit == 1 && (meta.y & 0x200); ++hu) {
@@ -832,7 +861,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       const float4 q4 = reinterpret_cast<const float4*>(gb + LY.gb_qf)[lane];
       const float gamma = co[3 * C + CO_GAMMA];
       if (KIND == 0) {
-        const uint16_t* xb = reinterpret_cast<const uint16_t*>(st + LY.st_rec + static_cast<size_t>(hu) * al16(C * P * 2));
+        const uint16_t* xb = reinterpret_cast<const uint16_t*>(st + LY.st_rec + static_cast<size_t>(hu) * LY.rec_stride);
         if (MR == 16 && RW == 16 && flush) {
           // flush unit, both of this warp's 8-row blocks in one pass over the records:
           // the keys are loaded once for the two, and the two blocks' accumulations
@@ -1176,7 +1205,9 @@ cudaError_t launch128(const LayerDev& d, const TokenIn& in, float* y, cudaStream
   if (grid > total / hr) grid = total / hr;
   int per = ((total + grid - 1) / grid + hr - 1) / hr * hr;
   // a weighted share may stretch to kWFlush / kWPlain times the even share
-  auto span_seqs = [&](int p) { return (balanced(LY, d.B) ? p * kWFlush / kWPlain : p) / (d.H * SPL) + 2; };
+  auto span_seqs = [&](int p) {
+    return (balanced(LY, d.B, d.H * SPL) ? p * kWFlush / kWPlain : p) / (d.H * SPL) + 2;
+  };
   while (span_seqs(per) > kMaxSeq128) {
     grid *= 2;
     per = ((total + grid - 1) / grid + hr - 1) / hr * hr;
