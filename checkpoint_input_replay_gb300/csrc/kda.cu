@@ -287,6 +287,256 @@ __global__ void __launch_bounds__(kKdaThreads, 4) kda_kernel(const LayerDev d, c
   }
 }
 
+// ---- persistent decode step for d_state 128 ---------------------------------
+//
+// The same arithmetic as kda_kernel, organised like the other d_state-128 decode
+// kernels: a CTA (two per SM) takes a contiguous range of units (sequence, head,
+// block of 64 rows) and a producer warp stages the next unit -- its checkpoint
+// rows, the buffered records (log decays and keys over the key channels, the
+// deltas of its rows), this token's log decay, key, query and values -- by bulk
+// copies into the other of two shared-memory stages while the eight computing
+// warps work on the current one: the channel-wise suffix scan (warps 0-3), the
+// record dot products (a warp per item), then eight rows a warp: the two
+// checkpoint dot products (a transpose-reduce over the row's lanes), the records'
+// terms (four lanes a row split the records), u, o and, on a flush step, the
+// folded rows.  The CTAs read their sequences' cursors once, at the start; the
+// last CTA of a sequence to count its units in advances the cursor.
+
+constexpr int kPN = 128;                 // d_state
+constexpr int kPR = 64;                  // state rows per unit
+constexpr int kPThreads = kThreads + 32;  // eight computing warps and the producer warp
+constexpr int kPMaxSeq = 64;             // sequences one CTA may cover
+constexpr int kUStride = kPR + 8;        // floats per record row of the staged deltas
+
+struct KdaPStage {  // byte offsets within one stage
+  int tile, g, kb, u, tg, tk, tq, tv, vec, dots, size;
+};
+
+__host__ __device__ __forceinline__ KdaPStage kdap_stage(int C) {
+  KdaPStage m;
+  int o = 0;
+  m.tile = o; o += kPR * kPN * 4;       // the unit's checkpoint rows
+  m.g = o;    o += C * kPN * 4;         // records' log decays [j][N]; decayed keys k_j W'_j in place
+  m.kb = o;   o += C * kPN * 2;         // records' keys, bf16 [j][N]
+  m.u = o;    o += C * kUStride * 4;    // records' deltas of the unit's rows [j][kUStride]
+  m.tg = o;   o += kPN * 4;             // this token's log decay over the channels
+  m.tk = o;   o += kPN * 2;             // this token's key, bf16
+  m.tq = o;   o += kPN * 2;             // this token's query, bf16
+  m.tv = o;   o += kPR * 2;             // this token's values of the unit's rows, bf16
+  m.vec = o;  o += 3 * kPN * 4;         // G', G' k, G' q
+  m.dots = o; o += (2 * C + 4) * 4;     // (k_j W'_j) . k and . q interleaved, then k . q
+  m.size = (o + 127) & ~127;
+  return m;
+}
+
+__host__ __device__ __forceinline__ int kdap_pers_bytes() { return 32 + 16 * kPMaxSeq + 16; }
+
+__global__ void __launch_bounds__(kPThreads, 2) kdap_kernel(const LayerDev d, const TokenIn in,
+                                                            float* __restrict__ y, const int per) {
+  extern __shared__ __align__(128) unsigned char psm[];
+  const int H = d.H, G = d.G, C = d.C, L = d.L, P = d.P;
+  const int parts = P / kPR, ups = H * parts;  // units of a sequence
+  const int total = d.B * ups;
+  const int u0 = static_cast<int>(blockIdx.x) * per, u1 = min(u0 + per, total);
+  if (u0 >= u1) return;
+  const KdaPStage M = kdap_stage(C);
+  unsigned char* pers = psm + 2 * M.size;
+  uint64_t* full = reinterpret_cast<uint64_t*>(pers);  // [2] stage landed
+  uint64_t* empty = full + 2;                          // [2] stage released by the eight computing warps
+  int4* scur = reinterpret_cast<int4*>(pers + 32);     // per covered sequence: head, count, flags (1 ok, 2 flush)
+  volatile int* sabort = reinterpret_cast<volatile int*>(pers + 32 + 16 * kPMaxSeq);
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int b0 = u0 / ups, nseq = (u1 - 1) / ups - b0 + 1;
+  if (t < nseq) {
+    const int b = b0 + t;
+    const int4 cv = reinterpret_cast<const int4*>(d.cursor)[b];
+    const bool ok = static_cast<unsigned>(cv.x) < static_cast<unsigned>(C) &&
+                    static_cast<unsigned>(cv.y) < static_cast<unsigned>(L);
+    const bool fl = ok && cv.y + 1 == L;
+    scur[t] = make_int4(ok ? cv.x : 0, ok ? cv.y : 0, (ok ? 1 : 0) | (fl ? 2 : 0), 0);
+    // count this CTA's units of the sequence in (after its cursor has been read);
+    // the last CTA of the sequence advances the cursor
+    const int cnt = min(u1, (b + 1) * ups) - max(u0, b * ups);
+    const int prev = atomicAdd(d.arrive + b, cnt);
+    if (prev + cnt == ups) {
+      atomicExch(d.arrive + b, 0);
+      if (!ok) report_error(d.err, DEVERR_CURSOR, b);
+      else if (fl) reinterpret_cast<int4*>(d.cursor)[b] = make_int4(kslot(cv.x, cv.y + 1, C), 0, 1, cv.w);
+      else reinterpret_cast<int4*>(d.cursor)[b] = make_int4(cv.x, cv.y + 1, 0, cv.w);
+    }
+  }
+  if (t == kThreads) {
+    mbar_init(full, 1);
+    mbar_init(full + 1, 1);
+    mbar_init(empty, kThreads / 32);
+    mbar_init(empty + 1, kThreads / 32);
+    *sabort = 0;
+  }
+  __syncthreads();
+
+  if (warp == kThreads / 32) {
+    // ================================ producer ================================
+    if (lane == 0) {
+      int k = 0;  // units staged
+      for (int uu = u0; uu < u1; ++uu) {
+        const int b = uu / ups, rem = uu - b * ups, h = rem / parts, part = rem - h * parts;
+        const int4 cs = scur[b - b0];
+        if (!(cs.z & 1)) continue;
+        const int s = k & 1;
+        if (k >= 2 && !mbar_wait_bounded(empty + s, static_cast<uint32_t>(((k >> 1) - 1) & 1))) {
+          report_error(d.err, DEVERR_TIMEOUT, b);
+          *sabort = 1;
+          break;
+        }
+        if (*sabort) break;
+        unsigned char* st = psm + static_cast<size_t>(s) * M.size;
+        const int head = cs.x, n = cs.y;
+        const size_t bh = static_cast<size_t>(b) * H + h, bg = static_cast<size_t>(b) * G + h / (H / G);
+        const int r0 = part * kPR;
+        const int seg1 = min(n, C - head), seg2 = n - seg1;
+        uint64_t* bar = full + s;
+        mbar_expect_tx(bar, static_cast<uint32_t>(kPR * kPN * 4 + n * (kPN * 6 + kPR * 4) + kPN * 8 + kPR * 2));
+        bulk_g2s(st + M.tile, d.ckpt + (bh * P + r0) * kPN, kPR * kPN * 4, bar);
+        if (seg1) {
+          bulk_g2s(st + M.g, d.r_g + (bh * C + head) * kPN, seg1 * kPN * 4, bar);
+          bulk_g2s(st + M.kb, d.r_k + (bg * C + head) * kPN, seg1 * kPN * 2, bar);
+        }
+        if (seg2) {
+          bulk_g2s(st + M.g + seg1 * kPN * 4, d.r_g + bh * C * kPN, seg2 * kPN * 4, bar);
+          bulk_g2s(st + M.kb + seg1 * kPN * 2, d.r_k + bg * C * kPN, seg2 * kPN * 2, bar);
+        }
+        for (int j = 0; j < n; ++j)
+          bulk_g2s(st + M.u + j * kUStride * 4, d.r_u + (bh * C + kslot(head, j, C)) * P + r0, kPR * 4, bar);
+        bulk_g2s(st + M.tg, in.g + bh * kPN, kPN * 4, bar);
+        bulk_g2s(st + M.tk, in.k + bg * kPN, kPN * 2, bar);
+        bulk_g2s(st + M.tq, in.q + bg * kPN, kPN * 2, bar);
+        bulk_g2s(st + M.tv, in.v + bh * P + r0, kPR * 2, bar);
+        ++k;
+      }
+      // the copies in flight land before the CTA's shared memory is released
+      for (int j = max(0, k - 2); j < k; ++j) mbar_wait_bounded(full + (j & 1), static_cast<uint32_t>((j >> 1) & 1));
+    }
+    return;
+  }
+
+  // ============================== computing warps ==============================
+  const int rq = (lane >> 2) & 7, jl = lane & 3;  // row of the warp's eight, record lane
+  int k = 0;
+  for (int uu = u0; uu < u1; ++uu) {
+    const int b = uu / ups, rem = uu - b * ups, h = rem / parts, part = rem - h * parts;
+    const int4 cs = scur[b - b0];
+    if (!(cs.z & 1)) continue;
+    const int s = k & 1;
+    const uint32_t par = static_cast<uint32_t>((k >> 1) & 1);
+    ++k;
+    const size_t bh = static_cast<size_t>(b) * H + h, bg = static_cast<size_t>(b) * G + h / (H / G);
+    const int r0 = part * kPR;
+    const int head = cs.x, n = cs.y;
+    const bool flush = (cs.z & 2) != 0;
+    const float beta = in.beta[bh];  // in flight during the scan
+    if (!compute_sync_and(mbar_wait_bounded(full + s, par))) {
+      if (t == 0) {
+        report_error(d.err, DEVERR_TIMEOUT, b);
+        *sabort = 1;
+      }
+      break;
+    }
+    unsigned char* st = psm + static_cast<size_t>(s) * M.size;
+    float* kt = reinterpret_cast<float*>(st + M.g);
+    const uint16_t* kb = reinterpret_cast<const uint16_t*>(st + M.kb);
+    const float* su = reinterpret_cast<const float*>(st + M.u);
+    const float* tg = reinterpret_cast<const float*>(st + M.tg);
+    const uint16_t* tk = reinterpret_cast<const uint16_t*>(st + M.tk);
+    const uint16_t* tq = reinterpret_cast<const uint16_t*>(st + M.tq);
+    const uint16_t* tv = reinterpret_cast<const uint16_t*>(st + M.tv);
+    float* vec = reinterpret_cast<float*>(st + M.vec);
+    float* dots = reinterpret_cast<float*>(st + M.dots);
+    // channel-wise suffix scan: W'_j = exp(sum of the log decays after record j, this
+    // token's included), decayed key k_j W'_j in place of the log decays; G' = exp(all)
+    if (t < kPN) {
+      float acc = tg[t];
+      for (int j = n - 1; j >= 0; --j) {
+        const float gj = kt[j * kPN + t];
+        kt[j * kPN + t] = bf(kb[j * kPN + t]) * expf(acc);
+        acc += gj;
+      }
+      const float Gp = expf(acc);
+      vec[t] = Gp;
+      vec[kPN + t] = Gp * bf(tk[t]);
+      vec[2 * kPN + t] = Gp * bf(tq[t]);
+    }
+    compute_sync();
+    // record dots (k_j W'_j) . k and . q (items 2 j and 2 j + 1), and k . q (item 2 n)
+    for (int it = warp; it < 2 * n + 1; it += kThreads / 32) {
+      const float4 a4 = it < 2 * n ? reinterpret_cast<const float4*>(kt + (it >> 1) * kPN)[lane]
+                                   : bf4(reinterpret_cast<const uint2*>(tk)[lane]);
+      const float4 b4 = bf4(reinterpret_cast<const uint2*>((it < 2 * n && (it & 1) == 0) ? tk : tq)[lane]);
+      const float v = seg_sum<32>(dot4(a4, b4));
+      if (lane == 0) dots[it] = v;
+    }
+    compute_sync();
+    // the warp's eight rows: checkpoint dot products, records' terms, u and o
+    const int lr = 8 * warp + rq;  // this lane's row (of the unit) after the reductions
+    const float4* tile4 = reinterpret_cast<const float4*>(st + M.tile);
+    const float4 gk4 = reinterpret_cast<const float4*>(vec + kPN)[lane];
+    const float4 gq4 = reinterpret_cast<const float4*>(vec + 2 * kPN)[lane];
+    float4 srow[8];
+    float pk[8], pq[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      srow[e] = tile4[(8 * warp + e) * (kPN / 4) + lane];
+      pk[e] = dot4(srow[e], gk4);
+      pq[e] = dot4(srow[e], gq4);
+    }
+    const float sk = reduce8(pk, lane), sq = reduce8(pq, lane);
+    float rk = 0.f, rqv = 0.f;
+    for (int j = jl; j < n; j += 4) {
+      const float uj = su[j * kUStride + lr];
+      rk = fmaf(uj, dots[2 * j], rk);
+      rqv = fmaf(uj, dots[2 * j + 1], rqv);
+    }
+    rk += __shfl_xor_sync(0xffffffffu, rk, 1);
+    rk += __shfl_xor_sync(0xffffffffu, rk, 2);
+    rqv += __shfl_xor_sync(0xffffffffu, rqv, 1);
+    rqv += __shfl_xor_sync(0xffffffffu, rqv, 2);
+    const float kq = dots[2 * n];
+    const float ut = beta * (bf(tv[lr]) - (sk + rk));  // u = b (v - S k')
+    if (jl == 0) {
+      y[bh * P + r0 + lr] = fmaf(ut, kq, sq + rqv);  // o = S q' + u (k . q)
+      if (!flush) d.r_u[(bh * C + kslot(head, n, C)) * P + r0 + lr] = ut;
+    }
+    if (flush) {
+      // S_new = S_ckpt Diag(G') + sum_j u_j (k_j W'_j)^T + u k^T, stored once
+      const float4 G4 = reinterpret_cast<const float4*>(vec)[lane];
+      const float4 k4 = bf4(reinterpret_cast<const uint2*>(tk)[lane]);
+      float4 acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        acc[e] = make_float4(srow[e].x * G4.x, srow[e].y * G4.y, srow[e].z * G4.z, srow[e].w * G4.w);
+      for (int j = 0; j < n; ++j) {
+        const float4 kt4 = reinterpret_cast<const float4*>(kt + j * kPN)[lane];
+        const float* uj = su + j * kUStride + 8 * warp;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = axpy4(uj[e], kt4, acc[e]);
+      }
+      float4* gS4 = reinterpret_cast<float4*>(d.ckpt + (bh * P + r0 + 8 * warp) * kPN);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float ue = __shfl_sync(0xffffffffu, ut, 4 * e);
+        __stcs(gS4 + e * (kPN / 4) + lane, axpy4(ue, k4, acc[e]));
+      }
+    } else if (part == 0 && t < kPN) {
+      // this token's record: g over the key channels per head, k once per key group
+      const int slot = kslot(head, n, C);
+      d.r_g[(bh * C + slot) * kPN + t] = tg[t];
+      if (h % (H / G) == 0) d.r_k[(bg * C + slot) * kPN + t] = tk[t];
+    }
+    // the warp is done with the stage
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty + s);
+  }
+}
+
 template <int N, bool FOLD>
 cudaError_t launch_kda_n(const LayerDev& d, const TokenIn& in, float* y, const uint8_t* mask, cudaStream_t s) {
   const int R = kda_rows(N, d.P);
@@ -296,6 +546,37 @@ cudaError_t launch_kda_n(const LayerDev& d, const TokenIn& in, float* y, const u
   const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
   kernel<<<d.B * d.H * parts, kKdaThreads, smem, s>>>(d, in, y, mask);
+  return cudaGetLastError();
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// the persistent decode: d_state 128, whole 64-row units, every staged source
+// 16-byte aligned, two stages in shared memory
+size_t kdap_smem(const LayerDev& d) { return 2 * static_cast<size_t>(kdap_stage(d.C).size) + kdap_pers_bytes(); }
+
+bool kdap_supports(const LayerDev& d, const TokenIn& in) {
+  return d.N == kPN && d.P % kPR == 0 && d.H % d.G == 0 && kdap_smem(d) <= 227u * 1024u && aligned16(d.ckpt) &&
+         aligned16(d.r_g) && aligned16(d.r_k) && aligned16(d.r_u) && aligned16(in.g) && aligned16(in.k) &&
+         aligned16(in.q) && aligned16(in.v);
+}
+
+cudaError_t launch_kdap(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s) {
+  const size_t smem = kdap_smem(d);
+  const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kdap_kernel), smem);
+  if (e != cudaSuccess) return e;
+  const int ups = d.H * (d.P / kPR);
+  const int total = d.B * ups;
+  const int per_sm = smem + 1024 <= 114u * 1024u ? 2 : 1;
+  int grid = (d.num_sms > 0 ? d.num_sms : 1) * per_sm;
+  if (grid > total) grid = total;
+  int per = (total + grid - 1) / grid;
+  while (per / ups + 2 > kPMaxSeq) {  // sequences a CTA covers
+    grid *= 2;
+    per = (total + grid - 1) / grid;
+  }
+  grid = (total + per - 1) / per;
+  kdap_kernel<<<grid, kPThreads, smem, s>>>(d, in, y, per);
   return cudaGetLastError();
 }
 
@@ -313,6 +594,7 @@ cudaError_t launch_kda_any(const LayerDev& d, const TokenIn& in, float* y, const
 }  // namespace
 
 cudaError_t launch_kda_decode(const LayerDev& d, const TokenIn& in, float* y, cudaStream_t s) {
+  if (kdap_supports(d, in)) return launch_kdap(d, in, y, s);
   return launch_kda_any<false>(d, in, y, nullptr, s);
 }
 
