@@ -971,16 +971,14 @@ def main(argv=None):
 
     hbm, peak_kind = peaks()
     achieved = m2["bytes_total"] / (m2["launch_ms_total"] * 1e6)
-    tr = ncu_record("decode_mamba2_b256") if wl1.shape.batch == 256 else None
+    # DRAM bytes per launch: the mean over one captured L = 16 window of the same
+    # workload (ncu, uncached), like `achieved`, which is over whole-window mixes
+    win = ncu_record("decode_mamba2_window_b256") if wl1.shape.batch == 256 else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": tr["traffic_bytes_per_launch"] if tr else None, "peak_kind": peak_kind,
+                "traffic": (sum(r["dram_bytes"] for r in win["launches"]) / len(win["launches"])) if win else None,
+                "peak_kind": peak_kind,
                 "nonflush_gbs": m2["nonflush_gbs"], "nonflush_frac": m2["nonflush_gbs"] / hbm,
                 "flush_gbs": m2["flush_gbs"], "nonflush_us": m2["nonflush_us"], "flush_us": m2["flush_us"]}
-    if tr:
-        # a non-flush launch: DRAM bytes (ncu) over the algorithmic bytes of the same launch
-        roofline["traffic_launch"] = tr["launch"]
-        roofline["traffic_over_algorithmic"] = tr["traffic_bytes_per_launch"] / tr["algorithmic_bytes_per_launch"]
-    win = ncu_record("decode_mamba2_window_b64")
     if win:
         roofline.update(window_state_ratio(win, configs.CONFIG1.with_batch(win["batch"])))
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,

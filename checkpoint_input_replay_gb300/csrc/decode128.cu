@@ -71,7 +71,7 @@ enum : int { CO_GAMMA = 0, CO_A = 1, CO_BETA = 2, CO_KQ = 3, CO_MATSCALE = 4 };
 
 // Shared-memory layout (bytes): [stages][3 group buffers][persistent].
 struct Lay128 {
-  int st_tile, st_rec, st_meta, st_size, rec_stride;
+  int st_tile, st_rec, st_meta, st_size, rec_stride, urow;
   int gb_key, gb_q, gb_cur, gb_la, gb_dt, gb_s1, gb_s2, gb_rs, gb_ms, gb_qf, gb_kf, gb_coef, gb_size;
   int pe_A, pe_bars, pe_seq, pe_misc, pe_cnt, pe_mtab, pe_dq, pe_size;
 };
@@ -92,7 +92,10 @@ __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int
   l.st_tile = o;  o += rpu * N * 4;
   // a read-copy unit's heads' record blocks sit 16 bytes off the 128-byte bank period
   l.rec_stride = al16(C * P * 2) + (read == READ_NONE ? 0 : 16);
-  l.st_rec = o;   o += kind == 0 ? read_heads(read) * l.rec_stride : C * rpu * 4;
+  // a Gated DeltaNet record row (the unit's rows of u_j) is padded by 16 floats, so
+  // that the two lanes of a row reading records of either parity hit other banks
+  l.urow = rpu + 16;
+  l.st_rec = o;   o += kind == 0 ? read_heads(read) * l.rec_stride : C * l.urow * 4;
   l.st_meta = o;  o += 32;              // int4 descriptor, NVFP4 amax word
   l.st_size = al128(o);
   o = 0;
@@ -480,7 +483,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       const unsigned char* rsrc = KIND == 0 ? reinterpret_cast<const unsigned char*>(d.r_x)
                                             : reinterpret_cast<const unsigned char*>(d.r_u);
       constexpr size_t rrow = static_cast<size_t>(P) * esz;
-      if (SPL == 1) {
+      if (KIND == 0) {
         for (int hu = 0; hu < nh; ++hu) {
           unsigned char* rdst = st + LY.st_rec + static_cast<size_t>(hu) * LY.rec_stride;
           const size_t uh = u + hu;
@@ -488,9 +491,9 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
           if (seg2) bulk_g2s(rdst + seg1 * rrow, rsrc + uh * C * rrow, seg2 * rrow, bar);
         }
       } else {
-        // this part's rows of each buffered record: one copy per record
+        // this unit's rows of each buffered record: one copy per record, rows padded
         for (int j = 0; j < n; ++j)
-          bulk_g2s(st + LY.st_rec + static_cast<size_t>(j) * RPU * esz,
+          bulk_g2s(st + LY.st_rec + static_cast<size_t>(j) * LY.urow * esz,
                    rsrc + (u * C + ring_slot(head, j, C)) * rrow + static_cast<size_t>(w.sp) * RPU * esz, RPU * esz,
                    bar);
       }
@@ -1061,48 +1064,61 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
         const float kq_dot = co[3 * C + CO_KQ];
         float* urow = d.r_u + (u * C + slot) * P + sp * RPU;
         if (!flush) {
-          // the warp's 8-row blocks side by side, so that their chains (record terms,
-          // row dots, transpose-reduces) interleave
-          constexpr int NBK = RW / 8;
-          float rk[NBK], rq[NBK], tk[NBK], tq[NBK];
+          // Lane 8 rq + cb takes the 16 channels 4 (8 i + cb) .. + 3 (i < 4: the eight
+          // lanes of a row read 128 contiguous bytes a load) of the warp's rows
+          // RW tw + 4 f + rq, pass f; its 2 NPASS partial dot products (S k, S q per
+          // pass) are summed over the row's eight lanes by transpose-reduces, which
+          // leave S k and S q of one row in the lane pair (cb = 2 f', 2 f' + 1); that
+          // pair splits the row's records by parity and writes u and o.
+          constexpr int NPASS = RW / 4;
+          static_assert(KIND != 1 || NPASS % 4 == 0, "rows per warp: a multiple of 16");
+          const int rq = lane >> 3, cbk = lane & 7;
+          float2 kv[8], qv[8];
 #pragma unroll
-          for (int bk = 0; bk < NBK; ++bk) {
-            rk[bk] = 0.f;
-            rq[bk] = 0.f;
+          for (int i = 0; i < 4; ++i) {
+            const float4 k4 = reinterpret_cast<const float4*>(gb + LY.gb_kf)[8 * i + cbk];
+            const float4 qq = reinterpret_cast<const float4*>(gb + LY.gb_qf)[8 * i + cbk];
+            kv[2 * i] = make_float2(k4.x, k4.y);
+            kv[2 * i + 1] = make_float2(k4.z, k4.w);
+            qv[2 * i] = make_float2(qq.x, qq.y);
+            qv[2 * i + 1] = make_float2(qq.z, qq.w);
           }
-          for (int j = jl; j < n; j += 4) {
-            const float ck = co[j], cq = co[C + j];
 #pragma unroll
-            for (int bk = 0; bk < NBK; ++bk) {
-              const float uj = ub[j * RPU + tw + TW * (8 * bk + kq)];
-              rk[bk] = fmaf(ck, uj, rk[bk]);
-              rq[bk] = fmaf(cq, uj, rq[bk]);
+          for (int g4 = 0; g4 < NPASS / 4; ++g4) {
+            float v[8];
+#pragma unroll
+            for (int f4 = 0; f4 < 4; ++f4) {
+              const int R = RW * tw + 4 * (4 * g4 + f4) + rq;
+              float2 ak0 = make_float2(0.f, 0.f), ak1 = ak0, aq0 = ak0, aq1 = ak0;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float4 s4 = sT4[R * SEG + 8 * i + cbk];
+                const float2 lo = make_float2(s4.x, s4.y), hi = make_float2(s4.z, s4.w);
+                ak0 = fma2(lo, kv[2 * i], ak0);
+                ak1 = fma2(hi, kv[2 * i + 1], ak1);
+                aq0 = fma2(lo, qv[2 * i], aq0);
+                aq1 = fma2(hi, qv[2 * i + 1], aq1);
+              }
+              v[2 * f4] = (ak0.x + ak0.y) + (ak1.x + ak1.y);
+              v[2 * f4 + 1] = (aq0.x + aq0.y) + (aq1.x + aq1.y);
             }
-          }
-#pragma unroll
-          for (int bk = 0; bk < NBK; ++bk) {
-            float pk[8], pq[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float4 s4 = sT4[(tw + TW * (8 * bk + e)) * SEG + lane];
-              pk[e] = dot4p(s4, kc4);
-              pq[e] = dot4p(s4, q4);
+            // this lane: value cb = dot (cb & 1) of pass 4 g4 + cb / 2
+            const float tot = reduce8_lanes3(v, lane);
+            const float oth = __shfl_xor_sync(0xffffffffu, tot, 1);
+            const float tk = (cbk & 1) ? oth : tot, tq = (cbk & 1) ? tot : oth;
+            const int R = RW * tw + 4 * (4 * g4 + (cbk >> 1)) + rq;
+            float r1 = 0.f, r2 = 0.f;
+            for (int j = cbk & 1; j < n; j += 2) {
+              const float uj = ub[j * LY.urow + R];
+              r1 = fmaf(co[j], uj, r1);
+              r2 = fmaf(co[C + j], uj, r2);
             }
-            tk[bk] = reduce8(pk, lane);
-            tq[bk] = reduce8(pq, lane);
-          }
-#pragma unroll
-          for (int bk = 0; bk < NBK; ++bk) {
-            float r1 = rk[bk], r2 = rq[bk];
             r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
-            r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
             r2 += __shfl_xor_sync(0xffffffffu, r2, 1);
-            r2 += __shfl_xor_sync(0xffffffffu, r2, 2);
-            const int Rq = tw + TW * (8 * bk + kq);
-            const float uu = beta * (bf(cur[Rq]) - a * fmaf(gamma, tk[bk], r1));
-            if (jl == 0) {
-              yrow[Rq] = fmaf(a, fmaf(gamma, tq[bk], r2), uu * kq_dot);
-              urow[Rq] = uu;
+            const float uu = beta * (bf(cur[R]) - a * fmaf(gamma, tk, r1));
+            if ((cbk & 1) == 0) {
+              yrow[R] = fmaf(a, fmaf(gamma, tq, r2), uu * kq_dot);
+              urow[R] = uu;
             }
           }
         }
@@ -1111,7 +1127,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
           const int Rq = tw + TW * (r0 + kq);
           float rk = 0.f, rq = 0.f;
           for (int j = jl; j < n; j += 4) {
-            const float uj = ub[j * RPU + Rq];
+            const float uj = ub[j * LY.urow + Rq];
             rk = fmaf(co[j], uj, rk);
             rq = fmaf(co[C + j], uj, rq);
           }
@@ -1141,7 +1157,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
             // the end of the last quad), then four records per broadcast read
             for (int jc = 0; 4 * jc < n; ++jc) {
               const int j = 4 * jc + jl;
-              mt[kq * kMtabRow + j] = j < n ? co[2 * C + j] * ub[j * RPU + Rq] : 0.f;
+              mt[kq * kMtabRow + j] = j < n ? co[2 * C + j] * ub[j * LY.urow + Rq] : 0.f;
             }
             __syncwarp();
             float4 acc[8];

@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(kKdaThreads, 4) kda_kernel(const LayerDev d, c
 // kernels: a CTA (two per SM) takes a contiguous range of units (sequence, head,
 // block of 64 rows) and a producer warp stages the next unit -- its checkpoint
 // rows, the buffered records (log decays and keys over the key channels, the
-// deltas of its rows), this token's log decay, key, query and values -- by bulk
+// deltas of the head's rows), this token's log decay, key, query and values -- by bulk
 // copies into the other of two shared-memory stages while the eight computing
 // warps work on the current one: the channel-wise suffix scan (warps 0-3), the
 // record dot products (a warp per item), then eight rows a warp: the two
@@ -306,19 +306,18 @@ constexpr int kPN = 128;                 // d_state
 constexpr int kPR = 64;                  // state rows per unit
 constexpr int kPThreads = kThreads + 32;  // eight computing warps and the producer warp
 constexpr int kPMaxSeq = 64;             // sequences one CTA may cover
-constexpr int kUStride = kPR + 8;        // floats per record row of the staged deltas
 
 struct KdaPStage {  // byte offsets within one stage
   int tile, g, kb, u, tg, tk, tq, tv, vec, dots, size;
 };
 
-__host__ __device__ __forceinline__ KdaPStage kdap_stage(int C) {
+__host__ __device__ __forceinline__ KdaPStage kdap_stage(int C, int P) {
   KdaPStage m;
   int o = 0;
   m.tile = o; o += kPR * kPN * 4;       // the unit's checkpoint rows
   m.g = o;    o += C * kPN * 4;         // records' log decays [j][N]; decayed keys k_j W'_j in place
   m.kb = o;   o += C * kPN * 2;         // records' keys, bf16 [j][N]
-  m.u = o;    o += C * kUStride * 4;    // records' deltas of the unit's rows [j][kUStride]
+  m.u = o;    o += C * P * 4;           // records' deltas, all rows of the head [j][P] (two copies at most)
   m.tg = o;   o += kPN * 4;             // this token's log decay over the channels
   m.tk = o;   o += kPN * 2;             // this token's key, bf16
   m.tq = o;   o += kPN * 2;             // this token's query, bf16
@@ -339,7 +338,7 @@ __global__ void __launch_bounds__(kPThreads, 2) kdap_kernel(const LayerDev d, co
   const int total = d.B * ups;
   const int u0 = static_cast<int>(blockIdx.x) * per, u1 = min(u0 + per, total);
   if (u0 >= u1) return;
-  const KdaPStage M = kdap_stage(C);
+  const KdaPStage M = kdap_stage(C, P);
   unsigned char* pers = psm + 2 * M.size;
   uint64_t* full = reinterpret_cast<uint64_t*>(pers);  // [2] stage landed
   uint64_t* empty = full + 2;                          // [2] stage released by the eight computing warps
@@ -395,18 +394,18 @@ __global__ void __launch_bounds__(kPThreads, 2) kdap_kernel(const LayerDev d, co
         const int r0 = part * kPR;
         const int seg1 = min(n, C - head), seg2 = n - seg1;
         uint64_t* bar = full + s;
-        mbar_expect_tx(bar, static_cast<uint32_t>(kPR * kPN * 4 + n * (kPN * 6 + kPR * 4) + kPN * 8 + kPR * 2));
+        mbar_expect_tx(bar, static_cast<uint32_t>(kPR * kPN * 4 + n * (kPN * 6 + P * 4) + kPN * 8 + kPR * 2));
         bulk_g2s(st + M.tile, d.ckpt + (bh * P + r0) * kPN, kPR * kPN * 4, bar);
         if (seg1) {
           bulk_g2s(st + M.g, d.r_g + (bh * C + head) * kPN, seg1 * kPN * 4, bar);
           bulk_g2s(st + M.kb, d.r_k + (bg * C + head) * kPN, seg1 * kPN * 2, bar);
+          bulk_g2s(st + M.u, d.r_u + (bh * C + head) * P, seg1 * P * 4, bar);
         }
         if (seg2) {
           bulk_g2s(st + M.g + seg1 * kPN * 4, d.r_g + bh * C * kPN, seg2 * kPN * 4, bar);
           bulk_g2s(st + M.kb + seg1 * kPN * 2, d.r_k + bg * C * kPN, seg2 * kPN * 2, bar);
+          bulk_g2s(st + M.u + seg1 * P * 4, d.r_u + bh * C * P, seg2 * P * 4, bar);
         }
-        for (int j = 0; j < n; ++j)
-          bulk_g2s(st + M.u + j * kUStride * 4, d.r_u + (bh * C + kslot(head, j, C)) * P + r0, kPR * 4, bar);
         bulk_g2s(st + M.tg, in.g + bh * kPN, kPN * 4, bar);
         bulk_g2s(st + M.tk, in.k + bg * kPN, kPN * 2, bar);
         bulk_g2s(st + M.tq, in.q + bg * kPN, kPN * 2, bar);
@@ -453,14 +452,16 @@ __global__ void __launch_bounds__(kPThreads, 2) kdap_kernel(const LayerDev d, co
     float* dots = reinterpret_cast<float*>(st + M.dots);
     // channel-wise suffix scan: W'_j = exp(sum of the log decays after record j, this
     // token's included), decayed key k_j W'_j in place of the log decays; G' = exp(all)
+    // (the fast exponential: its relative error, a few 1e-7 at these arguments, is far
+    // below the FP32 path's tolerance)
     if (t < kPN) {
       float acc = tg[t];
       for (int j = n - 1; j >= 0; --j) {
         const float gj = kt[j * kPN + t];
-        kt[j * kPN + t] = bf(kb[j * kPN + t]) * expf(acc);
+        kt[j * kPN + t] = bf(kb[j * kPN + t]) * __expf(acc);
         acc += gj;
       }
-      const float Gp = expf(acc);
+      const float Gp = __expf(acc);
       vec[t] = Gp;
       vec[kPN + t] = Gp * bf(tk[t]);
       vec[2 * kPN + t] = Gp * bf(tq[t]);
@@ -485,13 +486,13 @@ __global__ void __launch_bounds__(kPThreads, 2) kdap_kernel(const LayerDev d, co
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       srow[e] = tile4[(8 * warp + e) * (kPN / 4) + lane];
-      pk[e] = dot4(srow[e], gk4);
-      pq[e] = dot4(srow[e], gq4);
+      pk[e] = dot4p(srow[e], gk4);
+      pq[e] = dot4p(srow[e], gq4);
     }
     const float sk = reduce8(pk, lane), sq = reduce8(pq, lane);
     float rk = 0.f, rqv = 0.f;
     for (int j = jl; j < n; j += 4) {
-      const float uj = su[j * kUStride + lr];
+      const float uj = su[j * P + r0 + lr];
       rk = fmaf(uj, dots[2 * j], rk);
       rqv = fmaf(uj, dots[2 * j + 1], rqv);
     }
@@ -515,9 +516,11 @@ __global__ void __launch_bounds__(kPThreads, 2) kdap_kernel(const LayerDev d, co
         acc[e] = make_float4(srow[e].x * G4.x, srow[e].y * G4.y, srow[e].z * G4.z, srow[e].w * G4.w);
       for (int j = 0; j < n; ++j) {
         const float4 kt4 = reinterpret_cast<const float4*>(kt + j * kPN)[lane];
-        const float* uj = su + j * kUStride + 8 * warp;
+        const float4* uj4 = reinterpret_cast<const float4*>(su + j * P + r0 + 8 * warp);
+        const float4 ua = uj4[0], ub = uj4[1];
+        const float ue[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = axpy4(uj[e], kt4, acc[e]);
+        for (int e = 0; e < 8; ++e) acc[e] = axpy4x2(ue[e], kt4, acc[e]);
       }
       float4* gS4 = reinterpret_cast<float4*>(d.ckpt + (bh * P + r0 + 8 * warp) * kPN);
 #pragma unroll
@@ -553,7 +556,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // the persistent decode: d_state 128, whole 64-row units, every staged source
 // 16-byte aligned, two stages in shared memory
-size_t kdap_smem(const LayerDev& d) { return 2 * static_cast<size_t>(kdap_stage(d.C).size) + kdap_pers_bytes(); }
+size_t kdap_smem(const LayerDev& d) { return 2 * static_cast<size_t>(kdap_stage(d.C, d.P).size) + kdap_pers_bytes(); }
 
 bool kdap_supports(const LayerDev& d, const TokenIn& in) {
   return d.N == kPN && d.P % kPR == 0 && d.H % d.G == 0 && kdap_smem(d) <= 227u * 1024u && aligned16(d.ckpt) &&
