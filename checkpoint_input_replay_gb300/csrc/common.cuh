@@ -254,6 +254,21 @@ __device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
   return __half22float2(hv);
 }
 
+// eight packed e2m1 codes (one word, element 0 in the low nibble) -> eight floats
+__device__ __forceinline__ void e2m1x8_to_f32x2(uint32_t word, float2 out[4]) {
+  uint32_t h[4];
+  asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+      "mov.b32 {q0, q1, q2, q3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, q0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, q1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, q2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, q3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(word));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) out[i] = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
+}
+
 // x / d rounded to nearest for many x over one divisor d, given r = the
 // correctly rounded reciprocal of d (__frcp_rn): q = x r is within one ulp of
 // x / d, and one fused correction q + (x - q d) r rounds it correctly

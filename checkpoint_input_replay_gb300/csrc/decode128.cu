@@ -816,10 +816,12 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
             const uint32_t wd[2] = {wv.x, wv.y};
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-              a0 = fma2(e2m1x2_to_f32x2(wd[i] & 0xFFu), qv[4 * i], a0);
-              a1 = fma2(e2m1x2_to_f32x2((wd[i] >> 8) & 0xFFu), qv[4 * i + 1], a1);
-              a0 = fma2(e2m1x2_to_f32x2((wd[i] >> 16) & 0xFFu), qv[4 * i + 2], a0);
-              a1 = fma2(e2m1x2_to_f32x2(wd[i] >> 24), qv[4 * i + 3], a1);
+              float2 c[4];
+              e2m1x8_to_f32x2(wd[i], c);
+              a0 = fma2(c[0], qv[4 * i], a0);
+              a1 = fma2(c[1], qv[4 * i + 1], a1);
+              a0 = fma2(c[2], qv[4 * i + 2], a0);
+              a1 = fma2(c[3], qv[4 * i + 3], a1);
             }
             const float bs = e4m3_to_f32(gb[LY.gb_rs + ((hh0 + hu) * P + R) * (N / 16) + cbk]);
             v[f * HR + hu] = bs * ((a0.x + a0.y) + (a1.x + a1.y));

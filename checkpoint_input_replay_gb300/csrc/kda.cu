@@ -291,39 +291,56 @@ __global__ void __launch_bounds__(kKdaThreads, 4) kda_kernel(const LayerDev d, c
 //
 // The same arithmetic as kda_kernel, organised like the other d_state-128 decode
 // kernels: a CTA (two per SM) takes a contiguous range of units (sequence, head,
-// block of 64 rows) and a producer warp stages the next unit -- its checkpoint
-// rows, the buffered records (log decays and keys over the key channels, the
-// deltas of the head's rows), this token's log decay, key, query and values -- by bulk
-// copies into the other of two shared-memory stages while the eight computing
-// warps work on the current one: the channel-wise suffix scan (warps 0-3), the
-// record dot products (a warp per item), then eight rows a warp: the two
-// checkpoint dot products (a transpose-reduce over the row's lanes), the records'
-// terms (four lanes a row split the records), u, o and, on a flush step, the
-// folded rows.  The CTAs read their sequences' cursors once, at the start; the
-// last CTA of a sequence to count its units in advances the cursor.
+// block of 64 rows) and a producer warp stages the next unit by bulk copies into
+// the other of two shared-memory stages while the eight computing warps work on
+// the current one.  The first unit of a head stages the buffered records (log
+// decays and keys over the key channels, the deltas of its rows) and this
+// token's log decay, key, query and values, and builds the head's tables: the
+// channel-wise suffix scan (warps 0-3) gives the decayed keys k_j W'_j and G',
+// then the record dot products (a warp per item).  The head's next units, when
+// this CTA takes them right after, reuse those tables and stage only their
+// checkpoint rows, their rows of the deltas and values.  Then eight rows a warp:
+// the two checkpoint dot products (a transpose-reduce over the row's lanes), the
+// records' terms (four lanes a row split the records), u, o and, on a flush
+// step, the folded rows.  The CTAs read their sequences' cursors once, at the
+// start; the last CTA of a sequence to count its units in advances the cursor.
 
 constexpr int kPN = 128;                 // d_state
 constexpr int kPR = 64;                  // state rows per unit
 constexpr int kPThreads = kThreads + 32;  // eight computing warps and the producer warp
 constexpr int kPMaxSeq = 64;             // sequences one CTA may cover
+constexpr int kUStride = kPR + 8;        // floats per record row of the staged deltas (bank skew)
 
 struct KdaPStage {  // byte offsets within one stage
-  int tile, g, kb, u, tg, tk, tq, tv, vec, dots, size;
+  int tile, g, kb, u, tg, tk, tq, tv, size;
 };
 
-__host__ __device__ __forceinline__ KdaPStage kdap_stage(int C, int P) {
+__host__ __device__ __forceinline__ KdaPStage kdap_stage(int C) {
   KdaPStage m;
   int o = 0;
   m.tile = o; o += kPR * kPN * 4;       // the unit's checkpoint rows
-  m.g = o;    o += C * kPN * 4;         // records' log decays [j][N]; decayed keys k_j W'_j in place
-  m.kb = o;   o += C * kPN * 2;         // records' keys, bf16 [j][N]
-  m.u = o;    o += C * P * 4;           // records' deltas, all rows of the head [j][P] (two copies at most)
+  m.g = o;    o += C * kPN * 4;         // records' log decays [j][N] (first unit of a head)
+  m.kb = o;   o += C * kPN * 2;         // records' keys, bf16 [j][N] (first unit of a head)
+  m.u = o;    o += C * kUStride * 4;    // records' deltas of the unit's rows [j][kUStride]
   m.tg = o;   o += kPN * 4;             // this token's log decay over the channels
   m.tk = o;   o += kPN * 2;             // this token's key, bf16
   m.tq = o;   o += kPN * 2;             // this token's query, bf16
   m.tv = o;   o += kPR * 2;             // this token's values of the unit's rows, bf16
+  m.size = (o + 127) & ~127;
+  return m;
+}
+
+struct KdaPTab {  // byte offsets of the head's tables (one set per CTA)
+  int kt, vec, dots, ktok, size;
+};
+
+__host__ __device__ __forceinline__ KdaPTab kdap_tab(int C) {
+  KdaPTab m;
+  int o = 0;
+  m.kt = o;   o += C * kPN * 4;         // decayed keys k_j W'_j [j][N]
   m.vec = o;  o += 3 * kPN * 4;         // G', G' k, G' q
   m.dots = o; o += (2 * C + 4) * 4;     // (k_j W'_j) . k and . q interleaved, then k . q
+  m.ktok = o; o += kPN * 2;             // this token's key, bf16 (for the fold)
   m.size = (o + 127) & ~127;
   return m;
 }
@@ -338,8 +355,10 @@ __global__ void __launch_bounds__(kPThreads, 2) kdap_kernel(const LayerDev d, co
   const int total = d.B * ups;
   const int u0 = static_cast<int>(blockIdx.x) * per, u1 = min(u0 + per, total);
   if (u0 >= u1) return;
-  const KdaPStage M = kdap_stage(C, P);
-  unsigned char* pers = psm + 2 * M.size;
+  const KdaPStage M = kdap_stage(C);
+  const KdaPTab TB = kdap_tab(C);
+  unsigned char* tab = psm + 2 * M.size;
+  unsigned char* pers = tab + TB.size;
   uint64_t* full = reinterpret_cast<uint64_t*>(pers);  // [2] stage landed
   uint64_t* empty = full + 2;                          // [2] stage released by the eight computing warps
   int4* scur = reinterpret_cast<int4*>(pers + 32);     // per covered sequence: head, count, flags (1 ok, 2 flush)
@@ -376,11 +395,15 @@ __global__ void __launch_bounds__(kPThreads, 2) kdap_kernel(const LayerDev d, co
   if (warp == kThreads / 32) {
     // ================================ producer ================================
     if (lane == 0) {
-      int k = 0;  // units staged
+      int k = 0;           // units staged
+      long long prev = -1;  // (b H + h) parts + part of the last staged unit
       for (int uu = u0; uu < u1; ++uu) {
         const int b = uu / ups, rem = uu - b * ups, h = rem / parts, part = rem - h * parts;
         const int4 cs = scur[b - b0];
         if (!(cs.z & 1)) continue;
+        const long long key = static_cast<long long>(uu);
+        const bool reuse = part > 0 && prev == key - 1;  // the head's tables are in place
+        prev = key;
         const int s = k & 1;
         if (k >= 2 && !mbar_wait_bounded(empty + s, static_cast<uint32_t>(((k >> 1) - 1) & 1))) {
           report_error(d.err, DEVERR_TIMEOUT, b);
@@ -392,24 +415,27 @@ __global__ void __launch_bounds__(kPThreads, 2) kdap_kernel(const LayerDev d, co
         const int head = cs.x, n = cs.y;
         const size_t bh = static_cast<size_t>(b) * H + h, bg = static_cast<size_t>(b) * G + h / (H / G);
         const int r0 = part * kPR;
-        const int seg1 = min(n, C - head), seg2 = n - seg1;
         uint64_t* bar = full + s;
-        mbar_expect_tx(bar, static_cast<uint32_t>(kPR * kPN * 4 + n * (kPN * 6 + P * 4) + kPN * 8 + kPR * 2));
+        mbar_expect_tx(bar, static_cast<uint32_t>(kPR * kPN * 4 + n * kPR * 4 + kPR * 2 +
+                                                  (reuse ? 0 : n * kPN * 6 + kPN * 8)));
         bulk_g2s(st + M.tile, d.ckpt + (bh * P + r0) * kPN, kPR * kPN * 4, bar);
-        if (seg1) {
-          bulk_g2s(st + M.g, d.r_g + (bh * C + head) * kPN, seg1 * kPN * 4, bar);
-          bulk_g2s(st + M.kb, d.r_k + (bg * C + head) * kPN, seg1 * kPN * 2, bar);
-          bulk_g2s(st + M.u, d.r_u + (bh * C + head) * P, seg1 * P * 4, bar);
-        }
-        if (seg2) {
-          bulk_g2s(st + M.g + seg1 * kPN * 4, d.r_g + bh * C * kPN, seg2 * kPN * 4, bar);
-          bulk_g2s(st + M.kb + seg1 * kPN * 2, d.r_k + bg * C * kPN, seg2 * kPN * 2, bar);
-          bulk_g2s(st + M.u + seg1 * P * 4, d.r_u + bh * C * P, seg2 * P * 4, bar);
-        }
-        bulk_g2s(st + M.tg, in.g + bh * kPN, kPN * 4, bar);
-        bulk_g2s(st + M.tk, in.k + bg * kPN, kPN * 2, bar);
-        bulk_g2s(st + M.tq, in.q + bg * kPN, kPN * 2, bar);
+        for (int j = 0; j < n; ++j)
+          bulk_g2s(st + M.u + j * kUStride * 4, d.r_u + (bh * C + kslot(head, j, C)) * P + r0, kPR * 4, bar);
         bulk_g2s(st + M.tv, in.v + bh * P + r0, kPR * 2, bar);
+        if (!reuse) {
+          const int seg1 = min(n, C - head), seg2 = n - seg1;
+          if (seg1) {
+            bulk_g2s(st + M.g, d.r_g + (bh * C + head) * kPN, seg1 * kPN * 4, bar);
+            bulk_g2s(st + M.kb, d.r_k + (bg * C + head) * kPN, seg1 * kPN * 2, bar);
+          }
+          if (seg2) {
+            bulk_g2s(st + M.g + seg1 * kPN * 4, d.r_g + bh * C * kPN, seg2 * kPN * 4, bar);
+            bulk_g2s(st + M.kb + seg1 * kPN * 2, d.r_k + bg * C * kPN, seg2 * kPN * 2, bar);
+          }
+          bulk_g2s(st + M.tg, in.g + bh * kPN, kPN * 4, bar);
+          bulk_g2s(st + M.tk, in.k + bg * kPN, kPN * 2, bar);
+          bulk_g2s(st + M.tq, in.q + bg * kPN, kPN * 2, bar);
+        }
         ++k;
       }
       // the copies in flight land before the CTA's shared memory is released
@@ -420,11 +446,18 @@ __global__ void __launch_bounds__(kPThreads, 2) kdap_kernel(const LayerDev d, co
 
   // ============================== computing warps ==============================
   const int rq = (lane >> 2) & 7, jl = lane & 3;  // row of the warp's eight, record lane
+  float* kt = reinterpret_cast<float*>(tab + TB.kt);
+  float* vec = reinterpret_cast<float*>(tab + TB.vec);
+  float* dots = reinterpret_cast<float*>(tab + TB.dots);
+  uint16_t* ktok = reinterpret_cast<uint16_t*>(tab + TB.ktok);
   int k = 0;
+  long long prev = -1;
   for (int uu = u0; uu < u1; ++uu) {
     const int b = uu / ups, rem = uu - b * ups, h = rem / parts, part = rem - h * parts;
     const int4 cs = scur[b - b0];
     if (!(cs.z & 1)) continue;
+    const bool reuse = part > 0 && prev == static_cast<long long>(uu) - 1;
+    prev = uu;
     const int s = k & 1;
     const uint32_t par = static_cast<uint32_t>((k >> 1) & 1);
     ++k;
@@ -433,6 +466,8 @@ __global__ void __launch_bounds__(kPThreads, 2) kdap_kernel(const LayerDev d, co
     const int head = cs.x, n = cs.y;
     const bool flush = (cs.z & 2) != 0;
     const float beta = in.beta[bh];  // in flight during the scan
+    // (also the barrier that keeps the head's tables until every warp is past the
+    // previous unit)
     if (!compute_sync_and(mbar_wait_bounded(full + s, par))) {
       if (t == 0) {
         report_error(d.err, DEVERR_TIMEOUT, b);
@@ -441,41 +476,41 @@ __global__ void __launch_bounds__(kPThreads, 2) kdap_kernel(const LayerDev d, co
       break;
     }
     unsigned char* st = psm + static_cast<size_t>(s) * M.size;
-    float* kt = reinterpret_cast<float*>(st + M.g);
-    const uint16_t* kb = reinterpret_cast<const uint16_t*>(st + M.kb);
     const float* su = reinterpret_cast<const float*>(st + M.u);
-    const float* tg = reinterpret_cast<const float*>(st + M.tg);
-    const uint16_t* tk = reinterpret_cast<const uint16_t*>(st + M.tk);
-    const uint16_t* tq = reinterpret_cast<const uint16_t*>(st + M.tq);
     const uint16_t* tv = reinterpret_cast<const uint16_t*>(st + M.tv);
-    float* vec = reinterpret_cast<float*>(st + M.vec);
-    float* dots = reinterpret_cast<float*>(st + M.dots);
-    // channel-wise suffix scan: W'_j = exp(sum of the log decays after record j, this
-    // token's included), decayed key k_j W'_j in place of the log decays; G' = exp(all)
-    // (the fast exponential: its relative error, a few 1e-7 at these arguments, is far
-    // below the FP32 path's tolerance)
-    if (t < kPN) {
-      float acc = tg[t];
-      for (int j = n - 1; j >= 0; --j) {
-        const float gj = kt[j * kPN + t];
-        kt[j * kPN + t] = bf(kb[j * kPN + t]) * __expf(acc);
-        acc += gj;
+    if (!reuse) {
+      const float* rg = reinterpret_cast<const float*>(st + M.g);
+      const uint16_t* kb = reinterpret_cast<const uint16_t*>(st + M.kb);
+      const float* tg = reinterpret_cast<const float*>(st + M.tg);
+      const uint16_t* tk = reinterpret_cast<const uint16_t*>(st + M.tk);
+      const uint16_t* tq = reinterpret_cast<const uint16_t*>(st + M.tq);
+      // channel-wise suffix scan: W'_j = exp(sum of the log decays after record j, this
+      // token's included), decayed key k_j W'_j; G' = exp(all).  (The fast exponential:
+      // its relative error, a few 1e-7 at these arguments, is far below the FP32
+      // path's tolerance.)
+      if (t < kPN) {
+        float acc = tg[t];
+        for (int j = n - 1; j >= 0; --j) {
+          kt[j * kPN + t] = bf(kb[j * kPN + t]) * __expf(acc);
+          acc += rg[j * kPN + t];
+        }
+        const float Gp = __expf(acc);
+        vec[t] = Gp;
+        vec[kPN + t] = Gp * bf(tk[t]);
+        vec[2 * kPN + t] = Gp * bf(tq[t]);
+        ktok[t] = tk[t];
       }
-      const float Gp = __expf(acc);
-      vec[t] = Gp;
-      vec[kPN + t] = Gp * bf(tk[t]);
-      vec[2 * kPN + t] = Gp * bf(tq[t]);
+      compute_sync();
+      // record dots (k_j W'_j) . k and . q (items 2 j and 2 j + 1), and k . q (item 2 n)
+      for (int it = warp; it < 2 * n + 1; it += kThreads / 32) {
+        const float4 a4 = it < 2 * n ? reinterpret_cast<const float4*>(kt + (it >> 1) * kPN)[lane]
+                                     : bf4(reinterpret_cast<const uint2*>(tk)[lane]);
+        const float4 b4 = bf4(reinterpret_cast<const uint2*>((it < 2 * n && (it & 1) == 0) ? tk : tq)[lane]);
+        const float v = seg_sum<32>(dot4(a4, b4));
+        if (lane == 0) dots[it] = v;
+      }
+      compute_sync();
     }
-    compute_sync();
-    // record dots (k_j W'_j) . k and . q (items 2 j and 2 j + 1), and k . q (item 2 n)
-    for (int it = warp; it < 2 * n + 1; it += kThreads / 32) {
-      const float4 a4 = it < 2 * n ? reinterpret_cast<const float4*>(kt + (it >> 1) * kPN)[lane]
-                                   : bf4(reinterpret_cast<const uint2*>(tk)[lane]);
-      const float4 b4 = bf4(reinterpret_cast<const uint2*>((it < 2 * n && (it & 1) == 0) ? tk : tq)[lane]);
-      const float v = seg_sum<32>(dot4(a4, b4));
-      if (lane == 0) dots[it] = v;
-    }
-    compute_sync();
     // the warp's eight rows: checkpoint dot products, records' terms, u and o
     const int lr = 8 * warp + rq;  // this lane's row (of the unit) after the reductions
     const float4* tile4 = reinterpret_cast<const float4*>(st + M.tile);
@@ -492,7 +527,7 @@ __global__ void __launch_bounds__(kPThreads, 2) kdap_kernel(const LayerDev d, co
     const float sk = reduce8(pk, lane), sq = reduce8(pq, lane);
     float rk = 0.f, rqv = 0.f;
     for (int j = jl; j < n; j += 4) {
-      const float uj = su[j * P + r0 + lr];
+      const float uj = su[j * kUStride + lr];
       rk = fmaf(uj, dots[2 * j], rk);
       rqv = fmaf(uj, dots[2 * j + 1], rqv);
     }
@@ -509,14 +544,14 @@ __global__ void __launch_bounds__(kPThreads, 2) kdap_kernel(const LayerDev d, co
     if (flush) {
       // S_new = S_ckpt Diag(G') + sum_j u_j (k_j W'_j)^T + u k^T, stored once
       const float4 G4 = reinterpret_cast<const float4*>(vec)[lane];
-      const float4 k4 = bf4(reinterpret_cast<const uint2*>(tk)[lane]);
+      const float4 k4 = bf4(reinterpret_cast<const uint2*>(ktok)[lane]);
       float4 acc[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e)
         acc[e] = make_float4(srow[e].x * G4.x, srow[e].y * G4.y, srow[e].z * G4.z, srow[e].w * G4.w);
       for (int j = 0; j < n; ++j) {
         const float4 kt4 = reinterpret_cast<const float4*>(kt + j * kPN)[lane];
-        const float4* uj4 = reinterpret_cast<const float4*>(su + j * P + r0 + 8 * warp);
+        const float4* uj4 = reinterpret_cast<const float4*>(su + j * kUStride + 8 * warp);
         const float4 ua = uj4[0], ub = uj4[1];
         const float ue[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
@@ -530,9 +565,10 @@ __global__ void __launch_bounds__(kPThreads, 2) kdap_kernel(const LayerDev d, co
       }
     } else if (part == 0 && t < kPN) {
       // this token's record: g over the key channels per head, k once per key group
+      // (the first unit of a head stages this token's inputs)
       const int slot = kslot(head, n, C);
-      d.r_g[(bh * C + slot) * kPN + t] = tg[t];
-      if (h % (H / G) == 0) d.r_k[(bg * C + slot) * kPN + t] = tk[t];
+      d.r_g[(bh * C + slot) * kPN + t] = reinterpret_cast<const float*>(st + M.tg)[t];
+      if (h % (H / G) == 0) d.r_k[(bg * C + slot) * kPN + t] = ktok[t];
     }
     // the warp is done with the stage
     __syncwarp();
@@ -556,7 +592,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // the persistent decode: d_state 128, whole 64-row units, every staged source
 // 16-byte aligned, two stages in shared memory
-size_t kdap_smem(const LayerDev& d) { return 2 * static_cast<size_t>(kdap_stage(d.C, d.P).size) + kdap_pers_bytes(); }
+size_t kdap_smem(const LayerDev& d) {
+  return 2 * static_cast<size_t>(kdap_stage(d.C).size) + kdap_tab(d.C).size + kdap_pers_bytes();
+}
 
 bool kdap_supports(const LayerDev& d, const TokenIn& in) {
   return d.N == kPN && d.P % kPR == 0 && d.H % d.G == 0 && kdap_smem(d) <= 227u * 1024u && aligned16(d.ckpt) &&
