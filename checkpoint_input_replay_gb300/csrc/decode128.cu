@@ -17,11 +17,13 @@
 //    query, the current tokens of all its heads, the ring's per-head decay rows,
 //    the current per-head scalars, the read-copy scales -- is staged once per
 //    group, one group ahead, into one of three group buffers;
-//  * builder warps (two for Mamba-2, one for Gated DeltaNet), one group ahead of
-//    the computing warps: the query (and current key) in FP32, the group's key
-//    dot products (eight keys per transpose-reduce), the per-head coefficient
-//    tables (one decay suffix scan per head, two heads at once in 16-lane
-//    halves when the records fit), and the ring appends of the group's current
+//  * two builder warps, one group ahead of the computing warps: the query (and
+//    current key) in FP32, the group's key dot products (eight keys per
+//    transpose-reduce; on Gated DeltaNet layers, whose groups hold two heads,
+//    one builder takes the k_j . q and the other the k_j . k_cur), the per-head
+//    coefficient tables (one decay suffix scan per head; on Mamba-2 layers two
+//    heads at once in 16-lane halves when the records fit, on Gated DeltaNet
+//    layers one head per builder), and the ring appends of the group's current
 //    tokens;
 //  * a prologue warp publishes per unit a 16-byte descriptor and signals
 //    `ready` (at a group's first unit, once its tables are in place);
@@ -76,6 +78,22 @@ struct Lay128 {
   int pe_A, pe_bars, pe_seq, pe_misc, pe_cnt, pe_mtab, pe_dq, pe_size;
 };
 
+// Barriers of the two builder warps (named barrier 3, 64 threads); the _and form
+// returns whether `v` held in both.
+__device__ __forceinline__ void builder_pair_sync() { asm volatile("bar.sync 3, 64;" ::: "memory"); }
+__device__ __forceinline__ bool builder_pair_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 3, 64, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+
 // heads in a non-flush unit of a read-copy layer: 4 heads' codes fit where one
 // FP32 matrix goes, and the unit's fixed costs are shared by 4 heads
 __host__ __device__ __forceinline__ int read_heads(int read) { return read == READ_NONE ? 1 : 4; }
@@ -92,9 +110,9 @@ __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int
   l.st_tile = o;  o += rpu * N * 4;
   // a read-copy unit's heads' record blocks sit 16 bytes off the 128-byte bank period
   l.rec_stride = al16(C * P * 2) + (read == READ_NONE ? 0 : 16);
-  // a Gated DeltaNet record row (the unit's rows of u_j) is padded by 16 floats, so
-  // that the two lanes of a row reading records of either parity hit other banks
-  l.urow = rpu + 16;
+  // Gated DeltaNet records are staged whole (all P rows of u_j, both units of a
+  // head), by at most two copies per unit
+  l.urow = P;
   l.st_rec = o;   o += kind == 0 ? read_heads(read) * l.rec_stride : C * l.urow * 4;
   l.st_meta = o;  o += 32;              // int4 descriptor, NVFP4 amax word
   l.st_size = al128(o);
@@ -120,7 +138,7 @@ __host__ __device__ __forceinline__ Lay128 lay128(int kind, int read, int P, int
   l.pe_misc = o;  o += 16;
   l.pe_cnt = o;   o += 16;  // computing warps that have finished this CTA's units
   l.pe_mtab = o;  o += (kThreads / 32) * mtab_rows(kind, read, P) * kMtabRow * 4;  // per computing warp: fold coefficients [rows][records]
-  l.pe_dq = o;    o += 2 * 2 * kMaxRec * 4;                 // per builder: k_j . q, k_j . k_cur
+  l.pe_dq = o;    o += 2 * 2 * kMaxRec * 4;                 // key dots: per builder (Mamba-2) or per group parity (GDN)
   l.pe_size = al128(o);
   return l;
 }
@@ -254,7 +272,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   static_assert(TEAMS == 1 || TEAMS == 2 || TEAMS == 4, "teams: a power of two dividing the 8 computing warps");
   constexpr int TW = 8 / TEAMS;                         // warps of a team
   constexpr int RW = RPU / TW;                          // rows per computing warp and unit
-  constexpr int NB = KIND == 0 ? 2 : 1;                 // builder warps (Mamba-2 groups hold more heads)
+  constexpr int NB = 2;                                  // builder warps
   constexpr int tile = P * N;                           // floats of one head's state
   constexpr int HR = READ == READ_NONE ? 1 : 4;         // heads of a non-flush read-copy unit
   const int H = d.H, G = d.G, C = d.C, L = d.L, Cp = d.Cp;
@@ -476,7 +494,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
       constexpr int esz = KIND == 0 ? 2 : 4;
       const int nh = step_of(w.b);  // heads in this unit
       const uint32_t tb = (READ == READ_NONE || flush) ? RPU * N * 4 : (READ == READ_FP8 ? tile : tile / 2);
-      mbar_expect_tx(bar, nh * (tb + static_cast<uint32_t>(n) * RPU * esz));
+      mbar_expect_tx(bar, nh * (tb + static_cast<uint32_t>(n) * (KIND == 0 ? RPU : P) * esz));
       // the unit: state matrix (or read copy) and this head's buffered records
       if (READ == READ_NONE || flush) bulk_g2s(st + LY.st_tile, d.ckpt + u * tile + w.sp * RPU * N, tb, bar);
       else bulk_g2s(st + LY.st_tile, d.rc_codes + u * tb, nh * tb, bar);  // nh consecutive heads
@@ -491,11 +509,9 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
           if (seg2) bulk_g2s(rdst + seg1 * rrow, rsrc + uh * C * rrow, seg2 * rrow, bar);
         }
       } else {
-        // this unit's rows of each buffered record: one copy per record, rows padded
-        for (int j = 0; j < n; ++j)
-          bulk_g2s(st + LY.st_rec + static_cast<size_t>(j) * LY.urow * esz,
-                   rsrc + (u * C + ring_slot(head, j, C)) * rrow + static_cast<size_t>(w.sp) * RPU * esz, RPU * esz,
-                   bar);
+        // the head's buffered records, whole (the ring's slots are contiguous up to the wrap)
+        if (seg1) bulk_g2s(st + LY.st_rec, rsrc + (u * C + head) * rrow, seg1 * rrow, bar);
+        if (seg2) bulk_g2s(st + LY.st_rec + seg1 * rrow, rsrc + u * C * rrow, seg2 * rrow, bar);
       }
       smisc[1] = i + 1;
       if (first && gn.ui0 < u1) {
@@ -512,20 +528,32 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
   if (warp >= kBuilderWarp) {
     const int bi = warp - kBuilderWarp;
     if (bi >= NB) return;
-    float* pdq = reinterpret_cast<float*>(pbase + LY.pe_dq) + bi * 2 * kMaxRec;  // k_j . q
-    float* pdk = pdq + kMaxRec;                                                   // k_j . k_cur
+    float* pdq = reinterpret_cast<float*>(pbase + LY.pe_dq) + bi * 2 * kMaxRec;  // k_j . q (Mamba-2)
     GWalk gw;
     gw.start(u0, H, hpg, SPL);
     int built = 0;
     for (int gi = 0; gw.ui0 < u1; ++gi, gw.next(H, G, hpg, SPL)) {
-      if (smisc[0]) break;
       const int x = gi % kGroupBufs;
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(gfull + x, static_cast<uint32_t>((gi / kGroupBufs) & 1)))) {
-        if (lane == 0) {
-          report_error(d.err, DEVERR_TIMEOUT, gw.b);
-          smisc[0] = 1;
+      if (KIND == 1) {
+        // the two builders split each group's work and meet at a barrier, so they
+        // decide together whether to go on
+        const bool go = !smisc[0] && mbar_wait_bounded(gfull + x, static_cast<uint32_t>((gi / kGroupBufs) & 1));
+        if (!builder_pair_and(go)) {
+          if (lane == 0 && !smisc[0]) {
+            report_error(d.err, DEVERR_TIMEOUT, gw.b);
+            smisc[0] = 1;
+          }
+          break;
         }
-        break;
+      } else {
+        if (smisc[0]) break;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(gfull + x, static_cast<uint32_t>((gi / kGroupBufs) & 1)))) {
+          if (lane == 0) {
+            report_error(d.err, DEVERR_TIMEOUT, gw.b);
+            smisc[0] = 1;
+          }
+          break;
+        }
       }
       built = gi + 1;
       const int k = gw.b - b0;
@@ -545,31 +573,36 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
           reinterpret_cast<float4*>(gb + LY.gb_qf)[lane] = q4;
           if (KIND == 1) reinterpret_cast<float4*>(gb + LY.gb_kf)[lane] = kc4;
         }
-        // key dot products of records 0..n, eight keys per transpose-reduce
+        // key dot products of records 0..n, eight keys per transpose-reduce (Gated
+        // DeltaNet: builder 0 the k_j . q, builder 1 the k_j . k_cur, into tables of
+        // the group's parity that both read)
+        float* gdq = reinterpret_cast<float*>(pbase + LY.pe_dq) + (gi & 1) * 2 * kMaxRec;
+        float* gdk = gdq + kMaxRec;
+        const float4 o4 = (KIND == 1 && bi == 1) ? kc4 : q4;
         for (int jb = 0; jb <= n; jb += 8) {
-          float pq[8], pk[8];
+          float pq[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float4 kj = jb + e <= n ? bf4(reinterpret_cast<const uint2*>(kb + (jb + e) * N)[lane])
                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-            pq[e] = dot4(kj, q4);
-            pk[e] = KIND == 1 ? dot4(kj, kc4) : 0.f;
+            pq[e] = dot4(kj, o4);
           }
           const float tq = reduce8(pq, lane);
-          const float tk = KIND == 1 ? reduce8(pk, lane) : 0.f;
           const int j = jb + (lane >> 2);
           if ((lane & 3) == 0 && j <= n) {
-            pdq[j] = tq;
-            if (KIND == 1) pdk[j] = tk;
+            if (KIND == 0) pdq[j] = tq;
+            else (bi == 0 ? gdq : gdk)[j] = tq;
           }
         }
-        __syncwarp();
+        if (KIND == 1) builder_pair_sync();
+        else __syncwarp();
         // coefficient tables: two heads at once in the 16-lane halves when records
         // 0..n fit in 16 lanes; passes shared out over the builders
-        const int sw = n < 16 ? 16 : 32;
+        // (Gated DeltaNet: one head per builder and pass)
+        const int sw = (KIND == 0 && n < 16) ? 16 : 32;
         const int jl = lane & (sw - 1);
-        const float dq = jl <= n ? pdq[jl] : 0.f;
-        const float dk = (KIND == 1 && jl <= n) ? pdk[jl] : 0.f;
+        const float dq = jl <= n ? (KIND == 0 ? pdq : gdq)[jl] : 0.f;
+        const float dk = (KIND == 1 && jl <= n) ? gdk[jl] : 0.f;
         const int slot_j = jl < n ? ring_slot(head, jl, C) : 0;
         for (int e0 = gw.hh0 + bi * (32 / sw); e0 < hh_hi; e0 += NB * (32 / sw)) {
           const int e = e0 + lane / sw;
@@ -1060,7 +1093,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
           }
         }
       } else {
-        const float* ub = reinterpret_cast<const float*>(st + LY.st_rec);
+        const float* ub = reinterpret_cast<const float*>(st + LY.st_rec) + sp * RPU;  // this unit's rows
         const float4 kc4 = reinterpret_cast<const float4*>(gb + LY.gb_kf)[lane];
         const float a = co[3 * C + CO_A], beta = co[3 * C + CO_BETA];
         const float kq_dot = co[3 * C + CO_KQ];

@@ -296,7 +296,8 @@ __global__ void __launch_bounds__(kKdaThreads, 4) kda_kernel(const LayerDev d, c
 // the current one.  The first unit of a head stages the buffered records (log
 // decays and keys over the key channels, the deltas of its rows) and this
 // token's log decay, key, query and values, and builds the head's tables: the
-// channel-wise suffix scan (warps 0-3) gives the decayed keys k_j W'_j and G',
+// channel-wise suffix scan (the eight warps, two halves of the records) gives the
+// decayed keys k_j W'_j and G',
 // then the record dot products (a warp per item).  The head's next units, when
 // this CTA takes them right after, reuse those tables and stage only their
 // checkpoint rows, their rows of the deltas and values.  Then eight rows a warp:
@@ -488,17 +489,25 @@ __global__ void __launch_bounds__(kPThreads, 2) kdap_kernel(const LayerDev d, co
       // token's included), decayed key k_j W'_j; G' = exp(all).  (The fast exponential:
       // its relative error, a few 1e-7 at these arguments, is far below the FP32
       // path's tolerance.)
-      if (t < kPN) {
-        float acc = tg[t];
-        for (int j = n - 1; j >= 0; --j) {
-          kt[j * kPN + t] = bf(kb[j * kPN + t]) * __expf(acc);
-          acc += rg[j * kPN + t];
+      // All eight warps: threads 128-255 take records m..n-1 (m = n / 2), threads 0-127
+      // records 0..m-1 after adding up the later records' log decays themselves.
+      {
+        const int ch = t & (kPN - 1), m = n >> 1;
+        const bool late = t >= kPN;
+        float acc = tg[ch];
+        if (!late)
+          for (int j = n - 1; j >= m; --j) acc += rg[j * kPN + ch];
+        for (int j = late ? n - 1 : m - 1; j >= (late ? m : 0); --j) {
+          kt[j * kPN + ch] = bf(kb[j * kPN + ch]) * __expf(acc);
+          acc += rg[j * kPN + ch];
         }
-        const float Gp = __expf(acc);
-        vec[t] = Gp;
-        vec[kPN + t] = Gp * bf(tk[t]);
-        vec[2 * kPN + t] = Gp * bf(tq[t]);
-        ktok[t] = tk[t];
+        if (!late) {
+          const float Gp = __expf(acc);
+          vec[ch] = Gp;
+          vec[kPN + ch] = Gp * bf(tk[ch]);
+          vec[2 * kPN + ch] = Gp * bf(tq[ch]);
+          ktok[ch] = tk[ch];
+        }
       }
       compute_sync();
       // record dots (k_j W'_j) . k and . q (items 2 j and 2 j + 1), and k . q (item 2 n)
