@@ -435,6 +435,7 @@ def read_copy_leg(wl, dev, mode, K, W):
     elapsed, per = run_decode_loop(cache, steps, K, W, dev, lambda: None)
     nf = [(t, p) for t, p in enumerate(per) if (W + t) % L != L - 1]
     nonflush = [p for _, p in nf]
+    fl = [p for t, p in enumerate(per) if (W + t) % L == L - 1]
     H, P, N = s.n_heads, s.d_head, s.d_state
     state = H * P * N * 4
     rc = H * P * N + H * P * 4 if mode == "fp8" else H * P * N // 2 + H * P * N // 16 + H * 4
@@ -445,6 +446,8 @@ def read_copy_leg(wl, dev, mode, K, W):
     del cache
     torch.cuda.empty_cache()
     return {"mode": mode, "nonflush_us": 1e3 * statistics.mean(nonflush),
+            "flush_us": 1e3 * statistics.mean(fl) if fl else None,
+            "window_us_per_step": 1e3 * (sum(nonflush) / len(nonflush) * (L - 1) + (statistics.mean(fl) if fl else 0)) / L,
             "nonflush_gbs": nf_bytes / (sum(nonflush) * 1e6),
             "copy_bytes_per_seq": rc, "seq_steps_per_s": s.batch * K / (elapsed / 1e3)}
 
