@@ -269,6 +269,10 @@ __device__ __forceinline__ void e2m1x8_to_f32x2(uint32_t word, float2 out[4]) {
   for (int i = 0; i < 4; ++i) out[i] = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
 }
 
+// the correctly rounded reciprocal of 448 (the FP8 e4m3 maximum), for div_by: an
+// FP8 row scale amax / 448 is correctly rounded for every amax above 2^-117
+constexpr float kInv448 = 1.0f / 448.0f;
+
 // x / d rounded to nearest for many x over one divisor d, given r = the
 // correctly rounded reciprocal of d (__frcp_rn): q = x r is within one ulp of
 // x / d, and one fused correction q + (x - q d) r rounds it correctly
@@ -299,6 +303,30 @@ __device__ __forceinline__ float reduce8_lanes3(const float v[8], int lane) {
     x[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
   }
   return (b0 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, b0 ? x[0] : x[1], 1);
+}
+
+// Maximum of each of v[0..7] over the 32 lanes of the warp (transpose-reduce: 9
+// shuffles).  Lane L returns the maximum of v[(L >> 2) & 7].
+__device__ __forceinline__ float reduce8_max(const float v[8], int lane) {
+  const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
+  float w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = b4 ? v[i] : v[i + 4];
+    const float keep = b4 ? v[i + 4] : v[i];
+    w[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  }
+  float x[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = b3 ? w[i] : w[i + 2];
+    const float keep = b3 ? w[i + 2] : w[i];
+    x[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+  float z = fmaxf(b2 ? x[1] : x[0], __shfl_xor_sync(0xffffffffu, b2 ? x[0] : x[1], 4));
+  z = fmaxf(z, __shfl_xor_sync(0xffffffffu, z, 2));
+  z = fmaxf(z, __shfl_xor_sync(0xffffffffu, z, 1));
+  return z;
 }
 
 // Sum each of v[0..7] over the 32 lanes of the warp (transpose-reduce: 9

@@ -1019,32 +1019,40 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               __stcs(gS4 + (tw + TW * (r0 + e)) * SEG + lane, acc[e]);
-              if (READ != READ_NONE) sT4[(tw + TW * (r0 + e)) * SEG + lane] = acc[e];
+              if (READ == READ_NVFP4) sT4[(tw + TW * (r0 + e)) * SEG + lane] = acc[e];
+            }
+            if (READ == READ_FP8) {
+              // refresh the FP8 copy of these eight rows from the folded rows in registers:
+              // the rows' amax by one transpose-reduce, then per row scale = amax / 448 and
+              // code = e4m3(x / scale), both divisions correctly rounded
+              float am[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                am[e] = fmaxf(fmaxf(fabsf(acc[e].x), fabsf(acc[e].y)), fmaxf(fabsf(acc[e].z), fabsf(acc[e].w)));
+              const float amx = reduce8_max(am, lane);  // row (lane >> 2) & 7
+              uint32_t* codes = reinterpret_cast<uint32_t*>(d.rc_codes + u * tile);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int R = tw + TW * (r0 + e);
+                const float mx = __shfl_sync(0xffffffffu, amx, 4 * e);
+                const float scale = div_by(mx, 448.0f, kInv448);
+                uint32_t packed = 0;
+                if (scale != 0.0f) {
+                  const float rs = __frcp_rn(scale);
+                  const uint32_t lo = f32x2_to_e4m3x2(div_by(acc[e].x, scale, rs), div_by(acc[e].y, scale, rs));
+                  const uint32_t hi = f32x2_to_e4m3x2(div_by(acc[e].z, scale, rs), div_by(acc[e].w, scale, rs));
+                  packed = lo | (hi << 16);
+                }
+                codes[R * SEG + lane] = packed;
+                if (lane == 0) d.rc_rowscale[u * P + R] = scale;
+              }
             }
           }
         }
-        if (READ != READ_NONE && flush) {
-          // refresh the read copy of this warp's rows from the folded rows in shared memory
-          if (READ == READ_FP8) {
-            uint32_t* codes = reinterpret_cast<uint32_t*>(d.rc_codes + u * tile);
-#pragma unroll
-            for (int m = 0; m < RW; ++m) {
-              const int R = tw + TW * m;
-              const float4 v4 = sT4[R * SEG + lane];
-              float mx = fmaxf(fmaxf(fabsf(v4.x), fabsf(v4.y)), fmaxf(fabsf(v4.z), fabsf(v4.w)));
-              mx = seg_max<32>(mx);
-              const float scale = __fdiv_rn(mx, 448.0f);
-              uint32_t packed = 0;
-              if (scale != 0.0f) {
-                const float rs = __frcp_rn(scale);
-                const uint32_t lo = f32x2_to_e4m3x2(div_by(v4.x, scale, rs), div_by(v4.y, scale, rs));
-                const uint32_t hi = f32x2_to_e4m3x2(div_by(v4.z, scale, rs), div_by(v4.w, scale, rs));
-                packed = lo | (hi << 16);
-              }
-              codes[R * SEG + lane] = packed;
-              if (lane == 0) d.rc_rowscale[u * P + R] = scale;
-            }
-          } else {
+        if (READ == READ_NVFP4 && flush) {
+          // refresh the NVFP4 copy of this warp's rows from the folded rows in shared memory
+          // (the matrix scale needs the amax of the whole head first)
+          {
             float mloc = 0.f;
 #pragma unroll
             for (int m = 0; m < RW; ++m) {
@@ -1068,6 +1076,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
               const float amax = __int_as_float(*reinterpret_cast<volatile int*>(slot_amax));
               const float smat = __fdiv_rn(amax, 2688.0f);  // 448 * 6
               const float six_s = __fmul_rn(6.0f, smat);
+              const float r6 = six_s != 0.0f ? __frcp_rn(six_s) : 0.0f;
               uint16_t* codes = reinterpret_cast<uint16_t*>(d.rc_codes + u * (tile / 2));
               uint8_t* blk = d.rc_blkscale + u * (tile / 16);
 #pragma unroll
@@ -1077,7 +1086,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
                 float mb = fmaxf(fmaxf(fabsf(v4.x), fabsf(v4.y)), fmaxf(fabsf(v4.z), fabsf(v4.w)));
                 mb = seg_max<4>(mb);  // 4 lanes = one 16-element block
                 uint32_t bcode = 0;
-                if (six_s != 0.0f) bcode = f32x2_to_e4m3x2(__fdiv_rn(mb, six_s), 0.0f) & 0xFFu;
+                if (six_s != 0.0f) bcode = f32x2_to_e4m3x2(div_by(mb, six_s, r6), 0.0f) & 0xFFu;
                 const float dd = __fmul_rn(e4m3_to_f32(bcode), smat);
                 uint32_t qv = 0;
                 if (dd != 0.0f) {

@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         const float4 v4 = sT4[R * SEG + lane];
         float mx = fmaxf(fmaxf(fabsf(v4.x), fabsf(v4.y)), fmaxf(fabsf(v4.z), fabsf(v4.w)));
         mx = seg_max<32>(mx);
-        const float scale = __fdiv_rn(mx, 448.0f);
+        const float scale = div_by(mx, 448.0f, kInv448);
         uint32_t packed = 0;
         if (scale != 0.0f) {
           const float rs = __frcp_rn(scale);
@@ -450,6 +450,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         const float amax = __int_as_float(*reinterpret_cast<volatile int*>(slot_amax));
         const float smat = __fdiv_rn(amax, 2688.0f);  // 448 * 6
         const float six_s = __fmul_rn(6.0f, smat);
+        const float r6 = six_s != 0.0f ? __frcp_rn(six_s) : 0.0f;
         uint16_t* codes = reinterpret_cast<uint16_t*>(d.rc_codes + u * (tile / 2));
         uint8_t* blk = d.rc_blkscale + u * (tile / 16);
 #pragma unroll
@@ -459,7 +460,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           float mb = fmaxf(fmaxf(fabsf(v4.x), fabsf(v4.y)), fmaxf(fabsf(v4.z), fabsf(v4.w)));
           mb = seg_max<4>(mb);  // 4 lanes = one 16-element block
           uint32_t bcode = 0;
-          if (six_s != 0.0f) bcode = f32x2_to_e4m3x2(__fdiv_rn(mb, six_s), 0.0f) & 0xFFu;
+          if (six_s != 0.0f) bcode = f32x2_to_e4m3x2(div_by(mb, six_s, r6), 0.0f) & 0xFFu;
           const float dd = __fmul_rn(e4m3_to_f32(bcode), smat);
           uint32_t qv = 0;
           if (dd != 0.0f) {
