@@ -559,6 +559,61 @@ def snapshot_leg(wl, dev, rounds, W):
             "tokens_per_s": s.batch * T * rounds / (total / 1e3), "rounds": rounds}
 
 
+def tree_verify_leg(wl, dev, rounds, W):
+    """Tree-shaped speculation (four drafts: draft 0, two alternatives 1 and 2 after it,
+    draft 3 after draft 1) verified in one pass, then each sequence's accepted
+    root-to-draft path committed by index list; B = 512, same workload as the chain
+    verify leg.  The accepted path per sequence and round comes from the workload's
+    accepted count: 0 -> [], 1 -> [0], 2 -> [0, 1] or [0, 2] by sequence parity,
+    3 or 4 -> [0, 1, 3]."""
+    import torch
+    T = 4
+    parents = [-1, 0, 0, 1]
+    cache = make_cache(wl, dev)
+    s = wl.shape
+    A = torch.from_numpy(wl.A()).to(dev) if s.kind == 0 else None
+    drafts, lens, paths = [], [], []
+    for r in range(4):
+        inp = upload(wl.draft(r, T), dev)
+        if A is not None:
+            inp["A"] = A
+        drafts.append(inp)
+        acc = wl.accepted(r, T)
+        pl = np.zeros(s.batch, dtype=np.int32)
+        pt = np.zeros((s.batch, cache.T_max), dtype=np.int32)
+        for b in range(s.batch):
+            a = int(acc[b])
+            path = [] if a == 0 else [0] if a == 1 else ([0, 1] if b % 2 == 0 else [0, 2]) if a == 2 else [0, 1, 3]
+            pl[b] = len(path)
+            pt[b, :len(path)] = path
+        lens.append(torch.from_numpy(pl).to(dev))
+        paths.append(torch.from_numpy(pt).to(dev))
+    y = torch.empty(s.batch, T, s.n_heads, s.d_head, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for r in range(W):
+        cache.verify_tree(T, parents, drafts[r % 4], y, stream=stream)
+        cache.commit_path(lens[r % 4], paths[r % 4], stream=stream)
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(rounds)]
+    for r in range(rounds):
+        ev[r][0].record(stream)
+        cache.verify_tree(T, parents, drafts[r % 4], y, stream=stream)
+        ev[r][1].record(stream)
+        cache.commit_path(lens[r % 4], paths[r % 4], stream=stream)
+        ev[r][2].record(stream)
+    torch.cuda.synchronize(dev)
+    ver = [a.elapsed_time(b) for a, b, _ in ev]
+    com = [b.elapsed_time(c) for _, b, c in ev]
+    total = ev[0][0].elapsed_time(ev[-1][2])
+    assert cache.device_error() == 0
+    del cache
+    torch.cuda.empty_cache()
+    return {"workload": f"{'mamba2' if s.kind == 0 else 'gdn'} tree verify (parents {parents}) + path commit, "
+                        f"B={s.batch}",
+            "verify_us": 1e3 * statistics.mean(ver), "commit_us": 1e3 * statistics.mean(com),
+            "round_us": 1e3 * total / rounds, "rounds": rounds}
+
+
 def read_copy_error_leg(wl, dev, mode, steps):
     """Per-window rel-L2 of the read-copy outputs against the FP32-checkpoint outputs of
     the same kernels on the same inputs (two caches side by side; the FP32 path itself
@@ -779,6 +834,9 @@ def extras(line, args, dev, hbm, m2):
     for v in ver:
         v["verify_frac"] = v["verify_state_gbs"] / hbm
     line["verify"] = ver
+    with nvtx_range("tree verify + path commit"):
+        line["tree_verify"] = [tree_verify_leg(configs.config3_mamba2(), dev, 32, 4),
+                               tree_verify_leg(configs.config3_gdn(), dev, 32, 4)]
     rc = []
     for mode in ("fp8", "nvfp4"):
         with nvtx_range(f"decode read copy {mode}"):

@@ -74,28 +74,32 @@ __global__ void __launch_bounds__(kCompactThreads) tree_compact_kernel(const Lay
   const int len = smove;
   if (len == 0) return;
   const size_t bH = static_cast<size_t>(b) * H, bG = static_cast<size_t>(b) * G;
+  // rows of a slot move 16 bytes at a time (P and N are multiples of 8, the ring's
+  // sections 16-byte aligned)
   if (d.kind == RS_MAMBA2) {
     // x [B][H][C][P], dt and log a [B][H][Cp] per head, B [B][G][C][N] per group
-    move_section<uint16_t>(H * P, len, sp, head, n, C, [&](int slot, int e) {
-      const int h = e / P, p = e - h * P;
-      return d.r_x + ((bH + h) * C + slot) * P + p;
+    const int xv = P / 8, bv = N / 8;  // uint4 per row
+    move_section<uint4>(H * xv, len, sp, head, n, C, [&](int slot, int e) {
+      const int h = e / xv, c = e - h * xv;
+      return reinterpret_cast<uint4*>(d.r_x + ((bH + h) * C + slot) * P) + c;
     });
     move_section<uint16_t>(H, len, sp, head, n, C, [&](int slot, int h) { return d.r_dt + (bH + h) * Cp + slot; });
     move_section<float>(H, len, sp, head, n, C, [&](int slot, int h) { return d.r_la + (bH + h) * Cp + slot; });
-    move_section<uint16_t>(G * N, len, sp, head, n, C, [&](int slot, int e) {
-      const int g = e / N, c = e - g * N;
-      return d.r_B + ((bG + g) * C + slot) * N + c;
+    move_section<uint4>(G * bv, len, sp, head, n, C, [&](int slot, int e) {
+      const int g = e / bv, c = e - g * bv;
+      return reinterpret_cast<uint4*>(d.r_B + ((bG + g) * C + slot) * N) + c;
     });
   } else {
     // u [B][H][C][P], g [B][H][Cp] per head, k [B][G][C][N] per group
-    move_section<float>(H * P, len, sp, head, n, C, [&](int slot, int e) {
-      const int h = e / P, p = e - h * P;
-      return d.r_u + ((bH + h) * C + slot) * P + p;
+    const int uv = P / 4, kv = N / 8;
+    move_section<uint4>(H * uv, len, sp, head, n, C, [&](int slot, int e) {
+      const int h = e / uv, c = e - h * uv;
+      return reinterpret_cast<uint4*>(d.r_u + ((bH + h) * C + slot) * P) + c;
     });
     move_section<float>(H, len, sp, head, n, C, [&](int slot, int h) { return d.r_g + (bH + h) * Cp + slot; });
-    move_section<uint16_t>(G * N, len, sp, head, n, C, [&](int slot, int e) {
-      const int g = e / N, c = e - g * N;
-      return d.r_k + ((bG + g) * C + slot) * N + c;
+    move_section<uint4>(G * kv, len, sp, head, n, C, [&](int slot, int e) {
+      const int g = e / kv, c = e - g * kv;
+      return reinterpret_cast<uint4*>(d.r_k + ((bG + g) * C + slot) * N) + c;
     });
   }
 }
