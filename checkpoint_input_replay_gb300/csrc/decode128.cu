@@ -1019,7 +1019,55 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               __stcs(gS4 + (tw + TW * (r0 + e)) * SEG + lane, acc[e]);
-              if (READ == READ_NVFP4) sT4[(tw + TW * (r0 + e)) * SEG + lane] = acc[e];
+              if (READ == READ_NVFP4 && RW != 8) sT4[(tw + TW * (r0 + e)) * SEG + lane] = acc[e];
+            }
+            if (READ == READ_NVFP4 && RW == 8) {
+              // NVFP4 with the warp's rows all in registers: the head's amax over the team
+              // (its matrix scale), then these rows' codes straight from the registers
+              float mloc = 0.f;
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                mloc = fmaxf(mloc, fmaxf(fmaxf(fabsf(acc[e].x), fabsf(acc[e].y)), fmaxf(fabsf(acc[e].z), fabsf(acc[e].w))));
+              mloc = seg_max<32>(mloc);
+              int* slot_amax = reinterpret_cast<int*>(st + LY.st_meta) + 4;
+              if (lane == 0) atomicMax(slot_amax, __float_as_int(mloc));  // non-negative floats order as ints
+              __syncwarp();
+              if (lane == 0) mbar_arrive(amaxbar + 8 * team + s);
+              const bool got =
+                  __all_sync(0xffffffffu, mbar_wait_bounded(amaxbar + 8 * team + s, (amax_phase >> s) & 1u));
+              amax_phase ^= 1u << s;
+              if (!got) {
+                if (lane == 0) {
+                  report_error(d.err, DEVERR_TIMEOUT, static_cast<int>(u / H));
+                  smisc[0] = 1;
+                }
+              } else {
+                const float amax = __int_as_float(*reinterpret_cast<volatile int*>(slot_amax));
+                const float smat = __fdiv_rn(amax, 2688.0f);  // 448 * 6
+                const float six_s = __fmul_rn(6.0f, smat);
+                const float r6 = six_s != 0.0f ? __frcp_rn(six_s) : 0.0f;
+                uint16_t* codes = reinterpret_cast<uint16_t*>(d.rc_codes + u * (tile / 2));
+                uint8_t* blk = d.rc_blkscale + u * (tile / 16);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const int R = tw + TW * (r0 + e);
+                  const float4 v4 = acc[e];
+                  float mb = fmaxf(fmaxf(fabsf(v4.x), fabsf(v4.y)), fmaxf(fabsf(v4.z), fabsf(v4.w)));
+                  mb = seg_max<4>(mb);  // 4 lanes = one 16-element block
+                  uint32_t bcode = 0;
+                  if (six_s != 0.0f) bcode = f32x2_to_e4m3x2(div_by(mb, six_s, r6), 0.0f) & 0xFFu;
+                  const float dd = __fmul_rn(e4m3_to_f32(bcode), smat);
+                  uint32_t qv = 0;
+                  if (dd != 0.0f) {
+                    const float rd = __frcp_rn(dd);
+                    qv = f32x4_to_e2m1x4(div_by(v4.x, dd, rd), div_by(v4.y, dd, rd), div_by(v4.z, dd, rd),
+                                         div_by(v4.w, dd, rd));
+                  }
+                  codes[R * SEG + lane] = static_cast<uint16_t>(qv);
+                  if ((lane & 3) == 0) blk[R * (N / 16) + (lane >> 2)] = static_cast<uint8_t>(bcode);
+                }
+                if (tw == 0 && lane == 0) d.rc_matscale[u] = smat;
+              }
             }
             if (READ == READ_FP8) {
               // refresh the FP8 copy of these eight rows from the folded rows in registers:
@@ -1049,7 +1097,7 @@ __global__ void __launch_bounds__(kThreads128, 1) decode128_kernel(const LayerDe
             }
           }
         }
-        if (READ == READ_NVFP4 && flush) {
+        if (READ == READ_NVFP4 && RW != 8 && flush) {
           // refresh the NVFP4 copy of this warp's rows from the folded rows in shared memory
           // (the matrix scale needs the amax of the whole head first)
           {
