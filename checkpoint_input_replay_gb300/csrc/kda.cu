@@ -297,10 +297,10 @@ __global__ void __launch_bounds__(kKdaThreads, 4) kda_kernel(const LayerDev d, c
 // decays and keys over the key channels, the deltas of its rows) and this
 // token's log decay, key, query and values, and builds the head's tables: the
 // channel-wise suffix scan (the eight warps, two halves of the records) gives the
-// decayed keys k_j W'_j and G',
-// then the record dot products (a warp per item).  The head's next units, when
-// this CTA takes them right after, reuse those tables and stage only their
-// checkpoint rows, their rows of the deltas and values.  Then eight rows a warp:
+// decayed keys k_j W'_j and G', then the record dot products (a warp per item).
+// The head's next units, when this CTA takes them right after, reuse those
+// tables and stage only their checkpoint rows, their rows of the deltas and
+// values.  Then eight rows a warp:
 // the two checkpoint dot products (a transpose-reduce over the row's lanes), the
 // records' terms (four lanes a row split the records), u, o and, on a flush
 // step, the folded rows.  The CTAs read their sequences' cursors once, at the
