@@ -101,6 +101,7 @@ __device__ __forceinline__ int ring_slot(int head, int j, int C) {
 // heads per warp per batch, held in registers) before any arithmetic.
 constexpr int kPrepWarps = kPrepThreads / 32;
 constexpr int kHB = 4;  // heads per warp per batch
+constexpr int kKeyRow = N / 4 + 8;  // uint2 per padded key row (320 bytes)
 
 template <int KIND>
 __global__ void __launch_bounds__(kPrepThreads, 8) verify_prep_kernel(const LayerDev d, const TokenIn in, const int T) {
@@ -111,8 +112,13 @@ __global__ void __launch_bounds__(kPrepThreads, 8) verify_prep_kernel(const Laye
   // the main kernel may be scheduled as SMs free up: it waits for this grid only
   // before it reads the coefficient tables (programmatic dependent launch)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  __shared__ uint2 skey[kMaxRec][N / 4];  // keys of records 0..n+T-1 (committed, then drafts)
-  __shared__ uint2 sq[kT][N / 4];         // draft queries
+  constexpr int kNCol = KIND == 0 ? kT : 2 * kT;
+  // keys of records 0..n+T-1 (committed, then drafts) as bf16, each row padded to
+  // 320 bytes so that the four rows a warp reads at once fill both bank halves
+  __shared__ __align__(16) uint2 skey[kMaxRec][kKeyRow];
+  // dot-product columns in FP32: the draft queries in 0..3, the drafts' keys
+  // (GDN) in 4..7, zero for tau >= T
+  __shared__ __align__(16) float scol[kNCol][N];
   __shared__ float sdq[kMaxRec][kT];      // k_j . q_tau
   __shared__ float sdk[kMaxRec][kT];      // k_j . k_{n+tau} (GDN)
 
@@ -165,41 +171,90 @@ __global__ void __launch_bounds__(kPrepThreads, 8) verify_prep_kernel(const Laye
   uint16_t* rk = (KIND == 0 ? d.r_B : d.r_k) + static_cast<size_t>(bg) * C * N;
   const uint16_t* kin = KIND == 0 ? in.Bm : in.k;
   const uint16_t* qin = KIND == 0 ? in.Cm : in.q;
-  for (int e = t; e < nr * (N / 4); e += kPrepThreads) {
-    const int j = e / (N / 4), c = e - j * (N / 4);
+  // 16-byte pieces: 16 per 128-channel bf16 row
+  for (int e = t; e < nr * 16; e += kPrepThreads) {
+    const int j = e >> 4, c = e & 15;
     const uint16_t* src = j < n ? rk + static_cast<size_t>(ring_slot(head, j, C)) * N
                                 : kin + ((static_cast<size_t>(b) * T + (j - n)) * G + g) * N;
-    skey[j][c] = reinterpret_cast<const uint2*>(src)[c];
+    const uint4 raw = reinterpret_cast<const uint4*>(src)[c];
+    reinterpret_cast<uint4*>(&skey[j][0])[c] = raw;
+    if constexpr (KIND == 1) {
+      if (j >= n) {
+        float4* dst = reinterpret_cast<float4*>(&scol[kT + j - n][8 * c]);
+        dst[0] = bf4(make_uint2(raw.x, raw.y));
+        dst[1] = bf4(make_uint2(raw.z, raw.w));
+      }
+    }
   }
-  for (int e = t; e < T * (N / 4); e += kPrepThreads) {
-    const int tau = e / (N / 4), c = e - tau * (N / 4);
-    sq[tau][c] = reinterpret_cast<const uint2*>(qin + ((static_cast<size_t>(b) * T + tau) * G + g) * N)[c];
+  for (int e = t; e < kT * 16; e += kPrepThreads) {
+    const int tau = e >> 4, c = e & 15;
+    float4* dst = reinterpret_cast<float4*>(&scol[tau][8 * c]);
+    if (tau < T) {
+      const uint4 raw = reinterpret_cast<const uint4*>(qin + ((static_cast<size_t>(b) * T + tau) * G + g) * N)[c];
+      dst[0] = bf4(make_uint2(raw.x, raw.y));
+      dst[1] = bf4(make_uint2(raw.z, raw.w));
+    } else {
+      dst[0] = dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if constexpr (KIND == 1) {
+        float4* dk4 = reinterpret_cast<float4*>(&scol[kT + tau][8 * c]);
+        dk4[0] = dk4[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
   }
   load_heads(0);
   __syncthreads();
   // the drafts' keys into the ring, after the committed records
-  for (int e = t; e < T * (N / 4); e += kPrepThreads) {
-    const int tau = e / (N / 4), c = e - tau * (N / 4);
-    reinterpret_cast<uint2*>(rk + static_cast<size_t>(ring_slot(head, n + tau, C)) * N)[c] = skey[n + tau][c];
+  for (int e = t; e < T * 16; e += kPrepThreads) {
+    const int tau = e >> 4, c = e & 15;
+    reinterpret_cast<uint4*>(rk + static_cast<size_t>(ring_slot(head, n + tau, C)) * N)[c] =
+        reinterpret_cast<const uint4*>(&skey[n + tau][0])[c];
   }
-  // key dot products: item = (8 records, one column), one warp per item
+  // key dot products.  A pass of one warp covers 4 * RPL records: lane 8 rq + cb
+  // holds channels 4 (8 i + cb) .. + 3 (i < 4) of record jb + 4 r + rq (r < RPL)
+  // and forms its partial dots with every column; the transpose-reduce over the
+  // eight lanes of rq leaves value cb = r * kNCol + col in lane cb.
   {
-    const int ncol = KIND == 0 ? T : 2 * T;
-    const int nblk = (nr + 7) >> 3;
-    for (int it = warp; it < nblk * ncol; it += kPrepWarps) {
-      const int jb = it / ncol, c = it - jb * ncol;
-      const float4 o4 = bf4(c < T ? sq[c][lane] : skey[n + c - T][lane]);
+    constexpr int RPL = 8 / kNCol;
+    const int rq = lane >> 3, cb = lane & 7;
+    const int npass = (nr + 4 * RPL - 1) / (4 * RPL);
+    for (int p = warp; p < npass; p += kPrepWarps) {
+      const int jb = p * 4 * RPL;
+      int jr[RPL];
+#pragma unroll
+      for (int r = 0; r < RPL; ++r) jr[r] = min(jb + 4 * r + rq, nr - 1);
+      float2 acc[RPL][kNCol];
+#pragma unroll
+      for (int r = 0; r < RPL; ++r)
+#pragma unroll
+        for (int col = 0; col < kNCol; ++col) acc[r][col] = make_float2(0.f, 0.f);
+#pragma unroll 1
+      for (int i = 0; i < 4; ++i) {
+        float4 kr[RPL];
+#pragma unroll
+        for (int r = 0; r < RPL; ++r) kr[r] = bf4(skey[jr[r]][8 * i + cb]);
+#pragma unroll
+        for (int col = 0; col < kNCol; ++col) {
+          const float4 o = reinterpret_cast<const float4*>(scol[col])[8 * i + cb];
+#pragma unroll
+          for (int r = 0; r < RPL; ++r) {
+            acc[r][col] = fma2(make_float2(kr[r].x, kr[r].y), make_float2(o.x, o.y), acc[r][col]);
+            acc[r][col] = fma2(make_float2(kr[r].z, kr[r].w), make_float2(o.z, o.w), acc[r][col]);
+          }
+        }
+      }
       float part[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int j = 8 * jb + e;
-        part[e] = j < nr ? dot4(bf4(skey[j][lane]), o4) : 0.f;
-      }
-      const float tot = reduce8(part, lane);
-      const int j = 8 * jb + (lane >> 2);
-      if ((lane & 3) == 0 && j < nr) {
-        if (c < T) sdq[j][c] = tot;
-        else sdk[j][c - T] = tot;
+      for (int r = 0; r < RPL; ++r)
+#pragma unroll
+        for (int col = 0; col < kNCol; ++col) part[r * kNCol + col] = acc[r][col].x + acc[r][col].y;
+      const float tot = reduce8_lanes3(part, lane);
+      const int j = jb + 4 * (cb / kNCol) + rq, col = cb % kNCol;
+      if (j < nr) {
+        if (col < kT) {
+          if (col < T) sdq[j][col] = tot;
+        } else if (col - kT < T) {
+          sdk[j][col - kT] = tot;
+        }
       }
     }
   }
@@ -242,9 +297,9 @@ __global__ void __launch_bounds__(kPrepThreads, 8) verify_prep_kernel(const Laye
           // w_j = prod_{i=j+1..n+tau} a_i, D = prod_{i<=n+tau} a_i
           const float ex = __shfl_down_sync(0xffffffffu, v[tau], 1);
           const bool onp = lane < n || on_tree_path(d.tree_anc, tau, sigma);  // record on draft tau's path
-          const float W = onp ? expf(lane < n + tau ? ex : 0.f) : 0.f;
+          const float W = onp ? __expf(lane < n + tau ? ex : 0.f) : 0.f;
           c1[tau] = tau < T ? W * dq[tau] * dtj : 0.f;
-          Dv[tau] = tau < T ? expf(__shfl_sync(0xffffffffu, v[tau], 0)) : 0.f;
+          Dv[tau] = tau < T ? __expf(__shfl_sync(0xffffffffu, v[tau], 0)) : 0.f;
         }
         if (lane < nr) reinterpret_cast<float4*>(co)[lane] = make_float4(c1[0], c1[1], c1[2], c1[3]);
         if (lane == 0) reinterpret_cast<float4*>(co)[C] = make_float4(Dv[0], Dv[1], Dv[2], Dv[3]);
@@ -282,15 +337,15 @@ __global__ void __launch_bounds__(kPrepThreads, 8) verify_prep_kernel(const Laye
           // tW_j = prod_{i=j+1..m} a_i (j <= m), tWk_j = prod_{i=j+1..m-1} a_i (j < m)
           const float exq = __shfl_down_sync(0xffffffffu, vq[tau], 1);
           const float exk = __shfl_down_sync(0xffffffffu, vk[tau], 1);
-          const float tW = lane <= m ? expf(lane < m ? exq : 0.f) : 0.f;
-          const float tWk = lane < m ? expf(lane + 1 < m ? exk : 0.f) : 0.f;
+          const float tW = lane <= m ? __expf(lane < m ? exq : 0.f) : 0.f;
+          const float tWk = lane < m ? __expf(lane + 1 < m ? exk : 0.f) : 0.f;
           const float v0q = __shfl_sync(0xffffffffu, vq[tau], 0), v0k = __shfl_sync(0xffffffffu, vk[tau], 0);
           const float gm = __shfl_sync(0xffffffffu, g_d, m < 32 ? m : 31);
           const float bm = __shfl_sync(0xffffffffu, beta_d, m < 32 ? m : 31);
           const bool live = tau < T;
-          G2[tau] = live ? expf(v0q) : 0.f;
-          G1[tau] = live ? (m > 0 ? expf(v0k) : 1.f) : 0.f;
-          a_t[tau] = live ? expf(gm) : 0.f;
+          G2[tau] = live ? __expf(v0q) : 0.f;
+          G1[tau] = live ? (m > 0 ? __expf(v0k) : 1.f) : 0.f;
+          a_t[tau] = live ? __expf(gm) : 0.f;
           b_t[tau] = live ? bm : 0.f;
           c1[tau] = (live && lane < n) ? tWk * dk[tau] : 0.f;  // coefficient of u_j[r] in S k_tau
           c2[tau] = (live && lane < n) ? tW * dq[tau] : 0.f;   // coefficient of u_j[r] in S q_tau

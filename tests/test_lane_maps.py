@@ -137,3 +137,60 @@ def test_gdn_tile_loads_are_conflict_free_per_quarter_warp():
             chunks = [(rq * SEG + 8 * i + cb) for cb in range(8)]
             banks = {(c * 16 // 4) % 32 // 4 for c in chunks}
             assert len(banks) == 8
+
+
+@pytest.mark.parametrize("ncol", [4, 8])
+@pytest.mark.parametrize("T", [1, 3, 4])
+@pytest.mark.parametrize("n", [0, 5, 15, 28])
+def test_verify_prep_dots_cover_every_record_and_column_once(ncol, T, n):
+    """Verify prep (d_state 128): a pass takes 4 RPL records (RPL = 8 / ncol); lane
+    8 rq + cb holds channels 4 (8 i + cb) .. + 3 of record jb + 4 r + rq (clamped to the
+    last record) and forms value r ncol + col; after the transpose-reduce lane cb holds
+    record jb + 4 (cb // ncol) + rq, column cb % ncol.  Columns 0..3 are the queries,
+    4..7 the drafts' keys; those with tau >= T are not written."""
+    nr = n + T
+    if nr > 32:
+        pytest.skip("more records than a ring holds")
+    RPL = 8 // ncol
+    rng = np.random.default_rng(ncol * 100 + n * 10 + T)
+    keys = rng.standard_normal((nr, 128))
+    cols = rng.standard_normal((ncol, 128))
+    written = {}
+    npass = (nr + 4 * RPL - 1) // (4 * RPL)
+    for p in range(npass):
+        jb = p * 4 * RPL
+        V = np.zeros((32, 8))
+        for L in range(32):
+            rq, cb = L >> 3, L & 7
+            ch = np.concatenate([np.arange(4 * (8 * i + cb), 4 * (8 * i + cb) + 4) for i in range(4)])
+            for r in range(RPL):
+                j = min(jb + 4 * r + rq, nr - 1)
+                for c in range(ncol):
+                    V[L][r * ncol + c] = keys[j, ch] @ cols[c, ch]
+        tot = reduce8_lanes3(V)
+        for L in range(32):
+            rq, cb = L >> 3, L & 7
+            j, c = jb + 4 * (cb // ncol) + rq, cb % ncol
+            if j < nr and (c % 4) < T:
+                assert (j, c) not in written
+                written[(j, c)] = tot[L]
+    want = {(j, c) for j in range(nr) for c in range(ncol) if c % 4 < T}
+    assert set(written) == want
+    for (j, c), v in written.items():
+        assert np.isclose(v, keys[j] @ cols[c])
+
+
+def test_verify_prep_key_rows_fill_both_bank_halves():
+    """Key rows padded to 320 bytes: the four consecutive records one pass reads (64
+    contiguous bytes each, chunk i) fall on alternate 64-byte halves of the 128-byte bank
+    period, so the warp's 256 bytes need the minimum two wavefronts."""
+    row = 320
+    for j0 in range(29):
+        for i in range(4):
+            per_bank = {}
+            for L in range(32):
+                rq, cb = L >> 3, L & 7
+                byte = (j0 + rq) * row + 8 * (8 * i + cb)
+                for w in (byte // 4, byte // 4 + 1):
+                    per_bank.setdefault(w % 32, set()).add(w)
+            assert max(len(v) for v in per_bank.values()) == 2
