@@ -101,18 +101,7 @@ __device__ __forceinline__ int ring_slot(int head, int j, int C) {
 // heads per warp per batch, held in registers) before any arithmetic.
 constexpr int kPrepWarps = kPrepThreads / 32;
 constexpr int kHB = 4;  // heads per warp per batch
-constexpr int kKeyRow = N / 4 + 2;  // uint2 per padded bf16 row (272 bytes)
-
-// D += A B for one m16n8k16 tile, bf16 operands, FP32 accumulation; a0..a3 and
-// b0, b1 hold the A (row-major) and B (column-major) fragments, two bf16 each
-__device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
+constexpr int kKeyRow = N / 4 + 8;  // uint2 per padded key row (320 bytes)
 
 template <int KIND>
 __global__ void __launch_bounds__(kPrepThreads, 8) verify_prep_kernel(const LayerDev d, const TokenIn in, const int T) {
@@ -123,12 +112,13 @@ __global__ void __launch_bounds__(kPrepThreads, 8) verify_prep_kernel(const Laye
   // the main kernel may be scheduled as SMs free up: it waits for this grid only
   // before it reads the coefficient tables (programmatic dependent launch)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // keys of records 0..n+T-1 (committed, then drafts) and the dot-product columns
-  // (the draft queries in 0..3, the drafts' keys in 4..7 for GDN), bf16 rows
-  // padded to 272 bytes so that the fragment loads of the MMA below hit 32
-  // distinct banks
+  constexpr int kNCol = KIND == 0 ? kT : 2 * kT;
+  // keys of records 0..n+T-1 (committed, then drafts) as bf16, each row padded to
+  // 320 bytes so that the four rows a warp reads at once fill both bank halves
   __shared__ __align__(16) uint2 skey[kMaxRec][kKeyRow];
-  __shared__ __align__(16) uint2 scol[8][kKeyRow];
+  // dot-product columns in FP32: the draft queries in 0..3, the drafts' keys
+  // (GDN) in 4..7, zero for tau >= T
+  __shared__ __align__(16) float scol[kNCol][N];
   __shared__ float sdq[kMaxRec][kT];      // k_j . q_tau
   __shared__ float sdk[kMaxRec][kT];      // k_j . k_{n+tau} (GDN)
 
@@ -189,50 +179,83 @@ __global__ void __launch_bounds__(kPrepThreads, 8) verify_prep_kernel(const Laye
     const uint4 raw = reinterpret_cast<const uint4*>(src)[c];
     reinterpret_cast<uint4*>(&skey[j][0])[c] = raw;
     if constexpr (KIND == 1) {
-      if (j >= n) reinterpret_cast<uint4*>(&scol[kT + j - n][0])[c] = raw;
+      if (j >= n) {
+        float4* dst = reinterpret_cast<float4*>(&scol[kT + j - n][8 * c]);
+        dst[0] = bf4(make_uint2(raw.x, raw.y));
+        dst[1] = bf4(make_uint2(raw.z, raw.w));
+      }
     }
   }
-  for (int e = t; e < T * 16; e += kPrepThreads) {
+  for (int e = t; e < kT * 16; e += kPrepThreads) {
     const int tau = e >> 4, c = e & 15;
-    reinterpret_cast<uint4*>(&scol[tau][0])[c] =
-        reinterpret_cast<const uint4*>(qin + ((static_cast<size_t>(b) * T + tau) * G + g) * N)[c];
+    float4* dst = reinterpret_cast<float4*>(&scol[tau][8 * c]);
+    if (tau < T) {
+      const uint4 raw = reinterpret_cast<const uint4*>(qin + ((static_cast<size_t>(b) * T + tau) * G + g) * N)[c];
+      dst[0] = bf4(make_uint2(raw.x, raw.y));
+      dst[1] = bf4(make_uint2(raw.z, raw.w));
+    } else {
+      dst[0] = dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if constexpr (KIND == 1) {
+        float4* dk4 = reinterpret_cast<float4*>(&scol[kT + tau][8 * c]);
+        dk4[0] = dk4[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
   }
   load_heads(0);
   __syncthreads();
-  // key dot products on the tensor cores: D[j][c] = k_j . column c, records by
-  // columns, one m16n8k16 MMA chain over the 128 channels per 16 records (warp w
-  // takes records 16 w .. 16 w + 15).  The product of two bf16 is exact in FP32
-  // and the MMA accumulates in FP32.  Rows past the last record and columns past
-  // T hold stale data; every output depends on its own row and column only, and
-  // those outputs are not stored.
-  if (warp < 2 && 16 * warp < nr) {
-    const int gq = lane >> 2, tq = lane & 3;
-    const uint32_t* A0 = reinterpret_cast<const uint32_t*>(&skey[16 * warp + gq][0]);
-    const uint32_t* A1 = reinterpret_cast<const uint32_t*>(&skey[16 * warp + gq + 8][0]);
-    const uint32_t* Bc = reinterpret_cast<const uint32_t*>(&scol[gq][0]);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  // the drafts' keys into the ring, after the committed records
+  for (int e = t; e < T * 16; e += kPrepThreads) {
+    const int tau = e >> 4, c = e & 15;
+    reinterpret_cast<uint4*>(rk + static_cast<size_t>(ring_slot(head, n + tau, C)) * N)[c] =
+        reinterpret_cast<const uint4*>(&skey[n + tau][0])[c];
+  }
+  // key dot products.  A pass of one warp covers 4 * RPL records: lane 8 rq + cb
+  // holds channels 4 (8 i + cb) .. + 3 (i < 4) of record jb + 4 r + rq (r < RPL)
+  // and forms its partial dots with every column; the transpose-reduce over the
+  // eight lanes of rq leaves value cb = r * kNCol + col in lane cb.
+  {
+    constexpr int RPL = 8 / kNCol;
+    const int rq = lane >> 3, cb = lane & 7;
+    const int npass = (nr + 4 * RPL - 1) / (4 * RPL);
+    for (int p = warp; p < npass; p += kPrepWarps) {
+      const int jb = p * 4 * RPL;
+      int jr[RPL];
 #pragma unroll
-    for (int ks = 0; ks < N / 16; ++ks) {
-      const int w = 8 * ks + tq;  // 32-bit word holding channels 16 ks + 2 tq, + 1
-      mma16816(acc, A0[w], A1[w], A0[w + 4], A1[w + 4], Bc[w], Bc[w + 4]);
-    }
+      for (int r = 0; r < RPL; ++r) jr[r] = min(jb + 4 * r + rq, nr - 1);
+      float2 acc[RPL][kNCol];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int j = 16 * warp + gq + 8 * (q >> 1), col = 2 * tq + (q & 1);
-      if (j < nr) {
-        if (col < kT) {
-          if (col < T) sdq[j][col] = acc[q];
-        } else if (KIND == 1 && col - kT < T) {
-          sdk[j][col - kT] = acc[q];
+      for (int r = 0; r < RPL; ++r)
+#pragma unroll
+        for (int col = 0; col < kNCol; ++col) acc[r][col] = make_float2(0.f, 0.f);
+#pragma unroll 1
+      for (int i = 0; i < 4; ++i) {
+        float4 kr[RPL];
+#pragma unroll
+        for (int r = 0; r < RPL; ++r) kr[r] = bf4(skey[jr[r]][8 * i + cb]);
+#pragma unroll
+        for (int col = 0; col < kNCol; ++col) {
+          const float4 o = reinterpret_cast<const float4*>(scol[col])[8 * i + cb];
+#pragma unroll
+          for (int r = 0; r < RPL; ++r) {
+            acc[r][col] = fma2(make_float2(kr[r].x, kr[r].y), make_float2(o.x, o.y), acc[r][col]);
+            acc[r][col] = fma2(make_float2(kr[r].z, kr[r].w), make_float2(o.z, o.w), acc[r][col]);
+          }
         }
       }
-    }
-  } else if (warp >= 2) {
-    // the drafts' keys into the ring, after the committed records
-    for (int e = t - 64; e < T * 16; e += kPrepThreads - 64) {
-      const int tau = e >> 4, c = e & 15;
-      reinterpret_cast<uint4*>(rk + static_cast<size_t>(ring_slot(head, n + tau, C)) * N)[c] =
-          reinterpret_cast<const uint4*>(&skey[n + tau][0])[c];
+      float part[8];
+#pragma unroll
+      for (int r = 0; r < RPL; ++r)
+#pragma unroll
+        for (int col = 0; col < kNCol; ++col) part[r * kNCol + col] = acc[r][col].x + acc[r][col].y;
+      const float tot = reduce8_lanes3(part, lane);
+      const int j = jb + 4 * (cb / kNCol) + rq, col = cb % kNCol;
+      if (j < nr) {
+        if (col < kT) {
+          if (col < T) sdq[j][col] = tot;
+        } else if (col - kT < T) {
+          sdk[j][col - kT] = tot;
+        }
+      }
     }
   }
   __syncthreads();

@@ -139,87 +139,61 @@ def test_gdn_tile_loads_are_conflict_free_per_quarter_warp():
             assert len(banks) == 8
 
 
-def _mma16816(afrag, bfrag):
-    """m16n8k16 with the fragment layout of the PTX ISA (groupID g = lane >> 2,
-    t = lane & 3): a0 = A[g][2t, 2t+1], a1 = A[g+8][2t, 2t+1], a2 = A[g][2t+8, 2t+9],
-    a3 = A[g+8][2t+8, 2t+9]; b0 = B[2t, 2t+1][g], b1 = B[2t+8, 2t+9][g]; the result
-    c0, c1 = D[g][2t, 2t+1], c2, c3 = D[g+8][2t, 2t+1]."""
-    A, B = np.zeros((16, 16)), np.zeros((16, 8))
-    for L in range(32):
-        g, t = L >> 2, L & 3
-        for q, (r, k) in enumerate([(g, 2 * t), (g + 8, 2 * t), (g, 2 * t + 8), (g + 8, 2 * t + 8)]):
-            A[r, k:k + 2] = afrag[L][q]
-        for q, k in enumerate([2 * t, 2 * t + 8]):
-            B[k:k + 2, g] = bfrag[L][q]
-    D = A @ B
-    return [[D[L >> 2, 2 * (L & 3)], D[L >> 2, 2 * (L & 3) + 1],
-             D[(L >> 2) + 8, 2 * (L & 3)], D[(L >> 2) + 8, 2 * (L & 3) + 1]] for L in range(32)]
-
-
-@pytest.mark.parametrize("gdn", [False, True])
+@pytest.mark.parametrize("ncol", [4, 8])
 @pytest.mark.parametrize("T", [1, 3, 4])
-@pytest.mark.parametrize("n", [0, 5, 12, 15, 28])
-def test_verify_prep_mma_dots_cover_every_record_and_column_once(gdn, T, n):
-    """Verify prep (d_state 128): warp w runs an m16n8k16 chain over records 16 w ..
-    16 w + 15 (while 16 w < n + T) and the eight columns (queries 0..3, the drafts'
-    keys 4..7 for GDN); lane (g, t) loads 32-bit words 8 ks + t and 8 ks + t + 4 of
-    key rows 16 w + g, 16 w + g + 8 and of column row g; result q goes to record
-    16 w + g + 8 (q >> 1), column 2 t + (q & 1).  Rows past the last record and
-    columns past T carry stale values that must not reach a stored output."""
+@pytest.mark.parametrize("n", [0, 5, 15, 28])
+def test_verify_prep_dots_cover_every_record_and_column_once(ncol, T, n):
+    """Verify prep (d_state 128): a pass takes 4 RPL records (RPL = 8 / ncol); lane
+    8 rq + cb holds channels 4 (8 i + cb) .. + 3 of record jb + 4 r + rq (clamped to the
+    last record) and forms value r ncol + col; after the transpose-reduce lane cb holds
+    record jb + 4 (cb // ncol) + rq, column cb % ncol.  Columns 0..3 are the queries,
+    4..7 the drafts' keys; those with tau >= T are not written."""
     nr = n + T
     if nr > 32:
         pytest.skip("more records than a ring holds")
-    rng = np.random.default_rng(1000 * gdn + 10 * n + T)
-    keys = np.full((32, 128), np.nan)
-    keys[:nr] = rng.standard_normal((nr, 128))
-    cols = np.full((8, 128), np.nan)
-    cols[:T] = rng.standard_normal((T, 128))
-    if gdn:
-        cols[4:4 + T] = keys[n:n + T]
-    sdq, sdk = {}, {}
-    for w in range(2):
-        if 16 * w >= nr:
-            continue
-        acc = np.zeros((32, 4))
-        for ks in range(8):
-            af, bf = [], []
-            for L in range(32):
-                g, t = L >> 2, L & 3
-                word = 8 * ks + t
-                ch = lambda wd: slice(2 * wd, 2 * wd + 2)
-                af.append([keys[16 * w + g, ch(word)], keys[16 * w + g + 8, ch(word)],
-                           keys[16 * w + g, ch(word + 4)], keys[16 * w + g + 8, ch(word + 4)]])
-                bf.append([cols[g, ch(word)], cols[g, ch(word + 4)]])
-            with np.errstate(invalid="ignore"):
-                acc += np.array(_mma16816(af, bf))
+    RPL = 8 // ncol
+    rng = np.random.default_rng(ncol * 100 + n * 10 + T)
+    keys = rng.standard_normal((nr, 128))
+    cols = rng.standard_normal((ncol, 128))
+    written = {}
+    npass = (nr + 4 * RPL - 1) // (4 * RPL)
+    for p in range(npass):
+        jb = p * 4 * RPL
+        V = np.zeros((32, 8))
         for L in range(32):
-            g, t = L >> 2, L & 3
-            for q in range(4):
-                j, col = 16 * w + g + 8 * (q >> 1), 2 * t + (q & 1)
-                if j < nr:
-                    if col < 4:
-                        if col < T:
-                            assert (j, col) not in sdq
-                            sdq[(j, col)] = acc[L][q]
-                    elif gdn and col - 4 < T:
-                        assert (j, col - 4) not in sdk
-                        sdk[(j, col - 4)] = acc[L][q]
-    assert set(sdq) == {(j, c) for j in range(nr) for c in range(T)}
-    assert set(sdk) == ({(j, c) for j in range(nr) for c in range(T)} if gdn else set())
-    for (j, c), v in sdq.items():
+            rq, cb = L >> 3, L & 7
+            ch = np.concatenate([np.arange(4 * (8 * i + cb), 4 * (8 * i + cb) + 4) for i in range(4)])
+            for r in range(RPL):
+                j = min(jb + 4 * r + rq, nr - 1)
+                for c in range(ncol):
+                    V[L][r * ncol + c] = keys[j, ch] @ cols[c, ch]
+        tot = reduce8_lanes3(V)
+        for L in range(32):
+            rq, cb = L >> 3, L & 7
+            j, c = jb + 4 * (cb // ncol) + rq, cb % ncol
+            if j < nr and (c % 4) < T:
+                assert (j, c) not in written
+                written[(j, c)] = tot[L]
+    want = {(j, c) for j in range(nr) for c in range(ncol) if c % 4 < T}
+    assert set(written) == want
+    for (j, c), v in written.items():
         assert np.isclose(v, keys[j] @ cols[c])
-    for (j, c), v in sdk.items():
-        assert np.isclose(v, keys[j] @ keys[n + c])
 
 
-def test_verify_prep_fragment_loads_hit_distinct_banks():
-    """Rows of 272 bytes (68 words): lane (g, t) reads word 68 (r0 + g) + 8 ks + t (+ 4);
-    the 32 lanes of every such load fall on 32 distinct banks."""
-    for r0 in (0, 8, 16, 24):
-        for ks in range(8):
-            for off in (0, 4):
-                banks = {(68 * (r0 + (L >> 2)) + 8 * ks + (L & 3) + off) % 32 for L in range(32)}
-                assert len(banks) == 32
+def test_verify_prep_key_rows_fill_both_bank_halves():
+    """Key rows padded to 320 bytes: the four consecutive records one pass reads (64
+    contiguous bytes each, chunk i) fall on alternate 64-byte halves of the 128-byte bank
+    period, so the warp's 256 bytes need the minimum two wavefronts."""
+    row = 320
+    for j0 in range(29):
+        for i in range(4):
+            per_bank = {}
+            for L in range(32):
+                rq, cb = L >> 3, L & 7
+                byte = (j0 + rq) * row + 8 * (8 * i + cb)
+                for w in (byte // 4, byte // 4 + 1):
+                    per_bank.setdefault(w % 32, set()).add(w)
+            assert max(len(v) for v in per_bank.values()) == 2
 
 
 def _anc_mask(parents):
