@@ -227,6 +227,8 @@ __global__ void __launch_bounds__(kPrepThreads, 8) verify_prep_kernel(const Laye
       for (int r = 0; r < RPL; ++r)
 #pragma unroll
         for (int col = 0; col < kNCol; ++col) acc[r][col] = make_float2(0.f, 0.f);
+      // one 16-byte chunk of channels at a time (unrolled, the loop's column loads are
+      // all hoisted and the registers spill)
 #pragma unroll 1
       for (int i = 0; i < 4; ++i) {
         float4 kr[RPL];
