@@ -82,6 +82,9 @@ def test_null_and_alignment_errors_need_no_device():
     assert rs.rs_verify(None, 1, rs.rs_inputs(), 0, 0) == rs.RS_ERR_NULL
     assert rs.rs_commit(None, 0, 0) == rs.RS_ERR_NULL
     assert rs.rs_flush(None, None, 0) == rs.RS_ERR_NULL
+    # tree-shaped drafts: null handle, parents or path are rejected before any CUDA call
+    assert rs.rs_verify_tree(None, 2, [-1, 0], rs.rs_inputs(), 0, 0) == rs.RS_ERR_NULL
+    assert rs.rs_commit_path(None, 4096, 8192, 0) == rs.RS_ERR_NULL
     st, code = rs.rs_get_device_error(None, 0)
     assert st == rs.RS_ERR_NULL
     rs.rs_destroy_cache(None)
