@@ -103,8 +103,11 @@ constexpr int kPrepWarps = kPrepThreads / 32;
 constexpr int kHB = 4;  // heads per warp per batch
 constexpr int kKeyRow = N / 4 + 8;  // uint2 per padded key row (320 bytes)
 
+// CTAs per SM the registers must allow: Mamba-2 (many heads per group, a long
+// per-head phase) gains from ten; GDN (two heads per group) from fewer spills at eight
 template <int KIND>
-__global__ void __launch_bounds__(kPrepThreads, 8) verify_prep_kernel(const LayerDev d, const TokenIn in, const int T) {
+__global__ void __launch_bounds__(kPrepThreads, KIND == 0 ? 10 : 8)
+    verify_prep_kernel(const LayerDev d, const TokenIn in, const int T) {
   const int H = d.H, G = d.G, C = d.C, L = d.L, Cp = d.Cp;
   const int hpg = H / G, HS = head_stride(KIND, C);
   const int bg = blockIdx.x, b = bg / G, g = bg - b * G;
